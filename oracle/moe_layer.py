@@ -58,18 +58,25 @@ def decode_bf16(bits: np.ndarray) -> np.ndarray:
     return u.view(np.float32).astype(np.float64)
 
 
-def decode_e4m3(codes: np.ndarray) -> np.ndarray:
-    """OCP FP8 E4M3 codes -> fp64: sign, 4 exponent bits (bias 7), 3 mantissa
+def _e4m3_value(c: int) -> float:
+    """OCP FP8 E4M3 code -> value: sign, 4 exponent bits (bias 7), 3 mantissa
     bits, subnormals at exponent 0, S.1111.111 is NaN, no infinities."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
-    sign = np.where(c & 0x80, -1.0, 1.0)
+    sign = -1.0 if c & 0x80 else 1.0
     ex = (c >> 3) & 0xF
-    man = (c & 0x7).astype(np.float64)
-    normal = np.ldexp(1.0 + man / 8.0, ex - 7)
-    sub = np.ldexp(man / 8.0, -6)
-    v = sign * np.where(ex == 0, sub, normal)
-    v = np.where((c & 0x7F) == 0x7F, np.nan, v)
-    return v
+    man = c & 0x7
+    if ex == 0xF and man == 0x7:
+        return float("nan")
+    if ex == 0:
+        return sign * (man / 8.0) * 2.0 ** -6
+    return sign * (1.0 + man / 8.0) * 2.0 ** (ex - 7)
+
+
+_E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 codes -> fp64, through the 256-entry table of ``_e4m3_value``."""
+    return _E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
 def expert_matrices(w: Dict[str, np.ndarray], dtype: str) -> Tuple[np.ndarray, np.ndarray]:
@@ -87,9 +94,13 @@ def expert_matrices(w: Dict[str, np.ndarray], dtype: str) -> Tuple[np.ndarray, n
         out = []
         for m, s in ((gu, w["scale_gate_up"]), (dn, w["scale_down"])):
             v = decode_e4m3(m)
+            R, K = v.shape
             sc = np.asarray(s, np.float32).astype(np.float64)
-            sc_full = np.repeat(np.repeat(sc, 128, axis=0), 128, axis=1)[: v.shape[0], : v.shape[1]]
-            out.append(v * sc_full)
+            if R % 128 or K % 128:
+                raise OracleError("FP8 blocks need both dimensions to be multiples of 128")
+            # block (r // 128, c // 128) of the matrix times its scale
+            v = (v.reshape(R // 128, 128, K // 128, 128) * sc[:, None, :, None]).reshape(R, K)
+            out.append(v)
         return out[0], out[1]
     raise OracleError(f"dtype {dtype}")
 
@@ -176,7 +187,9 @@ def union_permute(ids: np.ndarray, E: int) -> Dict[str, np.ndarray]:
     inv = np.zeros(T * k, dtype=np.int32)
     for pos, (_, t, j) in enumerate(pairs):
         inv[t * k + j] = pos
-    ratio = np.float32(np.float32(len(uniq)) / np.float32(T * k))
+    # Reading: an empty verify set (T = 0) has reuse ratio 0 (the page defines
+    # the ratio only for s >= 1 tokens).
+    ratio = np.float32(np.float32(len(uniq)) / np.float32(T * k)) if T * k > 0 else np.float32(0.0)
     return {"n_unique": len(uniq), "unique": np.array(uniq, dtype=np.int32),
             "offsets": np.array(offsets, dtype=np.int32), "perm_token": perm_token,
             "perm_slot": perm_slot, "inv": inv, "reuse_ratio": ratio}

@@ -142,6 +142,11 @@ def test_union_csr_properties_random():
                 assert pt[p] == t and ps[p] == j
 
 
+def test_union_empty_is_zero_ratio():
+    up = ml.union_permute(np.zeros((0, 3), dtype=np.int32), 8)
+    assert up["n_unique"] == 0 and up["reuse_ratio"] == 0.0 and up["offsets"].tolist() == [0]
+
+
 def test_union_rejects_duplicates_and_range():
     with pytest.raises(ml.OracleError):
         ml.union_permute(np.array([[1, 1]], dtype=np.int32), 4)

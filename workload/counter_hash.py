@@ -56,10 +56,17 @@ def hash_at(key: int, idx: np.ndarray) -> np.ndarray:
     """``mix64(key + (idx + 1) * GOLDEN)`` for a uint64 index array."""
     idx = np.asarray(idx, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        z = np.uint64(key) + (idx + np.uint64(1)) * np.uint64(GOLDEN)
-        z = (z ^ (z >> np.uint64(30))) * np.uint64(MIX1)
-        z = (z ^ (z >> np.uint64(27))) * np.uint64(MIX2)
-        z = z ^ (z >> np.uint64(31))
+        z = idx + np.uint64(1)
+        z *= np.uint64(GOLDEN)
+        z += np.uint64(key)
+        t = z >> np.uint64(30)
+        z ^= t
+        z *= np.uint64(MIX1)
+        np.right_shift(z, np.uint64(27), out=t)
+        z ^= t
+        z *= np.uint64(MIX2)
+        np.right_shift(z, np.uint64(31), out=t)
+        z ^= t
     return z
 
 
@@ -89,18 +96,20 @@ def scale_values(h: np.ndarray) -> np.ndarray:
     return v.astype(np.float32)
 
 
-def fill_host(kind: int, key: int, idx0: int, n: int) -> np.ndarray:
+def fill_host(kind: int, key: int, idx0: int, n: int, chunk: int = 1 << 20) -> np.ndarray:
     """Host twin of the device fill: elements ``idx0 .. idx0+n-1`` of a stream.
 
     Returns uint16 (bf16 bits), float32 or uint8 (e4m3 codes) by ``kind``.
+    Works in chunks so the uint64 temporaries stay small.
     """
-    h = hash_at(key, np.arange(idx0, idx0 + n, dtype=np.uint64))
-    if kind == KIND_GRID8_BF16:
-        return grid8_bf16_bits(h)
-    if kind == KIND_GRID8_F32:
-        return grid8_values(h)
-    if kind == KIND_E4M3:
-        return e4m3_codes(h)
-    if kind == KIND_SCALE_F32:
-        return scale_values(h)
-    raise ValueError(f"unknown fill kind {kind}")
+    dt = {KIND_GRID8_BF16: np.uint16, KIND_GRID8_F32: np.float32, KIND_E4M3: np.uint8,
+          KIND_SCALE_F32: np.float32}
+    if kind not in dt:
+        raise ValueError(f"unknown fill kind {kind}")
+    out = np.empty(n, dtype=dt[kind])
+    fn = {KIND_GRID8_BF16: grid8_bf16_bits, KIND_GRID8_F32: grid8_values, KIND_E4M3: e4m3_codes,
+          KIND_SCALE_F32: scale_values}[kind]
+    for a in range(0, n, chunk):
+        b = min(n, a + chunk)
+        out[a:b] = fn(hash_at(key, np.arange(idx0 + a, idx0 + b, dtype=np.uint64)))
+    return out
