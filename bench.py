@@ -1,0 +1,436 @@
+"""Benchmark of the MoE speculative verify step on GB300.
+
+One step = EcoSpec selection over the draft tree(s) + every MoE layer's route
+(optionally reuse-biased), expert union/permutation, grouped SwiGLU expert FFN
+and combine, on the workload's synthetic inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Metric: HBM GB/s on the bytes of the unique experts the step must read
+(sum over layers of |union| x expert bytes) divided by the device time of the
+step.  Also reported: verify-step latency, tokens/s, the roofline of the
+dominant kernel (FFN gate/up), clocks during the timed region, the end-to-end
+number through the C ABI with host buffers, and the CPU oracle baseline.
+Multi-GPU: independent replicas (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "qwen3_235b_like"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-layers", type=int, default=0,
+                    help="layers in the CPU oracle sample (0: auto, about 10-30 s)")
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash():
+    """Hash of the FFN gate/up kernel sources (ties committed ncu traffic to the code)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "serving_router_softmax_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("ffn") or f == "common.cuh":
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(config_name):
+    """Per-launch DRAM bytes of the gate/up kernel from a committed ncu summary,
+    only if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"ffn_gate_up_traffic_{config_name}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.split("=", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_unit_expert"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------- our arm
+def expert_bytes(cfg):
+    elem = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.dtype]
+    b = 3 * cfg.H * cfg.I * elem
+    if cfg.dtype == "e4m3":
+        b += 4 * ((2 * cfg.I // 128) * (cfg.H // 128) + (cfg.H // 128) * (cfg.I // 128))
+    return b
+
+
+def gate_up_bytes(cfg):
+    elem = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.dtype]
+    b = 2 * cfg.H * cfg.I * elem
+    if cfg.dtype == "e4m3":
+        b += 4 * (2 * cfg.I // 128) * (cfg.H // 128)
+    return b
+
+
+def ours(args, rank, ws, local):
+    import torch
+
+    import serving_router_softmax_gb300 as mv
+    from workload import CONFIGS, gen
+    from workload import device as wdev
+
+    cfg = CONFIGS[args.config]
+    dev = torch.device("cuda", local)
+    wl = gen.make_workload(cfg)
+    layers = []
+    for l in range(cfg.L):
+        gu, dn, sgu, sdn = wdev.make_layer_tensors(cfg, l, dev)
+        layers.append(mv.ExpertLayer(gu, dn, cfg.dtype, sgu, sdn))
+    t = wdev.workload_tensors(wl, dev)
+    gmax = int(wl.gamma.max())
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k,
+                       H=cfg.H, I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=gmax, mode=cfg.mode,
+                       eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap, alpha=cfg.alpha)
+    step = mv.VerifyStep(spec, layers, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        step(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    if int(step.dev_err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(step.dev_err.item())}")
+    n_unique = step.n_unique.cpu().tolist()
+    bytes_step = sum(n_unique) * expert_bytes(cfg)
+
+    # ---- device-timed region: inputs resident in HBM, weights >> L2.
+    launches0 = mv.launch_count()
+    mv.profile_begin(max_launches=max(64, args.steps * (1 + 5 * cfg.L) + 16))
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    prof = mv.profile_end()
+    launches = mv.launch_count() - launches0
+    ms_local = e0.elapsed_time(e1)
+    ms_total = max_over_ranks(ms_local, ws)
+    ms_step = ms_total / args.steps
+    total_bytes = sum_over_ranks(bytes_step * args.steps, ws)
+    value = total_bytes / (ms_total / 1e3) / 1e9
+    tokens = sum_over_ranks(wl.T * args.steps, ws)
+
+    # ---- roofline of the dominant kernel (FFN gate/up), live from this run.
+    gu = prof["ffn_gate_up"]
+    gu_bytes = sum(n_unique) * gate_up_bytes(cfg) * args.steps
+    gu_ms = gu["ms"]
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9 if gu_ms > 0 else None
+    peak, peak_kind = peaks()
+    traffic_unit = committed_traffic(args.config)
+    traffic = None
+    if traffic_unit is not None and gu["launches"]:
+        traffic = traffic_unit * sum(n_unique) / cfg.L
+    roofline = {"bound": "hbm", "kernel": "ffn_gate_up", "achieved": achieved, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": (achieved / peak) if achieved else None,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": sum(n_unique) * gate_up_bytes(cfg) / cfg.L,
+                "avg_launch_us": gu_ms * 1e3 / max(gu["launches"], 1),
+                "launches": gu["launches"]}
+    step_frac = value / peak / ws
+
+    # ---- end to end through the C ABI with host buffers.
+    pinned = {k: v.cpu().pin_memory() for k, v in t.items()}
+    y_host = torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = y_host.numel() * y_host.element_size()
+    dev_in = {k: torch.empty_like(v) for k, v in t.items()}
+
+    def one_e2e():
+        for k in pinned:
+            dev_in[k].copy_(pinned[k], non_blocking=True)
+        step(dev_in["P"], dev_in["parent"], dev_in["own_fp"], dev_in["gamma"], dev_in["logits"],
+             dev_in["x"])
+        y_host.copy_(step.y, non_blocking=True)
+
+    for _ in range(2):
+        one_e2e()
+    torch.cuda.synchronize()
+    barrier(ws)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        one_e2e()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), ws)
+    e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
+
+    result = {
+        "metric": "verify-step HBM GB/s on unique-expert bytes",
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded workload generator; counter-hash weights)",
+        "config": {"workload": cfg.name, "layers": cfg.L, "hidden": cfg.H, "experts": cfg.E,
+                   "top_k": cfg.k, "intermediate": cfg.I, "weights": cfg.dtype,
+                   "batch": cfg.nseq, "verify_tokens": wl.T, "gamma": wl.gamma.tolist(),
+                   "reuse_bias": cfg.use_bias, "selection": "marginal" if cfg.mode == 0 else "static",
+                   "l2": "inputs larger than L2 (unique-expert bytes per step >> 129 MB)",
+                   "parallelism": "replicas" if ws > 1 else "single-gpu"},
+        "latency_us": ms_step * 1e3,
+        "tokens_per_s": tokens / (ms_total / 1e3),
+        "unique_experts_per_layer": n_unique,
+        "unique_expert_gb_per_step": bytes_step / 1e9,
+        "frac_of_peak_step": step_frac,
+        "frac_of_8tbs_step": value / 8000.0 / ws,
+        "roofline": roofline,
+        "kernel_ms_per_step": {k: v["ms"] / args.steps for k, v in prof.items()},
+        "control_path_frac": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))
+        / max(ms_local, 1e-9),
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms / args.steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+    }
+    return result, wl, cfg
+
+
+# ---------------------------------------------------------------------- oracle
+def oracle_sample(cfg, wl, n_layers, time_budget_s=25.0):
+    """Times the CPU oracle on the first n_layers of the step (all verify tokens).
+    Host weight generation is outside the timed region; decoding is inside."""
+    from oracle import moe_layer as ml
+    from oracle import verify_step as ovs
+    from workload import gen
+
+    sels, _ = ovs.run_selection(wl)
+    rows = ovs.verify_rows(wl.parent.shape[0], sels)
+    conf = ovs.token_conf(wl.P, sels)
+    stored = {}
+    unions = []
+    for l in range(n_layers):
+        lg = wl.logits[l].reshape(-1, cfg.E)[rows]
+        if cfg.use_bias:
+            lg = ml.reuse_bias(lg, conf, cfg.k, cfg.cap, cfg.alpha)
+        ids, _ = ml.route(lg, cfg.k)
+        u = sorted(set(ids.ravel().tolist()))
+        unions.append(len(u))
+        for e in u:
+            stored[(l, e)] = gen.expert_weights_host(cfg, l, e)
+    x_dec = (lambda a: np.asarray(a, np.float32).astype(np.float64)) if cfg.dtype == "f32" else ml.decode_bf16
+    t0 = time.perf_counter()
+    ovs.run_step(wl, lambda l: (lambda e: ml.expert_matrices(stored[(l, e)], cfg.dtype)),
+                 layers=list(range(n_layers)), x_decode=x_dec)
+    dt = time.perf_counter() - t0
+    return dt, sum(unions) * expert_bytes(cfg)
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] or [1])
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def auto_layers(cfg):
+    per = {"f32": 1, "bf16": 2, "e4m3": 1}[cfg.dtype]
+    return max(1, min(cfg.L, {"toy": 1}.get(cfg.name, per)))
+
+
+def reference(args, rank, ws):
+    """The reference arm: the CPU oracle as it stands, on the same workload."""
+    from workload import CONFIGS, gen
+    if rank != 0:
+        return None
+    cfg = CONFIGS[args.config]
+    wl = gen.make_workload(cfg)
+    n_layers = args.cpu_layers or 1
+    times, nbytes = [], 0
+    for i in range(args.warmup + args.steps):
+        dt, b = oracle_sample(cfg, wl, n_layers)
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes = b
+    tot = sum(times)
+    value = nbytes * len(times) / tot / 1e9
+    cores = cpu_threads()
+    sample = f"oracle verify step restricted to layer(s) 0..{n_layers - 1} of {cfg.L}, all {wl.T} verify tokens"
+    return {
+        "impl": "reference", "metric": "verify-step HBM GB/s on unique-expert bytes",
+        "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / len(times) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "layers_sampled": n_layers, "verify_tokens": wl.T},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        res = reference(args, rank, ws)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    rank, ws, local = dist_setup(args.gpus)
+    res, wl, cfg = ours(args, rank, ws, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        n_layers = args.cpu_layers or auto_layers(cfg)
+        dt, nbytes = oracle_sample(cfg, wl, n_layers)
+        res["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cpu_threads(),
+                               "kind": "oracle",
+                               "sample": f"oracle on layer(s) 0..{n_layers - 1} of {cfg.L}, all {wl.T} verify tokens, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(res))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

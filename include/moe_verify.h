@@ -1,0 +1,277 @@
+/*
+ * moe_verify.h -- C ABI of the MoE speculative-verify library (libmoeverify.so).
+ *
+ * The library computes the data-parallel hot path of one speculative-decoding
+ * verify step of a Mixture-of-Experts model:
+ *   eco_select         EcoSpec cost-aware greedy draft selection
+ *   moe_route          router top-k + softmax weights, optional S2-MoE reuse bias
+ *   moe_union_permute  expert union of the verify tokens, per-expert token groups
+ *   moe_verify_ffn     grouped SwiGLU expert FFN over the union + weighted combine
+ *   moe_verify_step    all of the above for L layers in one call
+ *
+ * Conventions shared by every entry point
+ *   - Every array argument is a DEVICE pointer owned by the caller, unless a
+ *     comment says "host".  The library never frees caller memory and keeps no
+ *     pointer past the call.  The library allocates no device memory; kernels
+ *     that need scratch space take a caller-provided workspace whose size the
+ *     matching *_workspace() query returns.
+ *   - `stream` is a cudaStream_t (passed as void*).  Every call only enqueues
+ *     work on that stream and returns; it never synchronises the host.
+ *   - The return value reports errors the host can see before launching
+ *     (MOE_ERR_ARG for a bad size or NULL pointer, MOE_ERR_UNSUPPORTED for a
+ *     shape outside the documented limits, MOE_ERR_CUDA for a launch failure,
+ *     MOE_ERR_WORKSPACE for a too-small workspace).  Nothing is enqueued when a
+ *     call returns an error.
+ *   - Errors only the device can see (NaN logits, ids out of range, malformed
+ *     trees, bounded waits that gave up) are OR-ed as MOE_DEV_* bits into
+ *     `*dev_err` (an int32 in device memory that the caller zeroes and reads
+ *     after synchronising).  Kernels never trap; when they flag an error they
+ *     write the documented "invalid" values (-1 ids, zero counts) and return.
+ *   - Arrays are row-major and densely packed.  Element types are as declared;
+ *     bf16 tensors are passed as their 16-bit patterns, FP8 tensors as bytes.
+ *   - Target: NVIDIA GB300 (sm_103a).  The library is built for that
+ *     architecture only.
+ */
+#ifndef MOE_VERIFY_H
+#define MOE_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_CUDA = 3,
+  MOE_ERR_WORKSPACE = 4
+};
+
+/* Device error bits (OR-ed into *dev_err). */
+#define MOE_DEV_NAN_LOGIT 0x01  /* a router logit was NaN: that token's ids are -1, weights 0  */
+#define MOE_DEV_BAD_ID    0x02  /* an expert id outside [0, E)                                   */
+#define MOE_DEV_DUP_ID    0x04  /* a token lists the same expert twice                           */
+#define MOE_DEV_BAD_TREE  0x08  /* parent[t] not in [-1, t) or gamma outside [0, gamma_max]     */
+#define MOE_DEV_BAD_PROB  0x10  /* a path probability / confidence weight is NaN or negative    */
+#define MOE_DEV_TIMEOUT   0x20  /* a bounded device-side wait gave up                            */
+#define MOE_DEV_CAPACITY  0x40  /* a count exceeded the capacity the caller sized buffers for   */
+
+/* Weight storage types. */
+enum {
+  MOE_DTYPE_F32 = 0,       /* fp32 weights and activations                                  */
+  MOE_DTYPE_BF16 = 1,      /* bf16 weights and activations                                  */
+  MOE_DTYPE_E4M3_B128 = 2  /* FP8 E4M3 weights with one fp32 scale per 128x128 block;
+                              bf16 activations                                              */
+};
+
+/* ---------------------------------------------------------------- routing
+ * moe_route -- per token: top-k experts of the router logits and their weights.
+ *
+ * Defined by: EcoSpec write-up section 3.1 (softmax, then top-K per layer) and
+ * section 2 (S_l(x_t), the expert set token t routes to); with use_bias, the
+ * S2-MoE write-up's component 2 (reuse-aware expert gating, steps 1-3, Fig. 5).
+ *
+ *   logits  [T, E] fp32.
+ *   w_conf  [T] fp32 confidence weight per token (>= 0); read only when
+ *           cfg->use_bias != 0, may be NULL otherwise.
+ *   ids     [T, k] int32 out: expert ids in decreasing logit order; equal
+ *           logits go to the lower id; -0.0 == +0.0.
+ *   w       [T, k] fp32 out: softmax over the k selected logits (equal to the
+ *           full softmax renormalised over the selected experts).
+ * With use_bias the logits are first biased, in fp32 with this exact op order:
+ *   g_e   = sum_{b = 0..T-1} w_conf[b] * [e in TopK(logits[b])]  (plain adds)
+ *   E*    = the `cap` experts with the largest g_e among g_e > 0 (ties: lower id)
+ *   lam_b = alpha * (logits[b]_(1) - logits[b]_(k+1))   ((j) = j-th largest)
+ *   l'_b,e = logits[b,e] + lam_b for e in E*, unchanged otherwise
+ * and ids/w are computed from l'.  Requires E >= k+1, cap >= 1.
+ * Limits: 1 <= k <= 16, k <= E <= 1024, T >= 0; with use_bias T <= 256.
+ * Device errors: MOE_DEV_NAN_LOGIT (token's ids = -1, w = 0),
+ * MOE_DEV_BAD_PROB (w_conf NaN or negative; all ids -1).
+ */
+typedef struct {
+  int32_t T, E, k;
+  int32_t use_bias, cap;
+  float alpha;
+} moe_route_cfg;
+
+int moe_route(const float* logits, const float* w_conf, const moe_route_cfg* cfg,
+              int32_t* ids, float* w, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------- union
+ * moe_union_permute -- the experts the verify tokens need, each once.
+ *
+ * Defined by: EcoSpec write-up section 2 (the verify expert set is the union
+ * of the tokens' routed experts; the weights to load are that union) and the
+ * S2-MoE write-up, challenge 2 (reuse ratio |union| / (s * k), s = tokens).
+ *
+ *   ids         [T, k] int32 in.
+ *   n_unique    [1] int32 out: U = |union|.
+ *   unique      [min(E, T*k)] int32 out: the U expert ids, ascending.
+ *   offsets     [min(E, T*k) + 1] int32 out: token group of unique[u] is
+ *               perm positions offsets[u] .. offsets[u+1]-1; offsets[U] = T*k.
+ *   perm_token  [T*k] int32 out: token of each perm position (expert
+ *               ascending, then token ascending).
+ *   perm_slot   [T*k] int32 out: the slot j with ids[t, j] == expert.
+ *   inv         [T*k] int32 out: inv[t*k + j] = perm position of (t, j).
+ *   reuse_ratio [1] fp32 out: U / (T*k) rounded once to fp32; 0 when T == 0.
+ * Limits: 1 <= k <= 16, 1 <= E <= 1024, T*k <= 65536, T*E <= 1048576.
+ * Device errors: MOE_DEV_BAD_ID, MOE_DEV_DUP_ID (then n_unique = 0).
+ */
+int moe_union_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E,
+                      int32_t* n_unique, int32_t* unique, int32_t* offsets,
+                      int32_t* perm_token, int32_t* perm_slot, int32_t* inv,
+                      float* reuse_ratio, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------- expert FFN
+ * One layer's expert weights, expert-major with each expert contiguous:
+ *   w_gate_up [E, 2I, H]: rows 0..I-1 are W_gate, rows I..2I-1 are W_up.
+ *   w_down    [E, H, I].
+ *   FP8 only: scales_gate_up [E, 2I/128, H/128] and scales_down
+ *   [E, H/128, I/128] fp32; weight (r, c) of a matrix is code(r, c) *
+ *   scale[r/128, c/128].  NULL for the other dtypes.
+ * Pointers must be 16-byte aligned.  Limits: H and I multiples of 64
+ * (of 128 for FP8), E <= 1024.
+ */
+typedef struct {
+  int32_t H, I, E, dtype;
+  const void* w_gate_up;
+  const void* w_down;
+  const float* scales_gate_up;
+  const float* scales_down;
+} moe_layer_weights;
+
+/* Bytes of workspace moe_verify_ffn needs for T tokens with top-k routing. */
+size_t moe_verify_ffn_workspace(const moe_layer_weights* lw, int32_t T, int32_t k);
+
+/*
+ * moe_verify_ffn -- y_t = sum_{j<k} w[t,j] * FFN_{ids[t,j]}(x_t), reading the
+ * weights of each expert in the union from HBM once.
+ *
+ * Defined by: EcoSpec write-up section 1 (an MoE layer's cost is set by the
+ * union of experts the tokens activate) and the S2-MoE write-up's background
+ * (each token passes its top-k experts; verification reuses loaded weights).
+ * FFN_e(x) = W_down,e (silu(W_gate,e x) * (W_up,e x)), silu(a) = a/(1+e^-a).
+ *
+ *   x        [T, H] activations: fp32 for MOE_DTYPE_F32, bf16 bits otherwise.
+ *   n_unique, unique, offsets, perm_token, inv: as written by
+ *            moe_union_permute for the same ids.
+ *   w        [T, k] fp32 routing weights.
+ *   y        [T, H] fp32 out.  The combine sums slots j = 0..k-1 in order.
+ * Arithmetic: fp32 accumulation; for bf16/FP8 weights the SwiGLU
+ * intermediate is rounded to bf16 before the down projection.
+ * Limits: 1 <= T <= 256, 1 <= k <= 16.
+ * Device errors: MOE_DEV_CAPACITY (n_unique > min(E, T*k)), MOE_DEV_BAD_ID.
+ */
+int moe_verify_ffn(const void* x, int32_t T, int32_t k, const moe_layer_weights* lw,
+                   const int32_t* n_unique, const int32_t* unique, const int32_t* offsets,
+                   const int32_t* perm_token, const int32_t* inv, const float* w,
+                   float* y, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------- selection
+ * eco_select -- EcoSpec cost-aware draft selection, one tree per sequence.
+ *
+ * Defined by: EcoSpec write-up section 3.2 (expert buffer B, empty at the
+ * start of every speculative step) and section 3.3 (score
+ * S(t) = P(t) / (|E_traj(t) \ B| + eps); greedy: take the argmax, add it to
+ * S, B |= E_traj(best), until gamma nodes are chosen; prefix consistency).
+ * mode 1 is the static ablation of section 4.3: denominator |E_traj(t)|.
+ *
+ *   P        [nseq, N] fp32 path probabilities (product of draft
+ *            probabilities from the root), finite and >= 0.
+ *   parent   [nseq, N] int32: parent draft node, -1 for a child of the root;
+ *            parent[t] < t (breadth-first numbering).
+ *   own_fp   [nseq, N, W] uint32: each node's own predicted footprint;
+ *            bit l*E + e (word (l*E+e)/32, bit (l*E+e)%32) marks (layer l,
+ *            expert e).  E_traj(t) is the OR of own_fp along the path to t.
+ *   gamma_per_seq [nseq] int32 per-sequence budget in [0, gamma_max], or
+ *            NULL for gamma_max everywhere.  Budgets above N select all nodes.
+ *   selected [nseq, gamma_max] int32 out: chosen nodes in selection order;
+ *            unused slots are -1.
+ *   union_size [nseq] int32 out: |B| after the last round.
+ * Scores are compared exactly: a beats b when
+ * P_a * (c_b + eps) > P_b * (c_a + eps), computed in fp64 (exact under the
+ * limits below); equal scores go to the lower node index.
+ * Limits: eps = 2^-s with 0 <= s <= 20; W*32*2^s < 2^29; 1 <= N <= 1024;
+ * 1 <= W <= 4096; N*W <= 40960.
+ * Device errors: MOE_DEV_BAD_TREE, MOE_DEV_BAD_PROB (that sequence's
+ * selected = -1, union_size = 0).
+ */
+typedef struct {
+  int32_t N, W, gamma_max, mode;
+  float eps;
+} eco_cfg;
+
+int eco_select(const float* P, const int32_t* parent, const uint32_t* own_fp, int32_t nseq,
+               const int32_t* gamma_per_seq, const eco_cfg* cfg, int32_t* selected,
+               int32_t* union_size, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------- whole step
+ * moe_verify_step -- one verify step: selection, then for each of L layers
+ * route (optionally biased) -> union/permute -> expert FFN + combine.
+ *
+ * Defined by: EcoSpec write-up section 2 (a round drafts a tree, selects
+ * gamma nodes and verifies gamma+1 tokens in one target forward) and the
+ * calls above.  Verify tokens are, per sequence, the root token followed by
+ * the selected nodes in selection order; sequences are concatenated.  The
+ * reuse-bias confidence of a token is its path probability (1 for a root).
+ *
+ *   node_logits [L, nseq, N+1, E] fp32 router logits of every tree node per
+ *               layer; row 0 of each sequence is the root token.
+ *   node_x      [L, nseq, N+1, H] layer inputs of every tree node (fp32 or
+ *               bf16 bits, by dtype).
+ *   layers      HOST array of L moe_layer_weights (same H, I, E, dtype).
+ *   selected, union_size: as eco_select.
+ *   n_unique    [L] int32 out: union size per layer.
+ *   y           [L, T, H] fp32 out.
+ * cfg->T must equal sum over sequences of (gamma_i + 1) with gamma_i clamped
+ * to N; the device checks it (MOE_DEV_CAPACITY if not).
+ */
+typedef struct {
+  int32_t L, nseq, N, W, E, k, H, I, dtype;
+  int32_t T, gamma_max, mode;
+  float eps;
+  int32_t use_bias, cap;
+  float alpha;
+} moe_step_cfg;
+
+size_t moe_verify_step_workspace(const moe_step_cfg* cfg);
+
+int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* parent,
+                    const uint32_t* own_fp, const int32_t* gamma_per_seq,
+                    const float* node_logits, const void* node_x,
+                    const moe_layer_weights* layers, int32_t* selected, int32_t* union_size,
+                    int32_t* n_unique, float* y, void* workspace, size_t ws_bytes,
+                    int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------- timing
+ * Optional per-kernel timing.  Between moe_profile_begin and moe_profile_end
+ * the library records a CUDA event pair on the launching stream around each
+ * of its kernel launches (at most max_launches pairs; later launches are not
+ * recorded).  moe_profile_end synchronises those events (host blocking) and
+ * writes, per kernel class, the summed milliseconds and the launch count.
+ * Classes: 0 eco_select, 1 route, 2 union/permute, 3 FFN prep,
+ * 4 FFN gate/up, 5 FFN down, 6 combine.  Not for use under stream capture.
+ */
+enum { MOE_PROF_CLASSES = 7 };
+int moe_profile_begin(int32_t max_launches);
+int moe_profile_end(float* ms_per_class, int32_t* launches_per_class, int32_t n_classes);
+
+/* ---------------------------------------------------------------- misc */
+/* Static string for a status code. */
+const char* moe_status_str(int status);
+
+/* Number of kernels the library launched since load (host counter). */
+uint64_t moe_launch_count(void);
+
+/* Library ABI version (major * 100 + minor). */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_VERIFY_H */

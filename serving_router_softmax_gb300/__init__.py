@@ -1,0 +1,13 @@
+"""GB300-native MoE speculative-verify hot path (router, reuse bias, expert
+union, grouped SwiGLU expert FFN, EcoSpec draft selection).
+
+The computation lives in ``libmoeverify.so`` (hand-written CUDA for sm_103a,
+C ABI in ``include/moe_verify.h``); this package only marshals arguments.
+Importing it loads the library and raises if it has not been built.
+"""
+from . import _lib
+from .api import (ExpertLayer, MoEError, StepSpec, VerifyStep, eco_select, ffn_workspace_bytes,  # noqa: F401
+                  launch_count, new_dev_err, profile_begin, profile_end, route, step_workspace_bytes,
+                  union_permute, verify_ffn)
+
+_lib.load()

@@ -1,0 +1,265 @@
+"""Thin PyTorch binding of libmoeverify: argument checks and pointer marshalling.
+
+Every computation happens in the library's CUDA kernels; torch only provides
+device memory and the current stream.  Calls raise ``MoEError`` on a non-OK
+host status.  Device-side error bits land in the ``dev_err`` tensor (int32,
+one element), which callers may pass in and inspect after synchronising.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+from . import _lib as L
+
+
+class MoEError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != L.MOE_OK:
+        msg = L.load().moe_status_str(status).decode()
+        raise MoEError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise MoEError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise MoEError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, shape: Sequence[int], name: str):
+    if t.dtype != dtype:
+        raise MoEError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise MoEError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def new_dev_err(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+DTYPES = {"f32": L.DTYPE_F32, "bf16": L.DTYPE_BF16, "e4m3": L.DTYPE_E4M3_B128}
+
+
+@dataclass
+class ExpertLayer:
+    """One layer's expert weights on the device (expert-major, contiguous).
+
+    gate_up: [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up); down: [E, H, I].
+    Storage: float32, bfloat16 (or int16/uint16 bf16 bits) or uint8 FP8 codes.
+    FP8 adds scales_gate_up [E, 2I/128, H/128] and scales_down [E, H/128, I/128].
+    """
+    gate_up: torch.Tensor
+    down: torch.Tensor
+    dtype: str
+    scales_gate_up: Optional[torch.Tensor] = None
+    scales_down: Optional[torch.Tensor] = None
+
+    @property
+    def E(self):
+        return self.gate_up.shape[0]
+
+    @property
+    def I(self):
+        return self.gate_up.shape[1] // 2
+
+    @property
+    def H(self):
+        return self.gate_up.shape[2]
+
+    def struct(self) -> L.LayerWeights:
+        return L.LayerWeights(self.H, self.I, self.E, DTYPES[self.dtype], _ptr(self.gate_up),
+                              _ptr(self.down), _ptr(self.scales_gate_up), _ptr(self.scales_down))
+
+
+# ------------------------------------------------------------------ calls
+def route(logits: torch.Tensor, k: int, w_conf: Optional[torch.Tensor] = None, cap: int = 0,
+          alpha: float = 0.0, dev_err: Optional[torch.Tensor] = None, stream=None):
+    """Top-k ids [T, k] int32 and weights [T, k] fp32 (optionally reuse-biased)."""
+    lib = L.load()
+    T, E = logits.shape
+    _need(logits, torch.float32, (T, E), "logits")
+    use_bias = w_conf is not None
+    if use_bias:
+        _need(w_conf, torch.float32, (T,), "w_conf")
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    cfg = L.RouteCfg(T, E, k, int(use_bias), cap, alpha)
+    _check(lib.moe_route(_ptr(logits), _ptr(w_conf), C.byref(cfg), _ptr(ids), _ptr(w),
+                         _ptr(dev_err), _stream(stream)), "moe_route")
+    return ids, w
+
+
+def union_permute(ids: torch.Tensor, E: int, dev_err: Optional[torch.Tensor] = None,
+                  stream=None) -> Dict[str, torch.Tensor]:
+    lib = L.load()
+    T, k = ids.shape
+    _need(ids, torch.int32, (T, k), "ids")
+    dev = ids.device
+    cap = min(E, T * k)
+    out = {
+        "n_unique": torch.empty(1, dtype=torch.int32, device=dev),
+        "unique": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+        "offsets": torch.empty(cap + 1, dtype=torch.int32, device=dev),
+        "perm_token": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+        "perm_slot": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+        "inv": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+        "reuse_ratio": torch.empty(1, dtype=torch.float32, device=dev),
+    }
+    _check(lib.moe_union_permute(_ptr(ids), T, k, E, _ptr(out["n_unique"]), _ptr(out["unique"]),
+                                 _ptr(out["offsets"]), _ptr(out["perm_token"]),
+                                 _ptr(out["perm_slot"]), _ptr(out["inv"]),
+                                 _ptr(out["reuse_ratio"]), _ptr(dev_err), _stream(stream)),
+           "moe_union_permute")
+    return out
+
+
+def ffn_workspace_bytes(layer: ExpertLayer, T: int, k: int) -> int:
+    st = layer.struct()
+    return int(L.load().moe_verify_ffn_workspace(C.byref(st), T, k))
+
+
+def verify_ffn(x: torch.Tensor, k: int, layer: ExpertLayer, union: Dict[str, torch.Tensor],
+               w: torch.Tensor, y: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """y [T, H] fp32 = sum_j w[t, j] * FFN_{ids[t, j]}(x[t])."""
+    lib = L.load()
+    T, H = x.shape
+    if H != layer.H:
+        raise MoEError("x hidden size does not match the layer")
+    _need(w, torch.float32, (T, k), "w")
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _need(y, torch.float32, (T, H), "y")
+    need = ffn_workspace_bytes(layer, T, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    st = layer.struct()
+    _check(lib.moe_verify_ffn(_ptr(x), T, k, C.byref(st), _ptr(union["n_unique"]),
+                              _ptr(union["unique"]), _ptr(union["offsets"]),
+                              _ptr(union["perm_token"]), _ptr(union["inv"]), _ptr(w), _ptr(y),
+                              _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream(stream)),
+           "moe_verify_ffn")
+    return y
+
+
+def eco_select(P: torch.Tensor, parent: torch.Tensor, own_fp: torch.Tensor, gamma_max: int,
+               gamma_per_seq: Optional[torch.Tensor] = None, eps: float = 2.0 ** -10,
+               mode: int = 0, dev_err: Optional[torch.Tensor] = None, stream=None):
+    """Selected node ids [nseq, gamma_max] (selection order, -1 padded) and |B| [nseq]."""
+    lib = L.load()
+    nseq, N = P.shape
+    W = own_fp.shape[-1]
+    _need(P, torch.float32, (nseq, N), "P")
+    _need(parent, torch.int32, (nseq, N), "parent")
+    if own_fp.dtype not in (torch.int32, torch.uint32):
+        raise MoEError("own_fp must be int32/uint32 words")
+    if tuple(own_fp.shape) != (nseq, N, W):
+        raise MoEError("own_fp shape")
+    if gamma_per_seq is not None:
+        _need(gamma_per_seq, torch.int32, (nseq,), "gamma_per_seq")
+    sel = torch.empty((nseq, max(gamma_max, 1)), dtype=torch.int32, device=P.device)
+    usz = torch.empty(nseq, dtype=torch.int32, device=P.device)
+    cfg = L.EcoCfg(N, W, gamma_max, mode, eps)
+    _check(lib.eco_select(_ptr(P), _ptr(parent), _ptr(own_fp), nseq, _ptr(gamma_per_seq),
+                          C.byref(cfg), _ptr(sel), _ptr(usz), _ptr(dev_err), _stream(stream)),
+           "eco_select")
+    return sel[:, :gamma_max], usz
+
+
+@dataclass
+class StepSpec:
+    L: int
+    nseq: int
+    N: int
+    W: int
+    E: int
+    k: int
+    H: int
+    I: int
+    dtype: str
+    T: int
+    gamma_max: int
+    mode: int = 0
+    eps: float = 2.0 ** -10
+    use_bias: bool = False
+    cap: int = 0
+    alpha: float = 0.0
+
+    def struct(self) -> L.StepCfg:
+        return L.StepCfg(self.L, self.nseq, self.N, self.W, self.E, self.k, self.H, self.I,
+                         DTYPES[self.dtype], self.T, self.gamma_max, self.mode, self.eps,
+                         int(self.use_bias), self.cap, self.alpha)
+
+
+def step_workspace_bytes(spec: StepSpec) -> int:
+    st = spec.struct()
+    return int(L.load().moe_verify_step_workspace(C.byref(st)))
+
+
+class VerifyStep:
+    """Pre-bound whole verify step: owns the output tensors and the workspace,
+    so each call enqueues the L-layer step with no allocation."""
+
+    def __init__(self, spec: StepSpec, layers: List[ExpertLayer], device="cuda"):
+        if len(layers) != spec.L:
+            raise MoEError("one ExpertLayer per layer required")
+        self.spec = spec
+        self.layers = layers
+        self.device = torch.device(device)
+        self._cfg = spec.struct()
+        arr = (L.LayerWeights * spec.L)()
+        for i, ly in enumerate(layers):
+            arr[i] = ly.struct()
+        self._layers = arr
+        nbytes = step_workspace_bytes(spec)
+        if nbytes == 0:
+            raise MoEError("unsupported step configuration")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self.selected = torch.empty((spec.nseq, max(spec.gamma_max, 1)), dtype=torch.int32,
+                                    device=self.device)
+        self.union_size = torch.empty(spec.nseq, dtype=torch.int32, device=self.device)
+        self.n_unique = torch.empty(spec.L, dtype=torch.int32, device=self.device)
+        self.y = torch.empty((spec.L, spec.T, spec.H), dtype=torch.float32, device=self.device)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def __call__(self, P, parent, own_fp, gamma_per_seq, node_logits, node_x, stream=None):
+        lib = L.load()
+        _check(lib.moe_verify_step(C.byref(self._cfg), _ptr(P), _ptr(parent), _ptr(own_fp),
+                                   _ptr(gamma_per_seq), _ptr(node_logits), _ptr(node_x),
+                                   self._layers, _ptr(self.selected), _ptr(self.union_size),
+                                   _ptr(self.n_unique), _ptr(self.y), _ptr(self.workspace),
+                                   self.workspace.numel(), _ptr(self.dev_err), _stream(stream)),
+               "moe_verify_step")
+        return self.y
+
+
+def profile_begin(max_launches: int = 65536):
+    _check(L.load().moe_profile_begin(max_launches), "moe_profile_begin")
+
+
+def profile_end() -> Dict[str, Dict[str, float]]:
+    n = len(L.PROF_CLASSES)
+    ms = (C.c_float * n)()
+    cnt = (C.c_int32 * n)()
+    _check(L.load().moe_profile_end(ms, cnt, n), "moe_profile_end")
+    return {name: {"ms": float(ms[i]), "launches": int(cnt[i])} for i, name in enumerate(L.PROF_CLASSES)}
+
+
+def launch_count() -> int:
+    return int(L.load().moe_launch_count())

@@ -1,0 +1,114 @@
+// Shared device/host helpers of libmoeverify (internal header).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_verify.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+
+// Host-side launch bookkeeping (launch counter + optional event timing).
+void note_launch(int cls, cudaStream_t s, bool before);
+struct LaunchScope {
+  int cls;
+  cudaStream_t s;
+  LaunchScope(int c, cudaStream_t st) : cls(c), s(st) { note_launch(cls, s, true); }
+  ~LaunchScope() { note_launch(cls, s, false); }
+};
+
+enum ProfClass { kProfEco = 0, kProfRoute = 1, kProfUnion = 2, kProfPrep = 3, kProfGateUp = 4,
+                 kProfDown = 5, kProfCombine = 6 };
+
+int sm_count();
+
+inline int check_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+__device__ __forceinline__ void flag_error(int32_t* dev_err, int32_t bits) {
+  if (dev_err) atomicOr(dev_err, bits);
+}
+
+// Total order used by every top-k: larger value first, equal values -> lower id.
+__device__ __forceinline__ bool topk_better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits_rn(float f) {
+  // Round to nearest even; inputs here are finite.
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Host-side FFN internals shared by the standalone call and the whole step.
+struct FfnArgs {
+  const void* x;            // [*, H] activations (fp32 or bf16 bits)
+  const int32_t* x_rows;    // optional row map: token t uses row x_rows[t] of x
+  int32_t x_rows_limit;     // rows of x (bound for x_rows)
+  int32_t T, k;
+  moe_layer_weights lw;
+  const int32_t* n_unique;
+  const int32_t* unique;
+  const int32_t* offsets;
+  const int32_t* perm_token;
+  const int32_t* inv;
+  const float* w;
+  float* y;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* dev_err;
+  cudaStream_t stream;
+};
+size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k);
+int ffn_validate(const moe_layer_weights& lw, int T, int k);
+int ffn_launch(const FfnArgs& a);
+
+// Route internals (optional row map into a node table, optional confidence map).
+struct RouteArgs {
+  const float* logits;      // [*, E]
+  const int32_t* rows;      // optional: token t uses logits row rows[t]
+  int32_t rows_limit;       // rows of logits (bound for rows)
+  const float* w_conf;      // [T] or NULL
+  moe_route_cfg cfg;
+  int32_t* ids;
+  float* w;
+  int32_t* dev_err;
+  cudaStream_t stream;
+};
+int route_validate(const moe_route_cfg& c, bool have_conf);
+int route_launch(const RouteArgs& a);
+
+int union_validate(int T, int k, int E);
+int union_launch(const int32_t* ids, int T, int k, int E, int32_t* n_unique, int32_t* unique,
+                 int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, int32_t* inv,
+                 float* reuse_ratio, int32_t* dev_err, cudaStream_t s);
+
+struct EcoArgs {
+  const float* P;
+  const int32_t* parent;
+  const uint32_t* own_fp;
+  int32_t nseq;
+  const int32_t* gamma;
+  eco_cfg cfg;
+  int32_t* selected;
+  int32_t* union_size;
+  int32_t* dev_err;
+  // Optional outputs for the whole step: verify token rows into the
+  // [nseq, N+1] node table and the token confidences (path probabilities).
+  int32_t* verify_rows;
+  float* verify_conf;
+  int32_t T_expected;
+  cudaStream_t stream;
+};
+int eco_validate(const eco_cfg& c, int nseq);
+int eco_launch(const EcoArgs& a);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace moe

@@ -1,0 +1,229 @@
+// eco_select: EcoSpec cost-aware draft selection.
+//
+// EcoSpec write-up, section 3.2 (the expert buffer B, rebuilt from the empty
+// set in every speculative step) and section 3.3 (score
+// S(t) = P(t) / (|E_traj(t) \ B| + eps), greedy: take the arg-max node, add it
+// to S and merge its path footprint into B, repeat gamma times).  mode 1 is
+// the static-cost ablation of section 4.3 (denominator |E_traj(t)|).
+//
+// Design: one CTA per sequence.  Path footprints E_traj are built once in
+// shared memory as bitsets (parent index < child index, so one breadth-first
+// pass suffices); every round each warp popcounts (E_traj(t) & ~B) for its
+// nodes, warp 0 takes the exact arg-max and all threads OR the winner into B.
+// Scores are compared by cross-multiplication in fp64, which is exact because
+// P is fp32 (24-bit significand) and c + eps = c + 2^-s has at most 29
+// significant bits (checked on the host).
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxN = 1024;
+constexpr int kMaxW = 4096;
+constexpr int kMaxNW = 40960;  // N*W words of trajectory bitsets (160 KB)
+
+// a beats b: P_a / (c_a + eps) > P_b / (c_b + eps), ties -> lower index.
+__device__ __forceinline__ bool score_better(float pa, int ca, int ia, float pb, int cb, int ib,
+                                             double eps) {
+  double lhs = static_cast<double>(pa) * (static_cast<double>(cb) + eps);
+  double rhs = static_cast<double>(pb) * (static_cast<double>(ca) + eps);
+  return lhs > rhs || (lhs == rhs && ia < ib);
+}
+
+__global__ void __launch_bounds__(512) eco_kernel(
+    const float* __restrict__ P, const int32_t* __restrict__ parent,
+    const uint32_t* __restrict__ own_fp, const int32_t* __restrict__ gamma_per_seq, int N, int W,
+    int gamma_max, int mode, double eps, int32_t* __restrict__ selected,
+    int32_t* __restrict__ union_size, int32_t* dev_err, int32_t* __restrict__ verify_rows,
+    float* __restrict__ verify_conf, int T_expected, int nseq) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* traj = smem;                 // [N][W]
+  uint32_t* B = traj + (size_t)N * W;    // [W]
+  __shared__ int32_t cost[kMaxN];
+  __shared__ uint8_t chosen[kMaxN];
+  __shared__ int bad;
+  __shared__ int best_s;
+
+  const int s = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const float* Ps = P + (size_t)s * N;
+  const int32_t* par = parent + (size_t)s * N;
+  const uint32_t* own = own_fp + (size_t)s * N * W;
+  int32_t* sel = selected + (size_t)s * gamma_max;
+
+  int gamma = gamma_per_seq ? gamma_per_seq[s] : gamma_max;
+
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < N; t += blockDim.x) {
+    int p = par[t];
+    if (p < -1 || p >= t) atomicOr(&bad, MOE_DEV_BAD_TREE);
+    float pt = Ps[t];
+    if (!(pt >= 0.f) || pt == INFINITY) atomicOr(&bad, MOE_DEV_BAD_PROB);
+    chosen[t] = 0;
+  }
+  if (threadIdx.x == 0 && (gamma < 0 || gamma > gamma_max)) atomicOr(&bad, MOE_DEV_BAD_TREE);
+  for (int w = threadIdx.x; w < W; w += blockDim.x) B[w] = 0;
+  __syncthreads();
+
+  // Optional verify-token map for the whole step (root + selected per sequence).
+  int tok0 = 0;
+  if (verify_rows) {
+    for (int q = 0; q < s; ++q) {
+      int gq = gamma_per_seq ? gamma_per_seq[q] : gamma_max;
+      gq = gq < 0 ? 0 : (gq > N ? N : gq);
+      tok0 += gq + 1;
+    }
+  }
+
+  if (bad) {
+    if (threadIdx.x == 0) {
+      flag_error(dev_err, bad);
+      union_size[s] = 0;
+    }
+    for (int r = threadIdx.x; r < gamma_max; r += blockDim.x) sel[r] = -1;
+    if (verify_rows) {
+      // Keep the downstream gathers in bounds: every token of this sequence
+      // points at its root row.
+      int g = gamma < 0 ? 0 : (gamma > N ? N : gamma);
+      for (int q = threadIdx.x; q <= g; q += blockDim.x)
+        if (tok0 + q < T_expected) {
+          verify_rows[tok0 + q] = s * (N + 1);
+          verify_conf[tok0 + q] = 1.f;
+        }
+    }
+    return;
+  }
+  if (gamma > N) gamma = N;
+
+  // E_traj(t) = own(t) | E_traj(parent(t)), in breadth-first order.
+  for (int t = 0; t < N; ++t) {
+    const int p = par[t];
+    for (int w = threadIdx.x; w < W; w += blockDim.x) {
+      uint32_t v = own[(size_t)t * W + w];
+      if (p >= 0) v |= traj[(size_t)p * W + w];
+      traj[(size_t)t * W + w] = v;
+    }
+    __syncthreads();
+  }
+
+  for (int r = 0; r < gamma; ++r) {
+    // Costs: |E_traj(t) \ B| (marginal) or |E_traj(t)| (static).
+    for (int t = warp; t < N; t += nwarps) {
+      int c = 0;
+      if (!chosen[t]) {
+        const uint32_t* tt = traj + (size_t)t * W;
+        for (int w = lane; w < W; w += 32) c += __popc(mode == 0 ? (tt[w] & ~B[w]) : tt[w]);
+        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+      }
+      if (lane == 0) cost[t] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float bp = 0.f;
+      int bc = 0, bi = -1;
+      for (int t = lane; t < N; t += 32) {
+        if (chosen[t]) continue;
+        if (bi < 0 || score_better(Ps[t], cost[t], t, bp, bc, bi, eps)) {
+          bp = Ps[t];
+          bc = cost[t];
+          bi = t;
+        }
+      }
+      for (int off = 16; off > 0; off >>= 1) {
+        float op = __shfl_xor_sync(0xFFFFFFFFu, bp, off);
+        int oc = __shfl_xor_sync(0xFFFFFFFFu, bc, off);
+        int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+        if (oi >= 0 && (bi < 0 || score_better(op, oc, oi, bp, bc, bi, eps))) {
+          bp = op;
+          bc = oc;
+          bi = oi;
+        }
+      }
+      if (lane == 0) {
+        best_s = bi;
+        chosen[bi] = 1;
+        sel[r] = bi;
+      }
+    }
+    __syncthreads();
+    const uint32_t* tb = traj + (size_t)best_s * W;
+    for (int w = threadIdx.x; w < W; w += blockDim.x) B[w] |= tb[w];
+    __syncthreads();
+  }
+
+  // |B| and the unused slots.
+  if (warp == 0) {
+    int c = 0;
+    for (int w = lane; w < W; w += 32) c += __popc(B[w]);
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+    if (lane == 0) union_size[s] = c;
+  }
+  for (int r = gamma + threadIdx.x; r < gamma_max; r += blockDim.x) sel[r] = -1;
+
+  if (verify_rows) {
+    // Token tok0 is the root (row s*(N+1)); then the selected nodes in order.
+    for (int q = threadIdx.x; q <= gamma; q += blockDim.x) {
+      int row = s * (N + 1) + (q == 0 ? 0 : 1 + sel[q - 1]);
+      float conf = q == 0 ? 1.f : Ps[sel[q - 1]];
+      if (tok0 + q < T_expected) {
+        verify_rows[tok0 + q] = row;
+        verify_conf[tok0 + q] = conf;
+      }
+    }
+    if (threadIdx.x == 0 && s == nseq - 1 && tok0 + gamma + 1 != T_expected)
+      flag_error(dev_err, MOE_DEV_CAPACITY);
+  }
+}
+
+}  // namespace
+
+int eco_validate(const eco_cfg& c, int nseq) {
+  if (nseq < 0 || c.N < 1 || c.N > kMaxN || c.W < 1 || c.W > kMaxW) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c.N) * c.W > kMaxNW) return MOE_ERR_UNSUPPORTED;
+  if (c.gamma_max < 0 || (c.mode != 0 && c.mode != 1)) return MOE_ERR_ARG;
+  // eps must be 2^-s, 0 <= s <= 20, and W*32 * 2^s < 2^29 so that c + eps is
+  // exact in <= 29 bits and P * (c + eps) is exact in fp64.
+  int s = -1;
+  for (int q = 0; q <= 20; ++q)
+    if (c.eps == static_cast<float>(1.0 / static_cast<double>(1u << q))) s = q;
+  if (s < 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<double>(c.W) * 32.0 * static_cast<double>(1u << s) >= 536870912.0)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int eco_launch(const EcoArgs& a) {
+  if (a.nseq == 0) return MOE_OK;
+  const auto& c = a.cfg;
+  size_t smem = (static_cast<size_t>(c.N) * c.W + c.W) * sizeof(uint32_t);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(eco_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int threads = c.W >= 256 || c.N >= 16 ? 512 : 256;
+  LaunchScope ls(kProfEco, a.stream);
+  eco_kernel<<<a.nseq, threads, smem, a.stream>>>(a.P, a.parent, a.own_fp, a.gamma, c.N, c.W,
+                                                  c.gamma_max, c.mode, static_cast<double>(c.eps),
+                                                  a.selected, a.union_size, a.dev_err,
+                                                  a.verify_rows, a.verify_conf, a.T_expected,
+                                                  a.nseq);
+  return check_launch();
+}
+
+}  // namespace moe
+
+extern "C" int eco_select(const float* P, const int32_t* parent, const uint32_t* own_fp,
+                          int32_t nseq, const int32_t* gamma_per_seq, const eco_cfg* cfg,
+                          int32_t* selected, int32_t* union_size, int32_t* dev_err, void* stream) {
+  if (!cfg) return MOE_ERR_ARG;
+  int st = moe::eco_validate(*cfg, nseq);
+  if (st != MOE_OK) return st;
+  if (nseq > 0 && (!P || !parent || !own_fp || !union_size || (cfg->gamma_max > 0 && !selected)))
+    return MOE_ERR_ARG;
+  moe::EcoArgs a{P, parent, own_fp, nseq, gamma_per_seq, *cfg, selected, union_size, dev_err,
+                 nullptr, nullptr, 0, static_cast<cudaStream_t>(stream)};
+  return moe::eco_launch(a);
+}

@@ -1,0 +1,18 @@
+// Internal interface between the FFN front end and its kernel paths.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Carve-up of the caller's FFN workspace.
+struct FfnWorkspace {
+  void* h;        // SwiGLU intermediate, [T*k, I] (fp32 for the fp32 dtype, bf16 otherwise)
+  float* o;       // per-(token, slot) expert outputs, [T*k, H] fp32
+};
+
+FfnWorkspace ffn_carve(const moe_layer_weights& lw, int T, int k, void* base);
+int ffn_simt_launch(const FfnArgs& a, const FfnWorkspace& ws);
+int combine_launch(const FfnArgs& a, const float* o);
+
+}  // namespace moe

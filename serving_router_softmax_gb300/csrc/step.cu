@@ -1,0 +1,130 @@
+// moe_verify_step: one speculative verify step, selection plus L MoE layers,
+// enqueued on one stream with no host synchronisation (capturable).
+//
+// EcoSpec write-up, section 2: a round drafts a tree, selects gamma nodes and
+// verifies gamma+1 tokens in one target forward; in every MoE layer the
+// verify tokens route to their top-k experts and the union is loaded once.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+struct StepWs {
+  int32_t* verify_rows;
+  float* verify_conf;
+  int32_t* ids;
+  float* w;
+  int32_t* unique;
+  int32_t* offsets;
+  int32_t* perm_token;
+  int32_t* perm_slot;
+  int32_t* inv;
+  float* ratio;
+  void* ffn;
+  size_t ffn_bytes;
+};
+
+size_t step_ws(const moe_step_cfg& c, void* base, StepWs* out) {
+  const size_t T = c.T, TK = static_cast<size_t>(c.T) * c.k;
+  const size_t cap = static_cast<size_t>(c.E) < TK ? c.E : TK;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  size_t o_rows = take(T * 4), o_conf = take(T * 4), o_ids = take(TK * 4), o_w = take(TK * 4);
+  size_t o_u = take(cap * 4), o_off = take((cap + 1) * 4), o_pt = take(TK * 4), o_ps = take(TK * 4);
+  size_t o_inv = take(TK * 4), o_ratio = take(4);
+  moe_layer_weights lw{c.H, c.I, c.E, c.dtype, nullptr, nullptr, nullptr, nullptr};
+  size_t fb = ffn_workspace_bytes(lw, c.T, c.k);
+  size_t o_ffn = take(fb);
+  if (out) {
+    char* b = static_cast<char*>(base);
+    out->verify_rows = reinterpret_cast<int32_t*>(b + o_rows);
+    out->verify_conf = reinterpret_cast<float*>(b + o_conf);
+    out->ids = reinterpret_cast<int32_t*>(b + o_ids);
+    out->w = reinterpret_cast<float*>(b + o_w);
+    out->unique = reinterpret_cast<int32_t*>(b + o_u);
+    out->offsets = reinterpret_cast<int32_t*>(b + o_off);
+    out->perm_token = reinterpret_cast<int32_t*>(b + o_pt);
+    out->perm_slot = reinterpret_cast<int32_t*>(b + o_ps);
+    out->inv = reinterpret_cast<int32_t*>(b + o_inv);
+    out->ratio = reinterpret_cast<float*>(b + o_ratio);
+    out->ffn = b + o_ffn;
+    out->ffn_bytes = fb;
+  }
+  return off;
+}
+
+int step_validate(const moe_step_cfg& c) {
+  if (c.L < 1 || c.nseq < 1 || c.T < 1) return MOE_ERR_ARG;
+  if (c.T < c.nseq) return MOE_ERR_ARG;
+  eco_cfg ec{c.N, c.W, c.gamma_max, c.mode, c.eps};
+  int st = eco_validate(ec, c.nseq);
+  if (st != MOE_OK) return st;
+  if (static_cast<long long>(c.L) * c.E > static_cast<long long>(c.W) * 32) return MOE_ERR_ARG;
+  moe_route_cfg rc{c.T, c.E, c.k, c.use_bias, c.cap, c.alpha};
+  if ((st = route_validate(rc, true)) != MOE_OK) return st;
+  if ((st = union_validate(c.T, c.k, c.E)) != MOE_OK) return st;
+  moe_layer_weights lw{c.H, c.I, c.E, c.dtype, reinterpret_cast<void*>(256),
+                       reinterpret_cast<void*>(256), reinterpret_cast<float*>(256),
+                       reinterpret_cast<float*>(256)};
+  return ffn_validate(lw, c.T, c.k);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" size_t moe_verify_step_workspace(const moe_step_cfg* cfg) {
+  if (!cfg || moe::step_validate(*cfg) != MOE_OK) return 0;
+  return moe::step_ws(*cfg, nullptr, nullptr);
+}
+
+extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* parent,
+                               const uint32_t* own_fp, const int32_t* gamma_per_seq,
+                               const float* node_logits, const void* node_x,
+                               const moe_layer_weights* layers, int32_t* selected,
+                               int32_t* union_size, int32_t* n_unique, float* y, void* workspace,
+                               size_t ws_bytes, int32_t* dev_err, void* stream) {
+  using namespace moe;
+  if (!cfg) return MOE_ERR_ARG;
+  const moe_step_cfg& c = *cfg;
+  int st = step_validate(c);
+  if (st != MOE_OK) return st;
+  if (!P || !parent || !own_fp || !node_logits || !node_x || !layers || !union_size || !n_unique ||
+      !y || (c.gamma_max > 0 && !selected))
+    return MOE_ERR_ARG;
+  if (!workspace || ws_bytes < step_ws(c, nullptr, nullptr)) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return MOE_ERR_ARG;
+  for (int l = 0; l < c.L; ++l) {
+    const moe_layer_weights& lw = layers[l];
+    if (lw.H != c.H || lw.I != c.I || lw.E != c.E || lw.dtype != c.dtype) return MOE_ERR_ARG;
+    if ((st = ffn_validate(lw, c.T, c.k)) != MOE_OK) return st;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StepWs ws;
+  step_ws(c, workspace, &ws);
+
+  EcoArgs ea{P, parent, own_fp, c.nseq, gamma_per_seq, {c.N, c.W, c.gamma_max, c.mode, c.eps},
+             selected, union_size, dev_err, ws.verify_rows, ws.verify_conf, c.T, s};
+  if ((st = eco_launch(ea)) != MOE_OK) return st;
+
+  const int rows = c.nseq * (c.N + 1);
+  const size_t xelem = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
+  for (int l = 0; l < c.L; ++l) {
+    RouteArgs ra{node_logits + static_cast<size_t>(l) * rows * c.E, ws.verify_rows, rows,
+                 c.use_bias ? ws.verify_conf : nullptr, {c.T, c.E, c.k, c.use_bias, c.cap, c.alpha},
+                 ws.ids, ws.w, dev_err, s};
+    if ((st = route_launch(ra)) != MOE_OK) return st;
+    if ((st = union_launch(ws.ids, c.T, c.k, c.E, n_unique + l, ws.unique, ws.offsets, ws.perm_token,
+                           ws.perm_slot, ws.inv, ws.ratio, dev_err, s)) != MOE_OK)
+      return st;
+    FfnArgs fa{static_cast<const char*>(node_x) + static_cast<size_t>(l) * rows * c.H * xelem,
+               ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
+               ws.perm_token, ws.inv, ws.w, y + static_cast<size_t>(l) * c.T * c.H, ws.ffn,
+               ws.ffn_bytes, dev_err, s};
+    if ((st = ffn_launch(fa)) != MOE_OK) return st;
+  }
+  return MOE_OK;
+}

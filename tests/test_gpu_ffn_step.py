@@ -1,0 +1,196 @@
+"""GPU parity of the expert FFN and of the whole verify step against the oracle.
+
+Tolerance (written from the arithmetic): the oracle is exact fp64 on the
+stored weights; the GPU accumulates in fp32 and, for bf16/FP8 weights, rounds
+the SwiGLU intermediate to bf16 (relative error <= 2^-9 per element), so the
+row-wise normwise error max_t |y_t - ref_t|_inf / |ref_t|_inf is bounded by
+2e-2 for bf16/FP8 and 1e-4 for fp32 weights, the bounds the workloads state.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2, "e4m3": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def mv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import serving_router_softmax_gb300 as m
+    return m
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def rowwise_err(y, ref):
+    den = np.max(np.abs(ref), axis=1)
+    den = np.where(den == 0, 1.0, den)
+    return float(np.max(np.max(np.abs(y - ref), axis=1) / den))
+
+
+def make_layer(mv, cfg, l):
+    from workload import device as wdev
+    gu, dn, sgu, sdn = wdev.make_layer_tensors(cfg, l)
+    return mv.ExpertLayer(gu, dn, cfg.dtype, sgu, sdn)
+
+
+def host_experts(cfg, l):
+    from oracle import moe_layer as ml
+    from workload import gen
+    return lambda e: ml.expert_matrices(gen.expert_weights_host(cfg, l, e), cfg.dtype)
+
+
+def x_decode(cfg):
+    from oracle import moe_layer as ml
+    if cfg.dtype == "f32":
+        return lambda a: np.asarray(a, np.float32).astype(np.float64)
+    return ml.decode_bf16
+
+
+FFN_CASES = [
+    # dtype, H, I, E, k, T
+    ("bf16", 576, 320, 16, 4, 5),
+    ("bf16", 576, 320, 16, 4, 1),
+    ("bf16", 256, 192, 8, 8, 19),      # E == k: every expert used
+    ("bf16", 128, 64, 32, 2, 256),     # maximum T
+    ("bf16", 640, 384, 64, 16, 9),     # maximum k
+    ("f32", 256, 512, 16, 2, 5),       # the fp32 toy shape
+    ("f32", 320, 192, 12, 3, 17),
+    ("e4m3", 640, 384, 16, 4, 5),
+    ("e4m3", 256, 256, 32, 8, 28),
+]
+
+
+@pytest.mark.parametrize("dtype,H,I,E,k,T", FFN_CASES)
+def test_ffn_matches_oracle(mv, dtype, H, I, E, k, T):
+    from oracle import moe_layer as ml
+    from workload import gen
+    cfg = gen.MoEConfig("ffn_case", L=1, H=H, E=E, k=k, I=I, dtype=dtype, seed=H + I + T)
+    layer = make_layer(mv, cfg, 0)
+    rng = np.random.default_rng(T * 31 + k)
+    lg = (rng.standard_normal((T, E)) - 0.1 * rng.permutation(E)).astype(np.float32)
+    xs = rng.standard_normal((T, H)).astype(np.float32)
+    if dtype == "f32":
+        x_host = xs
+        x_dev = cuda(xs)
+    else:
+        x_host = gen.bf16_bits_rne(xs)
+        x_dev = cuda(x_host.view(np.int16))
+    dev_err = mv.new_dev_err()
+    ids, w = mv.route(cuda(lg), k, dev_err=dev_err)
+    up = mv.union_permute(ids, E, dev_err=dev_err)
+    y = mv.verify_ffn(x_dev, k, layer, up, w, dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert dev_err.item() == 0
+    ref = ml.layer_forward(lg, x_decode(cfg)(x_host), k, E, host_experts(cfg, 0))
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    err = rowwise_err(y.cpu().numpy().astype(np.float64), ref["y"])
+    assert err < TOL[dtype], err
+
+
+def test_ffn_device_fill_matches_host_generator(mv):
+    """The device weight fill and the host regeneration agree bit for bit."""
+    from workload import gen
+    for dtype in ("bf16", "f32", "e4m3"):
+        cfg = gen.MoEConfig("fillcheck", L=1, H=256, E=4, k=2, I=128, dtype=dtype, seed=77)
+        layer = make_layer(mv, cfg, 0)
+        for e in (0, 3):
+            hw = gen.expert_weights_host(cfg, 0, e)
+            gu = layer.gate_up[e].cpu().numpy()
+            dn = layer.down[e].cpu().numpy()
+            if dtype == "bf16":
+                gu, dn = gu.view(np.uint16), dn.view(np.uint16)
+            assert np.array_equal(gu, hw["gate_up"]) and np.array_equal(dn, hw["down"])
+            if dtype == "e4m3":
+                assert np.array_equal(layer.scales_gate_up[e].cpu().numpy(), hw["scale_gate_up"])
+                assert np.array_equal(layer.scales_down[e].cpu().numpy(), hw["scale_down"])
+
+
+# ------------------------------------------------------------------ whole step
+def run_step(mv, cfg, sample_tokens=None, sample_layers=None):
+    """Runs the GPU step and the oracle; returns (gpu dict, oracle dict)."""
+    from oracle import verify_step as ovs
+    from workload import device as wdev
+    from workload import gen
+    wl = gen.make_workload(cfg)
+    layers = [make_layer(mv, cfg, l) for l in range(cfg.L)]
+    t = wdev.workload_tensors(wl)
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k,
+                       H=cfg.H, I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()),
+                       mode=cfg.mode, eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap,
+                       alpha=cfg.alpha)
+    step = mv.VerifyStep(spec, layers)
+    step(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    torch.cuda.synchronize()
+    got = {"selected": step.selected.cpu().numpy(), "union_size": step.union_size.cpu().tolist(),
+           "n_unique": step.n_unique.cpu().tolist(), "y": step.y.cpu().numpy(),
+           "dev_err": int(step.dev_err.item())}
+    del step, layers
+    torch.cuda.empty_cache()
+    ref = ovs.run_step(wl, lambda l: host_experts(cfg, l), layers=sample_layers,
+                       tokens=sample_tokens, x_decode=x_decode(cfg))
+    return wl, got, ref
+
+
+def check_step(wl, got, ref, tol, sample_tokens=None):
+    from oracle import moe_layer as ml
+    cfg = wl.cfg
+    assert got["dev_err"] == 0
+    for s in range(cfg.nseq):
+        assert got["selected"][s, : wl.gamma[s]].tolist() == ref["selected"][s]
+    assert got["union_size"] == ref["union_size"]
+    # union size of every layer, from oracle routing on all layers
+    from oracle import verify_step as ovs
+    for l in range(cfg.L):
+        lg = wl.logits[l].reshape(-1, cfg.E)[ref["rows"]]
+        if cfg.use_bias:
+            lg = ml.reuse_bias(lg, ref["conf"], cfg.k, cfg.cap, cfg.alpha)
+        ids, _ = ml.route(lg, cfg.k)
+        assert got["n_unique"][l] == ml.union_permute(ids, cfg.E)["n_unique"], l
+    for l, r in ref["layers"].items():
+        toks = list(range(wl.T)) if sample_tokens is None else sample_tokens
+        err = rowwise_err(got["y"][l][toks].astype(np.float64), r["y"])
+        assert err < tol, (l, err)
+
+
+SMALL = {
+    "toy": {},
+    "qwen3_235b_like": dict(L=3, H=512, I=256),
+    "gpt_oss_120b_like": dict(L=3, H=576, I=320),
+    "deepseek_v3_like": dict(L=2, H=512, I=256),
+    "batched_qwen_like": dict(L=2, H=512, I=256),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_step_small_shapes_full_compare(mv, name):
+    """Every workload's routing/selection structure at reduced H/I: all outputs compared."""
+    from workload import CONFIGS
+    cfg = CONFIGS[name].replace(**SMALL[name])
+    wl, got, ref = run_step(mv, cfg)
+    check_step(wl, got, ref, TOL[cfg.dtype])
+
+
+@pytest.mark.parametrize("name", ["toy", "qwen3_235b_like", "gpt_oss_120b_like", "deepseek_v3_like",
+                                  "batched_qwen_like"])
+def test_step_full_size_sampled(mv, name):
+    """Full-size workloads as the bench runs them: exact selection and unions on
+    every layer; FFN outputs on a sample of (layer, token) pairs."""
+    from workload import CONFIGS
+    cfg = CONFIGS[name]
+    free, _ = torch.cuda.mem_get_info()
+    from workload import gen
+    need = cfg.L * sum(int(np.prod(s)) for s in gen.weight_shapes(cfg).values()) * gen.ELEM_BYTES[cfg.dtype]
+    if need > free * 0.9:
+        pytest.skip(f"needs {need / 2**30:.1f} GiB of device memory")
+    layers = [0, cfg.L - 1] if cfg.L > 1 else [0]
+    wl_T = gen.make_workload(cfg).T
+    tokens = sorted({0, wl_T // 2, wl_T - 1})
+    wl, got, ref = run_step(mv, cfg, sample_tokens=tokens, sample_layers=layers)
+    check_step(wl, got, ref, TOL[cfg.dtype], sample_tokens=tokens)
