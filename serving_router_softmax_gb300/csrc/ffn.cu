@@ -9,12 +9,17 @@ namespace {
 size_t elem_bytes_h(const moe_layer_weights& lw) { return lw.dtype == MOE_DTYPE_F32 ? 4 : 2; }
 }  // namespace
 
-size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
+size_t ffn_simt_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
   const size_t TK = static_cast<size_t>(T) * k;
   size_t b = 0;
   b += align_up(TK * lw.I * elem_bytes_h(lw), 256);
   b += align_up(TK * lw.H * sizeof(float), 256);
   return b;
+}
+
+size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
+  if (ffn_tc_supported(lw, T, k)) return ffn_tc_workspace_bytes(lw, T, k);
+  return ffn_simt_workspace_bytes(lw, T, k);
 }
 
 FfnWorkspace ffn_carve(const moe_layer_weights& lw, int T, int k, void* base) {
@@ -45,6 +50,7 @@ int ffn_launch(const FfnArgs& a) {
   if (a.T == 0) return MOE_OK;
   if (a.ws_bytes < ffn_workspace_bytes(a.lw, a.T, a.k) || !a.ws) return MOE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(a.ws) & 255) return MOE_ERR_ARG;
+  if (ffn_tc_supported(a.lw, a.T, a.k)) return ffn_tc_launch(a);
   FfnWorkspace ws = ffn_carve(a.lw, a.T, a.k, a.ws);
   return ffn_simt_launch(a, ws);
 }

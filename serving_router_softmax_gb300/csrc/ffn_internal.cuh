@@ -15,4 +15,9 @@ FfnWorkspace ffn_carve(const moe_layer_weights& lw, int T, int k, void* base);
 int ffn_simt_launch(const FfnArgs& a, const FfnWorkspace& ws);
 int combine_launch(const FfnArgs& a, const float* o);
 
+// Tensor-core path (bf16 weights).
+bool ffn_tc_supported(const moe_layer_weights& lw, int T, int k);
+size_t ffn_tc_workspace_bytes(const moe_layer_weights& lw, int T, int k);
+int ffn_tc_launch(const FfnArgs& a);
+
 }  // namespace moe

@@ -1,0 +1,707 @@
+// moe_verify_ffn, tensor-core path (bf16 weights): TMA-streamed expert weights
+// feeding tcgen05 MMAs with fp32 accumulators in TMEM.
+//
+// The verify step's MoE cost is the union of the experts its tokens activate
+// (EcoSpec write-up, sections 1-2); this path reads each unique expert's
+// weights from HBM exactly once and applies them to all of that expert's
+// tokens.  Per layer:
+//   prep     padded per-expert token groups: gathers x rows into Xp (each
+//            expert's group starts on a 16-row boundary, pad rows zeroed),
+//            zeroes the fixup counters.
+//   gate/up  h = silu(W_gate x) * (W_up x) for every (expert, token) pair,
+//            written as bf16 into Hp (same padded rows).
+//   down     o = W_down h, then y_t = sum_j w_tj o_(t,j) in slot order.
+//
+// Tiling: a tile is 128 weight rows of one expert (the MMA's M) times all of
+// that expert's tokens (N = group size rounded up to 16, at most 256); K is
+// streamed in 64-element (128-byte) blocks through a TMA -> shared memory ring.
+// The weights are the A operand, the tokens the B operand, both K-major with
+// the 128-byte swizzle.  The skinny N makes the kernels HBM-bound; tensor
+// cores only keep the arithmetic off the critical path.
+//
+// Load balance: the number of unique experts is only known on the device, so
+// the grid is persistent (one CTA per SM) and splits the layer's k-blocks
+// evenly (stream-K).  A tile cut between CTAs is finished by the last CTA to
+// arrive (atomic counter, no waiting), which sums the fp32 partials of all
+// contributors in CTA order, so results do not depend on timing.  The down
+// kernel also counts finished tiles per 128-row block of y; the CTA that
+// completes a block does the weighted combine for it.
+//
+// Roles per CTA (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues MMAs, warps 2-5 drain accumulators (TMEM lane quarter = warp % 4).
+// Every wait on an mbarrier is bounded; on time-out the CTA raises
+// MOE_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ffn_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;          // weight rows per tile (MMA M)
+constexpr int kBK = 64;           // K elements per stage (128 bytes of bf16)
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+
+struct TcParams {
+  int T, k, E, cap;
+  int M, K;          // rows of each expert matrix, reduction length
+  int NM;            // max padded token columns (multiple of 16, <= 256)
+  int Rmax;          // rows of Xp / Hp
+  int stages;
+  int acc_stages;
+  uint32_t tmem_cols;
+  const int32_t* n_unique;
+  const int32_t* unique;
+  const int32_t* offsets;
+  const int32_t* poff;
+  uint16_t* hp;      // gate/up output, [R_pad_max][M] bf16
+  float* o;          // down output, [T*k][M] fp32 (perm order)
+  float* partials;   // [grid][2][2*NM][128] fp32
+  int32_t* tile_cnt; // [cap * MT]
+  int32_t* done_cnt; // [MT] (down)
+  const int32_t* inv;
+  const float* w;
+  float* y;          // [T][M] (down)
+  int32_t* dev_err;
+};
+
+struct Tile {
+  int u, m, e, ne, np, prow, off;
+  bool ok;
+};
+
+__device__ __forceinline__ long long seg_owner(long long x, long long total, int G) {
+  return ((x + 1) * G - 1) / total;
+}
+
+__device__ __forceinline__ Tile tile_info(const TcParams& p, int U, int t) {
+  Tile ti;
+  ti.m = t / U;
+  ti.u = t - ti.m * U;
+  ti.e = p.unique[ti.u];
+  ti.off = p.offsets[ti.u];
+  ti.ne = p.offsets[ti.u + 1] - ti.off;
+  ti.np = (ti.ne + 15) & ~15;
+  ti.prow = p.poff[ti.u];
+  ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
+          ti.off + ti.ne <= p.T * p.k && ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
+  return ti;
+}
+
+__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                  const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  constexpr int nA = kGateUp ? 2 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int bBytes = p.NM * 128;
+  const int stageBytes = nA * kABytes + bBytes;
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * stageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  uint64_t* acce = accf + 2;
+  uint64_t* drain = acce + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* bcast = abort_flag + 1;
+  volatile int* issued = bcast + 1;
+  volatile int* consumed = issued + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&accf[a], 1);
+      tc::mbar_init(&acce[a], kEpiThreads);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *issued = 0;
+    *consumed = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tmA0);
+    if (kGateUp) tc::tma_prefetch_desc(&tmA1);
+    tc::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, p.tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int U = *p.n_unique;
+  const bool valid = U >= 1 && U <= p.cap;
+  if (!valid && blockIdx.x == 0 && threadIdx.x == 0 && U != 0) flag_error(p.dev_err, MOE_DEV_CAPACITY);
+  const int MT = (p.M + kBM - 1) / kBM;
+  const int KB = p.K / kBK;
+  const long long total = valid ? (long long)U * MT * KB : 0;
+  // Partition over at most `total` CTAs so that every range is non-empty and
+  // the CTAs sharing a tile are exactly the consecutive owners of its k-blocks.
+  const int G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
+  const int c = blockIdx.x;
+  const long long s0 = c < G ? total * c / G : total;
+  const long long s1 = c < G ? total * (c + 1) / G : total;
+  const int acc_cols = nA * p.NM;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (tc::elect_one()) {
+      const uint64_t polA = tc::policy_evict_first();
+      const uint64_t polB = tc::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int n_issued = 0;
+      for (long long x = s0; x < s1 && !*abort_flag;) {
+        const int t = static_cast<int>(x / KB);
+        const int kb0 = static_cast<int>(x - (long long)t * KB);
+        const int kb1 = static_cast<int>(kb0 + (s1 - x) < KB ? kb0 + (s1 - x) : KB);
+        x += kb1 - kb0;
+        const Tile ti = tile_info(p, U, t);
+        if (!ti.ok) continue;
+        const uint32_t tx = nA * kABytes + ti.np * 128;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!tc::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetNs)) {
+            *abort_flag = 1;
+            flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+            break;
+          }
+          uint8_t* sA = base + (size_t)stage * stageBytes;
+          uint8_t* sB = sA + nA * kABytes;
+          tc::mbar_arrive_expect_tx(&full[stage], tx);
+          tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+          if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+          for (int j = 0; j < ti.np / 16; ++j)
+            tc::tma_load_2d(sB + j * 2048, &tmB, kb * kBK, ti.prow + 16 * j, &full[stage], polB);
+          ++n_issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      *issued = n_issued;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (tc::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase[2] = {0, 0};
+      int n_consumed = 0;
+      bool stop = false;
+      for (long long x = s0; x < s1 && !stop;) {
+        const int t = static_cast<int>(x / KB);
+        const int kb0 = static_cast<int>(x - (long long)t * KB);
+        const int kb1 = static_cast<int>(kb0 + (s1 - x) < KB ? kb0 + (s1 - x) : KB);
+        x += kb1 - kb0;
+        const Tile ti = tile_info(p, U, t);
+        if (!ti.ok) continue;
+        if (!tc::mbar_wait_bounded(&acce[acc], acc_phase[acc] ^ 1u, abort_flag, kWaitBudgetNs)) {
+          *abort_flag = 1;
+          flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d0 = tmem_base + acc * acc_cols;
+        const uint32_t idesc = tc::idesc_bf16_f32(kBM, ti.np);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!tc::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetNs)) {
+            *abort_flag = 1;
+            flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+            stop = true;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t aAddr = tc::smem_u32(base + (size_t)stage * stageBytes);
+          const uint32_t bAddr = aAddr + nA * kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+            const uint64_t bdesc = tc::smem_desc_sw128(bAddr + kk * 32);
+            tc::mma_bf16(d0, tc::smem_desc_sw128(aAddr + kk * 32), bdesc, idesc, accum);
+            if (kGateUp) tc::mma_bf16(d0 + p.NM, tc::smem_desc_sw128(aAddr + kABytes + kk * 32), bdesc, idesc, accum);
+          }
+          tc::mma_commit(&empty[stage]);
+          ++n_consumed;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+        tc::mma_commit(&accf[acc]);
+        acc_phase[acc] ^= 1u;
+        if (p.acc_stages == 2) acc ^= 1;
+      }
+      *consumed = n_consumed;
+      // All MMAs issued by this thread complete before the drain barrier flips.
+      tc::mma_commit(drain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int etid = threadIdx.x - 64;  // 0..127
+    int acc = 0;
+    uint32_t acc_phase[2] = {0, 0};
+    const int first_tile_c = KB > 0 ? static_cast<int>(s0 / KB) : 0;
+    for (long long x = s0; x < s1;) {
+      const int t = static_cast<int>(x / KB);
+      const int kb0 = static_cast<int>(x - (long long)t * KB);
+      const int kb1 = static_cast<int>(kb0 + (s1 - x) < KB ? kb0 + (s1 - x) : KB);
+      x += kb1 - kb0;
+      const Tile ti = tile_info(p, U, t);
+      if (!ti.ok) {
+        if (etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+        continue;
+      }
+      // Every epilogue thread waits; the outcome is made uniform through a
+      // shared vote so that no thread is left behind at a named barrier.
+      if (!tc::mbar_wait_bounded(&accf[acc], acc_phase[acc], abort_flag, kWaitBudgetNs)) {
+        *abort_flag = 1;
+        flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+      }
+      tc::named_bar_sync(1, kEpiThreads);
+      if (*abort_flag) break;
+      tc::tc_fence_after();
+      const bool whole = kb0 == 0 && kb1 == KB;
+      const int row = ti.m * kBM + r;
+      const bool row_ok = row < p.M;
+      const uint32_t tacc = tmem_base + lane_off + acc * acc_cols;
+      float* P = p.partials + ((size_t)c * 2 + (t == first_tile_c ? 0 : 1)) * (size_t)(2 * p.NM * 128);
+      for (int cc = 0; cc < ti.np / 16; ++cc) {
+        float g[16], v[16];
+        tc::tmem_ld16(tacc + cc * 16, g);
+        if (kGateUp) tc::tmem_ld16(tacc + p.NM + cc * 16, v);
+        tc::tmem_ld_wait();
+        if (whole) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = cc * 16 + j;
+            if (n < ti.ne && row_ok) {
+              if (kGateUp)
+                p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
+              else
+                p.o[(size_t)(ti.off + n) * p.M + row] = g[j];
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            P[(size_t)(cc * 16 + j) * 128 + r] = g[j];
+            if (kGateUp) P[(size_t)(p.NM + cc * 16 + j) * 128 + r] = v[j];
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acce[acc]);
+      acc_phase[acc] ^= 1u;
+      if (p.acc_stages == 2) acc ^= 1;
+
+      bool finished = whole;
+      if (!whole) {
+        // Last-arriver fixup across the CTAs that share this tile.
+        __threadfence();
+        tc::named_bar_sync(1, kEpiThreads);
+        if (etid == 0) *bcast = atomicAdd(&p.tile_cnt[t], 1);
+        tc::named_bar_sync(1, kEpiThreads);
+        const int arrived = *bcast;
+        const long long t0 = (long long)t * KB;
+        const int cf = static_cast<int>(seg_owner(t0, total, G));
+        const int cl = static_cast<int>(seg_owner(t0 + KB - 1, total, G));
+        tc::named_bar_sync(1, kEpiThreads);
+        if (arrived == cl - cf) {
+          __threadfence();
+          finished = true;
+          for (int cc = 0; cc < ti.np / 16; ++cc) {
+            float g[16], v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) g[j] = v[j] = 0.f;
+            for (int q2 = cf; q2 <= cl; ++q2) {
+              const int ft = static_cast<int>((total * q2 / G) / KB);
+              const float* P2 = p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                g[j] += __ldcg(&P2[(size_t)(cc * 16 + j) * 128 + r]);
+                if (kGateUp) v[j] += __ldcg(&P2[(size_t)(p.NM + cc * 16 + j) * 128 + r]);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = cc * 16 + j;
+              if (n < ti.ne && row_ok) {
+                if (kGateUp)
+                  p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
+                else
+                  p.o[(size_t)(ti.off + n) * p.M + row] = g[j];
+              }
+            }
+          }
+        }
+      }
+      if (!kGateUp && finished) {
+        // Count the finished tile for its 128-row block of y; the CTA that
+        // completes the block combines it.
+        __threadfence();
+        tc::named_bar_sync(1, kEpiThreads);
+        if (etid == 0) *bcast = atomicAdd(&p.done_cnt[ti.m], 1);
+        tc::named_bar_sync(1, kEpiThreads);
+        const int done = *bcast;
+        tc::named_bar_sync(1, kEpiThreads);
+        if (done == U - 1) {
+          __threadfence();
+          const int TK = p.T * p.k;
+          for (int tok = 0; tok < p.T && row_ok; ++tok) {
+            float s = 0.f;
+            for (int j = 0; j < p.k; ++j) {
+              const int pos = p.inv[tok * p.k + j];
+              if (pos < 0 || pos >= TK) {
+                flag_error(p.dev_err, MOE_DEV_BAD_ID);
+                continue;
+              }
+              s = fmaf(p.w[tok * p.k + j], __ldcg(&p.o[(size_t)pos * p.M + row]), s);
+            }
+            p.y[(size_t)tok * p.M + row] = s;
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag) {
+    // Drain: wait (bounded) for issued-but-unconsumed copies and for every
+    // issued MMA before the shared memory and TMEM are given back.
+    if (threadIdx.x == 0) {
+      for (int i = *consumed; i < *issued; ++i)
+        tc::mbar_wait_bounded(&full[i % S], static_cast<uint32_t>((i / S) & 1), nullptr, 100000000ull);
+    }
+  }
+  if (warp == 1) {
+    tc::mbar_wait_bounded(drain, 0, nullptr, 100000000ull);
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// Builds Xp (padded token groups), poff and zeroes the fixup counters.
+__global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restrict__ x,
+                                                       const int32_t* __restrict__ x_rows,
+                                                       int x_rows_limit, int T, int k, int H, int cap,
+                                                       const int32_t* __restrict__ n_unique,
+                                                       const int32_t* __restrict__ offsets,
+                                                       const int32_t* __restrict__ perm_token,
+                                                       uint16_t* __restrict__ xp, int32_t* __restrict__ poff,
+                                                       int32_t* __restrict__ counters, int n_counters,
+                                                       float* __restrict__ y, int32_t* dev_err) {
+  __shared__ int32_t spoff[1025];
+  __shared__ int s_bad;
+  const int TK = T * k;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x)
+    counters[i] = 0;
+  int U = *n_unique;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if (U < 1 || U > cap) {
+    // No usable union (the union call flagged why, or U is out of range):
+    // y is defined as zero.
+    if (U != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(dev_err, MOE_DEV_CAPACITY);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * H;
+         i += (long long)gridDim.x * blockDim.x)
+      y[i] = 0.f;
+    return;
+  }
+  // Padded group starts: warp 0 scans ceil16(n_e) over u.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (U + 31) / 32;
+    const int u0 = lane * per;
+    int sum = 0;
+    for (int u = u0; u < u0 + per && u < U; ++u) {
+      const int a = offsets[u], b = offsets[u + 1];
+      if (a < 0 || b > TK || b - a < 1 || b - a > T) s_bad = 1;
+      sum += ((b - a) + 15) & ~15;
+    }
+    int ex = sum;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, ex, off);
+      if (lane >= off) ex += v;
+    }
+    ex -= sum;
+    for (int u = u0; u < u0 + per && u < U; ++u) {
+      spoff[u] = ex;
+      ex += ((offsets[u + 1] - offsets[u]) + 15) & ~15;
+    }
+    if (lane == 31) spoff[U] = ex;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * H;
+         i += (long long)gridDim.x * blockDim.x)
+      y[i] = 0.f;
+    return;
+  }
+  if (blockIdx.x == 0)
+    for (int u = threadIdx.x; u <= U; u += blockDim.x) poff[u] = spoff[u];
+  // Copy / zero-fill: one 16-byte chunk per thread-iteration.
+  const int R = spoff[U];
+  const int cpr = H / 8;  // chunks per row
+  const long long chunks = (long long)R * cpr;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < chunks;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int rr = static_cast<int>(i / cpr);
+    const int ch = static_cast<int>(i - (long long)rr * cpr);
+    // group of padded row rr: largest u with spoff[u] <= rr
+    int lo = 0, hi = U - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (spoff[mid] <= rr) lo = mid;
+      else hi = mid - 1;
+    }
+    const int n = rr - spoff[lo];
+    const int ne = offsets[lo + 1] - offsets[lo];
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (n < ne) {
+      const int tok = perm_token[offsets[lo] + n];
+      bool ok = tok >= 0 && tok < T;
+      int row = tok;
+      if (ok && x_rows) {
+        row = x_rows[tok];
+        ok = row >= 0 && row < x_rows_limit;
+      }
+      if (ok)
+        v = *reinterpret_cast<const uint4*>(x + (size_t)row * H + ch * 8);
+      else
+        flag_error(dev_err, MOE_DEV_BAD_ID);
+    }
+    *reinterpret_cast<uint4*>(xp + (size_t)rr * H + ch * 8) = v;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 tensor map: dims innermost first; box {64, box_rows[, 1]}; 128B swizzle.
+bool make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+  for (int i = 0; i < rank - 1; ++i) gstride[i] = strides_bytes[i];
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct TcGeom {
+  int NM, MT_gu, MT_d, Rmax, G;
+  int stages_gu, stages_d;
+  size_t smem_gu, smem_d;
+};
+
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kSmemExtra = 1024 /*align*/ + 256 /*barriers & flags*/;
+
+TcGeom tc_geom(const moe_layer_weights& lw, int T, int k) {
+  TcGeom g;
+  const int TK = T * k;
+  const int cap = lw.E < TK ? lw.E : TK;
+  const int nmax = T < 256 ? T : 256;
+  g.NM = (nmax + 15) & ~15;
+  g.MT_gu = (lw.I + kBM - 1) / kBM;
+  g.MT_d = (lw.H + kBM - 1) / kBM;
+  g.Rmax = TK + 15 * cap;
+  g.G = sm_count();
+  const size_t b = static_cast<size_t>(g.NM) * 128;
+  const size_t st_gu = 2 * kABytes + b, st_d = kABytes + b;
+  g.stages_gu = static_cast<int>((kSmemLimit - kSmemExtra) / st_gu);
+  g.stages_d = static_cast<int>((kSmemLimit - kSmemExtra) / st_d);
+  if (g.stages_gu > 8) g.stages_gu = 8;
+  if (g.stages_d > 12) g.stages_d = 12;
+  g.smem_gu = g.stages_gu * st_gu + kSmemExtra;
+  g.smem_d = g.stages_d * st_d + kSmemExtra;
+  return g;
+}
+
+uint32_t pow2_cols(int c) {
+  uint32_t v = 32;
+  while (v < static_cast<uint32_t>(c)) v <<= 1;
+  return v;
+}
+
+}  // namespace
+
+bool ffn_tc_supported(const moe_layer_weights& lw, int T, int k) {
+  if (lw.dtype != MOE_DTYPE_BF16) return false;
+  if (lw.H % kBK || lw.I % kBK) return false;
+  if (T < 1 || T > 256) return false;
+  TcGeom g = tc_geom(lw, T, k);
+  return g.stages_gu >= 2 && g.stages_d >= 2 && encode_fn() != nullptr;
+}
+
+size_t ffn_tc_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
+  TcGeom g = tc_geom(lw, T, k);
+  const int TK = T * k;
+  const int cap = lw.E < TK ? lw.E : TK;
+  size_t b = 0;
+  b += align_up(static_cast<size_t>(g.Rmax) * lw.H * 2, 256);                 // Xp
+  b += align_up(static_cast<size_t>(g.Rmax) * lw.I * 2, 256);                 // Hp
+  b += align_up(static_cast<size_t>(TK) * lw.H * 4, 256);                     // O
+  b += align_up(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4, 256);       // partials
+  b += align_up(static_cast<size_t>(cap + 1) * 4, 256);                       // poff
+  b += align_up((static_cast<size_t>(cap) * (g.MT_gu + g.MT_d) + g.MT_d) * 4, 256);  // counters
+  return b;
+}
+
+int ffn_tc_launch(const FfnArgs& a) {
+  const auto& lw = a.lw;
+  const int T = a.T, k = a.k, TK = T * k;
+  const int cap = lw.E < TK ? lw.E : TK;
+  TcGeom g = tc_geom(lw, T, k);
+  char* p = static_cast<char*>(a.ws);
+  uint16_t* xp = reinterpret_cast<uint16_t*>(p);
+  p += align_up(static_cast<size_t>(g.Rmax) * lw.H * 2, 256);
+  uint16_t* hp = reinterpret_cast<uint16_t*>(p);
+  p += align_up(static_cast<size_t>(g.Rmax) * lw.I * 2, 256);
+  float* o = reinterpret_cast<float*>(p);
+  p += align_up(static_cast<size_t>(TK) * lw.H * 4, 256);
+  float* partials = reinterpret_cast<float*>(p);
+  p += align_up(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4, 256);
+  int32_t* poff = reinterpret_cast<int32_t*>(p);
+  p += align_up(static_cast<size_t>(cap + 1) * 4, 256);
+  int32_t* cnt_gu = reinterpret_cast<int32_t*>(p);
+  int32_t* cnt_d = cnt_gu + static_cast<size_t>(cap) * g.MT_gu;
+  int32_t* done = cnt_d + static_cast<size_t>(cap) * g.MT_d;
+  const int n_counters = cap * (g.MT_gu + g.MT_d) + g.MT_d;
+
+  // Tensor maps (host-side encoding only; nothing is enqueued).
+  CUtensorMap tm_g, tm_u, tm_x, tm_wd, tm_h;
+  const uint64_t H = lw.H, I = lw.I, E = lw.E;
+  {
+    uint64_t dims[3] = {H, I, E}, str[2] = {H * 2, 2 * I * H * 2};
+    if (!make_tmap(&tm_g, lw.w_gate_up, 3, dims, str, kBM)) return MOE_ERR_CUDA;
+    const char* up = static_cast<const char*>(lw.w_gate_up) + I * H * 2;
+    if (!make_tmap(&tm_u, up, 3, dims, str, kBM)) return MOE_ERR_CUDA;
+  }
+  {
+    uint64_t dims[2] = {H, static_cast<uint64_t>(g.Rmax)}, str[1] = {H * 2};
+    if (!make_tmap(&tm_x, xp, 2, dims, str, 16)) return MOE_ERR_CUDA;
+  }
+  {
+    uint64_t dims[3] = {I, H, E}, str[2] = {I * 2, H * I * 2};
+    if (!make_tmap(&tm_wd, lw.w_down, 3, dims, str, kBM)) return MOE_ERR_CUDA;
+  }
+  {
+    uint64_t dims[2] = {I, static_cast<uint64_t>(g.Rmax)}, str[1] = {I * 2};
+    if (!make_tmap(&tm_h, hp, 2, dims, str, 16)) return MOE_ERR_CUDA;
+  }
+
+  cudaStream_t s = a.stream;
+  {
+    long long chunks = static_cast<long long>(g.Rmax) * (lw.H / 8);
+    int blocks = static_cast<int>((chunks + 255) / 256);
+    if (blocks > g.G * 4) blocks = g.G * 4;
+    if (blocks < 1) blocks = 1;
+    LaunchScope ls(kProfPrep, s);
+    ffn_prep_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, k,
+                                           lw.H, cap, a.n_unique, a.offsets, a.perm_token, xp, poff, cnt_gu,
+                                           n_counters, a.y, a.dev_err);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  }
+
+  TcParams tp{};
+  tp.T = T;
+  tp.k = k;
+  tp.E = lw.E;
+  tp.cap = cap;
+  tp.NM = g.NM;
+  tp.Rmax = g.Rmax;
+  tp.n_unique = a.n_unique;
+  tp.unique = a.unique;
+  tp.offsets = a.offsets;
+  tp.poff = poff;
+  tp.hp = hp;
+  tp.o = o;
+  tp.partials = partials;
+  tp.inv = a.inv;
+  tp.w = a.w;
+  tp.y = a.y;
+  tp.dev_err = a.dev_err;
+
+  // gate/up
+  tp.M = lw.I;
+  tp.K = lw.H;
+  tp.stages = g.stages_gu;
+  tp.acc_stages = 2 * 2 * g.NM <= 512 ? 2 : 1;
+  tp.tmem_cols = pow2_cols(tp.acc_stages * 2 * g.NM);
+  tp.tile_cnt = cnt_gu;
+  tp.done_cnt = nullptr;
+  if (cudaFuncSetAttribute(ffn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(g.smem_gu)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  {
+    LaunchScope ls(kProfGateUp, s);
+    ffn_tc_kernel<true><<<g.G, kThreads, g.smem_gu, s>>>(tm_g, tm_u, tm_x, tp);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  }
+
+  // down + combine
+  tp.M = lw.H;
+  tp.K = lw.I;
+  tp.stages = g.stages_d;
+  tp.acc_stages = 2 * g.NM <= 512 ? 2 : 1;
+  tp.tmem_cols = pow2_cols(tp.acc_stages * g.NM);
+  tp.tile_cnt = cnt_d;
+  tp.done_cnt = done;
+  if (cudaFuncSetAttribute(ffn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(g.smem_d)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  {
+    LaunchScope ls(kProfDown, s);
+    ffn_tc_kernel<false><<<g.G, kThreads, g.smem_d, s>>>(tm_wd, tm_wd, tm_h, tp);
+    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe
