@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: keep the first N layers of the workload (recorded in config)")
     ap.add_argument("--cpu-layers", type=int, default=0,
                     help="layers in the CPU oracle sample (0: auto, about 10-30 s)")
     return ap.parse_args()
@@ -202,6 +204,8 @@ def ours(args, rank, ws, local):
     from workload import device as wdev
 
     cfg = CONFIGS[args.config]
+    if args.layers:
+        cfg = cfg.replace(L=min(args.layers, cfg.L))
     dev = torch.device("cuda", local)
     wl = gen.make_workload(cfg)
     layers = []
@@ -310,7 +314,8 @@ def ours(args, rank, ws, local):
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic (seeded workload generator; counter-hash weights)",
-        "config": {"workload": cfg.name, "layers": cfg.L, "hidden": cfg.H, "experts": cfg.E,
+        "config": {"workload": cfg.name + (f" (first {cfg.L} layers, profiling run)" if args.layers else ""),
+                   "layers": cfg.L, "hidden": cfg.H, "experts": cfg.E,
                    "top_k": cfg.k, "intermediate": cfg.I, "weights": cfg.dtype,
                    "batch": cfg.nseq, "verify_tokens": wl.T, "gamma": wl.gamma.tolist(),
                    "reuse_bias": cfg.use_bias, "selection": "marginal" if cfg.mode == 0 else "static",
