@@ -171,6 +171,32 @@ int moe_verify_ffn(const void* x, int32_t T, int32_t k, const moe_layer_weights*
                    const int32_t* perm_token, const int32_t* inv, const float* w,
                    float* y, void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 
+/*
+ * moe_verify_ffn_noalloc -- moe_verify_ffn for callers that cannot allocate
+ * device memory.  The pages have no counterpart; this is a deployment aid.
+ *
+ * Who needs it: code running during CUDA graph capture (cudaMalloc is not
+ * allowed there), plugin / custom-op hosts that own the device allocator and
+ * forbid other allocations, and latency-critical serving loops where an
+ * allocation would synchronise the device.  Such callers pass inputs and
+ * outputs only; the scratch space lives in a static device array of 64 MiB
+ * inside the library, present on every GPU that loads the library until the
+ * process exits.  The call performs no cudaMalloc/cudaFree or other
+ * allocating routine.
+ *
+ * Arguments and results: exactly those of moe_verify_ffn, without the
+ * workspace.  Returns MOE_ERR_UNSUPPORTED when the FFN would need more than
+ * the 64 MiB of static scratch (moe_verify_ffn_workspace() tells the size).
+ * All calls on a device share the array and it keeps the previous call's
+ * contents (the kernels reset what must start at zero); calls that overlap
+ * on the GPU race on it.  The first call on a device looks up the array's
+ * address with that device current; make it before any stream capture.
+ */
+int moe_verify_ffn_noalloc(const void* x, int32_t T, int32_t k, const moe_layer_weights* lw,
+                           const int32_t* n_unique, const int32_t* unique, const int32_t* offsets,
+                           const int32_t* perm_token, const int32_t* inv, const float* w, float* y,
+                           int32_t* dev_err, void* stream);
+
 /* ---------------------------------------------------------------- selection
  * eco_select -- EcoSpec cost-aware draft selection, one tree per sequence.
  *
