@@ -36,8 +36,8 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -231,9 +231,9 @@ def ours(args, rank, ws, local):
     n_unique = step.n_unique.cpu().tolist()
     bytes_step = sum(n_unique) * expert_bytes(cfg)
 
-    # ---- device-timed region: inputs resident in HBM, weights >> L2.
+    # ---- pass A (headline): device-timed region, inputs resident in HBM,
+    # unique-expert bytes per step >> L2; no per-kernel events.
     launches0 = mv.launch_count()
-    mv.profile_begin(max_launches=max(64, args.steps * (1 + 5 * cfg.L) + 16))
     barrier(ws)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -245,7 +245,6 @@ def ours(args, rank, ws, local):
         e1.record(stream)
         torch.cuda.synchronize()
     barrier(ws)
-    prof = mv.profile_end()
     launches = mv.launch_count() - launches0
     ms_local = e0.elapsed_time(e1)
     ms_total = max_over_ranks(ms_local, ws)
@@ -254,8 +253,29 @@ def ours(args, rank, ws, local):
     value = total_bytes / (ms_total / 1e3) / 1e9
     tokens = sum_over_ranks(wl.T * args.steps, ws)
 
-    # ---- roofline of the dominant kernel (FFN gate/up), live from this run.
-    gu = prof["ffn_gate_up"]
+    # ---- pass B: the same K steps with CUDA events around the dominant
+    # kernel only (FFN gate/up), on the stream it runs on.
+    mv.profile_begin(max_launches=args.steps * cfg.L + 16, classes=["ffn_gate_up"])
+    torch.cuda.synchronize()
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(args.steps):
+        one()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    gu = mv.profile_end()["ffn_gate_up"]
+    ms_pass_b = b0.elapsed_time(b1)
+
+    # ---- pass C: per-kernel breakdown (events around every launch).
+    n_c = min(args.steps, 50)
+    mv.profile_begin(max_launches=n_c * (1 + 6 * cfg.L) + 16)
+    for _ in range(n_c):
+        one()
+    torch.cuda.synchronize()
+    prof = mv.profile_end()
+
+    # ---- roofline of the dominant kernel (FFN gate/up), from pass B.
     gu_bytes = sum(n_unique) * gate_up_bytes(cfg) * args.steps
     gu_ms = gu["ms"]
     achieved = gu_bytes / (gu_ms / 1e3) / 1e9 if gu_ms > 0 else None
@@ -270,7 +290,9 @@ def ours(args, rank, ws, local):
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": sum(n_unique) * gate_up_bytes(cfg) / cfg.L,
                 "avg_launch_us": gu_ms * 1e3 / max(gu["launches"], 1),
-                "launches": gu["launches"]}
+                "launches": gu["launches"],
+                "timed_in": "pass B: the K timed steps repeated with events around gate/up only",
+                "pass_b_ms_per_step": ms_pass_b / args.steps}
     step_frac = value / peak / ws
 
     # ---- end to end through the C ABI with host buffers.
@@ -328,9 +350,9 @@ def ours(args, rank, ws, local):
         "frac_of_peak_step": step_frac,
         "frac_of_8tbs_step": value / 8000.0 / ws,
         "roofline": roofline,
-        "kernel_ms_per_step": {k: v["ms"] / args.steps for k, v in prof.items()},
+        "kernel_ms_per_step": {k: v["ms"] / n_c for k, v in prof.items()},
         "control_path_frac": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))
-        / max(ms_local, 1e-9),
+        / n_c / max(ms_step, 1e-9),
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms / args.steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -340,9 +362,9 @@ def ours(args, rank, ws, local):
 
 
 # ---------------------------------------------------------------------- oracle
-def oracle_sample(cfg, wl, n_layers, time_budget_s=25.0):
-    """Times the CPU oracle on the first n_layers of the step (all verify tokens).
-    Host weight generation is outside the timed region; decoding is inside."""
+def oracle_prepare(cfg, wl, n_layers):
+    """Routing of the sampled layers and host copies of their unique experts
+    (input preparation, outside any timed region)."""
     from oracle import moe_layer as ml
     from oracle import verify_step as ovs
     from workload import gen
@@ -350,8 +372,7 @@ def oracle_sample(cfg, wl, n_layers, time_budget_s=25.0):
     sels, _ = ovs.run_selection(wl)
     rows = ovs.verify_rows(wl.parent.shape[0], sels)
     conf = ovs.token_conf(wl.P, sels)
-    stored = {}
-    unions = []
+    stored, unions = {}, []
     for l in range(n_layers):
         lg = wl.logits[l].reshape(-1, cfg.E)[rows]
         if cfg.use_bias:
@@ -361,12 +382,29 @@ def oracle_sample(cfg, wl, n_layers, time_budget_s=25.0):
         unions.append(len(u))
         for e in u:
             stored[(l, e)] = gen.expert_weights_host(cfg, l, e)
+    return stored, sum(unions) * expert_bytes(cfg)
+
+
+def oracle_run(cfg, wl, n_layers, stored):
+    """One timed pass of the oracle verify step restricted to the sampled layers
+    (selection, routing, union and FFN of every verify token; weight decoding
+    included).  Returns seconds."""
+    from oracle import moe_layer as ml
+    from oracle import verify_step as ovs
+
     x_dec = (lambda a: np.asarray(a, np.float32).astype(np.float64)) if cfg.dtype == "f32" else ml.decode_bf16
     t0 = time.perf_counter()
     ovs.run_step(wl, lambda l: (lambda e: ml.expert_matrices(stored[(l, e)], cfg.dtype)),
                  layers=list(range(n_layers)), x_decode=x_dec)
-    dt = time.perf_counter() - t0
-    return dt, sum(unions) * expert_bytes(cfg)
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(cfg, wl, n_layers, target_s=12.0, max_reps=200):
+    stored, nbytes = oracle_prepare(cfg, wl, n_layers)
+    times = []
+    while sum(times) < target_s and len(times) < max_reps:
+        times.append(oracle_run(cfg, wl, n_layers, stored))
+    return sum(times), nbytes * len(times), len(times)
 
 
 def cpu_threads():
@@ -378,11 +416,6 @@ def cpu_threads():
         return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
-def auto_layers(cfg):
-    per = {"f32": 1, "bf16": 2, "e4m3": 1}[cfg.dtype]
-    return max(1, min(cfg.L, {"toy": 1}.get(cfg.name, per)))
-
-
 def reference(args, rank, ws):
     """The reference arm: the CPU oracle as it stands, on the same workload."""
     from workload import CONFIGS, gen
@@ -391,12 +424,12 @@ def reference(args, rank, ws):
     cfg = CONFIGS[args.config]
     wl = gen.make_workload(cfg)
     n_layers = args.cpu_layers or 1
-    times, nbytes = [], 0
+    stored, nbytes = oracle_prepare(cfg, wl, n_layers)
+    times = []
     for i in range(args.warmup + args.steps):
-        dt, b = oracle_sample(cfg, wl, n_layers)
+        dt = oracle_run(cfg, wl, n_layers, stored)
         if i >= args.warmup:
             times.append(dt)
-            nbytes = b
     tot = sum(times)
     value = nbytes * len(times) / tot / 1e9
     cores = cpu_threads()
@@ -425,11 +458,11 @@ def main():
     rank, ws, local = dist_setup(args.gpus)
     res, wl, cfg = ours(args, rank, ws, local)
     if rank == 0 and not args.no_cpu_baseline:
-        n_layers = args.cpu_layers or auto_layers(cfg)
-        dt, nbytes = oracle_sample(cfg, wl, n_layers)
+        n_layers = args.cpu_layers or 1
+        dt, nbytes, reps = oracle_baseline(cfg, wl, n_layers)
         res["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cpu_threads(),
                                "kind": "oracle",
-                               "sample": f"oracle on layer(s) 0..{n_layers - 1} of {cfg.L}, all {wl.T} verify tokens, {dt:.1f} s"}
+                               "sample": f"oracle verify step on layer(s) 0..{n_layers - 1} of {cfg.L}, all {wl.T} verify tokens, repeated {reps}x: {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(res))
     if ws > 1:

@@ -276,14 +276,15 @@ int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* pare
 /* ---------------------------------------------------------------- timing
  * Optional per-kernel timing.  Between moe_profile_begin and moe_profile_end
  * the library records a CUDA event pair on the launching stream around each
- * of its kernel launches (at most max_launches pairs; later launches are not
- * recorded).  moe_profile_end synchronises those events (host blocking) and
- * writes, per kernel class, the summed milliseconds and the launch count.
- * Classes: 0 eco_select, 1 route, 2 union/permute, 3 FFN prep,
- * 4 FFN gate/up, 5 FFN down, 6 combine.  Not for use under stream capture.
+ * of its kernel launches whose class bit is set in class_mask (at most
+ * max_launches pairs; later launches are not recorded).  moe_profile_end
+ * synchronises those events (host blocking) and writes, per kernel class, the
+ * summed milliseconds and the launch count.  Classes: 0 eco_select, 1 route,
+ * 2 union/permute, 3 FFN prep, 4 FFN gate/up, 5 FFN down, 6 combine.
+ * Not for use under stream capture.
  */
 enum { MOE_PROF_CLASSES = 7 };
-int moe_profile_begin(int32_t max_launches);
+int moe_profile_begin(int32_t max_launches, int32_t class_mask);
 int moe_profile_end(float* ms_per_class, int32_t* launches_per_class, int32_t n_classes);
 
 /* ---------------------------------------------------------------- misc */

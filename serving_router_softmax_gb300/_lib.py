@@ -77,7 +77,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_verify_step.argtypes = [P(StepCfg), vp, vp, vp, vp, vp, vp, P(LayerWeights), vp, vp,
                                     vp, vp, vp, sz, vp, vp]
     lib.moe_verify_step.restype = C.c_int
-    lib.moe_profile_begin.argtypes = [i32]
+    lib.moe_profile_begin.argtypes = [i32, i32]
     lib.moe_profile_begin.restype = C.c_int
     lib.moe_profile_end.argtypes = [vp, vp, i32]
     lib.moe_profile_end.restype = C.c_int

@@ -249,8 +249,13 @@ class VerifyStep:
         return self.y
 
 
-def profile_begin(max_launches: int = 65536):
-    _check(L.load().moe_profile_begin(max_launches), "moe_profile_begin")
+def profile_begin(max_launches: int = 65536, classes: Optional[Sequence[str]] = None):
+    """Start event timing of the library's launches (all classes by default)."""
+    names = L.PROF_CLASSES if classes is None else classes
+    mask = 0
+    for n in names:
+        mask |= 1 << L.PROF_CLASSES.index(n)
+    _check(L.load().moe_profile_begin(max_launches, mask), "moe_profile_begin")
 
 
 def profile_end() -> Dict[str, Dict[str, float]]:

@@ -321,10 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       bool finished = whole;
       if (!whole) {
-        // Last-arriver fixup across the CTAs that share this tile.
-        __threadfence();
+        // Last-arriver fixup across the CTAs that share this tile.  The CTA
+        // barrier orders every thread's partial stores before thread 0's
+        // fence and atomic (release); the finisher fences after observing
+        // the count (acquire) before reading the other CTAs' partials.
         tc::named_bar_sync(1, kEpiThreads);
-        if (etid == 0) *bcast = atomicAdd(&p.tile_cnt[t], 1);
+        if (etid == 0) {
+          __threadfence();
+          *bcast = atomicAdd(&p.tile_cnt[t], 1);
+        }
         tc::named_bar_sync(1, kEpiThreads);
         const int arrived = *bcast;
         const long long t0 = (long long)t * KB;
@@ -362,10 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!kGateUp && finished) {
         // Count the finished tile for its 128-row block of y; the CTA that
-        // completes the block combines it.
-        __threadfence();
+        // completes the block combines it (same release/acquire pattern).
         tc::named_bar_sync(1, kEpiThreads);
-        if (etid == 0) *bcast = atomicAdd(&p.done_cnt[ti.m], 1);
+        if (etid == 0) {
+          __threadfence();
+          *bcast = atomicAdd(&p.done_cnt[ti.m], 1);
+        }
         tc::named_bar_sync(1, kEpiThreads);
         const int done = *bcast;
         tc::named_bar_sync(1, kEpiThreads);
@@ -373,15 +380,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           __threadfence();
           const int TK = p.T * p.k;
           for (int tok = 0; tok < p.T && row_ok; ++tok) {
-            float s = 0.f;
-            for (int j = 0; j < p.k; ++j) {
-              const int pos = p.inv[tok * p.k + j];
-              if (pos < 0 || pos >= TK) {
-                flag_error(p.dev_err, MOE_DEV_BAD_ID);
-                continue;
-              }
-              s = fmaf(p.w[tok * p.k + j], __ldcg(&p.o[(size_t)pos * p.M + row]), s);
+            // All k loads of a token in flight at once; sum in slot order.
+            int pos[16];
+            float wv[16], ov[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              pos[j] = j < p.k ? __ldg(&p.inv[tok * p.k + j]) : -1;
+              wv[j] = j < p.k ? __ldg(&p.w[tok * p.k + j]) : 0.f;
             }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const bool ok = pos[j] >= 0 && pos[j] < TK;
+              if (j < p.k && !ok) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+              ov[j] = ok ? __ldcg(&p.o[(size_t)pos[j] * p.M + row]) : 0.f;
+            }
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < p.k && pos[j] >= 0 && pos[j] < TK) s = fmaf(wv[j], ov[j], s);
             p.y[(size_t)tok * p.M + row] = s;
           }
         }

@@ -19,6 +19,7 @@ struct Prof {
   std::vector<int> cls;
   int n = 0;
   int pending_cls = -1;
+  int mask = 0;
 };
 Prof& prof() {
   static Prof p;
@@ -46,6 +47,7 @@ void note_launch(int c, cudaStream_t s, bool before) {
   if (!p.on) return;
   std::lock_guard<std::mutex> lk(p.mu);
   if (!p.on) return;
+  if (!((p.mask >> c) & 1)) return;
   if (before) {
     if (p.n >= p.max) return;
     cudaEventRecord(p.ev[2 * p.n], s);
@@ -61,7 +63,7 @@ void note_launch(int c, cudaStream_t s, bool before) {
 
 }  // namespace moe
 
-extern "C" int moe_profile_begin(int32_t max_launches) {
+extern "C" int moe_profile_begin(int32_t max_launches, int32_t class_mask) {
   using namespace moe;
   if (max_launches < 1 || max_launches > (1 << 20)) return MOE_ERR_ARG;
   Prof& p = prof();
@@ -74,6 +76,7 @@ extern "C" int moe_profile_begin(int32_t max_launches) {
   p.max = max_launches;
   p.n = 0;
   p.pending_cls = -1;
+  p.mask = class_mask;
   p.on = true;
   return MOE_OK;
 }
