@@ -127,22 +127,48 @@ int moe_union_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E,
                       float* reuse_ratio, int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------- expert FFN
- * One layer's expert weights, expert-major with each expert contiguous:
+ * One layer's expert weights.  Two layouts:
+ *
+ * MOE_LAYOUT_ROWMAJOR: expert-major, each expert contiguous:
  *   w_gate_up [E, 2I, H]: rows 0..I-1 are W_gate, rows I..2I-1 are W_up.
  *   w_down    [E, H, I].
  *   FP8 only: scales_gate_up [E, 2I/128, H/128] and scales_down
  *   [E, H/128, I/128] fp32; weight (r, c) of a matrix is code(r, c) *
  *   scale[r/128, c/128].  NULL for the other dtypes.
+ *
+ * MOE_LAYOUT_TILED (bf16 only; made once at load time by moe_pack_tiled):
+ * blocks of 64 reduction columns, each block contiguous, so that every
+ * pipeline stage of the FFN reads one 32 KB contiguous piece of HBM.
+ *   w_gate_up [E][MTg][H/64][256][64], MTg = ceil(I/128): block (e, m, kb)
+ *     holds rows m*128 .. m*128+127 of W_gate (columns kb*64 .. kb*64+63)
+ *     followed by the same rows of W_up; rows >= I are zero.
+ *   w_down [E][MTd][I/64][128][64], MTd = ceil(H/128): block (e, m, kb)
+ *     holds rows m*128 .. m*128+127 of W_down, columns kb*64 .. +63; rows
+ *     >= H are zero.
+ *
  * Pointers must be 16-byte aligned.  Limits: H and I multiples of 64
  * (of 128 for FP8), E <= 1024.
  */
+enum { MOE_LAYOUT_ROWMAJOR = 0, MOE_LAYOUT_TILED = 1 };
+
 typedef struct {
-  int32_t H, I, E, dtype;
+  int32_t H, I, E, dtype, layout;
   const void* w_gate_up;
   const void* w_down;
   const float* scales_gate_up;
   const float* scales_down;
 } moe_layer_weights;
+
+/* Bytes of the tiled copies of one layer's bf16 weights (gate/up and down,
+ * written to *gate_up_bytes / *down_bytes when not NULL); returns their sum,
+ * or 0 if the layer cannot be tiled. */
+size_t moe_tiled_bytes(const moe_layer_weights* lw, size_t* gate_up_bytes, size_t* down_bytes);
+
+/* Packs one layer's row-major bf16 weights (src->layout must be ROWMAJOR)
+ * into the MOE_LAYOUT_TILED layout at dst_gate_up / dst_down (caller-owned
+ * device buffers of the sizes moe_tiled_bytes reports, 16-byte aligned, not
+ * overlapping src).  A load-time step; enqueued on `stream`. */
+int moe_pack_tiled(const moe_layer_weights* src, void* dst_gate_up, void* dst_down, void* stream);
 
 /* Bytes of workspace moe_verify_ffn needs for T tokens with top-k routing. */
 size_t moe_verify_ffn_workspace(const moe_layer_weights* lw, int32_t T, int32_t k);
@@ -257,7 +283,7 @@ int eco_select(const float* P, const int32_t* parent, const uint32_t* own_fp, in
  * to N; the device checks it (MOE_DEV_CAPACITY if not).
  */
 typedef struct {
-  int32_t L, nseq, N, W, E, k, H, I, dtype;
+  int32_t L, nseq, N, W, E, k, H, I, dtype, layout;
   int32_t T, gamma_max, mode;
   float eps;
   int32_t use_bias, cap;

@@ -14,6 +14,7 @@ MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = 0, 1
 DEV_NAN_LOGIT, DEV_BAD_ID, DEV_DUP_ID, DEV_BAD_TREE, DEV_BAD_PROB, DEV_TIMEOUT, DEV_CAPACITY = (
     0x01, 0x02, 0x04, 0x08, 0x10, 0x20, 0x40)
 DTYPE_F32, DTYPE_BF16, DTYPE_E4M3_B128 = 0, 1, 2
+LAYOUT_ROWMAJOR, LAYOUT_TILED = 0, 1
 PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up", "ffn_down",
                 "combine"]
 
@@ -29,7 +30,7 @@ class RouteCfg(C.Structure):
 
 class LayerWeights(C.Structure):
     _fields_ = [("H", C.c_int32), ("I", C.c_int32), ("E", C.c_int32), ("dtype", C.c_int32),
-                ("w_gate_up", C.c_void_p), ("w_down", C.c_void_p),
+                ("layout", C.c_int32), ("w_gate_up", C.c_void_p), ("w_down", C.c_void_p),
                 ("scales_gate_up", C.c_void_p), ("scales_down", C.c_void_p)]
 
 
@@ -41,7 +42,7 @@ class EcoCfg(C.Structure):
 class StepCfg(C.Structure):
     _fields_ = [("L", C.c_int32), ("nseq", C.c_int32), ("N", C.c_int32), ("W", C.c_int32),
                 ("E", C.c_int32), ("k", C.c_int32), ("H", C.c_int32), ("I", C.c_int32),
-                ("dtype", C.c_int32), ("T", C.c_int32), ("gamma_max", C.c_int32),
+                ("dtype", C.c_int32), ("layout", C.c_int32), ("T", C.c_int32), ("gamma_max", C.c_int32),
                 ("mode", C.c_int32), ("eps", C.c_float), ("use_bias", C.c_int32),
                 ("cap", C.c_int32), ("alpha", C.c_float)]
 
@@ -65,6 +66,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_route.restype = C.c_int
     lib.moe_union_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.moe_union_permute.restype = C.c_int
+    lib.moe_tiled_bytes.argtypes = [P(LayerWeights), P(sz), P(sz)]
+    lib.moe_tiled_bytes.restype = sz
+    lib.moe_pack_tiled.argtypes = [P(LayerWeights), vp, vp, vp]
+    lib.moe_pack_tiled.restype = C.c_int
     lib.moe_verify_ffn_workspace.argtypes = [P(LayerWeights), i32, i32]
     lib.moe_verify_ffn_workspace.restype = sz
     lib.moe_verify_ffn.argtypes = [vp, i32, i32, P(LayerWeights), vp, vp, vp, vp, vp, vp, vp, vp,

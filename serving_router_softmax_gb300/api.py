@@ -55,35 +55,59 @@ def new_dev_err(device=None) -> torch.Tensor:
 DTYPES = {"f32": L.DTYPE_F32, "bf16": L.DTYPE_BF16, "e4m3": L.DTYPE_E4M3_B128}
 
 
+LAYOUTS = {"rowmajor": L.LAYOUT_ROWMAJOR, "tiled": L.LAYOUT_TILED}
+
+
 @dataclass
 class ExpertLayer:
-    """One layer's expert weights on the device (expert-major, contiguous).
+    """One layer's expert weights on the device.
 
-    gate_up: [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up); down: [E, H, I].
-    Storage: float32, bfloat16 (or int16/uint16 bf16 bits) or uint8 FP8 codes.
-    FP8 adds scales_gate_up [E, 2I/128, H/128] and scales_down [E, H/128, I/128].
+    Row-major layout: gate_up [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up) and
+    down [E, H, I]; storage float32, bf16 bits (int16/uint16/bfloat16) or
+    uint8 FP8 codes, with FP8 scales [E, 2I/128, H/128] / [E, H/128, I/128].
+    Tiled layout (bf16, from ``pack_tiled``): flat buffers; ``dims`` gives
+    (H, I, E).
     """
     gate_up: torch.Tensor
     down: torch.Tensor
     dtype: str
     scales_gate_up: Optional[torch.Tensor] = None
     scales_down: Optional[torch.Tensor] = None
+    layout: str = "rowmajor"
+    dims: Optional[tuple] = None
 
     @property
     def E(self):
-        return self.gate_up.shape[0]
+        return self.dims[2] if self.dims else self.gate_up.shape[0]
 
     @property
     def I(self):
-        return self.gate_up.shape[1] // 2
+        return self.dims[1] if self.dims else self.gate_up.shape[1] // 2
 
     @property
     def H(self):
-        return self.gate_up.shape[2]
+        return self.dims[0] if self.dims else self.gate_up.shape[2]
 
     def struct(self) -> L.LayerWeights:
-        return L.LayerWeights(self.H, self.I, self.E, DTYPES[self.dtype], _ptr(self.gate_up),
-                              _ptr(self.down), _ptr(self.scales_gate_up), _ptr(self.scales_down))
+        return L.LayerWeights(self.H, self.I, self.E, DTYPES[self.dtype], LAYOUTS[self.layout],
+                              _ptr(self.gate_up), _ptr(self.down), _ptr(self.scales_gate_up),
+                              _ptr(self.scales_down))
+
+
+def pack_tiled(layer: ExpertLayer, stream=None) -> ExpertLayer:
+    """Load-time repack of a row-major bf16 layer into the tiled layout."""
+    lib = L.load()
+    if layer.layout != "rowmajor" or layer.dtype != "bf16":
+        raise MoEError("pack_tiled needs a row-major bf16 layer")
+    st = layer.struct()
+    gu_b, dn_b = C.c_size_t(0), C.c_size_t(0)
+    if lib.moe_tiled_bytes(C.byref(st), C.byref(gu_b), C.byref(dn_b)) == 0:
+        raise MoEError("layer shape cannot be tiled")
+    dev = layer.gate_up.device
+    gu = torch.empty(gu_b.value // 2, dtype=torch.int16, device=dev)
+    dn = torch.empty(dn_b.value // 2, dtype=torch.int16, device=dev)
+    _check(lib.moe_pack_tiled(C.byref(st), _ptr(gu), _ptr(dn), _stream(stream)), "moe_pack_tiled")
+    return ExpertLayer(gu, dn, "bf16", layout="tiled", dims=(layer.H, layer.I, layer.E))
 
 
 # ------------------------------------------------------------------ calls
@@ -195,6 +219,7 @@ class StepSpec:
     dtype: str
     T: int
     gamma_max: int
+    layout: str = "rowmajor"
     mode: int = 0
     eps: float = 2.0 ** -10
     use_bias: bool = False
@@ -203,7 +228,7 @@ class StepSpec:
 
     def struct(self) -> L.StepCfg:
         return L.StepCfg(self.L, self.nseq, self.N, self.W, self.E, self.k, self.H, self.I,
-                         DTYPES[self.dtype], self.T, self.gamma_max, self.mode, self.eps,
+                         DTYPES[self.dtype], LAYOUTS[self.layout], self.T, self.gamma_max, self.mode, self.eps,
                          int(self.use_bias), self.cap, self.alpha)
 
 

@@ -52,6 +52,8 @@ struct TcParams {
   int M, K;          // rows of each expert matrix, reduction length
   int NM;            // max padded token columns (multiple of 16, <= 256)
   int Rmax;          // rows of Xp / Hp
+  int tiled;         // weights in the tile-packed layout (else row-major)
+  int KS;            // k-blocks per pipeline stage (1, or 2 for tiled down)
   int stages;
   int acc_stages;
   uint32_t tmem_cols;
@@ -102,8 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int nA = kGateUp ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int bBytes = p.NM * 128;
-  const int stageBytes = nA * kABytes + bBytes;
+  const int aBytes = kGateUp ? 2 * kABytes : p.KS * kABytes;
+  const int bStride = p.NM * 128;  // one k-block of B
+  const int stageBytes = aBytes + p.KS * bStride;
   const int S = p.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * stageBytes);
   uint64_t* empty = full + S;
@@ -153,7 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!valid && blockIdx.x == 0 && threadIdx.x == 0 && U != 0) flag_error(p.dev_err, MOE_DEV_CAPACITY);
   const int MT = (p.M + kBM - 1) / kBM;
   const int KB = p.K / kBK;
-  const long long total = valid ? (long long)U * MT * KB : 0;
+  const int KU = (KB + p.KS - 1) / p.KS;  // pipeline units (stages) per tile
+  const long long total = valid ? (long long)U * MT * KU : 0;
   // Partition over at most `total` CTAs so that every range is non-empty and
   // the CTAs sharing a tile are exactly the consecutive owners of its k-blocks.
   const int G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
@@ -171,26 +175,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int n_issued = 0;
       for (long long x = s0; x < s1 && !*abort_flag;) {
-        const int t = static_cast<int>(x / KB);
-        const int kb0 = static_cast<int>(x - (long long)t * KB);
-        const int kb1 = static_cast<int>(kb0 + (s1 - x) < KB ? kb0 + (s1 - x) : KB);
-        x += kb1 - kb0;
+        const int t = static_cast<int>(x / KU);
+        const int u0 = static_cast<int>(x - (long long)t * KU);
+        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
+        x += u1 - u0;
         const Tile ti = tile_info(p, U, t);
         if (!ti.ok) continue;
-        const uint32_t tx = nA * kABytes + ti.np * 128;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int uu = u0; uu < u1; ++uu) {
           if (!tc::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetNs)) {
             *abort_flag = 1;
             flag_error(p.dev_err, MOE_DEV_TIMEOUT);
             break;
           }
+          const int kb = uu * p.KS;
+          const int nq = KB - kb < p.KS ? KB - kb : p.KS;
           uint8_t* sA = base + (size_t)stage * stageBytes;
-          uint8_t* sB = sA + nA * kABytes;
+          uint8_t* sB = sA + aBytes;
+          const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * ti.np * 128;
           tc::mbar_arrive_expect_tx(&full[stage], tx);
-          tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
-          if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
-          for (int j = 0; j < ti.np / 16; ++j)
-            tc::tma_load_2d(sB + j * 2048, &tmB, kb * kBK, ti.prow + 16 * j, &full[stage], polB);
+          if (p.tiled) {
+            // Tile-packed weights: block (e, m, kb) is contiguous.  gate/up:
+            // one 256-row box holds the gate tile then the up tile; down: one
+            // box of nq consecutive 16 KB k-blocks.
+            const int blk = (ti.e * MT + ti.m) * KB + kb;
+            if (kGateUp || nq == 2)
+              tc::tma_load_3d(sA, &tmA0, 0, 0, blk, &full[stage], polA);
+            else
+              tc::tma_load_3d(sA, &tmA1, 0, 0, blk, &full[stage], polA);
+          } else {
+            tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+            if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+          }
+          for (int q = 0; q < nq; ++q)
+            for (int j = 0; j < ti.np / 16; ++j)
+              tc::tma_load_2d(sB + q * bStride + j * 2048, &tmB, (kb + q) * kBK, ti.prow + 16 * j,
+                              &full[stage], polB);
           ++n_issued;
           if (++stage == S) {
             stage = 0;
@@ -210,10 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n_consumed = 0;
       bool stop = false;
       for (long long x = s0; x < s1 && !stop;) {
-        const int t = static_cast<int>(x / KB);
-        const int kb0 = static_cast<int>(x - (long long)t * KB);
-        const int kb1 = static_cast<int>(kb0 + (s1 - x) < KB ? kb0 + (s1 - x) : KB);
-        x += kb1 - kb0;
+        const int t = static_cast<int>(x / KU);
+        const int u0 = static_cast<int>(x - (long long)t * KU);
+        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
+        x += u1 - u0;
         const Tile ti = tile_info(p, U, t);
         if (!ti.ok) continue;
         if (!tc::mbar_wait_bounded(&acce[acc], acc_phase[acc] ^ 1u, abort_flag, kWaitBudgetNs)) {
@@ -224,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_after();
         const uint32_t d0 = tmem_base + acc * acc_cols;
         const uint32_t idesc = tc::idesc_bf16_f32(kBM, ti.np);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int uu = u0; uu < u1; ++uu) {
           if (!tc::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetNs)) {
             *abort_flag = 1;
             flag_error(p.dev_err, MOE_DEV_TIMEOUT);
@@ -232,14 +251,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::tc_fence_after();
+          const int nq = KB - uu * p.KS < p.KS ? KB - uu * p.KS : p.KS;
           const uint32_t aAddr = tc::smem_u32(base + (size_t)stage * stageBytes);
-          const uint32_t bAddr = aAddr + nA * kABytes;
+          const uint32_t bAddr = aAddr + aBytes;
+          for (int q = 0; q < nq; ++q) {
+            // gate/up: A = gate tile, A + 16 KB = up tile; down: k-block q at A + q * 16 KB.
+            const uint32_t aq = aAddr + (kGateUp ? 0 : q * kABytes);
+            const uint32_t bq = bAddr + q * bStride;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
-            const uint64_t bdesc = tc::smem_desc_sw128(bAddr + kk * 32);
-            tc::mma_bf16(d0, tc::smem_desc_sw128(aAddr + kk * 32), bdesc, idesc, accum);
-            if (kGateUp) tc::mma_bf16(d0 + p.NM, tc::smem_desc_sw128(aAddr + kABytes + kk * 32), bdesc, idesc, accum);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint32_t accum = (uu > u0 || q > 0 || kk > 0) ? 1u : 0u;
+              const uint64_t bdesc = tc::smem_desc_sw128(bq + kk * 32);
+              tc::mma_bf16(d0, tc::smem_desc_sw128(aq + kk * 32), bdesc, idesc, accum);
+              if (kGateUp)
+                tc::mma_bf16(d0 + p.NM, tc::smem_desc_sw128(aq + kABytes + kk * 32), bdesc, idesc, accum);
+            }
           }
           tc::mma_commit(&empty[stage]);
           ++n_consumed;
@@ -265,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int etid = threadIdx.x - 64;  // 0..127
     int acc = 0;
     uint32_t acc_phase[2] = {0, 0};
-    const int first_tile_c = KB > 0 ? static_cast<int>(s0 / KB) : 0;
+    const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
     for (long long x = s0; x < s1;) {
-      const int t = static_cast<int>(x / KB);
-      const int kb0 = static_cast<int>(x - (long long)t * KB);
-      const int kb1 = static_cast<int>(kb0 + (s1 - x) < KB ? kb0 + (s1 - x) : KB);
-      x += kb1 - kb0;
+      const int t = static_cast<int>(x / KU);
+      const int u0 = static_cast<int>(x - (long long)t * KU);
+      const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
+      x += u1 - u0;
       const Tile ti = tile_info(p, U, t);
       if (!ti.ok) {
         if (etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
@@ -285,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::named_bar_sync(1, kEpiThreads);
       if (*abort_flag) break;
       tc::tc_fence_after();
-      const bool whole = kb0 == 0 && kb1 == KB;
+      const bool whole = u0 == 0 && u1 == KU;
       const int row = ti.m * kBM + r;
       const bool row_ok = row < p.M;
       const uint32_t tacc = tmem_base + lane_off + acc * acc_cols;
@@ -332,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::named_bar_sync(1, kEpiThreads);
         const int arrived = *bcast;
-        const long long t0 = (long long)t * KB;
+        const long long t0 = (long long)t * KU;
         const int cf = static_cast<int>(seg_owner(t0, total, G));
-        const int cl = static_cast<int>(seg_owner(t0 + KB - 1, total, G));
+        const int cl = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
         tc::named_bar_sync(1, kEpiThreads);
         if (arrived == cl - cf) {
           __threadfence();
@@ -344,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) g[j] = v[j] = 0.f;
             for (int q2 = cf; q2 <= cl; ++q2) {
-              const int ft = static_cast<int>((total * q2 / G) / KB);
+              const int ft = static_cast<int>((total * q2 / G) / KU);
               const float* P2 = p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -533,15 +559,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map: dims innermost first; box {64, box_rows[, 1]}; 128B swizzle.
+// bf16 tensor map with the 128-byte swizzle; dims/box innermost first.
 bool make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-               uint32_t box_rows) {
+               const uint32_t* box_dims) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3], gstride[2];
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    box[i] = box_dims[i];
+  }
   for (int i = 0; i < rank - 1; ++i) gstride[i] = strides_bytes[i];
   CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstride, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -550,7 +578,7 @@ bool make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims
 }
 
 struct TcGeom {
-  int NM, MT_gu, MT_d, Rmax, G;
+  int NM, MT_gu, MT_d, Rmax, G, KS_d;
   int stages_gu, stages_d;
   size_t smem_gu, smem_d;
 };
@@ -568,8 +596,9 @@ TcGeom tc_geom(const moe_layer_weights& lw, int T, int k) {
   g.MT_d = (lw.H + kBM - 1) / kBM;
   g.Rmax = TK + 15 * cap;
   g.G = sm_count();
+  g.KS_d = lw.layout == MOE_LAYOUT_TILED ? 2 : 1;
   const size_t b = static_cast<size_t>(g.NM) * 128;
-  const size_t st_gu = 2 * kABytes + b, st_d = kABytes + b;
+  const size_t st_gu = 2 * kABytes + b, st_d = g.KS_d * (kABytes + b);
   g.stages_gu = static_cast<int>((kSmemLimit - kSmemExtra) / st_gu);
   g.stages_d = static_cast<int>((kSmemLimit - kSmemExtra) / st_d);
   if (g.stages_gu > 8) g.stages_gu = 8;
@@ -589,6 +618,7 @@ uint32_t pow2_cols(int c) {
 
 bool ffn_tc_supported(const moe_layer_weights& lw, int T, int k) {
   if (lw.dtype != MOE_DTYPE_BF16) return false;
+  if (lw.layout != MOE_LAYOUT_ROWMAJOR && lw.layout != MOE_LAYOUT_TILED) return false;
   if (lw.H % kBK || lw.I % kBK) return false;
   if (T < 1 || T > 256) return false;
   TcGeom g = tc_geom(lw, T, k);
@@ -631,25 +661,45 @@ int ffn_tc_launch(const FfnArgs& a) {
   const int n_counters = cap * (g.MT_gu + g.MT_d) + g.MT_d;
 
   // Tensor maps (host-side encoding only; nothing is enqueued).
-  CUtensorMap tm_g, tm_u, tm_x, tm_wd, tm_h;
+  CUtensorMap tm_g, tm_u, tm_x, tm_wd, tm_wd1, tm_h;
   const uint64_t H = lw.H, I = lw.I, E = lw.E;
-  {
-    uint64_t dims[3] = {H, I, E}, str[2] = {H * 2, 2 * I * H * 2};
-    if (!make_tmap(&tm_g, lw.w_gate_up, 3, dims, str, kBM)) return MOE_ERR_CUDA;
-    const char* up = static_cast<const char*>(lw.w_gate_up) + I * H * 2;
-    if (!make_tmap(&tm_u, up, 3, dims, str, kBM)) return MOE_ERR_CUDA;
+  const uint64_t KBg = H / kBK, KBd = I / kBK;
+  if (lw.layout == MOE_LAYOUT_TILED) {
+    {
+      uint64_t dims[3] = {kBK, 2 * kBM, E * g.MT_gu * KBg}, str[2] = {kBK * 2, 2 * kABytes};
+      uint32_t box[3] = {kBK, 2 * kBM, 1};
+      if (!make_tmap(&tm_g, lw.w_gate_up, 3, dims, str, box)) return MOE_ERR_CUDA;
+      tm_u = tm_g;  // unused: one box carries both gate and up
+    }
+    {
+      uint64_t dims[3] = {kBK, kBM, E * g.MT_d * KBd}, str[2] = {kBK * 2, kABytes};
+      uint32_t box2[3] = {kBK, kBM, 2}, box1[3] = {kBK, kBM, 1};
+      if (!make_tmap(&tm_wd, lw.w_down, 3, dims, str, box2)) return MOE_ERR_CUDA;
+      if (!make_tmap(&tm_wd1, lw.w_down, 3, dims, str, box1)) return MOE_ERR_CUDA;
+    }
+  } else {
+    uint32_t box[3] = {kBK, kBM, 1};
+    {
+      uint64_t dims[3] = {H, I, E}, str[2] = {H * 2, 2 * I * H * 2};
+      if (!make_tmap(&tm_g, lw.w_gate_up, 3, dims, str, box)) return MOE_ERR_CUDA;
+      const char* up = static_cast<const char*>(lw.w_gate_up) + I * H * 2;
+      if (!make_tmap(&tm_u, up, 3, dims, str, box)) return MOE_ERR_CUDA;
+    }
+    {
+      uint64_t dims[3] = {I, H, E}, str[2] = {I * 2, H * I * 2};
+      if (!make_tmap(&tm_wd, lw.w_down, 3, dims, str, box)) return MOE_ERR_CUDA;
+      tm_wd1 = tm_wd;
+    }
   }
   {
     uint64_t dims[2] = {H, static_cast<uint64_t>(g.Rmax)}, str[1] = {H * 2};
-    if (!make_tmap(&tm_x, xp, 2, dims, str, 16)) return MOE_ERR_CUDA;
-  }
-  {
-    uint64_t dims[3] = {I, H, E}, str[2] = {I * 2, H * I * 2};
-    if (!make_tmap(&tm_wd, lw.w_down, 3, dims, str, kBM)) return MOE_ERR_CUDA;
+    uint32_t box[2] = {kBK, 16};
+    if (!make_tmap(&tm_x, xp, 2, dims, str, box)) return MOE_ERR_CUDA;
   }
   {
     uint64_t dims[2] = {I, static_cast<uint64_t>(g.Rmax)}, str[1] = {I * 2};
-    if (!make_tmap(&tm_h, hp, 2, dims, str, 16)) return MOE_ERR_CUDA;
+    uint32_t box[2] = {kBK, 16};
+    if (!make_tmap(&tm_h, hp, 2, dims, str, box)) return MOE_ERR_CUDA;
   }
 
   cudaStream_t s = a.stream;
@@ -683,8 +733,10 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.w = a.w;
   tp.y = a.y;
   tp.dev_err = a.dev_err;
+  tp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
 
   // gate/up
+  tp.KS = 1;
   tp.M = lw.I;
   tp.K = lw.H;
   tp.stages = g.stages_gu;
@@ -702,6 +754,7 @@ int ffn_tc_launch(const FfnArgs& a) {
   }
 
   // down + combine
+  tp.KS = g.KS_d;
   tp.M = lw.H;
   tp.K = lw.I;
   tp.stages = g.stages_d;
@@ -714,7 +767,7 @@ int ffn_tc_launch(const FfnArgs& a) {
     return MOE_ERR_CUDA;
   {
     LaunchScope ls(kProfDown, s);
-    ffn_tc_kernel<false><<<g.G, kThreads, g.smem_d, s>>>(tm_wd, tm_wd, tm_h, tp);
+    ffn_tc_kernel<false><<<g.G, kThreads, g.smem_d, s>>>(tm_wd, tm_wd1, tm_h, tp);
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
   }
   return MOE_OK;

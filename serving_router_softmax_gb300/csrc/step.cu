@@ -36,7 +36,7 @@ size_t step_ws(const moe_step_cfg& c, void* base, StepWs* out) {
   size_t o_rows = take(T * 4), o_conf = take(T * 4), o_ids = take(TK * 4), o_w = take(TK * 4);
   size_t o_u = take(cap * 4), o_off = take((cap + 1) * 4), o_pt = take(TK * 4), o_ps = take(TK * 4);
   size_t o_inv = take(TK * 4), o_ratio = take(4);
-  moe_layer_weights lw{c.H, c.I, c.E, c.dtype, nullptr, nullptr, nullptr, nullptr};
+  moe_layer_weights lw{c.H, c.I, c.E, c.dtype, c.layout, nullptr, nullptr, nullptr, nullptr};
   size_t fb = ffn_workspace_bytes(lw, c.T, c.k);
   size_t o_ffn = take(fb);
   if (out) {
@@ -67,7 +67,7 @@ int step_validate(const moe_step_cfg& c) {
   moe_route_cfg rc{c.T, c.E, c.k, c.use_bias, c.cap, c.alpha};
   if ((st = route_validate(rc, true)) != MOE_OK) return st;
   if ((st = union_validate(c.T, c.k, c.E)) != MOE_OK) return st;
-  moe_layer_weights lw{c.H, c.I, c.E, c.dtype, reinterpret_cast<void*>(256),
+  moe_layer_weights lw{c.H, c.I, c.E, c.dtype, c.layout, reinterpret_cast<void*>(256),
                        reinterpret_cast<void*>(256), reinterpret_cast<float*>(256),
                        reinterpret_cast<float*>(256)};
   return ffn_validate(lw, c.T, c.k);
@@ -99,7 +99,8 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return MOE_ERR_ARG;
   for (int l = 0; l < c.L; ++l) {
     const moe_layer_weights& lw = layers[l];
-    if (lw.H != c.H || lw.I != c.I || lw.E != c.E || lw.dtype != c.dtype) return MOE_ERR_ARG;
+    if (lw.H != c.H || lw.I != c.I || lw.E != c.E || lw.dtype != c.dtype || lw.layout != c.layout)
+      return MOE_ERR_ARG;
     if ((st = ffn_validate(lw, c.T, c.k)) != MOE_OK) return st;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -53,7 +53,7 @@ def test_host_only_calls(lib):
                                                        ctypes.POINTER(L.EcoCfg)] + [ctypes.c_void_p] * 4
     assert lib.eco_select(None, None, None, 1, None, ctypes.byref(ecfg), None, None, None,
                           None) == L.MOE_ERR_UNSUPPORTED
-    lw = L.LayerWeights(100, 64, 8, 1, None, None, None, None)  # H not a multiple of 64
+    lw = L.LayerWeights(100, 64, 8, 1, 0, None, None, None, None)  # H not a multiple of 64
     lib.moe_verify_ffn_workspace.argtypes = [ctypes.POINTER(L.LayerWeights), ctypes.c_int32, ctypes.c_int32]
     lib.moe_verify_ffn_workspace.restype = ctypes.c_size_t
     assert lib.moe_verify_ffn_workspace(ctypes.byref(lw), 4, 2) == 0

@@ -34,10 +34,13 @@ def rowwise_err(y, ref):
     return float(np.max(np.max(np.abs(y - ref), axis=1) / den))
 
 
-def make_layer(mv, cfg, l):
+def make_layer(mv, cfg, l, layout="rowmajor"):
     from workload import device as wdev
     gu, dn, sgu, sdn = wdev.make_layer_tensors(cfg, l)
-    return mv.ExpertLayer(gu, dn, cfg.dtype, sgu, sdn)
+    layer = mv.ExpertLayer(gu, dn, cfg.dtype, sgu, sdn)
+    if layout == "tiled":
+        layer = mv.pack_tiled(layer)
+    return layer
 
 
 def host_experts(cfg, l):
@@ -67,12 +70,15 @@ FFN_CASES = [
 ]
 
 
-@pytest.mark.parametrize("dtype,H,I,E,k,T", FFN_CASES)
-def test_ffn_matches_oracle(mv, dtype, H, I, E, k, T):
+FFN_CASES_ALL = [c + ("rowmajor",) for c in FFN_CASES] + [c + ("tiled",) for c in FFN_CASES if c[0] == "bf16"]
+
+
+@pytest.mark.parametrize("dtype,H,I,E,k,T,layout", FFN_CASES_ALL)
+def test_ffn_matches_oracle(mv, dtype, H, I, E, k, T, layout):
     from oracle import moe_layer as ml
     from workload import gen
     cfg = gen.MoEConfig("ffn_case", L=1, H=H, E=E, k=k, I=I, dtype=dtype, seed=H + I + T)
-    layer = make_layer(mv, cfg, 0)
+    layer = make_layer(mv, cfg, 0, layout)
     rng = np.random.default_rng(T * 31 + k)
     lg = (rng.standard_normal((T, E)) - 0.1 * rng.permutation(E)).astype(np.float32)
     xs = rng.standard_normal((T, H)).astype(np.float32)
@@ -112,19 +118,52 @@ def test_ffn_device_fill_matches_host_generator(mv):
                 assert np.array_equal(layer.scales_down[e].cpu().numpy(), hw["scale_down"])
 
 
+def test_pack_tiled_layout(mv):
+    """The tiled copy holds exactly the documented block arrangement."""
+    from workload import gen
+    for H, I in [(256, 192), (192, 320)]:
+        cfg = gen.MoEConfig("packcheck", L=1, H=H, E=3, k=2, I=I, dtype="bf16", seed=H * I)
+        layer = make_layer(mv, cfg, 0)
+        tl = mv.pack_tiled(layer)
+        torch.cuda.synchronize()
+        gu = tl.gate_up.cpu().numpy().view(np.uint16)
+        dn = tl.down.cpu().numpy().view(np.uint16)
+        MTg, MTd, KBg, KBd = -(-I // 128), -(-H // 128), H // 64, I // 64
+        gu = gu.reshape(3, MTg, KBg, 256, 64)
+        dn = dn.reshape(3, MTd, KBd, 128, 64)
+        for e in range(3):
+            w = gen.expert_weights_host(cfg, 0, e)
+            g, u, d = w["gate_up"][:I], w["gate_up"][I:], w["down"]
+            ref_g = np.zeros((MTg * 128, H), np.uint16)
+            ref_u = np.zeros((MTg * 128, H), np.uint16)
+            ref_d = np.zeros((MTd * 128, I), np.uint16)
+            ref_g[:I], ref_u[:I], ref_d[:H] = g, u, d
+            for m in range(MTg):
+                for kb in range(KBg):
+                    blk = gu[e, m, kb]
+                    assert np.array_equal(blk[:128], ref_g[m * 128:(m + 1) * 128, kb * 64:(kb + 1) * 64])
+                    assert np.array_equal(blk[128:], ref_u[m * 128:(m + 1) * 128, kb * 64:(kb + 1) * 64])
+            for m in range(MTd):
+                for kb in range(KBd):
+                    assert np.array_equal(dn[e, m, kb], ref_d[m * 128:(m + 1) * 128, kb * 64:(kb + 1) * 64])
+
+
 # ------------------------------------------------------------------ whole step
-def run_step(mv, cfg, sample_tokens=None, sample_layers=None):
+def run_step(mv, cfg, sample_tokens=None, sample_layers=None, layout="rowmajor"):
     """Runs the GPU step and the oracle; returns (gpu dict, oracle dict)."""
     from oracle import verify_step as ovs
     from workload import device as wdev
     from workload import gen
     wl = gen.make_workload(cfg)
-    layers = [make_layer(mv, cfg, l) for l in range(cfg.L)]
+    layers = []
+    for l in range(cfg.L):
+        layers.append(make_layer(mv, cfg, l, layout))
+        torch.cuda.empty_cache()
     t = wdev.workload_tensors(wl)
     spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k,
                        H=cfg.H, I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()),
                        mode=cfg.mode, eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap,
-                       alpha=cfg.alpha)
+                       alpha=cfg.alpha, layout=layout)
     step = mv.VerifyStep(spec, layers)
     step(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
     torch.cuda.synchronize()
@@ -168,12 +207,15 @@ SMALL = {
 }
 
 
-@pytest.mark.parametrize("name", list(SMALL))
-def test_step_small_shapes_full_compare(mv, name):
+SMALL_CASES = [(n, "rowmajor") for n in SMALL] + [(n, "tiled") for n in SMALL if n not in ("toy", "deepseek_v3_like")]
+
+
+@pytest.mark.parametrize("name,layout", SMALL_CASES)
+def test_step_small_shapes_full_compare(mv, name, layout):
     """Every workload's routing/selection structure at reduced H/I: all outputs compared."""
     from workload import CONFIGS
     cfg = CONFIGS[name].replace(**SMALL[name])
-    wl, got, ref = run_step(mv, cfg)
+    wl, got, ref = run_step(mv, cfg, layout=layout)
     check_step(wl, got, ref, TOL[cfg.dtype])
 
 
@@ -192,5 +234,6 @@ def test_step_full_size_sampled(mv, name):
     layers = [0, cfg.L - 1] if cfg.L > 1 else [0]
     wl_T = gen.make_workload(cfg).T
     tokens = sorted({0, wl_T // 2, wl_T - 1})
-    wl, got, ref = run_step(mv, cfg, sample_tokens=tokens, sample_layers=layers)
+    layout = "tiled" if cfg.dtype == "bf16" else "rowmajor"  # as the bench runs it
+    wl, got, ref = run_step(mv, cfg, sample_tokens=tokens, sample_layers=layers, layout=layout)
     check_step(wl, got, ref, TOL[cfg.dtype], sample_tokens=tokens)

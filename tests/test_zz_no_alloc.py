@@ -78,7 +78,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(mv):
     fn.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(L.LayerWeights)] + [C.c_void_p] * 9
     fn.restype = C.c_int
     # T = 256, k = 16, E = 1024 at H = I = 8192 needs far more than 64 MiB of scratch.
-    lw = L.LayerWeights(8192, 8192, 1024, L.DTYPE_BF16, 256, 256, None, None)
+    lw = L.LayerWeights(8192, 8192, 1024, L.DTYPE_BF16, L.LAYOUT_ROWMAJOR, 256, 256, None, None)
     dummy = 256
     st = fn(dummy, 256, 16, C.byref(lw), *([dummy] * 7), None, None)
     assert st == L.MOE_ERR_UNSUPPORTED

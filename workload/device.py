@@ -35,7 +35,8 @@ def fill(t: torch.Tensor, kind: int, key: int, idx0: int = 0):
 
 
 def make_layer_tensors(cfg: gen.MoEConfig, layer: int, device="cuda"):
-    """(gate_up, down, scales_gate_up, scales_down) device tensors of one layer."""
+    """(gate_up, down, scales_gate_up, scales_down) device tensors of one layer,
+    in the row-major layout."""
     shp = gen.weight_shapes(cfg)
     keys = gen.weight_stream_keys(cfg, layer)
     tdt = {"f32": torch.float32, "bf16": torch.int16, "e4m3": torch.uint8}[cfg.dtype]
