@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/moe_verify.h"
@@ -25,6 +26,30 @@ enum ProfClass { kProfEco = 0, kProfRoute = 1, kProfUnion = 2, kProfPrep = 3, kP
 int sm_count();
 
 inline int check_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Launches `kernel`, optionally with programmatic dependent launch: the
+// kernel may start before its predecessor in the stream finishes and must
+// execute griddepcontrol.wait before touching anything the predecessor writes
+// or reads.  Every kernel of this library that is launched this way does so.
+template <typename... KArgs, typename... Args>
+int launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Grid-dependency control (no-ops for kernels launched without PDL).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void flag_error(int32_t* dev_err, int32_t bits) {
   if (dev_err) atomicOr(dev_err, bits);
@@ -64,6 +89,7 @@ struct FfnArgs {
   size_t ws_bytes;
   int32_t* dev_err;
   cudaStream_t stream;
+  bool pdl_first;           // the first FFN kernel may start before the caller's previous kernel ends
 };
 size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_validate(const moe_layer_weights& lw, int T, int k);
@@ -85,6 +111,10 @@ int route_validate(const moe_route_cfg& c, bool have_conf);
 int route_launch(const RouteArgs& a);
 
 int union_validate(int T, int k, int E);
+
+// Fused route + union for one layer of the whole step (single CTA).
+int layer_head_launch(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets,
+                      int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl);
 int union_launch(const int32_t* ids, int T, int k, int E, int32_t* n_unique, int32_t* unique,
                  int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, int32_t* inv,
                  float* reuse_ratio, int32_t* dev_err, cudaStream_t s);

@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(512) eco_kernel(
   __shared__ int bad;
   __shared__ int best_s;
 
+  pdl_trigger();  // the first layer's head may launch while selection runs
   const int s = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;

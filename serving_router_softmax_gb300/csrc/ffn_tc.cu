@@ -46,6 +46,7 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+constexpr int kCombMax = 512;     // (token, slot) pairs whose inv/w the down epilogue keeps in smem
 
 struct TcParams {
   int T, k, E, cap;
@@ -55,6 +56,7 @@ struct TcParams {
   int tiled;         // weights in the tile-packed layout (else row-major)
   int KS;            // k-blocks per pipeline stage (1, or 2 for tiled down)
   int stages;
+  int pdl;           // launched with programmatic dependent launch
   int acc_stages;
   uint32_t tmem_cols;
   const int32_t* n_unique;
@@ -74,7 +76,7 @@ struct TcParams {
 
 struct Tile {
   int u, m, e, ne, np, prow, off;
-  bool ok;
+  bool ok, prow_ok;
 };
 
 __device__ __forceinline__ long long seg_owner(long long x, long long total, int G) {
@@ -91,7 +93,25 @@ __device__ __forceinline__ Tile tile_info(const TcParams& p, int U, int t) {
   ti.np = (ti.ne + 15) & ~15;
   ti.prow = p.poff[ti.u];
   ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
-          ti.off + ti.ne <= p.T * p.k && ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
+          ti.off + ti.ne <= p.T * p.k;
+  ti.prow_ok = ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
+  return ti;
+}
+
+// The part of tile_info that does not depend on the padded group offsets
+// (written by the kernel that runs just before gate/up).
+__device__ __forceinline__ Tile tile_core(const TcParams& p, int U, int t) {
+  Tile ti;
+  ti.m = t / U;
+  ti.u = t - ti.m * U;
+  ti.e = p.unique[ti.u];
+  ti.off = p.offsets[ti.u];
+  ti.ne = p.offsets[ti.u + 1] - ti.off;
+  ti.np = (ti.ne + 15) & ~15;
+  ti.prow = -1;
+  ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
+          ti.off + ti.ne <= p.T * p.k;
+  ti.prow_ok = false;
   return ti;
 }
 
@@ -118,6 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* bcast = abort_flag + 1;
   volatile int* issued = bcast + 1;
   volatile int* consumed = issued + 1;
+  int32_t* s_inv = reinterpret_cast<int32_t*>(base + (size_t)S * stageBytes + 256);
+  float* s_w = reinterpret_cast<float*>(s_inv + kCombMax);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -168,20 +190,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Under programmatic dependent launch the weights of the first S stages
+    // are requested before the previous kernel has finished (they depend only
+    // on the expert union, complete by then); their token operand follows
+    // once griddepcontrol.wait returns.
     if (tc::elect_one()) {
       const uint64_t polA = tc::policy_evict_first();
       const uint64_t polB = tc::policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       int n_issued = 0;
+      constexpr int kMaxPend = 16;
+      int pend_t[kMaxPend], pend_kb[kMaxPend], pend_nq[kMaxPend], pend_st[kMaxPend];
+      int npend = 0;
+      bool dep_done = !p.pdl;
+      if (dep_done) tc::griddep_launch_dependents();
+      auto issue_b = [&](int t, int kb, int nq, int st) {
+        const Tile ti = tile_info(p, U, t);
+        const int prow = ti.prow_ok ? ti.prow : 0;  // bad offsets: load something in bounds, epilogue skips
+        uint8_t* sB = base + (size_t)st * stageBytes + aBytes;
+        for (int q = 0; q < nq; ++q)
+          for (int j = 0; j < ti.np / 16; ++j)
+            tc::tma_load_2d(sB + q * bStride + j * 2048, &tmB, (kb + q) * kBK, prow + 16 * j, &full[st], polB);
+      };
+      auto resolve = [&]() {
+        tc::griddep_wait();
+        tc::griddep_launch_dependents();
+        for (int i = 0; i < npend; ++i) issue_b(pend_t[i], pend_kb[i], pend_nq[i], pend_st[i]);
+        npend = 0;
+        dep_done = true;
+      };
       for (long long x = s0; x < s1 && !*abort_flag;) {
         const int t = static_cast<int>(x / KU);
         const int u0 = static_cast<int>(x - (long long)t * KU);
         const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
         x += u1 - u0;
-        const Tile ti = tile_info(p, U, t);
+        const Tile ti = tile_core(p, U, t);
         if (!ti.ok) continue;
         for (int uu = u0; uu < u1; ++uu) {
+          if (!dep_done && npend == S) resolve();
           if (!tc::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetNs)) {
             *abort_flag = 1;
             flag_error(p.dev_err, MOE_DEV_TIMEOUT);
@@ -190,7 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb = uu * p.KS;
           const int nq = KB - kb < p.KS ? KB - kb : p.KS;
           uint8_t* sA = base + (size_t)stage * stageBytes;
-          uint8_t* sB = sA + aBytes;
           const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * ti.np * 128;
           tc::mbar_arrive_expect_tx(&full[stage], tx);
           if (p.tiled) {
@@ -206,10 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
             if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
           }
-          for (int q = 0; q < nq; ++q)
-            for (int j = 0; j < ti.np / 16; ++j)
-              tc::tma_load_2d(sB + q * bStride + j * 2048, &tmB, (kb + q) * kBK, ti.prow + 16 * j,
-                              &full[stage], polB);
+          if (dep_done) {
+            issue_b(t, kb, nq, stage);
+          } else {
+            pend_t[npend] = t;
+            pend_kb[npend] = kb;
+            pend_nq[npend] = nq;
+            pend_st[npend] = stage;
+            ++npend;
+          }
           ++n_issued;
           if (++stage == S) {
             stage = 0;
@@ -217,10 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (!dep_done) resolve();
       *issued = n_issued;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    tc::griddep_wait();
     if (tc::elect_one()) {
       int stage = 0;
       uint32_t phase = 0;
@@ -233,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u0 = static_cast<int>(x - (long long)t * KU);
         const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
         x += u1 - u0;
-        const Tile ti = tile_info(p, U, t);
+        const Tile ti = tile_core(p, U, t);
         if (!ti.ok) continue;
         if (!tc::mbar_wait_bounded(&acce[acc], acc_phase[acc] ^ 1u, abort_flag, kWaitBudgetNs)) {
           *abort_flag = 1;
@@ -289,6 +342,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int etid = threadIdx.x - 64;  // 0..127
+    tc::griddep_wait();
+    const int TKc = p.T * p.k;
+    const bool comb_smem = !kGateUp && TKc <= kCombMax;
+    if (comb_smem) {
+      // The combine's routing data, staged while the first tiles stream.
+      for (int i = etid; i < TKc; i += kEpiThreads) {
+        s_inv[i] = p.inv[i];
+        s_w[i] = p.w[i];
+      }
+      tc::named_bar_sync(1, kEpiThreads);
+    }
     int acc = 0;
     uint32_t acc_phase[2] = {0, 0};
     const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
@@ -302,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
         continue;
       }
+      if (kGateUp && !ti.prow_ok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
       // Every epilogue thread waits; the outcome is made uniform through a
       // shared vote so that no thread is left behind at a named barrier.
       if (!tc::mbar_wait_bounded(&accf[acc], acc_phase[acc], abort_flag, kWaitBudgetNs)) {
@@ -326,10 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             const int n = cc * 16 + j;
             if (n < ti.ne && row_ok) {
-              if (kGateUp)
-                p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
-              else
+              if (kGateUp) {
+                if (ti.prow_ok)
+                  p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
+              } else {
                 p.o[(size_t)(ti.off + n) * p.M + row] = g[j];
+              }
             }
           }
         } else {
@@ -382,10 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 16; ++j) {
               const int n = cc * 16 + j;
               if (n < ti.ne && row_ok) {
-                if (kGateUp)
-                  p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
-                else
+                if (kGateUp) {
+                  if (ti.prow_ok)
+                    p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
+                } else {
                   p.o[(size_t)(ti.off + n) * p.M + row] = g[j];
+                }
               }
             }
           }
@@ -405,26 +474,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (done == U - 1) {
           __threadfence();
           const int TK = p.T * p.k;
-          for (int tok = 0; tok < p.T && row_ok; ++tok) {
-            // All k loads of a token in flight at once; sum in slot order.
-            int pos[16];
-            float wv[16], ov[16];
+          // Two tokens per round, all their slots' loads in flight at once;
+          // each token's sum runs over its slots in order.
+          for (int tb = 0; tb < p.T && row_ok; tb += 2) {
+            int pos[2][16];
+            float wv[2][16], ov[2][16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              pos[j] = j < p.k ? __ldg(&p.inv[tok * p.k + j]) : -1;
-              wv[j] = j < p.k ? __ldg(&p.w[tok * p.k + j]) : 0.f;
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int tok = tb + a;
+                const bool in = tok < p.T && j < p.k;
+                const int idx = tok * p.k + j;
+                pos[a][j] = in ? (comb_smem ? s_inv[idx] : __ldg(&p.inv[idx])) : -1;
+                wv[a][j] = in ? (comb_smem ? s_w[idx] : __ldg(&p.w[idx])) : 0.f;
+              }
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const bool ok = pos[a][j] >= 0 && pos[a][j] < TK;
+                if (tb + a < p.T && j < p.k && !ok) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+                ov[a][j] = ok ? __ldcg(&p.o[(size_t)pos[a][j] * p.M + row]) : 0.f;
+              }
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              if (tb + a >= p.T) break;
+              float s = 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < p.k && pos[a][j] >= 0 && pos[a][j] < TK) s = fmaf(wv[a][j], ov[a][j], s);
+              p.y[(size_t)(tb + a) * p.M + row] = s;
             }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const bool ok = pos[j] >= 0 && pos[j] < TK;
-              if (j < p.k && !ok) flag_error(p.dev_err, MOE_DEV_BAD_ID);
-              ov[j] = ok ? __ldcg(&p.o[(size_t)pos[j] * p.M + row]) : 0.f;
-            }
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j < p.k && pos[j] >= 0 && pos[j] < TK) s = fmaf(wv[j], ov[j], s);
-            p.y[(size_t)tok * p.M + row] = s;
           }
         }
       }
@@ -461,6 +542,8 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
                                                        float* __restrict__ y, int32_t* dev_err) {
   __shared__ int32_t spoff[1025];
   __shared__ int s_bad;
+  pdl_wait();
+  pdl_trigger();
   const int TK = T * k;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x)
     counters[i] = 0;
@@ -497,7 +580,10 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
       spoff[u] = ex;
       ex += ((offsets[u + 1] - offsets[u]) + 15) & ~15;
     }
-    if (lane == 31) spoff[U] = ex;
+    if (lane == 31) {
+      spoff[U] = ex;
+      if (offsets[U] != TK || offsets[0] != 0) s_bad = 1;
+    }
   }
   __syncthreads();
   if (s_bad) {
@@ -509,38 +595,36 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
   }
   if (blockIdx.x == 0)
     for (int u = threadIdx.x; u <= U; u += blockDim.x) poff[u] = spoff[u];
-  // Copy / zero-fill: one 16-byte chunk per thread-iteration.
-  const int R = spoff[U];
+  // Gather the real token rows only (one 16-byte chunk per thread-iteration).
+  // Pad rows of a group are left as they are: a pad row of the B operand only
+  // feeds accumulator columns the epilogue never stores.
+  const int TKn = offsets[U];
   const int cpr = H / 8;  // chunks per row
-  const long long chunks = (long long)R * cpr;
+  const long long chunks = (long long)TKn * cpr;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < chunks;
        i += (long long)gridDim.x * blockDim.x) {
-    const int rr = static_cast<int>(i / cpr);
-    const int ch = static_cast<int>(i - (long long)rr * cpr);
-    // group of padded row rr: largest u with spoff[u] <= rr
+    const int pp = static_cast<int>(i / cpr);  // perm position
+    const int ch = static_cast<int>(i - (long long)pp * cpr);
+    // group of perm position pp: largest u with offsets[u] <= pp
     int lo = 0, hi = U - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (spoff[mid] <= rr) lo = mid;
+      if (offsets[mid] <= pp) lo = mid;
       else hi = mid - 1;
     }
-    const int n = rr - spoff[lo];
-    const int ne = offsets[lo + 1] - offsets[lo];
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (n < ne) {
-      const int tok = perm_token[offsets[lo] + n];
-      bool ok = tok >= 0 && tok < T;
-      int row = tok;
-      if (ok && x_rows) {
-        row = x_rows[tok];
-        ok = row >= 0 && row < x_rows_limit;
-      }
-      if (ok)
-        v = *reinterpret_cast<const uint4*>(x + (size_t)row * H + ch * 8);
-      else
-        flag_error(dev_err, MOE_DEV_BAD_ID);
+    const int rr = spoff[lo] + (pp - offsets[lo]);
+    const int tok = perm_token[pp];
+    bool ok = tok >= 0 && tok < T;
+    int row = tok;
+    if (ok && x_rows) {
+      row = x_rows[tok];
+      ok = row >= 0 && row < x_rows_limit;
     }
-    *reinterpret_cast<uint4*>(xp + (size_t)rr * H + ch * 8) = v;
+    if (ok)
+      *reinterpret_cast<uint4*>(xp + (size_t)rr * H + ch * 8) =
+          *reinterpret_cast<const uint4*>(x + (size_t)row * H + ch * 8);
+    else
+      flag_error(dev_err, MOE_DEV_BAD_ID);
   }
 }
 
@@ -584,7 +668,7 @@ struct TcGeom {
 };
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kSmemExtra = 1024 /*align*/ + 256 /*barriers & flags*/;
+constexpr size_t kSmemExtra = 1024 /*align*/ + 256 /*barriers & flags*/ + 8 * kCombMax /*combine inv/w*/;
 
 TcGeom tc_geom(const moe_layer_weights& lw, int T, int k) {
   TcGeom g;
@@ -709,10 +793,10 @@ int ffn_tc_launch(const FfnArgs& a) {
     if (blocks > g.G * 4) blocks = g.G * 4;
     if (blocks < 1) blocks = 1;
     LaunchScope ls(kProfPrep, s);
-    ffn_prep_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, k,
-                                           lw.H, cap, a.n_unique, a.offsets, a.perm_token, xp, poff, cnt_gu,
-                                           n_counters, a.y, a.dev_err);
-    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_k(ffn_prep_kernel, dim3(blocks), dim3(256), 0, s, a.pdl_first,
+                 static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, k, lw.H, cap, a.n_unique,
+                 a.offsets, a.perm_token, xp, poff, cnt_gu, n_counters, a.y, a.dev_err) != MOE_OK)
+      return MOE_ERR_CUDA;
   }
 
   TcParams tp{};
@@ -734,6 +818,7 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.y = a.y;
   tp.dev_err = a.dev_err;
   tp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
+  tp.pdl = 1;
 
   // gate/up
   tp.KS = 1;
@@ -749,8 +834,9 @@ int ffn_tc_launch(const FfnArgs& a) {
     return MOE_ERR_CUDA;
   {
     LaunchScope ls(kProfGateUp, s);
-    ffn_tc_kernel<true><<<g.G, kThreads, g.smem_gu, s>>>(tm_g, tm_u, tm_x, tp);
-    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_k(ffn_tc_kernel<true>, dim3(g.G), dim3(kThreads), g.smem_gu, s, true, tm_g, tm_u, tm_x, tp) !=
+        MOE_OK)
+      return MOE_ERR_CUDA;
   }
 
   // down + combine
@@ -767,8 +853,9 @@ int ffn_tc_launch(const FfnArgs& a) {
     return MOE_ERR_CUDA;
   {
     LaunchScope ls(kProfDown, s);
-    ffn_tc_kernel<false><<<g.G, kThreads, g.smem_d, s>>>(tm_wd, tm_wd1, tm_h, tp);
-    if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_k(ffn_tc_kernel<false>, dim3(g.G), dim3(kThreads), g.smem_d, s, true, tm_wd, tm_wd1, tm_h, tp) !=
+        MOE_OK)
+      return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }

@@ -1,0 +1,252 @@
+// Device-side routing building blocks shared by the moe_route kernels and the
+// fused layer-head kernel of the whole step.
+//
+// Routing: EcoSpec write-up, section 3.1 (softmax over the gate logits, top-K
+// per layer).  Reuse bias: S2-MoE write-up, component 2 (steps 1-3, Fig. 5).
+// One warp owns one token; each lane keeps ceil(E/32) logits in registers and
+// the top-k is k rounds of a warp-wide arg-max over a strict total order
+// (larger value, then lower id).
+#pragma once
+
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+
+namespace moe {
+namespace routing {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kMaxK = 16;
+
+template <int NPL>
+struct Row {
+  float v[NPL];
+  uint32_t taken;
+};
+
+// Loads one logits row; with `estar` set, adds lam to the preferred experts
+// (fp32 add, no contraction).  Returns true if any value is NaN.
+template <int NPL>
+__device__ __forceinline__ bool load_row(const float* __restrict__ row, int E, int lane, Row<NPL>& r,
+                                         const uint32_t* estar, float lam) {
+  bool nan = false;
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    int e = lane + 32 * j;
+    float x = -INFINITY;
+    if (e < E) {
+      x = row[e];
+      nan |= (x != x);
+      if (estar && ((estar[e >> 5] >> (e & 31)) & 1u)) x = __fadd_rn(x, lam);
+    }
+    r.v[j] = x;
+  }
+  r.taken = 0;
+  return __any_sync(kFull, nan);
+}
+
+// One arg-max round over the not-yet-taken entries; every lane gets the result.
+template <int NPL>
+__device__ __forceinline__ void argmax_round(Row<NPL>& r, int E, int lane, float& bv, int& bi) {
+  float lv = -INFINITY;
+  int li = INT_MAX;
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    int e = lane + 32 * j;
+    if (e < E && !((r.taken >> j) & 1u) && topk_better(r.v[j], e, lv, li)) {
+      lv = r.v[j];
+      li = e;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float ov = __shfl_xor_sync(kFull, lv, off);
+    int oi = __shfl_xor_sync(kFull, li, off);
+    if (topk_better(ov, oi, lv, li)) {
+      lv = ov;
+      li = oi;
+    }
+  }
+  if (li != INT_MAX && (li & 31) == lane) r.taken |= 1u << (li >> 5);
+  bv = lv;
+  bi = li;
+}
+
+// Top-k of a loaded row and softmax over the selected logits; writes the
+// token's ids and weights.  The weight sum runs over j = 0..k-1 in order.
+template <int NPL>
+__device__ __forceinline__ void topk_softmax_write(Row<NPL>& r, int E, int k, int lane, int32_t* ids,
+                                                   float* w) {
+  float sv[kMaxK];
+  int si[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < k) argmax_round(r, E, lane, sv[j], si[j]);
+  }
+  const float m = sv[0];
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k) s = __fadd_rn(s, expf(sv[j] - m));
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j < k && lane == j) {
+      ids[j] = si[j];
+      w[j] = __fdiv_rn(expf(sv[j] - m), s);
+    }
+  }
+}
+
+__device__ __forceinline__ void write_invalid(int k, int lane, int32_t* ids, float* w) {
+  for (int j = lane; j < k; j += 32) {
+    ids[j] = -1;
+    w[j] = 0.f;
+  }
+}
+
+// Plain routing: warps [warp0, warp0 + nwarps) of the grid loop over tokens.
+template <int NPL>
+__device__ __forceinline__ void route_plain_warps(const float* __restrict__ logits, const int32_t* __restrict__ rows,
+                                                  int rows_limit, int T, int E, int k, int32_t* __restrict__ ids,
+                                                  float* __restrict__ w, int32_t* dev_err, int warp, int nwarps) {
+  const int lane = threadIdx.x & 31;
+  for (int t = warp; t < T; t += nwarps) {
+    const long long row = rows ? rows[t] : t;
+    if (rows && (row < 0 || row >= rows_limit)) {
+      if (lane == 0) flag_error(dev_err, MOE_DEV_CAPACITY);
+      write_invalid(k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+      continue;
+    }
+    Row<NPL> r;
+    bool nan = load_row<NPL>(logits + row * E, E, lane, r, nullptr, 0.f);
+    if (nan) {
+      if (lane == 0) flag_error(dev_err, MOE_DEV_NAN_LOGIT);
+      write_invalid(k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+      continue;
+    }
+    topk_softmax_write<NPL>(r, E, k, lane, ids + (size_t)t * k, w + (size_t)t * k);
+  }
+}
+
+constexpr int kBiasMaxT = 256;
+constexpr int kMaxEW = 32;  // 1024 experts / 32
+
+struct BiasSmem {
+  uint32_t member[kBiasMaxT * kMaxEW];  // [t][EW] top-k membership bits
+  float v1[kBiasMaxT], vk1[kBiasMaxT];
+  uint8_t bad[kBiasMaxT];
+  float g[1024];
+  uint32_t estar[kMaxEW];
+  int conf_bad;
+};
+
+// Biased routing over the whole block (T <= 256, E <= 1024).  All threads of
+// the block must call it; it synchronises the block.
+template <int NPL>
+__device__ __forceinline__ void route_bias_block(const float* __restrict__ logits, const int32_t* __restrict__ rows,
+                                 int rows_limit, const float* __restrict__ w_conf, int T, int E, int k, int cap,
+                                 float alpha, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* dev_err,
+                                 BiasSmem& sm) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int EW = (E + 31) >> 5;
+
+  if (threadIdx.x == 0) sm.conf_bad = 0;
+  for (int i = threadIdx.x; i < kMaxEW; i += blockDim.x) sm.estar[i] = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    float c = w_conf[t];
+    if (!(c >= 0.f)) sm.conf_bad = 1;  // NaN or negative
+  }
+  // Pass 1: original top-(k+1) per token -> membership of TopK, l_(1), l_(k+1).
+  for (int t = warp; t < T; t += nwarps) {
+    const long long row = rows ? rows[t] : t;
+    for (int i = lane; i < EW; i += 32) sm.member[t * EW + i] = 0;
+    if (rows && (row < 0 || row >= rows_limit)) {
+      if (lane == 0) sm.bad[t] = 2;
+      continue;
+    }
+    Row<NPL> r;
+    bool nan = load_row<NPL>(logits + row * E, E, lane, r, nullptr, 0.f);
+    if (lane == 0) sm.bad[t] = nan ? 1 : 0;
+    if (nan) continue;
+    __syncwarp();
+    for (int j = 0; j <= k; ++j) {
+      float bv;
+      int bi;
+      argmax_round(r, E, lane, bv, bi);
+      if (lane == 0) {
+        if (j == 0) sm.v1[t] = bv;
+        if (j == k) sm.vk1[t] = bv;
+        if (j < k) sm.member[t * EW + (bi >> 5)] |= 1u << (bi & 31);
+      }
+    }
+  }
+  __syncthreads();
+  const bool conf_bad = sm.conf_bad != 0;
+  if (!conf_bad) {
+    // Step 1: g_e = sum over tokens (ascending) of w_b for tokens whose top-k holds e.
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float acc = 0.f;
+      for (int b = 0; b < T; ++b)
+        if (!sm.bad[b] && ((sm.member[b * EW + (e >> 5)] >> (e & 31)) & 1u)) acc = __fadd_rn(acc, w_conf[b]);
+      sm.g[e] = acc;
+    }
+  }
+  __syncthreads();
+  // Step 2: E* = top-cap experts by g among g > 0 (ties: lower id).
+  if (!conf_bad && warp == 0) {
+    uint32_t taken = 0;  // bit j: expert lane + 32 j
+    for (int c = 0; c < cap; ++c) {
+      float lv = -INFINITY;
+      int li = INT_MAX;
+      for (int j = 0; j < EW; ++j) {
+        int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && sm.g[e] > 0.f && topk_better(sm.g[e], e, lv, li)) {
+          lv = sm.g[e];
+          li = e;
+        }
+      }
+      for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(kFull, lv, off);
+        int oi = __shfl_xor_sync(kFull, li, off);
+        if (topk_better(ov, oi, lv, li)) {
+          lv = ov;
+          li = oi;
+        }
+      }
+      if (li == INT_MAX) break;  // no expert left with g > 0
+      if ((li & 31) == lane) taken |= 1u << (li >> 5);
+      if (lane == 0) sm.estar[li >> 5] |= 1u << (li & 31);
+    }
+  }
+  __syncthreads();
+  if (conf_bad) {
+    if (threadIdx.x == 0) flag_error(dev_err, MOE_DEV_BAD_PROB);
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+      ids[i] = -1;
+      w[i] = 0.f;
+    }
+    return;
+  }
+  // Step 3 + routing on the biased logits.
+  for (int t = warp; t < T; t += nwarps) {
+    int32_t* ti = ids + (size_t)t * k;
+    float* tw = w + (size_t)t * k;
+    if (sm.bad[t]) {
+      if (lane == 0) flag_error(dev_err, sm.bad[t] == 2 ? MOE_DEV_CAPACITY : MOE_DEV_NAN_LOGIT);
+      write_invalid(k, lane, ti, tw);
+      continue;
+    }
+    const float lam = __fmul_rn(alpha, __fsub_rn(sm.v1[t], sm.vk1[t]));
+    const long long row = rows ? rows[t] : t;
+    Row<NPL> r;
+    load_row<NPL>(logits + row * E, E, lane, r, sm.estar, lam);
+    topk_softmax_write<NPL>(r, E, k, lane, ti, tw);
+  }
+}
+
+}  // namespace routing
+}  // namespace moe

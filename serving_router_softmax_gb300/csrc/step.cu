@@ -117,14 +117,13 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     RouteArgs ra{node_logits + static_cast<size_t>(l) * rows * c.E, ws.verify_rows, rows,
                  c.use_bias ? ws.verify_conf : nullptr, {c.T, c.E, c.k, c.use_bias, c.cap, c.alpha},
                  ws.ids, ws.w, dev_err, s};
-    if ((st = route_launch(ra)) != MOE_OK) return st;
-    if ((st = union_launch(ws.ids, c.T, c.k, c.E, n_unique + l, ws.unique, ws.offsets, ws.perm_token,
-                           ws.perm_slot, ws.inv, ws.ratio, dev_err, s)) != MOE_OK)
+    if ((st = layer_head_launch(ra, n_unique + l, ws.unique, ws.offsets, ws.perm_token, ws.perm_slot, ws.inv,
+                                ws.ratio, true)) != MOE_OK)
       return st;
     FfnArgs fa{static_cast<const char*>(node_x) + static_cast<size_t>(l) * rows * c.H * xelem,
                ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
                ws.perm_token, ws.inv, ws.w, y + static_cast<size_t>(l) * c.T * c.H, ws.ffn,
-               ws.ffn_bytes, dev_err, s};
+               ws.ffn_bytes, dev_err, s, true};
     if ((st = ffn_launch(fa)) != MOE_OK) return st;
   }
   return MOE_OK;

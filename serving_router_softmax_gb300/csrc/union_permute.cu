@@ -11,11 +11,12 @@
 // rank inside its expert group (popcount of the expert's column over earlier
 // tokens), so the permutation is deterministic and needs no sort.
 #include "common.cuh"
+#include "union_dev.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kMaxE = 1024;
+constexpr int kMaxE = unions::kMaxE;
 constexpr int kMaxWords = 32768;  // T * ceil(E/32) bitmap words (128 KB)
 
 __global__ void __launch_bounds__(1024) union_kernel(const int32_t* __restrict__ ids, int T, int k,
@@ -28,92 +29,9 @@ __global__ void __launch_bounds__(1024) union_kernel(const int32_t* __restrict__
                                                      float* __restrict__ reuse_ratio,
                                                      int32_t* dev_err) {
   extern __shared__ uint32_t member[];  // [T][EW]
-  __shared__ int32_t count[kMaxE];
-  __shared__ int32_t ustart[kMaxE];     // expert -> first perm position of its group
-  __shared__ int err;
-
-  const int EW = (E + 31) >> 5;
-  const int TK = T * k;
-  for (int i = threadIdx.x; i < T * EW; i += blockDim.x) member[i] = 0;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) count[e] = 0;
-  if (threadIdx.x == 0) err = 0;
-  __syncthreads();
-
-  for (int p = threadIdx.x; p < TK; p += blockDim.x) {
-    int t = p / k;
-    int e = ids[p];
-    if (e < 0 || e >= E) {
-      atomicOr(&err, MOE_DEV_BAD_ID);
-      continue;
-    }
-    uint32_t bit = 1u << (e & 31);
-    uint32_t old = atomicOr(&member[t * EW + (e >> 5)], bit);
-    if (old & bit) atomicOr(&err, MOE_DEV_DUP_ID);
-    atomicAdd(&count[e], 1);
-  }
-  __syncthreads();
-  if (err) {
-    if (threadIdx.x == 0) {
-      flag_error(dev_err, err);
-      *n_unique = 0;
-      *reuse_ratio = 0.f;
-    }
-    return;
-  }
-
-  // Union + group starts: warp 0 scans experts in ascending order.
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per;
-    int nz = 0, tok = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e) {
-      nz += count[e] > 0;
-      tok += count[e];
-    }
-    int nz_ex = nz, tok_ex = tok;  // inclusive -> exclusive scan
-    for (int off = 1; off < 32; off <<= 1) {
-      int a = __shfl_up_sync(0xFFFFFFFFu, nz_ex, off);
-      int b = __shfl_up_sync(0xFFFFFFFFu, tok_ex, off);
-      if (lane >= off) {
-        nz_ex += a;
-        tok_ex += b;
-      }
-    }
-    nz_ex -= nz;
-    tok_ex -= tok;
-    for (int e = e0; e < e0 + per && e < E; ++e) {
-      if (count[e] > 0) {
-        ustart[e] = tok_ex;
-        unique[nz_ex] = e;
-        offsets[nz_ex] = tok_ex;
-        ++nz_ex;
-        tok_ex += count[e];
-      }
-    }
-    if (lane == 31) {
-      offsets[nz_ex] = tok_ex;  // == T*k
-      *n_unique = nz_ex;
-      *reuse_ratio = TK > 0 ? __fdiv_rn(static_cast<float>(nz_ex), static_cast<float>(TK)) : 0.f;
-    }
-  }
-  __syncthreads();
-
-  // Permutation: rank of token t in expert e's group = set bits of column e
-  // over tokens t' < t.
-  for (int p = threadIdx.x; p < TK; p += blockDim.x) {
-    int t = p / k;
-    int j = p - t * k;
-    int e = ids[p];
-    int word = e >> 5;
-    uint32_t bit = 1u << (e & 31);
-    int rank = 0;
-    for (int tt = 0; tt < t; ++tt) rank += (member[tt * EW + word] & bit) ? 1 : 0;
-    int pos = ustart[e] + rank;
-    perm_token[pos] = t;
-    perm_slot[pos] = j;
-    inv[p] = pos;
-  }
+  __shared__ unions::UnionSmem us;
+  unions::union_block(ids, T, k, E, member, us, n_unique, unique, offsets, perm_token, perm_slot, inv,
+                      reuse_ratio, dev_err);
 }
 
 }  // namespace
