@@ -210,14 +210,14 @@ def ours(args, rank, ws, local):
     wl = gen.make_workload(cfg)
     # Weights: filled row-major, then packed once into the tiled layout the
     # tensor-core FFN streams (bf16); a load-time step outside every timed region.
-    layout = "tiled" if cfg.dtype == "bf16" else "rowmajor"
+    layout = "tiled" if cfg.dtype in ("bf16", "e4m3") else "rowmajor"
     layers = []
     for l in range(cfg.L):
         gu, dn, sgu, sdn = wdev.make_layer_tensors(cfg, l, dev)
         layer = mv.ExpertLayer(gu, dn, cfg.dtype, sgu, sdn)
         if layout == "tiled":
             layer = mv.pack_tiled(layer)
-            del gu, dn
+            del gu, dn, sgu, sdn
             torch.cuda.synchronize()
             torch.cuda.empty_cache()
         layers.append(layer)

@@ -136,15 +136,17 @@ int moe_union_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E,
  *   [E, H/128, I/128] fp32; weight (r, c) of a matrix is code(r, c) *
  *   scale[r/128, c/128].  NULL for the other dtypes.
  *
- * MOE_LAYOUT_TILED (bf16 only; made once at load time by moe_pack_tiled):
- * blocks of 64 reduction columns, each block contiguous, so that every
- * pipeline stage of the FFN reads one 32 KB contiguous piece of HBM.
- *   w_gate_up [E][MTg][H/64][256][64], MTg = ceil(I/128): block (e, m, kb)
- *     holds rows m*128 .. m*128+127 of W_gate (columns kb*64 .. kb*64+63)
+ * MOE_LAYOUT_TILED (bf16 or FP8; made once at load time by moe_pack_tiled):
+ * blocks of 128 bytes of the reduction dimension (C = 64 bf16 or 128 FP8
+ * values), each block contiguous, so that every pipeline stage of the FFN
+ * reads one 32 KB contiguous piece of HBM.
+ *   w_gate_up [E][MTg][H/C][256][C], MTg = ceil(I/128): block (e, m, kb)
+ *     holds rows m*128 .. m*128+127 of W_gate (columns kb*C .. kb*C+C-1)
  *     followed by the same rows of W_up; rows >= I are zero.
- *   w_down [E][MTd][I/64][128][64], MTd = ceil(H/128): block (e, m, kb)
- *     holds rows m*128 .. m*128+127 of W_down, columns kb*64 .. +63; rows
+ *   w_down [E][MTd][I/C][128][C], MTd = ceil(H/128): block (e, m, kb)
+ *     holds rows m*128 .. m*128+127 of W_down, columns kb*C .. +C-1; rows
  *     >= H are zero.
+ *   FP8 block scales keep their row-major shape.
  *
  * Pointers must be 16-byte aligned.  Limits: H and I multiples of 64
  * (of 128 for FP8), E <= 1024.
@@ -159,15 +161,16 @@ typedef struct {
   const float* scales_down;
 } moe_layer_weights;
 
-/* Bytes of the tiled copies of one layer's bf16 weights (gate/up and down,
+/* Bytes of the tiled copies of one layer's bf16 or FP8 weights (gate/up and down,
  * written to *gate_up_bytes / *down_bytes when not NULL); returns their sum,
  * or 0 if the layer cannot be tiled. */
 size_t moe_tiled_bytes(const moe_layer_weights* lw, size_t* gate_up_bytes, size_t* down_bytes);
 
-/* Packs one layer's row-major bf16 weights (src->layout must be ROWMAJOR)
+/* Packs one layer's row-major bf16 or FP8 weights (src->layout must be ROWMAJOR)
  * into the MOE_LAYOUT_TILED layout at dst_gate_up / dst_down (caller-owned
  * device buffers of the sizes moe_tiled_bytes reports, 16-byte aligned, not
- * overlapping src).  A load-time step; enqueued on `stream`. */
+ * overlapping src).  FP8 scales are not copied: the tiled layer points at
+ * the same scale tensors.  A load-time step; enqueued on `stream`. */
 int moe_pack_tiled(const moe_layer_weights* src, void* dst_gate_up, void* dst_down, void* stream);
 
 /* Bytes of workspace moe_verify_ffn needs for T tokens with top-k routing. */
@@ -187,8 +190,12 @@ size_t moe_verify_ffn_workspace(const moe_layer_weights* lw, int32_t T, int32_t 
  *            moe_union_permute for the same ids.
  *   w        [T, k] fp32 routing weights.
  *   y        [T, H] fp32 out.  The combine sums slots j = 0..k-1 in order.
- * Arithmetic: fp32 accumulation; for bf16/FP8 weights the SwiGLU
- * intermediate is rounded to bf16 before the down projection.
+ * Arithmetic: fp32 accumulation.  bf16 weights: tensor cores on bf16
+ * operands; the SwiGLU intermediate is rounded to bf16.  FP8 weights with
+ * T <= 32: tensor cores on E4M3 operands, activations and the intermediate
+ * carried as a per-row-scaled E4M3 pair hi + lo/16 (relative error near
+ * 2^-8), block scales applied exactly in fp32 per 128-column block; larger T
+ * uses CUDA cores with exact decoding.  fp32 weights: CUDA cores.
  * Limits: 1 <= T <= 256, 1 <= k <= 16.
  * Device errors: MOE_DEV_CAPACITY (n_unique > min(E, T*k)), MOE_DEV_BAD_ID.
  */

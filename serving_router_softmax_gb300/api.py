@@ -97,17 +97,22 @@ class ExpertLayer:
 def pack_tiled(layer: ExpertLayer, stream=None) -> ExpertLayer:
     """Load-time repack of a row-major bf16 layer into the tiled layout."""
     lib = L.load()
-    if layer.layout != "rowmajor" or layer.dtype != "bf16":
-        raise MoEError("pack_tiled needs a row-major bf16 layer")
+    if layer.layout != "rowmajor" or layer.dtype not in ("bf16", "e4m3"):
+        raise MoEError("pack_tiled needs a row-major bf16 or FP8 layer")
     st = layer.struct()
     gu_b, dn_b = C.c_size_t(0), C.c_size_t(0)
     if lib.moe_tiled_bytes(C.byref(st), C.byref(gu_b), C.byref(dn_b)) == 0:
         raise MoEError("layer shape cannot be tiled")
     dev = layer.gate_up.device
-    gu = torch.empty(gu_b.value // 2, dtype=torch.int16, device=dev)
-    dn = torch.empty(dn_b.value // 2, dtype=torch.int16, device=dev)
+    if layer.dtype == "bf16":
+        gu = torch.empty(gu_b.value // 2, dtype=torch.int16, device=dev)
+        dn = torch.empty(dn_b.value // 2, dtype=torch.int16, device=dev)
+    else:
+        gu = torch.empty(gu_b.value, dtype=torch.uint8, device=dev)
+        dn = torch.empty(dn_b.value, dtype=torch.uint8, device=dev)
     _check(lib.moe_pack_tiled(C.byref(st), _ptr(gu), _ptr(dn), _stream(stream)), "moe_pack_tiled")
-    return ExpertLayer(gu, dn, "bf16", layout="tiled", dims=(layer.H, layer.I, layer.E))
+    return ExpertLayer(gu, dn, layer.dtype, layer.scales_gate_up, layer.scales_down, layout="tiled",
+                       dims=(layer.H, layer.I, layer.E))
 
 
 # ------------------------------------------------------------------ calls

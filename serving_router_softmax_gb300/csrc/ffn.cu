@@ -19,6 +19,7 @@ size_t ffn_simt_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
 
 size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
   if (ffn_tc_supported(lw, T, k)) return ffn_tc_workspace_bytes(lw, T, k);
+  if (ffn_fp8_supported(lw, T, k)) return ffn_fp8_workspace_bytes(lw, T, k);
   return ffn_simt_workspace_bytes(lw, T, k);
 }
 
@@ -40,7 +41,7 @@ int ffn_validate(const moe_layer_weights& lw, int T, int k) {
   const int mult = lw.dtype == MOE_DTYPE_E4M3_B128 ? 128 : 64;
   if (lw.H % mult || lw.I % mult) return MOE_ERR_UNSUPPORTED;
   if (lw.layout != MOE_LAYOUT_ROWMAJOR && lw.layout != MOE_LAYOUT_TILED) return MOE_ERR_ARG;
-  if (lw.layout == MOE_LAYOUT_TILED && lw.dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (lw.layout == MOE_LAYOUT_TILED && lw.dtype == MOE_DTYPE_F32) return MOE_ERR_UNSUPPORTED;
   if (!lw.w_gate_up || !lw.w_down) return MOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(lw.w_gate_up) | reinterpret_cast<uintptr_t>(lw.w_down)) & 15)
     return MOE_ERR_ARG;
@@ -53,6 +54,7 @@ int ffn_launch(const FfnArgs& a) {
   if (a.ws_bytes < ffn_workspace_bytes(a.lw, a.T, a.k) || !a.ws) return MOE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(a.ws) & 255) return MOE_ERR_ARG;
   if (ffn_tc_supported(a.lw, a.T, a.k)) return ffn_tc_launch(a);
+  if (ffn_fp8_supported(a.lw, a.T, a.k)) return ffn_fp8_launch(a);
   if (a.lw.layout != MOE_LAYOUT_ROWMAJOR) return MOE_ERR_UNSUPPORTED;  // CUDA-core path reads row-major only
   FfnWorkspace ws = ffn_carve(a.lw, a.T, a.k, a.ws);
   return ffn_simt_launch(a, ws);

@@ -1,0 +1,937 @@
+// moe_verify_ffn, tensor-core path for FP8 E4M3 weights with fp32 block scales
+// (one scale per 128 x 128 block of each expert matrix).
+//
+// Same method as the bf16 path (the union's experts are each streamed from HBM
+// once; EcoSpec write-up, sections 1-2), with the 8-bit operands fed straight
+// to tcgen05.mma kind::f8f6f4:
+//   * A = E4M3 weights exactly as stored: 128 rows x 128 reduction bytes per
+//     k-block, TMA-loaded with the 128-byte swizzle.
+//   * B = activations as two E4M3 matrices per row: with a per-row scale s,
+//     hi = e4m3(x / s) and lo = e4m3((x / s - hi) * 16), so that
+//     x ~= s * (hi + lo / 16) with relative error near 2^-8.  hi and lo rows
+//     are stacked, so one MMA of N = 2 * np produces both partial products.
+//   * The weight block scale changes every 128 reduction elements, so every
+//     k-block is multiplied into its own TMEM buffer (4 in rotation) and the
+//     epilogue warps promote it: acc += w_scale * s * (d_hi + d_lo / 16), in
+//     fp32 registers.
+//   * gate/up writes h = silu(gate) * up quantized the same way, with one
+//     scale per (token, 128-row block of I), which is exactly one k-block of
+//     the down projection.
+// Stream-K partitioning over the layer's k-blocks, the last-arriver fixup of
+// split tiles and the fused weighted combine follow the bf16 kernel.
+#include <cuda_fp8.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ffn_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;           // weight rows per tile (MMA M)
+constexpr int kBK = 128;           // reduction elements (bytes) per k-block
+constexpr int kABytes = kBM * kBK;  // 16 KB
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kNB = 4;             // TMEM promotion buffers
+constexpr int kMaxNM = 32;         // padded token columns handled by this path
+constexpr int kCombMax = 512;
+constexpr float kLoScale = 16.f;
+constexpr float kE4M3Max = 448.f;
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;
+constexpr int kBarRegion = 512;    // mbarriers + flags of the CTA
+static_assert((2 * 12 + 2 * kNB + 1) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
+
+struct Fp8Params {
+  int T, k, E, cap;
+  int M, K;             // rows of each expert matrix, reduction length
+  int NM;               // max padded token columns (<= 32)
+  int Rmax;
+  int tiled, KS, stages, pdl;
+  uint32_t tmem_cols;
+  const int32_t* n_unique;
+  const int32_t* unique;
+  const int32_t* offsets;
+  const int32_t* poff;
+  const float* wscale;  // block scales of this matrix: [E][scale_rows][K/128]
+  int scale_rows;       // gate/up: 2I/128 (gate blocks, then up blocks); down: H/128
+  const float* bscale;  // gate/up: [Rmax] per padded row; down: [Rmax][K/128]
+  uint8_t* hq_hi;       // gate/up output [Rmax][M]
+  uint8_t* hq_lo;
+  float* hscale;        // gate/up output [Rmax][M/128]
+  float* o;             // down output [T*k][M]
+  float* partials;      // [grid][2][2*NM][128]
+  int32_t* tile_cnt;
+  int32_t* done_cnt;
+  const int32_t* inv;
+  const float* w;
+  float* y;
+  int32_t* dev_err;
+};
+
+struct Tile {
+  int u, m, e, ne, np, prow, off;
+  bool ok, prow_ok;
+};
+
+__device__ __forceinline__ Tile tile_info(const Fp8Params& p, int U, int t, bool with_prow) {
+  Tile ti;
+  ti.m = t / U;
+  ti.u = t - ti.m * U;
+  ti.e = p.unique[ti.u];
+  ti.off = p.offsets[ti.u];
+  ti.ne = p.offsets[ti.u + 1] - ti.off;
+  ti.np = (ti.ne + 15) & ~15;
+  ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
+          ti.off + ti.ne <= p.T * p.k;
+  ti.prow = with_prow ? p.poff[ti.u] : -1;
+  ti.prow_ok = with_prow && ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
+  return ti;
+}
+
+__device__ __forceinline__ long long seg_owner(long long x, long long total, int G) {
+  return ((x + 1) * G - 1) / total;
+}
+
+__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+
+// Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B E4M3
+// (format 0 in bits 7-9 and 10-12), both K-major, N >> 3 (17-22), M >> 4 (24-28).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
+  return __half2float(*reinterpret_cast<__half*>(&h));
+}
+
+__device__ __forceinline__ uint8_t float_to_e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Splits v (already divided by its scale, |v| <= 448) into hi + lo / 16.
+__device__ __forceinline__ void split_e4m3(float v, uint8_t& hi, uint8_t& lo) {
+  hi = float_to_e4m3(v);
+  lo = float_to_e4m3((v - e4m3_to_float(hi)) * kLoScale);
+}
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
+                   const Fp8Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int aBytes = kGateUp ? 2 * kABytes : p.KS * kABytes;
+  const int bStride = 2 * p.NM * 128;  // hi + lo rows of one k-block
+  const int stageBytes = aBytes + p.KS * bStride;
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * stageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + kNB;
+  uint64_t* drain = tempty + kNB;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* bcast = abort_flag + 1;
+  volatile int* issued = bcast + 1;
+  volatile int* consumed = issued + 1;
+  // Barrier/flag block (at most 2*12 + 9 mbarriers + 5 words) then the combine's staging.
+  int32_t* s_inv = reinterpret_cast<int32_t*>(base + (size_t)S * stageBytes + kBarRegion);
+  float* s_w = reinterpret_cast<float*>(s_inv + kCombMax);
+  float* s_red = s_w + kCombMax;  // [4 warps][kMaxNM] column maxima
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kNB; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], kEpiThreads);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *issued = 0;
+    *consumed = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tmA0);
+    tc::tma_prefetch_desc(&tmA1);
+    tc::tma_prefetch_desc(&tmBhi);
+    tc::tma_prefetch_desc(&tmBlo);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, p.tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int U = *p.n_unique;
+  const bool valid = U >= 1 && U <= p.cap;
+  if (!valid && blockIdx.x == 0 && threadIdx.x == 0 && U != 0) flag_error(p.dev_err, MOE_DEV_CAPACITY);
+  const int MT = (p.M + kBM - 1) / kBM;
+  const int KB = p.K / kBK;
+  const int KU = (KB + p.KS - 1) / p.KS;
+  const long long total = valid ? (long long)U * MT * KU : 0;
+  const int G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
+  const int c = blockIdx.x;
+  const long long s0 = c < G ? total * c / G : total;
+  const long long s1 = c < G ? total * (c + 1) / G : total;
+  const uint32_t buf_cols = (kGateUp ? 4 : 2) * p.NM;  // per TMEM buffer: [gate hi|lo][up hi|lo]
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (tc::elect_one()) {
+      const uint64_t polA = tc::policy_evict_first();
+      const uint64_t polB = tc::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int n_issued = 0;
+      constexpr int kMaxPend = 16;
+      int pend_t[kMaxPend], pend_kb[kMaxPend], pend_nq[kMaxPend], pend_st[kMaxPend];
+      int npend = 0;
+      bool dep_done = !p.pdl;
+      if (dep_done) tc::griddep_launch_dependents();
+      auto issue_b = [&](int t, int kb, int nq, int st) {
+        const Tile ti = tile_info(p, U, t, true);
+        const int prow = ti.prow_ok ? ti.prow : 0;
+        uint8_t* sB = base + (size_t)st * stageBytes + aBytes;
+        for (int q = 0; q < nq; ++q)
+          for (int j = 0; j < ti.np / 16; ++j) {
+            tc::tma_load_2d(sB + q * bStride + j * 2048, &tmBhi, (kb + q) * kBK, prow + 16 * j, &full[st], polB);
+            tc::tma_load_2d(sB + q * bStride + ti.np * 128 + j * 2048, &tmBlo, (kb + q) * kBK, prow + 16 * j,
+                            &full[st], polB);
+          }
+      };
+      auto resolve = [&]() {
+        tc::griddep_wait();
+        tc::griddep_launch_dependents();
+        for (int i = 0; i < npend; ++i) issue_b(pend_t[i], pend_kb[i], pend_nq[i], pend_st[i]);
+        npend = 0;
+        dep_done = true;
+      };
+      for (long long x = s0; x < s1 && !*abort_flag;) {
+        const int t = static_cast<int>(x / KU);
+        const int u0 = static_cast<int>(x - (long long)t * KU);
+        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
+        x += u1 - u0;
+        const Tile ti = tile_info(p, U, t, false);
+        if (!ti.ok) continue;
+        for (int uu = u0; uu < u1; ++uu) {
+          if (!dep_done && npend == S) resolve();
+          if (!tc::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, kWaitBudgetNs)) {
+            *abort_flag = 1;
+            flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+            break;
+          }
+          const int kb = uu * p.KS;
+          const int nq = KB - kb < p.KS ? KB - kb : p.KS;
+          uint8_t* sA = base + (size_t)stage * stageBytes;
+          const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * 2 * ti.np * 128;
+          tc::mbar_arrive_expect_tx(&full[stage], tx);
+          if (p.tiled) {
+            const int blk = (ti.e * MT + ti.m) * KB + kb;
+            if (kGateUp || nq == 2)
+              tc::tma_load_3d(sA, &tmA0, 0, 0, blk, &full[stage], polA);
+            else
+              tc::tma_load_3d(sA, &tmA1, 0, 0, blk, &full[stage], polA);
+          } else {
+            tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+            if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+          }
+          if (dep_done) {
+            issue_b(t, kb, nq, stage);
+          } else {
+            pend_t[npend] = t;
+            pend_kb[npend] = kb;
+            pend_nq[npend] = nq;
+            pend_st[npend] = stage;
+            ++npend;
+          }
+          ++n_issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!dep_done) resolve();
+      *issued = n_issued;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    tc::griddep_wait();
+    if (tc::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int kc = 0;               // k-blocks issued (selects the TMEM buffer)
+      uint32_t tphase = 0;      // bit b: phase parity of buffer b
+      int n_consumed = 0;
+      bool stop = false;
+      for (long long x = s0; x < s1 && !stop;) {
+        const int t = static_cast<int>(x / KU);
+        const int u0 = static_cast<int>(x - (long long)t * KU);
+        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
+        x += u1 - u0;
+        const Tile ti = tile_info(p, U, t, false);
+        if (!ti.ok) continue;
+        const uint32_t idesc = idesc_e4m3_f32(kBM, 2 * ti.np);
+        for (int uu = u0; uu < u1 && !stop; ++uu) {
+          if (!tc::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetNs)) {
+            *abort_flag = 1;
+            flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+            stop = true;
+            break;
+          }
+          tc::tc_fence_after();
+          const int nq = KB - uu * p.KS < p.KS ? KB - uu * p.KS : p.KS;
+          const uint32_t aAddr = tc::smem_u32(base + (size_t)stage * stageBytes);
+          const uint32_t bAddr = aAddr + aBytes;
+          for (int q = 0; q < nq; ++q) {
+            const int b = kc % kNB;
+            if (!tc::mbar_wait_bounded(&tempty[b], ((tphase >> b) & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
+              *abort_flag = 1;
+              flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+              stop = true;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t d0 = tmem_base + b * buf_cols;
+            const uint32_t aq = aAddr + (kGateUp ? 0 : q * kABytes);
+            const uint32_t bq = bAddr + q * bStride;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 32; ++kk) {
+              const uint32_t accum = kk > 0 ? 1u : 0u;
+              const uint64_t bdesc = tc::smem_desc_sw128(bq + kk * 32);
+              mma_e4m3(d0, tc::smem_desc_sw128(aq + kk * 32), bdesc, idesc, accum);
+              if (kGateUp) mma_e4m3(d0 + 2 * p.NM, tc::smem_desc_sw128(aq + kABytes + kk * 32), bdesc, idesc, accum);
+            }
+            tc::mma_commit(&tfull[b]);
+            tphase ^= 1u << b;
+            ++kc;
+          }
+          if (stop) break;
+          tc::mma_commit(&empty[stage]);
+          ++n_consumed;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      *consumed = n_consumed;
+      tc::mma_commit(drain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int etid = threadIdx.x - 64;
+    tc::griddep_wait();
+    const int TKc = p.T * p.k;
+    const bool comb_smem = !kGateUp && TKc <= kCombMax;
+    if (comb_smem) {
+      for (int i = etid; i < TKc; i += kEpiThreads) {
+        s_inv[i] = p.inv[i];
+        s_w[i] = p.w[i];
+      }
+      tc::named_bar_sync(1, kEpiThreads);
+    }
+    const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
+    const int KBs = p.K / 128;  // scale blocks along K (== KB)
+    int kc = 0;
+    uint32_t tphase = 0;
+    bool stop = false;
+    for (long long x = s0; x < s1 && !stop;) {
+      const int t = static_cast<int>(x / KU);
+      const int u0 = static_cast<int>(x - (long long)t * KU);
+      const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
+      x += u1 - u0;
+      const Tile ti = tile_info(p, U, t, true);
+      if (!ti.ok) {
+        if (etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+        continue;
+      }
+      if (!ti.prow_ok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+      const int row = ti.m * kBM + r;
+      const bool row_ok = row < p.M;
+      float ga[kMaxNM], ua[kMaxNM];
+#pragma unroll
+      for (int n = 0; n < kMaxNM; ++n) ga[n] = ua[n] = 0.f;
+      // Per-row activation scales of gate/up are constant over the tile.
+      const int kb_first = u0 * p.KS;
+      const int kb_end = u1 * p.KS < KB ? u1 * p.KS : KB;
+      const float* wsg = p.wscale + ((size_t)ti.e * p.scale_rows + ti.m) * KBs;
+      const float* wsu = p.wscale + ((size_t)ti.e * p.scale_rows + p.M / 128 + ti.m) * KBs;
+      for (int kb = kb_first; kb < kb_end; ++kb) {
+        const int b = kc % kNB;
+        if (!tc::mbar_wait_bounded(&tfull[b], (tphase >> b) & 1u, abort_flag, kWaitBudgetNs)) {
+          *abort_flag = 1;
+          flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+        }
+        tc::named_bar_sync(1, kEpiThreads);
+        if (*abort_flag) {
+          stop = true;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t tb = tmem_base + lane_off + b * buf_cols;
+        const float sg = __ldg(&wsg[kb]);
+        const float su = kGateUp ? __ldg(&wsu[kb]) : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kMaxNM / 16; ++cc) {
+          if (cc < ti.np / 16) {
+            float gh[16], gl[16], uh[16], ul[16];
+            tc::tmem_ld16(tb + cc * 16, gh);
+            tc::tmem_ld16(tb + ti.np + cc * 16, gl);
+            if (kGateUp) {
+              tc::tmem_ld16(tb + 2 * p.NM + cc * 16, uh);
+              tc::tmem_ld16(tb + 2 * p.NM + ti.np + cc * 16, ul);
+            }
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = cc * 16 + j;
+              const int prow = ti.prow_ok ? ti.prow + n : 0;
+              const float sb = kGateUp ? __ldg(&p.bscale[prow]) : __ldg(&p.bscale[(size_t)prow * KBs + kb]);
+              ga[n] = fmaf(sg * sb, fmaf(gl[j], 1.f / kLoScale, gh[j]), ga[n]);
+              if (kGateUp) ua[n] = fmaf(su * sb, fmaf(ul[j], 1.f / kLoScale, uh[j]), ua[n]);
+            }
+          }
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&tempty[b]);
+        tphase ^= 1u << b;
+        ++kc;
+      }
+      if (stop) break;
+
+      const bool whole = u0 == 0 && u1 == KU;
+      bool finished = whole;
+      if (!whole) {
+        float* P = p.partials + ((size_t)c * 2 + (t == first_tile_c ? 0 : 1)) * (size_t)(2 * p.NM * 128);
+#pragma unroll
+        for (int n = 0; n < kMaxNM; ++n) {
+          if (n < ti.np) {
+            P[(size_t)n * 128 + r] = ga[n];
+            if (kGateUp) P[(size_t)(p.NM + n) * 128 + r] = ua[n];
+          }
+        }
+        tc::named_bar_sync(1, kEpiThreads);
+        if (etid == 0) {
+          __threadfence();
+          *bcast = atomicAdd(&p.tile_cnt[t], 1);
+        }
+        tc::named_bar_sync(1, kEpiThreads);
+        const int arrived = *bcast;
+        const long long t0 = (long long)t * KU;
+        const int cf = static_cast<int>(seg_owner(t0, total, G));
+        const int cl = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
+        tc::named_bar_sync(1, kEpiThreads);
+        if (arrived == cl - cf) {
+          __threadfence();
+          finished = true;
+#pragma unroll
+          for (int n = 0; n < kMaxNM; ++n) ga[n] = ua[n] = 0.f;
+          for (int q2 = cf; q2 <= cl; ++q2) {
+            const int ft = static_cast<int>((total * q2 / G) / KU);
+            const float* P2 = p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128);
+#pragma unroll
+            for (int n = 0; n < kMaxNM; ++n) {
+              if (n < ti.np) {
+                ga[n] += __ldcg(&P2[(size_t)n * 128 + r]);
+                if (kGateUp) ua[n] += __ldcg(&P2[(size_t)(p.NM + n) * 128 + r]);
+              }
+            }
+          }
+        }
+      }
+      if (!finished) continue;
+
+      if (kGateUp) {
+        // h = silu(gate) * up, quantized per (token, 128-row block) for the
+        // down projection: scale = max |h| over the block's rows / 448.
+        float h[kMaxNM];
+#pragma unroll
+        for (int n = 0; n < kMaxNM; ++n) h[n] = (n < ti.ne && row_ok) ? silu_mul(ga[n], ua[n]) : 0.f;
+#pragma unroll
+        for (int n = 0; n < kMaxNM; ++n) {
+          if (n < ti.np) {
+            float a = fabsf(h[n]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+            if (lane == 0) s_red[q4 * kMaxNM + n] = a;
+          }
+        }
+        tc::named_bar_sync(1, kEpiThreads);
+#pragma unroll
+        for (int n = 0; n < kMaxNM; ++n) {
+          if (n < ti.ne) {
+            const float amax = fmaxf(fmaxf(s_red[n], s_red[kMaxNM + n]), fmaxf(s_red[2 * kMaxNM + n], s_red[3 * kMaxNM + n]));
+            const float sc = amax > 0.f ? amax / kE4M3Max : 1.f;
+            uint8_t hi, lo;
+            split_e4m3(h[n] / sc, hi, lo);
+            if (ti.prow_ok && row_ok) {
+              p.hq_hi[(size_t)(ti.prow + n) * p.M + row] = hi;
+              p.hq_lo[(size_t)(ti.prow + n) * p.M + row] = lo;
+              if (r == 0) p.hscale[(size_t)(ti.prow + n) * (p.M / 128) + ti.m] = sc;
+            }
+          }
+        }
+        tc::named_bar_sync(1, kEpiThreads);  // s_red is reused by the next tile
+      } else {
+#pragma unroll
+        for (int n = 0; n < kMaxNM; ++n)
+          if (n < ti.ne && row_ok) p.o[(size_t)(ti.off + n) * p.M + row] = ga[n];
+        tc::named_bar_sync(1, kEpiThreads);
+        if (etid == 0) {
+          __threadfence();
+          *bcast = atomicAdd(&p.done_cnt[ti.m], 1);
+        }
+        tc::named_bar_sync(1, kEpiThreads);
+        const int done = *bcast;
+        tc::named_bar_sync(1, kEpiThreads);
+        if (done == U - 1) {
+          __threadfence();
+          const int TK = p.T * p.k;
+          for (int tb = 0; tb < p.T && row_ok; tb += 2) {
+            int pos[2][16];
+            float wv[2][16], ov[2][16];
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int tok = tb + a;
+                const bool in = tok < p.T && j < p.k;
+                const int idx = tok * p.k + j;
+                pos[a][j] = in ? (comb_smem ? s_inv[idx] : __ldg(&p.inv[idx])) : -1;
+                wv[a][j] = in ? (comb_smem ? s_w[idx] : __ldg(&p.w[idx])) : 0.f;
+              }
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const bool ok = pos[a][j] >= 0 && pos[a][j] < TK;
+                if (tb + a < p.T && j < p.k && !ok) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+                ov[a][j] = ok ? __ldcg(&p.o[(size_t)pos[a][j] * p.M + row]) : 0.f;
+              }
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              if (tb + a >= p.T) break;
+              float s = 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < p.k && pos[a][j] >= 0 && pos[a][j] < TK) s = fmaf(wv[a][j], ov[a][j], s);
+              p.y[(size_t)(tb + a) * p.M + row] = s;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      for (int i = *consumed; i < *issued; ++i)
+        tc::mbar_wait_bounded(&full[i % S], static_cast<uint32_t>((i / S) & 1), nullptr, 100000000ull);
+    }
+  }
+  if (warp == 1) {
+    tc::mbar_wait_bounded(drain, 0, nullptr, 100000000ull);
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// Padded group offsets, zeroed fixup counters and the quantized activations:
+// one warp per (token, slot) pair writes hi/lo E4M3 rows and the row scale.
+__global__ void __launch_bounds__(256) ffn_fp8_prep_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ x_rows, int x_rows_limit, int T, int k, int H,
+    int cap, const int32_t* __restrict__ n_unique, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ perm_token, uint8_t* __restrict__ xq_hi, uint8_t* __restrict__ xq_lo,
+    float* __restrict__ xscale, int32_t* __restrict__ poff, int32_t* __restrict__ counters, int n_counters,
+    float* __restrict__ y, int32_t* dev_err) {
+  __shared__ int32_t spoff[1025];
+  __shared__ int s_bad;
+  pdl_wait();
+  pdl_trigger();
+  const int TK = T * k;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x) counters[i] = 0;
+  const int U = *n_unique;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if (U < 1 || U > cap) {
+    if (U != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(dev_err, MOE_DEV_CAPACITY);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * H;
+         i += (long long)gridDim.x * blockDim.x)
+      y[i] = 0.f;
+    return;
+  }
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (U + 31) / 32;
+    const int u0 = lane * per;
+    int sum = 0;
+    for (int u = u0; u < u0 + per && u < U; ++u) {
+      const int a = offsets[u], b = offsets[u + 1];
+      if (a < 0 || b > TK || b - a < 1 || b - a > T) s_bad = 1;
+      sum += ((b - a) + 15) & ~15;
+    }
+    int ex = sum;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, ex, off);
+      if (lane >= off) ex += v;
+    }
+    ex -= sum;
+    for (int u = u0; u < u0 + per && u < U; ++u) {
+      spoff[u] = ex;
+      ex += ((offsets[u + 1] - offsets[u]) + 15) & ~15;
+    }
+    if (lane == 31) {
+      spoff[U] = ex;
+      if (offsets[U] != TK || offsets[0] != 0) s_bad = 1;
+    }
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * H;
+         i += (long long)gridDim.x * blockDim.x)
+      y[i] = 0.f;
+    return;
+  }
+  if (blockIdx.x == 0)
+    for (int u = threadIdx.x; u <= U; u += blockDim.x) poff[u] = spoff[u];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int pp = gw; pp < TK; pp += nw) {
+    int lo = 0, hi = U - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (offsets[mid] <= pp) lo = mid;
+      else hi = mid - 1;
+    }
+    const int rr = spoff[lo] + (pp - offsets[lo]);
+    const int tok = perm_token[pp];
+    bool ok = tok >= 0 && tok < T;
+    int row = tok;
+    if (ok && x_rows) {
+      row = x_rows[tok];
+      ok = row >= 0 && row < x_rows_limit;
+    }
+    if (!ok) {
+      if (lane == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
+      continue;
+    }
+    const uint16_t* xr = x + (size_t)row * H;
+    float amax = 0.f;
+    for (int c = lane * 8; c < H; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] & 0xFFFF0000u)));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const float sc = amax > 0.f ? amax / kE4M3Max : 1.f;
+    for (int c = lane * 8; c < H; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t h0 = 0, h1 = 0, l0 = 0, l1 = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint8_t ha, la, hb, lb;
+        split_e4m3(__uint_as_float(wv[i] << 16) / sc, ha, la);
+        split_e4m3(__uint_as_float(wv[i] & 0xFFFF0000u) / sc, hb, lb);
+        const uint32_t hh = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 8);
+        const uint32_t ll = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 8);
+        if (i < 2) {
+          h0 |= hh << (16 * i);
+          l0 |= ll << (16 * i);
+        } else {
+          h1 |= hh << (16 * (i - 2));
+          l1 |= ll << (16 * (i - 2));
+        }
+      }
+      *reinterpret_cast<uint2*>(xq_hi + (size_t)rr * H + c) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(xq_lo + (size_t)rr * H + c) = make_uint2(l0, l1);
+    }
+    if (lane == 0) xscale[rr] = sc;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool make_tmap_u8(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                  const uint32_t* box_dims) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    box[i] = box_dims[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) gstride[i] = strides_bytes[i];
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), gdim, gstride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Fp8Geom {
+  int NM, MT_gu, MT_d, Rmax, G, KS_d, stages_gu, stages_d;
+  size_t smem_gu, smem_d;
+};
+
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kSmemExtra = 1024 + kBarRegion + 8 * kCombMax + 4 * 4 * kMaxNM;
+
+Fp8Geom fp8_geom(const moe_layer_weights& lw, int T, int k) {
+  Fp8Geom g;
+  const int TK = T * k;
+  const int cap = lw.E < TK ? lw.E : TK;
+  g.NM = (T + 15) & ~15;
+  g.MT_gu = lw.I / kBM;
+  g.MT_d = lw.H / kBM;
+  g.Rmax = TK + 15 * cap;
+  g.G = sm_count();
+  g.KS_d = lw.layout == MOE_LAYOUT_TILED ? 2 : 1;
+  const size_t b = static_cast<size_t>(2 * g.NM) * 128;
+  const size_t st_gu = 2 * kABytes + b, st_d = g.KS_d * (kABytes + b);
+  g.stages_gu = static_cast<int>((kSmemLimit - kSmemExtra) / st_gu);
+  g.stages_d = static_cast<int>((kSmemLimit - kSmemExtra) / st_d);
+  if (g.stages_gu > 8) g.stages_gu = 8;
+  if (g.stages_d > 12) g.stages_d = 12;
+  g.smem_gu = g.stages_gu * st_gu + kSmemExtra;
+  g.smem_d = g.stages_d * st_d + kSmemExtra;
+  return g;
+}
+
+uint32_t pow2_cols(int c) {
+  uint32_t v = 32;
+  while (v < static_cast<uint32_t>(c)) v <<= 1;
+  return v;
+}
+
+struct Fp8Ws {
+  uint8_t *xq_hi, *xq_lo, *hq_hi, *hq_lo;
+  float *xscale, *hscale, *o, *partials;
+  int32_t *poff, *counters;
+  size_t bytes;
+};
+
+Fp8Ws fp8_carve(const moe_layer_weights& lw, int T, int k, void* base) {
+  Fp8Geom g = fp8_geom(lw, T, k);
+  const int TK = T * k;
+  const int cap = lw.E < TK ? lw.E : TK;
+  char* p0 = static_cast<char*>(base);
+  char* p = p0;
+  Fp8Ws w;
+  auto take = [&](size_t bytes) {
+    char* r = p;
+    p += align_up(bytes, 256);
+    return r;
+  };
+  w.xq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.H));
+  w.xq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.H));
+  w.xscale = reinterpret_cast<float*>(take(static_cast<size_t>(g.Rmax) * 4));
+  w.hq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.I));
+  w.hq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.I));
+  w.hscale = reinterpret_cast<float*>(take(static_cast<size_t>(g.Rmax) * (lw.I / 128) * 4));
+  w.o = reinterpret_cast<float*>(take(static_cast<size_t>(TK) * lw.H * 4));
+  w.partials = reinterpret_cast<float*>(take(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4));
+  w.poff = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cap + 1) * 4));
+  w.counters = reinterpret_cast<int32_t*>(take((static_cast<size_t>(cap) * (g.MT_gu + g.MT_d) + g.MT_d) * 4));
+  w.bytes = static_cast<size_t>(p - p0);
+  return w;
+}
+
+}  // namespace
+
+bool ffn_fp8_supported(const moe_layer_weights& lw, int T, int k) {
+  if (lw.dtype != MOE_DTYPE_E4M3_B128) return false;
+  if (lw.layout != MOE_LAYOUT_ROWMAJOR && lw.layout != MOE_LAYOUT_TILED) return false;
+  if (lw.H % kBK || lw.I % kBK) return false;
+  if (T < 1 || T > kMaxNM) return false;
+  Fp8Geom g = fp8_geom(lw, T, k);
+  return g.stages_gu >= 2 && g.stages_d >= 2 && encode_fn() != nullptr;
+}
+
+size_t ffn_fp8_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
+  return fp8_carve(lw, T, k, nullptr).bytes;
+}
+
+int ffn_fp8_launch(const FfnArgs& a) {
+  const auto& lw = a.lw;
+  const int T = a.T, k = a.k, TK = T * k;
+  const int cap = lw.E < TK ? lw.E : TK;
+  Fp8Geom g = fp8_geom(lw, T, k);
+  Fp8Ws ws = fp8_carve(lw, T, k, a.ws);
+  const int n_counters = cap * (g.MT_gu + g.MT_d) + g.MT_d;
+  int32_t* cnt_gu = ws.counters;
+  int32_t* cnt_d = cnt_gu + static_cast<size_t>(cap) * g.MT_gu;
+  int32_t* done = cnt_d + static_cast<size_t>(cap) * g.MT_d;
+
+  const uint64_t H = lw.H, I = lw.I, E = lw.E;
+  const uint64_t KBg = H / kBK, KBd = I / kBK;
+  CUtensorMap tm_g, tm_u, tm_xh, tm_xl, tm_wd, tm_wd1, tm_hh, tm_hl;
+  if (lw.layout == MOE_LAYOUT_TILED) {
+    {
+      uint64_t dims[3] = {kBK, 2 * kBM, E * g.MT_gu * KBg}, str[2] = {kBK, 2 * kABytes};
+      uint32_t box[3] = {kBK, 2 * kBM, 1};
+      if (!make_tmap_u8(&tm_g, lw.w_gate_up, 3, dims, str, box)) return MOE_ERR_CUDA;
+      tm_u = tm_g;
+    }
+    {
+      uint64_t dims[3] = {kBK, kBM, E * g.MT_d * KBd}, str[2] = {kBK, kABytes};
+      uint32_t box2[3] = {kBK, kBM, 2}, box1[3] = {kBK, kBM, 1};
+      if (!make_tmap_u8(&tm_wd, lw.w_down, 3, dims, str, box2)) return MOE_ERR_CUDA;
+      if (!make_tmap_u8(&tm_wd1, lw.w_down, 3, dims, str, box1)) return MOE_ERR_CUDA;
+    }
+  } else {
+    uint32_t box[3] = {kBK, kBM, 1};
+    {
+      uint64_t dims[3] = {H, I, E}, str[2] = {H, 2 * I * H};
+      if (!make_tmap_u8(&tm_g, lw.w_gate_up, 3, dims, str, box)) return MOE_ERR_CUDA;
+      const char* up = static_cast<const char*>(lw.w_gate_up) + I * H;
+      if (!make_tmap_u8(&tm_u, up, 3, dims, str, box)) return MOE_ERR_CUDA;
+    }
+    {
+      uint64_t dims[3] = {I, H, E}, str[2] = {I, H * I};
+      if (!make_tmap_u8(&tm_wd, lw.w_down, 3, dims, str, box)) return MOE_ERR_CUDA;
+      tm_wd1 = tm_wd;
+    }
+  }
+  {
+    uint64_t dims[2] = {H, static_cast<uint64_t>(g.Rmax)}, str[1] = {H};
+    uint32_t box[2] = {kBK, 16};
+    if (!make_tmap_u8(&tm_xh, ws.xq_hi, 2, dims, str, box)) return MOE_ERR_CUDA;
+    if (!make_tmap_u8(&tm_xl, ws.xq_lo, 2, dims, str, box)) return MOE_ERR_CUDA;
+  }
+  {
+    uint64_t dims[2] = {I, static_cast<uint64_t>(g.Rmax)}, str[1] = {I};
+    uint32_t box[2] = {kBK, 16};
+    if (!make_tmap_u8(&tm_hh, ws.hq_hi, 2, dims, str, box)) return MOE_ERR_CUDA;
+    if (!make_tmap_u8(&tm_hl, ws.hq_lo, 2, dims, str, box)) return MOE_ERR_CUDA;
+  }
+
+  cudaStream_t s = a.stream;
+  {
+    int blocks = (TK * 32 + 255) / 256;
+    if (blocks > g.G * 4) blocks = g.G * 4;
+    if (blocks < 1) blocks = 1;
+    LaunchScope ls(kProfPrep, s);
+    if (launch_k(ffn_fp8_prep_kernel, dim3(blocks), dim3(256), 0, s, a.pdl_first,
+                 static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, k, lw.H, cap, a.n_unique,
+                 a.offsets, a.perm_token, ws.xq_hi, ws.xq_lo, ws.xscale, ws.poff, cnt_gu, n_counters, a.y,
+                 a.dev_err) != MOE_OK)
+      return MOE_ERR_CUDA;
+  }
+
+  Fp8Params fp{};
+  fp.T = T;
+  fp.k = k;
+  fp.E = lw.E;
+  fp.cap = cap;
+  fp.NM = g.NM;
+  fp.Rmax = g.Rmax;
+  fp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
+  fp.pdl = 1;
+  fp.n_unique = a.n_unique;
+  fp.unique = a.unique;
+  fp.offsets = a.offsets;
+  fp.poff = ws.poff;
+  fp.hq_hi = ws.hq_hi;
+  fp.hq_lo = ws.hq_lo;
+  fp.hscale = ws.hscale;
+  fp.o = ws.o;
+  fp.partials = ws.partials;
+  fp.inv = a.inv;
+  fp.w = a.w;
+  fp.y = a.y;
+  fp.dev_err = a.dev_err;
+
+  // gate/up
+  fp.M = lw.I;
+  fp.K = lw.H;
+  fp.KS = 1;
+  fp.stages = g.stages_gu;
+  fp.tmem_cols = pow2_cols(kNB * 4 * g.NM);
+  fp.wscale = lw.scales_gate_up;
+  fp.scale_rows = 2 * lw.I / 128;
+  fp.bscale = ws.xscale;
+  fp.tile_cnt = cnt_gu;
+  fp.done_cnt = nullptr;
+  if (cudaFuncSetAttribute(ffn_fp8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(g.smem_gu)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  {
+    LaunchScope ls(kProfGateUp, s);
+    if (launch_k(ffn_fp8_kernel<true>, dim3(g.G), dim3(kThreads), g.smem_gu, s, true, tm_g, tm_u, tm_xh, tm_xl,
+                 fp) != MOE_OK)
+      return MOE_ERR_CUDA;
+  }
+  // down + combine
+  fp.M = lw.H;
+  fp.K = lw.I;
+  fp.KS = g.KS_d;
+  fp.stages = g.stages_d;
+  fp.tmem_cols = pow2_cols(kNB * 2 * g.NM);
+  fp.wscale = lw.scales_down;
+  fp.scale_rows = lw.H / 128;
+  fp.bscale = ws.hscale;
+  fp.tile_cnt = cnt_d;
+  fp.done_cnt = done;
+  if (cudaFuncSetAttribute(ffn_fp8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(g.smem_d)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  {
+    LaunchScope ls(kProfDown, s);
+    if (launch_k(ffn_fp8_kernel<false>, dim3(g.G), dim3(kThreads), g.smem_d, s, true, tm_wd, tm_wd1, tm_hh, tm_hl,
+                 fp) != MOE_OK)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

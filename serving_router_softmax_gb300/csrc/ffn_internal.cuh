@@ -20,4 +20,9 @@ bool ffn_tc_supported(const moe_layer_weights& lw, int T, int k);
 size_t ffn_tc_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_tc_launch(const FfnArgs& a);
 
+// Tensor-core path (FP8 E4M3 weights with 128 x 128 block scales).
+bool ffn_fp8_supported(const moe_layer_weights& lw, int T, int k);
+size_t ffn_fp8_workspace_bytes(const moe_layer_weights& lw, int T, int k);
+int ffn_fp8_launch(const FfnArgs& a);
+
 }  // namespace moe

@@ -47,6 +47,8 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
 constexpr int kCombMax = 512;     // (token, slot) pairs whose inv/w the down epilogue keeps in smem
+constexpr int kBarRegion = 512;   // mbarriers + flags of the CTA
+static_assert((2 * 12 + 5) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
 
 struct TcParams {
   int T, k, E, cap;
@@ -138,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* bcast = abort_flag + 1;
   volatile int* issued = bcast + 1;
   volatile int* consumed = issued + 1;
-  int32_t* s_inv = reinterpret_cast<int32_t*>(base + (size_t)S * stageBytes + 256);
+  // Barrier/flag block (at most 2*12 + 9 mbarriers + 5 words) then the combine's staging.
+  int32_t* s_inv = reinterpret_cast<int32_t*>(base + (size_t)S * stageBytes + kBarRegion);
   float* s_w = reinterpret_cast<float*>(s_inv + kCombMax);
 
   const int warp = threadIdx.x >> 5;
@@ -668,7 +671,7 @@ struct TcGeom {
 };
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kSmemExtra = 1024 /*align*/ + 256 /*barriers & flags*/ + 8 * kCombMax /*combine inv/w*/;
+constexpr size_t kSmemExtra = 1024 /*align*/ + kBarRegion /*barriers & flags*/ + 8 * kCombMax /*combine inv/w*/;
 
 TcGeom tc_geom(const moe_layer_weights& lw, int T, int k) {
   TcGeom g;

@@ -1,19 +1,21 @@
-// moe_pack_tiled: load-time repacking of one layer's bf16 expert weights into
-// the tile-contiguous layout the tensor-core FFN streams best (see
-// include/moe_verify.h, MOE_LAYOUT_TILED).  One thread per 16-byte vector of
-// the destination; rows past the matrix end are written as zeros.
+// moe_pack_tiled: load-time repacking of one layer's expert weights into the
+// tile-contiguous layout the tensor-core FFN streams best (include/moe_verify.h,
+// MOE_LAYOUT_TILED).  A block covers 128 rows and 128 bytes of the reduction
+// dimension (64 bf16 or 128 FP8 values); one thread per 16-byte vector of the
+// destination; rows past the matrix end are written as zeros.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kRowsPerTile = 128;
-constexpr int kColsPerBlock = 64;  // bf16 columns per block (128 bytes = 8 vectors)
+constexpr int kBlockBytes = 128;  // reduction bytes per block row (8 vectors)
 
-// gate/up: block (e, m, kb) = [256][64]: rows 0..127 gate, 128..255 up.
-__global__ void pack_gate_up_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int H, int I,
-                                    int E, int MT) {
-  const int KB = H / kColsPerBlock;
+// gate/up: block (e, m, kb) = [256][128 B]: rows 0..127 gate, 128..255 up.
+// src rows are row_bytes long; I rows of gate then I rows of up per expert.
+__global__ void pack_gate_up_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, long long row_bytes,
+                                    int I, int E, int MT) {
+  const int KB = static_cast<int>(row_bytes / kBlockBytes);
   const long long nvec = (long long)E * MT * KB * 256 * 8;
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
        v += (long long)gridDim.x * blockDim.x) {
@@ -29,16 +31,16 @@ __global__ void pack_gate_up_kernel(const uint16_t* __restrict__ src, uint16_t* 
     uint4 val = make_uint4(0, 0, 0, 0);
     if (row < I) {
       const long long srow = (long long)e * 2 * I + (r < 128 ? row : I + row);
-      val = *reinterpret_cast<const uint4*>(src + srow * H + kb * kColsPerBlock + vec * 8);
+      val = *reinterpret_cast<const uint4*>(src + srow * row_bytes + (long long)kb * kBlockBytes + vec * 16);
     }
-    *reinterpret_cast<uint4*>(dst + v * 8) = val;
+    *reinterpret_cast<uint4*>(dst + v * 16) = val;
   }
 }
 
-// down: block (e, m, kb) = [128][64] of W_down rows m*128.., columns kb*64..
-__global__ void pack_down_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int H, int I, int E,
-                                 int MT) {
-  const int KB = I / kColsPerBlock;
+// down: block (e, m, kb) = [128][128 B] of W_down rows m*128.., columns kb*128 B..
+__global__ void pack_down_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, long long row_bytes,
+                                 int H, int E, int MT) {
+  const int KB = static_cast<int>(row_bytes / kBlockBytes);
   const long long nvec = (long long)E * MT * KB * 128 * 8;
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < nvec;
        v += (long long)gridDim.x * blockDim.x) {
@@ -52,17 +54,23 @@ __global__ void pack_down_kernel(const uint16_t* __restrict__ src, uint16_t* __r
     const int e = static_cast<int>(em / MT);
     const int row = m * kRowsPerTile + r;
     uint4 val = make_uint4(0, 0, 0, 0);
-    if (row < H) val = *reinterpret_cast<const uint4*>(src + ((long long)e * H + row) * I + kb * kColsPerBlock + vec * 8);
-    *reinterpret_cast<uint4*>(dst + v * 8) = val;
+    if (row < H)
+      val = *reinterpret_cast<const uint4*>(src + ((long long)e * H + row) * row_bytes + (long long)kb * kBlockBytes +
+                                            vec * 16);
+    *reinterpret_cast<uint4*>(dst + v * 16) = val;
   }
 }
 
+int elem_bytes(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : (dtype == MOE_DTYPE_E4M3_B128 ? 1 : 0); }
+
 bool tiled_sizes(const moe_layer_weights& lw, size_t* gu, size_t* dn) {
-  if (lw.dtype != MOE_DTYPE_BF16 || lw.H < 64 || lw.I < 64 || lw.H % 64 || lw.I % 64 || lw.E < 1 || lw.E > 1024)
-    return false;
+  const int eb = elem_bytes(lw.dtype);
+  if (eb == 0 || lw.E < 1 || lw.E > 1024) return false;
+  const int mult = kBlockBytes / eb;  // reduction elements per block
+  if (lw.H < mult || lw.I < mult || lw.H % mult || lw.I % mult) return false;
   const size_t MTg = (lw.I + 127) / 128, MTd = (lw.H + 127) / 128;
-  *gu = static_cast<size_t>(lw.E) * MTg * (lw.H / 64) * 256 * 64 * 2;
-  *dn = static_cast<size_t>(lw.E) * MTd * (lw.I / 64) * 128 * 64 * 2;
+  *gu = static_cast<size_t>(lw.E) * MTg * 256 * static_cast<size_t>(lw.H) * eb;
+  *dn = static_cast<size_t>(lw.E) * MTd * 128 * static_cast<size_t>(lw.I) * eb;
   return true;
 }
 
@@ -88,11 +96,14 @@ extern "C" int moe_pack_tiled(const moe_layer_weights* src, void* dst_gate_up, v
     return MOE_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int blocks = sm_count() * 8;
+  const int eb = elem_bytes(src->dtype);
   const int MTg = (src->I + 127) / 128, MTd = (src->H + 127) / 128;
-  pack_gate_up_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(src->w_gate_up),
-                                             static_cast<uint16_t*>(dst_gate_up), src->H, src->I, src->E, MTg);
+  pack_gate_up_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t*>(src->w_gate_up),
+                                             static_cast<uint8_t*>(dst_gate_up), (long long)src->H * eb, src->I,
+                                             src->E, MTg);
   if (check_launch() != MOE_OK) return MOE_ERR_CUDA;
-  pack_down_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(src->w_down),
-                                          static_cast<uint16_t*>(dst_down), src->H, src->I, src->E, MTd);
+  pack_down_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t*>(src->w_down),
+                                          static_cast<uint8_t*>(dst_down), (long long)src->I * eb, src->H, src->E,
+                                          MTd);
   return check_launch();
 }

@@ -67,10 +67,13 @@ FFN_CASES = [
     ("f32", 320, 192, 12, 3, 17),
     ("e4m3", 640, 384, 16, 4, 5),
     ("e4m3", 256, 256, 32, 8, 28),
+    ("e4m3", 256, 256, 8, 8, 32),      # every expert, maximum T of the FP8 tensor-core path
+    ("e4m3", 384, 256, 16, 2, 40),     # T > 32: CUDA-core FP8 path
 ]
 
 
-FFN_CASES_ALL = [c + ("rowmajor",) for c in FFN_CASES] + [c + ("tiled",) for c in FFN_CASES if c[0] == "bf16"]
+FFN_CASES_ALL = [c + ("rowmajor",) for c in FFN_CASES] + [
+    c + ("tiled",) for c in FFN_CASES if c[0] == "bf16" or (c[0] == "e4m3" and c[5] <= 32)]
 
 
 @pytest.mark.parametrize("dtype,H,I,E,k,T,layout", FFN_CASES_ALL)
@@ -118,34 +121,36 @@ def test_ffn_device_fill_matches_host_generator(mv):
                 assert np.array_equal(layer.scales_down[e].cpu().numpy(), hw["scale_down"])
 
 
-def test_pack_tiled_layout(mv):
+@pytest.mark.parametrize("dtype,H,I", [("bf16", 256, 192), ("bf16", 192, 320), ("e4m3", 256, 384)])
+def test_pack_tiled_layout(mv, dtype, H, I):
     """The tiled copy holds exactly the documented block arrangement."""
     from workload import gen
-    for H, I in [(256, 192), (192, 320)]:
-        cfg = gen.MoEConfig("packcheck", L=1, H=H, E=3, k=2, I=I, dtype="bf16", seed=H * I)
-        layer = make_layer(mv, cfg, 0)
-        tl = mv.pack_tiled(layer)
-        torch.cuda.synchronize()
-        gu = tl.gate_up.cpu().numpy().view(np.uint16)
-        dn = tl.down.cpu().numpy().view(np.uint16)
-        MTg, MTd, KBg, KBd = -(-I // 128), -(-H // 128), H // 64, I // 64
-        gu = gu.reshape(3, MTg, KBg, 256, 64)
-        dn = dn.reshape(3, MTd, KBd, 128, 64)
-        for e in range(3):
-            w = gen.expert_weights_host(cfg, 0, e)
-            g, u, d = w["gate_up"][:I], w["gate_up"][I:], w["down"]
-            ref_g = np.zeros((MTg * 128, H), np.uint16)
-            ref_u = np.zeros((MTg * 128, H), np.uint16)
-            ref_d = np.zeros((MTd * 128, I), np.uint16)
-            ref_g[:I], ref_u[:I], ref_d[:H] = g, u, d
-            for m in range(MTg):
-                for kb in range(KBg):
-                    blk = gu[e, m, kb]
-                    assert np.array_equal(blk[:128], ref_g[m * 128:(m + 1) * 128, kb * 64:(kb + 1) * 64])
-                    assert np.array_equal(blk[128:], ref_u[m * 128:(m + 1) * 128, kb * 64:(kb + 1) * 64])
-            for m in range(MTd):
-                for kb in range(KBd):
-                    assert np.array_equal(dn[e, m, kb], ref_d[m * 128:(m + 1) * 128, kb * 64:(kb + 1) * 64])
+    cfg = gen.MoEConfig("packcheck", L=1, H=H, E=3, k=2, I=I, dtype=dtype, seed=H * I)
+    layer = make_layer(mv, cfg, 0)
+    tl = mv.pack_tiled(layer)
+    torch.cuda.synchronize()
+    nt = np.uint16 if dtype == "bf16" else np.uint8
+    C = 64 if dtype == "bf16" else 128  # reduction elements per 128-byte block
+    gu = tl.gate_up.cpu().numpy().view(nt)
+    dn = tl.down.cpu().numpy().view(nt)
+    MTg, MTd, KBg, KBd = -(-I // 128), -(-H // 128), H // C, I // C
+    gu = gu.reshape(3, MTg, KBg, 256, C)
+    dn = dn.reshape(3, MTd, KBd, 128, C)
+    for e in range(3):
+        w = gen.expert_weights_host(cfg, 0, e)
+        g, u, d = w["gate_up"][:I], w["gate_up"][I:], w["down"]
+        ref_g = np.zeros((MTg * 128, H), nt)
+        ref_u = np.zeros((MTg * 128, H), nt)
+        ref_d = np.zeros((MTd * 128, I), nt)
+        ref_g[:I], ref_u[:I], ref_d[:H] = g, u, d
+        for m in range(MTg):
+            for kb in range(KBg):
+                blk = gu[e, m, kb]
+                assert np.array_equal(blk[:128], ref_g[m * 128:(m + 1) * 128, kb * C:(kb + 1) * C])
+                assert np.array_equal(blk[128:], ref_u[m * 128:(m + 1) * 128, kb * C:(kb + 1) * C])
+        for m in range(MTd):
+            for kb in range(KBd):
+                assert np.array_equal(dn[e, m, kb], ref_d[m * 128:(m + 1) * 128, kb * C:(kb + 1) * C])
 
 
 # ------------------------------------------------------------------ whole step
@@ -207,7 +212,7 @@ SMALL = {
 }
 
 
-SMALL_CASES = [(n, "rowmajor") for n in SMALL] + [(n, "tiled") for n in SMALL if n not in ("toy", "deepseek_v3_like")]
+SMALL_CASES = [(n, "rowmajor") for n in SMALL] + [(n, "tiled") for n in SMALL if n != "toy"]
 
 
 @pytest.mark.parametrize("name,layout", SMALL_CASES)
@@ -234,6 +239,6 @@ def test_step_full_size_sampled(mv, name):
     layers = [0, cfg.L - 1] if cfg.L > 1 else [0]
     wl_T = gen.make_workload(cfg).T
     tokens = sorted({0, wl_T // 2, wl_T - 1})
-    layout = "tiled" if cfg.dtype == "bf16" else "rowmajor"  # as the bench runs it
+    layout = "tiled" if cfg.dtype in ("bf16", "e4m3") else "rowmajor"  # as the bench runs it
     wl, got, ref = run_step(mv, cfg, sample_tokens=tokens, sample_layers=layers, layout=layout)
     check_step(wl, got, ref, TOL[cfg.dtype], sample_tokens=tokens)
