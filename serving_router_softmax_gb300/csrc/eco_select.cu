@@ -43,6 +43,9 @@ __global__ void __launch_bounds__(512) eco_kernel(
   __shared__ uint8_t chosen[kMaxN];
   __shared__ int bad;
   __shared__ int best_s;
+  __shared__ int16_t par_s[kMaxN];
+  __shared__ int16_t depth_s[kMaxN];
+  __shared__ int max_depth;
 
   pdl_trigger();  // the first layer's head may launch while selection runs
   const int s = blockIdx.x;
@@ -99,13 +102,27 @@ __global__ void __launch_bounds__(512) eco_kernel(
   }
   if (gamma > N) gamma = N;
 
-  // E_traj(t) = own(t) | E_traj(parent(t)), in breadth-first order.
-  for (int t = 0; t < N; ++t) {
-    const int p = par[t];
-    for (int w = threadIdx.x; w < W; w += blockDim.x) {
-      uint32_t v = own[(size_t)t * W + w];
-      if (p >= 0) v |= traj[(size_t)p * W + w];
-      traj[(size_t)t * W + w] = v;
+  // E_traj(t) = own(t) | E_traj(parent(t)).  Own footprints come in with one
+  // coalesced pass; the ORs then run level by level (one barrier per tree
+  // level), deepest level last.
+  for (int i = threadIdx.x; i < N * W; i += blockDim.x) traj[i] = own[i];
+  for (int t = threadIdx.x; t < N; t += blockDim.x) par_s[t] = static_cast<int16_t>(par[t]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int maxd = 0;
+    for (int t = 0; t < N; ++t) {
+      const int p = par_s[t];
+      const int d = p < 0 ? 0 : depth_s[p] + 1;
+      depth_s[t] = static_cast<int16_t>(d);
+      maxd = d > maxd ? d : maxd;
+    }
+    max_depth = maxd;
+  }
+  __syncthreads();
+  for (int d = 1; d <= max_depth; ++d) {
+    for (int i = threadIdx.x; i < N * W; i += blockDim.x) {
+      const int t = i / W;
+      if (depth_s[t] == d) traj[i] |= traj[(size_t)par_s[t] * W + (i - t * W)];
     }
     __syncthreads();
   }

@@ -11,7 +11,8 @@
 //     x ~= s * (hi + lo / 16) with relative error near 2^-8.  hi and lo rows
 //     are stacked, so one MMA of N = 2 * np produces both partial products.
 //   * The weight block scale changes every 128 reduction elements, so every
-//     k-block is multiplied into its own TMEM buffer (4 in rotation) and the
+//     k-block is multiplied into its own TMEM buffer (up to 16 in rotation, as
+//     many as fit in the 512 columns) and the
 //     epilogue warps promote it: acc += w_scale * s * (d_hi + d_lo / 16), in
 //     fp32 registers.
 //   * gate/up writes h = silu(gate) * up quantized the same way, with one
@@ -34,14 +35,14 @@ constexpr int kBK = 128;           // reduction elements (bytes) per k-block
 constexpr int kABytes = kBM * kBK;  // 16 KB
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kNB = 4;             // TMEM promotion buffers
+constexpr int kNBMax = 16;         // TMEM promotion buffers (at most)
 constexpr int kMaxNM = 32;         // padded token columns handled by this path
 constexpr int kCombMax = 512;
 constexpr float kLoScale = 16.f;
 constexpr float kE4M3Max = 448.f;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 constexpr int kBarRegion = 512;    // mbarriers + flags of the CTA
-static_assert((2 * 12 + 2 * kNB + 1) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
+static_assert((2 * 12 + 2 * kNBMax + 1) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
 
 struct Fp8Params {
   int T, k, E, cap;
@@ -49,6 +50,7 @@ struct Fp8Params {
   int NM;               // max padded token columns (<= 32)
   int Rmax;
   int tiled, KS, stages, pdl;
+  int NB;               // TMEM promotion buffers in rotation
   uint32_t tmem_cols;
   const int32_t* n_unique;
   const int32_t* unique;
@@ -140,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * stageBytes);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
-  uint64_t* tempty = tfull + kNB;
-  uint64_t* drain = tempty + kNB;
+  uint64_t* tempty = tfull + kNBMax;
+  uint64_t* drain = tempty + kNBMax;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* bcast = abort_flag + 1;
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < kNB; ++b) {
+    for (int b = 0; b < p.NB; ++b) {
       tc::mbar_init(&tfull[b], 1);
       tc::mbar_init(&tempty[b], kEpiThreads);
     }
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t aAddr = tc::smem_u32(base + (size_t)stage * stageBytes);
           const uint32_t bAddr = aAddr + aBytes;
           for (int q = 0; q < nq; ++q) {
-            const int b = kc % kNB;
+            const int b = kc % p.NB;
             if (!tc::mbar_wait_bounded(&tempty[b], ((tphase >> b) & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
               *abort_flag = 1;
               flag_error(p.dev_err, MOE_DEV_TIMEOUT);
@@ -383,8 +385,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb_end = u1 * p.KS < KB ? u1 * p.KS : KB;
       const float* wsg = p.wscale + ((size_t)ti.e * p.scale_rows + ti.m) * KBs;
       const float* wsu = p.wscale + ((size_t)ti.e * p.scale_rows + p.M / 128 + ti.m) * KBs;
+      // Row scales of the B operand: per row for gate/up (constant over the
+      // tile), per (row, k-block) for down.
+      float sbr[kMaxNM];
+#pragma unroll
+      for (int n = 0; n < kMaxNM; ++n) {
+        const int prow = (ti.prow_ok && n < ti.np) ? ti.prow + n : 0;
+        sbr[n] = kGateUp ? __ldg(&p.bscale[prow]) : 0.f;
+      }
       for (int kb = kb_first; kb < kb_end; ++kb) {
-        const int b = kc % kNB;
+        const int b = kc % p.NB;
+        // Scales of this k-block are requested before waiting for its MMAs,
+        // so their latency hides behind the wait.
+        const float sg = __ldg(&wsg[kb]);
+        const float su = kGateUp ? __ldg(&wsu[kb]) : 0.f;
+        if (!kGateUp) {
+#pragma unroll
+          for (int n = 0; n < kMaxNM; ++n) {
+            const int prow = (ti.prow_ok && n < ti.np) ? ti.prow + n : 0;
+            sbr[n] = __ldg(&p.bscale[(size_t)prow * KBs + kb]);
+          }
+        }
         if (!tc::mbar_wait_bounded(&tfull[b], (tphase >> b) & 1u, abort_flag, kWaitBudgetNs)) {
           *abort_flag = 1;
           flag_error(p.dev_err, MOE_DEV_TIMEOUT);
@@ -396,8 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tc_fence_after();
         const uint32_t tb = tmem_base + lane_off + b * buf_cols;
-        const float sg = __ldg(&wsg[kb]);
-        const float su = kGateUp ? __ldg(&wsu[kb]) : 0.f;
 #pragma unroll
         for (int cc = 0; cc < kMaxNM / 16; ++cc) {
           if (cc < ti.np / 16) {
@@ -412,8 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int n = cc * 16 + j;
-              const int prow = ti.prow_ok ? ti.prow + n : 0;
-              const float sb = kGateUp ? __ldg(&p.bscale[prow]) : __ldg(&p.bscale[(size_t)prow * KBs + kb]);
+              const float sb = sbr[n];
               ga[n] = fmaf(sg * sb, fmaf(gl[j], 1.f / kLoScale, gh[j]), ga[n]);
               if (kGateUp) ua[n] = fmaf(su * sb, fmaf(ul[j], 1.f / kLoScale, uh[j]), ua[n]);
             }
@@ -747,6 +765,13 @@ Fp8Geom fp8_geom(const moe_layer_weights& lw, int T, int k) {
   return g;
 }
 
+// As many promotion buffers as fit in 512 TMEM columns (at most kNBMax), so
+// the MMA can run ahead of the epilogue by several k-blocks.
+int nb_for(int cols_per_buffer) {
+  int nb = 512 / cols_per_buffer;
+  return nb > kNBMax ? kNBMax : nb;
+}
+
 uint32_t pow2_cols(int c) {
   uint32_t v = 32;
   while (v < static_cast<uint32_t>(c)) v <<= 1;
@@ -896,7 +921,8 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.K = lw.H;
   fp.KS = 1;
   fp.stages = g.stages_gu;
-  fp.tmem_cols = pow2_cols(kNB * 4 * g.NM);
+  fp.NB = nb_for(4 * g.NM);
+  fp.tmem_cols = pow2_cols(fp.NB * 4 * g.NM);
   fp.wscale = lw.scales_gate_up;
   fp.scale_rows = 2 * lw.I / 128;
   fp.bscale = ws.xscale;
@@ -916,7 +942,8 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.K = lw.I;
   fp.KS = g.KS_d;
   fp.stages = g.stages_d;
-  fp.tmem_cols = pow2_cols(kNB * 2 * g.NM);
+  fp.NB = nb_for(2 * g.NM);
+  fp.tmem_cols = pow2_cols(fp.NB * 2 * g.NM);
   fp.wscale = lw.scales_down;
   fp.scale_rows = lw.H / 128;
   fp.bscale = ws.hscale;

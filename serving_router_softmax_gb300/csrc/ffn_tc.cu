@@ -791,7 +791,7 @@ int ffn_tc_launch(const FfnArgs& a) {
 
   cudaStream_t s = a.stream;
   {
-    long long chunks = static_cast<long long>(g.Rmax) * (lw.H / 8);
+    long long chunks = static_cast<long long>(TK) * (lw.H / 8);  // real rows only
     int blocks = static_cast<int>((chunks + 255) / 256);
     if (blocks > g.G * 4) blocks = g.G * 4;
     if (blocks < 1) blocks = 1;

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(256) route_bias_kernel(
     const float* __restrict__ w_conf, int T, int E, int k, int cap, float alpha,
     int32_t* __restrict__ ids, float* __restrict__ w, int32_t* dev_err) {
   __shared__ BiasSmem sm;
-  route_bias_block<NPL>(logits, rows, rows_limit, w_conf, T, E, k, cap, alpha, ids, w, dev_err, sm);
+  route_bias_block<NPL>(logits, rows, rows_limit, w_conf, T, E, k, cap, alpha, ids, w, dev_err, view_of(sm));
 }
 
 template <int NPL>

@@ -74,27 +74,31 @@ __device__ __forceinline__ void argmax_round(Row<NPL>& r, int E, int lane, float
 }
 
 // Top-k of a loaded row and softmax over the selected logits; writes the
-// token's ids and weights.  The weight sum runs over j = 0..k-1 in order.
+// token's ids and weights.  Lane j keeps slot j, so the rounds need no
+// per-slot arrays; the softmax denominator is a fixed-order warp sum.
 template <int NPL>
 __device__ __forceinline__ void topk_softmax_write(Row<NPL>& r, int E, int k, int lane, int32_t* ids,
                                                    float* w) {
-  float sv[kMaxK];
-  int si[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < k) argmax_round(r, E, lane, sv[j], si[j]);
-  }
-  const float m = sv[0];
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j)
-    if (j < k) s = __fadd_rn(s, expf(sv[j] - m));
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < k && lane == j) {
-      ids[j] = si[j];
-      w[j] = __fdiv_rn(expf(sv[j] - m), s);
+  float mine_v = -INFINITY, m = 0.f;
+  int mine_i = -1;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float bv;
+    int bi;
+    argmax_round(r, E, lane, bv, bi);
+    if (j == 0) m = bv;
+    if (lane == j) {
+      mine_v = bv;
+      mine_i = bi;
     }
+  }
+  const float ex = lane < k ? expf(mine_v - m) : 0.f;
+  float s = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  if (lane < k) {
+    ids[lane] = mine_i;
+    w[lane] = __fdiv_rn(ex, s);
   }
 }
 
@@ -141,24 +145,60 @@ struct BiasSmem {
   int conf_bad;
 };
 
+// Shared-memory working set of the biased routing, as pointers so that it can
+// live in a static struct (standalone kernel) or be sized to T and E.
+struct BiasView {
+  uint32_t* member;  // [T][EW]
+  float* v1;         // [T]
+  float* vk1;        // [T]
+  uint8_t* bad;      // [T]
+  float* g;          // [E]
+  uint32_t* estar;   // [EW]
+  int* conf_bad;
+};
+
+__device__ __forceinline__ BiasView view_of(BiasSmem& sm) {
+  return BiasView{sm.member, sm.v1, sm.vk1, sm.bad, sm.g, sm.estar, &sm.conf_bad};
+}
+
+// Bytes of a BiasView carved by carve_bias (4-byte aligned pieces).
+__host__ __device__ inline size_t bias_view_bytes(int T, int E) {
+  const int EW = (E + 31) / 32;
+  const size_t Tb = (static_cast<size_t>(T) + 3) & ~size_t(3);
+  return 4 * (static_cast<size_t>(T) * EW + 2 * T + E + EW + 1) + Tb;
+}
+
+__device__ __forceinline__ BiasView carve_bias(uint8_t* p, int T, int E) {
+  const int EW = (E + 31) / 32;
+  BiasView v;
+  v.member = reinterpret_cast<uint32_t*>(p);
+  v.v1 = reinterpret_cast<float*>(v.member + (size_t)T * EW);
+  v.vk1 = v.v1 + T;
+  v.g = v.vk1 + T;
+  v.estar = reinterpret_cast<uint32_t*>(v.g + E);
+  v.conf_bad = reinterpret_cast<int*>(v.estar + EW);
+  v.bad = reinterpret_cast<uint8_t*>(v.conf_bad + 1);
+  return v;
+}
+
 // Biased routing over the whole block (T <= 256, E <= 1024).  All threads of
 // the block must call it; it synchronises the block.
 template <int NPL>
 __device__ __forceinline__ void route_bias_block(const float* __restrict__ logits, const int32_t* __restrict__ rows,
                                  int rows_limit, const float* __restrict__ w_conf, int T, int E, int k, int cap,
                                  float alpha, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* dev_err,
-                                 BiasSmem& sm) {
+                                 BiasView sm) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const int EW = (E + 31) >> 5;
 
-  if (threadIdx.x == 0) sm.conf_bad = 0;
-  for (int i = threadIdx.x; i < kMaxEW; i += blockDim.x) sm.estar[i] = 0;
+  if (threadIdx.x == 0) *sm.conf_bad = 0;
+  for (int i = threadIdx.x; i < EW; i += blockDim.x) sm.estar[i] = 0;
   __syncthreads();
   for (int t = threadIdx.x; t < T; t += blockDim.x) {
     float c = w_conf[t];
-    if (!(c >= 0.f)) sm.conf_bad = 1;  // NaN or negative
+    if (!(c >= 0.f)) *sm.conf_bad = 1;  // NaN or negative
   }
   // Pass 1: original top-(k+1) per token -> membership of TopK, l_(1), l_(k+1).
   for (int t = warp; t < T; t += nwarps) {
@@ -185,7 +225,7 @@ __device__ __forceinline__ void route_bias_block(const float* __restrict__ logit
     }
   }
   __syncthreads();
-  const bool conf_bad = sm.conf_bad != 0;
+  const bool conf_bad = *sm.conf_bad != 0;
   if (!conf_bad) {
     // Step 1: g_e = sum over tokens (ascending) of w_b for tokens whose top-k holds e.
     for (int e = threadIdx.x; e < E; e += blockDim.x) {

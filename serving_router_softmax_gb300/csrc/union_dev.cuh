@@ -23,8 +23,26 @@ struct UnionSmem {
   int err;
 };
 
+struct UnionView {
+  int32_t* count;   // [E]
+  int32_t* ustart;  // [E]
+  int* err;
+};
+
+__device__ __forceinline__ UnionView view_of(UnionSmem& us) { return UnionView{us.count, us.ustart, &us.err}; }
+
+__host__ __device__ inline size_t union_view_bytes(int E) { return 4 * (2 * static_cast<size_t>(E) + 1); }
+
+__device__ __forceinline__ UnionView carve_union(uint8_t* p, int E) {
+  UnionView v;
+  v.count = reinterpret_cast<int32_t*>(p);
+  v.ustart = v.count + E;
+  v.err = v.ustart + E;
+  return v;
+}
+
 // All threads of the block must call it; `member` holds T * ceil(E/32) words.
-__device__ __forceinline__ void union_block(const int32_t* __restrict__ ids, int T, int k, int E, uint32_t* member, UnionSmem& us,
+__device__ __forceinline__ void union_block(const int32_t* __restrict__ ids, int T, int k, int E, uint32_t* member, UnionView us,
                             int32_t* __restrict__ n_unique, int32_t* __restrict__ unique,
                             int32_t* __restrict__ offsets, int32_t* __restrict__ perm_token,
                             int32_t* __restrict__ perm_slot, int32_t* __restrict__ inv,
@@ -33,23 +51,23 @@ __device__ __forceinline__ void union_block(const int32_t* __restrict__ ids, int
   const int TK = T * k;
   for (int i = threadIdx.x; i < T * EW; i += blockDim.x) member[i] = 0;
   for (int e = threadIdx.x; e < E; e += blockDim.x) us.count[e] = 0;
-  if (threadIdx.x == 0) us.err = 0;
+  if (threadIdx.x == 0) *us.err = 0;
   __syncthreads();
 
   for (int p = threadIdx.x; p < TK; p += blockDim.x) {
     int t = p / k;
     int e = ids[p];
     if (e < 0 || e >= E) {
-      atomicOr(&us.err, MOE_DEV_BAD_ID);
+      atomicOr(us.err, MOE_DEV_BAD_ID);
       continue;
     }
     uint32_t bit = 1u << (e & 31);
     uint32_t old = atomicOr(&member[t * EW + (e >> 5)], bit);
-    if (old & bit) atomicOr(&us.err, MOE_DEV_DUP_ID);
+    if (old & bit) atomicOr(us.err, MOE_DEV_DUP_ID);
     atomicAdd(&us.count[e], 1);
   }
   __syncthreads();
-  const int err = us.err;
+  const int err = *us.err;
   if (err) {
     if (threadIdx.x == 0) {
       flag_error(dev_err, err);

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(1024) union_kernel(const int32_t* __restrict__
                                                      int32_t* dev_err) {
   extern __shared__ uint32_t member[];  // [T][EW]
   __shared__ unions::UnionSmem us;
-  unions::union_block(ids, T, k, E, member, us, n_unique, unique, offsets, perm_token, perm_slot, inv,
+  unions::union_block(ids, T, k, E, member, unions::view_of(us), n_unique, unique, offsets, perm_token, perm_slot, inv,
                       reuse_ratio, dev_err);
 }
 
