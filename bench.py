@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of the workload (recorded in config)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling only: use this many experts per layer (recorded in config)")
     ap.add_argument("--cpu-layers", type=int, default=0,
                     help="layers in the CPU oracle sample (0: auto, about 10-30 s)")
     return ap.parse_args()
@@ -206,6 +208,8 @@ def ours(args, rank, ws, local):
     cfg = CONFIGS[args.config]
     if args.layers:
         cfg = cfg.replace(L=min(args.layers, cfg.L))
+    if args.experts:
+        cfg = cfg.replace(E=args.experts, cap=min(cfg.cap, args.experts - cfg.k) if cfg.use_bias else cfg.cap)
     dev = torch.device("cuda", local)
     wl = gen.make_workload(cfg)
     # Weights: filled row-major, then packed once into the tiled layout the
@@ -346,7 +350,8 @@ def ours(args, rank, ws, local):
         "vs_baseline": None,
         "dtype": cfg.dtype,
         "data": "synthetic (seeded workload generator; counter-hash weights)",
-        "config": {"workload": cfg.name + (f" (first {cfg.L} layers, profiling run)" if args.layers else ""),
+        "config": {"workload": cfg.name + (f" (first {cfg.L} layers, profiling run)" if args.layers else "")
+                   + (f" ({cfg.E} experts, profiling run)" if args.experts else ""),
                    "layers": cfg.L, "hidden": cfg.H, "experts": cfg.E,
                    "top_k": cfg.k, "intermediate": cfg.I, "weights": cfg.dtype,
                    "batch": cfg.nseq, "verify_tokens": wl.T, "gamma": wl.gamma.tolist(),

@@ -58,10 +58,11 @@ struct Fp8Params {
   const int32_t* poff;
   const float* wscale;  // block scales of this matrix: [E][scale_rows][K/128]
   int scale_rows;       // gate/up: 2I/128 (gate blocks, then up blocks); down: H/128
-  const float* bscale;  // gate/up: [Rmax] per padded row; down: [Rmax][K/128]
+  const float* bscale;  // gate/up: [Rmax] per padded row; down: [K/128][hs_stride]
   uint8_t* hq_hi;       // gate/up output [Rmax][M]
   uint8_t* hq_lo;
-  float* hscale;        // gate/up output [Rmax][M/128]
+  float* hscale;        // gate/up output [M/128][hs_stride]
+  int hs_stride;        // rows of hscale per k-block (Rmax rounded up to 16)
   float* o;             // down output [T*k][M]
   float* partials;      // [grid][2][2*NM][128]
   int32_t* tile_cnt;
@@ -350,15 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int etid = threadIdx.x - 64;
     tc::griddep_wait();
-    const int TKc = p.T * p.k;
-    const bool comb_smem = !kGateUp && TKc <= kCombMax;
-    if (comb_smem) {
-      for (int i = etid; i < TKc; i += kEpiThreads) {
-        s_inv[i] = p.inv[i];
-        s_w[i] = p.w[i];
-      }
-      tc::named_bar_sync(1, kEpiThreads);
-    }
     const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
     const int KBs = p.K / 128;  // scale blocks along K (== KB)
     int kc = 0;
@@ -386,12 +378,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* wsg = p.wscale + ((size_t)ti.e * p.scale_rows + ti.m) * KBs;
       const float* wsu = p.wscale + ((size_t)ti.e * p.scale_rows + p.M / 128 + ti.m) * KBs;
       // Row scales of the B operand: per row for gate/up (constant over the
-      // tile), per (row, k-block) for down.
+      // tile), per (k-block, row) for down, stored k-block-major so that a
+      // tile's rows are contiguous (four 16-byte loads per 16 rows).
       float sbr[kMaxNM];
 #pragma unroll
-      for (int n = 0; n < kMaxNM; ++n) {
-        const int prow = (ti.prow_ok && n < ti.np) ? ti.prow + n : 0;
-        sbr[n] = kGateUp ? __ldg(&p.bscale[prow]) : 0.f;
+      for (int n = 0; n < kMaxNM; ++n) sbr[n] = 0.f;
+      const int prow0 = ti.prow_ok ? ti.prow : 0;
+      if (kGateUp) {
+#pragma unroll
+        for (int cc = 0; cc < kMaxNM / 16; ++cc)
+          if (cc < ti.np / 16) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 v = __ldg(reinterpret_cast<const float4*>(p.bscale + prow0 + cc * 16 + q * 4));
+              sbr[cc * 16 + q * 4] = v.x;
+              sbr[cc * 16 + q * 4 + 1] = v.y;
+              sbr[cc * 16 + q * 4 + 2] = v.z;
+              sbr[cc * 16 + q * 4 + 3] = v.w;
+            }
+          }
       }
       for (int kb = kb_first; kb < kb_end; ++kb) {
         const int b = kc % p.NB;
@@ -400,40 +405,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sg = __ldg(&wsg[kb]);
         const float su = kGateUp ? __ldg(&wsu[kb]) : 0.f;
         if (!kGateUp) {
+          const float* src = p.bscale + (size_t)kb * p.hs_stride + prow0;
 #pragma unroll
-          for (int n = 0; n < kMaxNM; ++n) {
-            const int prow = (ti.prow_ok && n < ti.np) ? ti.prow + n : 0;
-            sbr[n] = __ldg(&p.bscale[(size_t)prow * KBs + kb]);
-          }
+          for (int cc = 0; cc < kMaxNM / 16; ++cc)
+            if (cc < ti.np / 16) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(src + cc * 16 + q * 4));
+                sbr[cc * 16 + q * 4] = v.x;
+                sbr[cc * 16 + q * 4 + 1] = v.y;
+                sbr[cc * 16 + q * 4 + 2] = v.z;
+                sbr[cc * 16 + q * 4 + 3] = v.w;
+              }
+            }
         }
-        if (!tc::mbar_wait_bounded(&tfull[b], (tphase >> b) & 1u, abort_flag, kWaitBudgetNs)) {
+        // Warp-uniform wait: a warp that gives up keeps walking the same
+        // loop (skipping the arithmetic) so every later barrier is reached.
+        bool ok = tc::mbar_wait_bounded(&tfull[b], (tphase >> b) & 1u, abort_flag, kWaitBudgetNs);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok && lane == 0) {
           *abort_flag = 1;
           flag_error(p.dev_err, MOE_DEV_TIMEOUT);
         }
-        tc::named_bar_sync(1, kEpiThreads);
-        if (*abort_flag) {
-          stop = true;
-          break;
-        }
-        tc::tc_fence_after();
-        const uint32_t tb = tmem_base + lane_off + b * buf_cols;
+        if (ok) {
+          tc::tc_fence_after();
+          const uint32_t tb = tmem_base + lane_off + b * buf_cols;
 #pragma unroll
-        for (int cc = 0; cc < kMaxNM / 16; ++cc) {
-          if (cc < ti.np / 16) {
-            float gh[16], gl[16], uh[16], ul[16];
-            tc::tmem_ld16(tb + cc * 16, gh);
-            tc::tmem_ld16(tb + ti.np + cc * 16, gl);
-            if (kGateUp) {
-              tc::tmem_ld16(tb + 2 * p.NM + cc * 16, uh);
-              tc::tmem_ld16(tb + 2 * p.NM + ti.np + cc * 16, ul);
-            }
-            tc::tmem_ld_wait();
+          for (int cc = 0; cc < kMaxNM / 16; ++cc) {
+            if (cc < ti.np / 16) {
+              float gh[16], gl[16], uh[16], ul[16];
+              tc::tmem_ld16(tb + cc * 16, gh);
+              tc::tmem_ld16(tb + ti.np + cc * 16, gl);
+              if (kGateUp) {
+                tc::tmem_ld16(tb + 2 * p.NM + cc * 16, uh);
+                tc::tmem_ld16(tb + 2 * p.NM + ti.np + cc * 16, ul);
+              }
+              tc::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = cc * 16 + j;
-              const float sb = sbr[n];
-              ga[n] = fmaf(sg * sb, fmaf(gl[j], 1.f / kLoScale, gh[j]), ga[n]);
-              if (kGateUp) ua[n] = fmaf(su * sb, fmaf(ul[j], 1.f / kLoScale, uh[j]), ua[n]);
+              for (int j = 0; j < 16; ++j) {
+                const int n = cc * 16 + j;
+                const float sb = sbr[n];
+                ga[n] = fmaf(sg * sb, fmaf(gl[j], 1.f / kLoScale, gh[j]), ga[n]);
+                if (kGateUp) ua[n] = fmaf(su * sb, fmaf(ul[j], 1.f / kLoScale, uh[j]), ua[n]);
+              }
             }
           }
         }
@@ -442,7 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tphase ^= 1u << b;
         ++kc;
       }
-      if (stop) break;
+      tc::named_bar_sync(1, kEpiThreads);
+      if (*abort_flag) {
+        stop = true;
+        break;
+      }
 
       const bool whole = u0 == 0 && u1 == KU;
       bool finished = whole;
@@ -512,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ti.prow_ok && row_ok) {
               p.hq_hi[(size_t)(ti.prow + n) * p.M + row] = hi;
               p.hq_lo[(size_t)(ti.prow + n) * p.M + row] = lo;
-              if (r == 0) p.hscale[(size_t)(ti.prow + n) * (p.M / 128) + ti.m] = sc;
+              if (r == 0) p.hscale[(size_t)ti.m * p.hs_stride + ti.prow + n] = sc;
             }
           }
         }
@@ -521,49 +539,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int n = 0; n < kMaxNM; ++n)
           if (n < ti.ne && row_ok) p.o[(size_t)(ti.off + n) * p.M + row] = ga[n];
-        tc::named_bar_sync(1, kEpiThreads);
-        if (etid == 0) {
-          __threadfence();
-          *bcast = atomicAdd(&p.done_cnt[ti.m], 1);
-        }
-        tc::named_bar_sync(1, kEpiThreads);
-        const int done = *bcast;
-        tc::named_bar_sync(1, kEpiThreads);
-        if (done == U - 1) {
-          __threadfence();
-          const int TK = p.T * p.k;
-          for (int tb = 0; tb < p.T && row_ok; tb += 2) {
-            int pos[2][16];
-            float wv[2][16], ov[2][16];
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int tok = tb + a;
-                const bool in = tok < p.T && j < p.k;
-                const int idx = tok * p.k + j;
-                pos[a][j] = in ? (comb_smem ? s_inv[idx] : __ldg(&p.inv[idx])) : -1;
-                wv[a][j] = in ? (comb_smem ? s_w[idx] : __ldg(&p.w[idx])) : 0.f;
-              }
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const bool ok = pos[a][j] >= 0 && pos[a][j] < TK;
-                if (tb + a < p.T && j < p.k && !ok) flag_error(p.dev_err, MOE_DEV_BAD_ID);
-                ov[a][j] = ok ? __ldcg(&p.o[(size_t)pos[a][j] * p.M + row]) : 0.f;
-              }
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-              if (tb + a >= p.T) break;
-              float s = 0.f;
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < p.k && pos[a][j] >= 0 && pos[a][j] < TK) s = fmaf(wv[a][j], ov[a][j], s);
-              p.y[(size_t)(tb + a) * p.M + row] = s;
-            }
-          }
-        }
       }
     }
   }
@@ -799,10 +774,10 @@ Fp8Ws fp8_carve(const moe_layer_weights& lw, int T, int k, void* base) {
   };
   w.xq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.H));
   w.xq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.H));
-  w.xscale = reinterpret_cast<float*>(take(static_cast<size_t>(g.Rmax) * 4));
+  w.xscale = reinterpret_cast<float*>(take(static_cast<size_t>((g.Rmax + 15) & ~15) * 4));
   w.hq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.I));
   w.hq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.I));
-  w.hscale = reinterpret_cast<float*>(take(static_cast<size_t>(g.Rmax) * (lw.I / 128) * 4));
+  w.hscale = reinterpret_cast<float*>(take(static_cast<size_t>((g.Rmax + 15) & ~15) * (lw.I / 128) * 4));
   w.o = reinterpret_cast<float*>(take(static_cast<size_t>(TK) * lw.H * 4));
   w.partials = reinterpret_cast<float*>(take(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4));
   w.poff = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cap + 1) * 4));
@@ -900,6 +875,7 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.cap = cap;
   fp.NM = g.NM;
   fp.Rmax = g.Rmax;
+  fp.hs_stride = (g.Rmax + 15) & ~15;
   fp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
   fp.pdl = 1;
   fp.n_unique = a.n_unique;
@@ -958,7 +934,8 @@ int ffn_fp8_launch(const FfnArgs& a) {
                  fp) != MOE_OK)
       return MOE_ERR_CUDA;
   }
-  return MOE_OK;
+  // Weighted combine of the per-(token, slot) outputs, slot order.
+  return combine_launch(a, ws.o, true);
 }
 
 }  // namespace moe

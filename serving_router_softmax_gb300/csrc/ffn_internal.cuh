@@ -13,7 +13,7 @@ struct FfnWorkspace {
 
 FfnWorkspace ffn_carve(const moe_layer_weights& lw, int T, int k, void* base);
 int ffn_simt_launch(const FfnArgs& a, const FfnWorkspace& ws);
-int combine_launch(const FfnArgs& a, const float* o);
+int combine_launch(const FfnArgs& a, const float* o, bool pdl);
 
 // Tensor-core path (bf16 weights).
 bool ffn_tc_supported(const moe_layer_weights& lw, int T, int k);

@@ -271,13 +271,17 @@ __global__ void __launch_bounds__(256) down_simt_kernel(
 
 }  // namespace
 
-// y[t, :] = sum_j w[t, j] * o[inv[t*k + j], :], slots in order.
+// y[t, :] = sum_j w[t, j] * o[inv[t*k + j], :], slots in order.  Shared by
+// all FFN paths; after the tensor-core down kernels it is launched with
+// programmatic dependent launch.
 __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, int E,
                                                       const int32_t* __restrict__ n_unique,
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w,
                                                       const float* __restrict__ o,
                                                       float* __restrict__ y, int32_t* dev_err) {
+  pdl_wait();
+  pdl_trigger();
   const int TK = T * k;
   int U = *n_unique;
   const bool valid = U > 0 && U <= min(E, TK);
@@ -338,10 +342,10 @@ int ffn_simt_launch(const FfnArgs& a, const FfnWorkspace& ws) {
     default:
       return MOE_ERR_UNSUPPORTED;
   }
-  return combine_launch(a, ws.o);
+  return combine_launch(a, ws.o, false);
 }
 
-int combine_launch(const FfnArgs& a, const float* o) {
+int combine_launch(const FfnArgs& a, const float* o, bool pdl) {
   const int H = a.lw.H;
   long long total = (long long)a.T * (H / 4);
   int blocks = static_cast<int>((total + 255) / 256);
@@ -349,9 +353,8 @@ int combine_launch(const FfnArgs& a, const float* o) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   LaunchScope ls(kProfCombine, a.stream);
-  combine_kernel<<<blocks, 256, 0, a.stream>>>(a.T, a.k, H, a.lw.E, a.n_unique, a.inv, a.w, o, a.y,
-                                               a.dev_err);
-  return check_launch();
+  return launch_k(combine_kernel, dim3(blocks), dim3(256), 0, a.stream, pdl, a.T, a.k, H, a.lw.E, a.n_unique,
+                  a.inv, a.w, o, a.y, a.dev_err);
 }
 
 }  // namespace moe

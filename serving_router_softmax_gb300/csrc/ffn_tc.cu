@@ -346,16 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int etid = threadIdx.x - 64;  // 0..127
     tc::griddep_wait();
-    const int TKc = p.T * p.k;
-    const bool comb_smem = !kGateUp && TKc <= kCombMax;
-    if (comb_smem) {
-      // The combine's routing data, staged while the first tiles stream.
-      for (int i = etid; i < TKc; i += kEpiThreads) {
-        s_inv[i] = p.inv[i];
-        s_w[i] = p.w[i];
-      }
-      tc::named_bar_sync(1, kEpiThreads);
-    }
     int acc = 0;
     uint32_t acc_phase[2] = {0, 0};
     const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
@@ -463,55 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!kGateUp && finished) {
-        // Count the finished tile for its 128-row block of y; the CTA that
-        // completes the block combines it (same release/acquire pattern).
-        tc::named_bar_sync(1, kEpiThreads);
-        if (etid == 0) {
-          __threadfence();
-          *bcast = atomicAdd(&p.done_cnt[ti.m], 1);
-        }
-        tc::named_bar_sync(1, kEpiThreads);
-        const int done = *bcast;
-        tc::named_bar_sync(1, kEpiThreads);
-        if (done == U - 1) {
-          __threadfence();
-          const int TK = p.T * p.k;
-          // Two tokens per round, all their slots' loads in flight at once;
-          // each token's sum runs over its slots in order.
-          for (int tb = 0; tb < p.T && row_ok; tb += 2) {
-            int pos[2][16];
-            float wv[2][16], ov[2][16];
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int tok = tb + a;
-                const bool in = tok < p.T && j < p.k;
-                const int idx = tok * p.k + j;
-                pos[a][j] = in ? (comb_smem ? s_inv[idx] : __ldg(&p.inv[idx])) : -1;
-                wv[a][j] = in ? (comb_smem ? s_w[idx] : __ldg(&p.w[idx])) : 0.f;
-              }
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const bool ok = pos[a][j] >= 0 && pos[a][j] < TK;
-                if (tb + a < p.T && j < p.k && !ok) flag_error(p.dev_err, MOE_DEV_BAD_ID);
-                ov[a][j] = ok ? __ldcg(&p.o[(size_t)pos[a][j] * p.M + row]) : 0.f;
-              }
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-              if (tb + a >= p.T) break;
-              float s = 0.f;
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < p.k && pos[a][j] >= 0 && pos[a][j] < TK) s = fmaf(wv[a][j], ov[a][j], s);
-              p.y[(size_t)(tb + a) * p.M + row] = s;
-            }
-          }
-        }
-      }
+
     }
   }
 
@@ -860,7 +802,8 @@ int ffn_tc_launch(const FfnArgs& a) {
         MOE_OK)
       return MOE_ERR_CUDA;
   }
-  return MOE_OK;
+  // Weighted combine of the per-(token, slot) outputs, slot order.
+  return combine_launch(a, o, true);
 }
 
 }  // namespace moe
