@@ -54,6 +54,14 @@ def make_layer_tensors(cfg: gen.MoEConfig, layer: int, device="cuda"):
     return gu, dn, sgu, sdn
 
 
+def make_router_tensor(cfg: gen.MoEConfig, layer: int, device="cuda"):
+    """W_r [E, H] of one layer on the device (int16 bf16 bits or float32)."""
+    f32 = gen.router_dtype(cfg) == "f32"
+    w = torch.empty((cfg.E, cfg.H), dtype=torch.float32 if f32 else torch.int16, device=device)
+    fill(w, ch.KIND_GRID8_F32 if f32 else ch.KIND_GRID8_BF16, gen.router_stream_key(cfg, layer))
+    return w
+
+
 def workload_tensors(wl: gen.Workload, device="cuda"):
     """Host arrays of the workload as device tensors (int16 view for bf16 bits)."""
     cfg = wl.cfg

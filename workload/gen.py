@@ -168,6 +168,25 @@ def weight_stream_keys(cfg: MoEConfig, layer: int) -> dict:
     }
 
 
+def router_stream_key(cfg: MoEConfig, layer: int) -> int:
+    """Counter-hash key of one layer's router matrix W_r [E, H]."""
+    return ch.stream_key(ch.mix64_int(0x5EED0000 + cfg.seed), layer * 16 + 4)
+
+
+def router_dtype(cfg: MoEConfig) -> str:
+    """Storage type of the router matrix: fp32 for fp32 models, else bf16
+    (FP8 models keep their router in bf16)."""
+    return "f32" if cfg.dtype == "f32" else "bf16"
+
+
+def router_weights_host(cfg: MoEConfig, layer: int) -> np.ndarray:
+    """Host copy of W_r [E, H] (storage bits for bf16, values for fp32); the
+    same grid values as the expert weights, odd multiples of 2^-13."""
+    kind = ch.KIND_GRID8_F32 if router_dtype(cfg) == "f32" else ch.KIND_GRID8_BF16
+    n = cfg.E * cfg.H
+    return ch.fill_host(kind, router_stream_key(cfg, layer), 0, n).reshape(cfg.E, cfg.H)
+
+
 def weight_shapes(cfg: MoEConfig) -> dict:
     """Per-layer tensor shapes (expert-major, each expert contiguous).
 
