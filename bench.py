@@ -153,12 +153,12 @@ class ClockSampler:
 
 
 def kernel_source_hash():
-    """Hash of the FFN gate/up kernel sources (ties committed ncu traffic to the code)."""
+    """Hash of the sources that define the bf16 FFN kernels (their translation
+    unit and its PTX wrappers); ties committed ncu traffic to the code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_router_softmax_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.startswith("ffn") or f == "common.cuh":
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ("ffn_tc.cu", "ffn_internal.cuh", "tc_ptx.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -196,6 +196,44 @@ def gate_up_bytes(cfg):
     if cfg.dtype == "e4m3":
         b += 4 * (2 * cfg.I // 128) * (cfg.H // 128)
     return b
+
+
+def router_measure(mv, cfg, wl, dev, stream, iters=200):
+    """Gate logits of the step's verify tokens (T x H activations against one
+    layer's E x H gate), timed with CUDA events over back-to-back launches that
+    cycle through enough distinct gate matrices to exceed L2."""
+    import torch
+    from workload import device as wdev
+
+    T = wl.T
+    rows = wl.x[0].reshape(-1, cfg.H)[:T]
+    x = torch.from_numpy(rows.copy() if cfg.dtype == "f32" else rows.view(np.int16).copy()).to(dev)
+    first = wdev.make_router_tensor(cfg, 0, dev)
+    per = first.numel() * first.element_size()
+    n_mats = max(2, -(-(256 << 20) // per))
+    mats = [first] + [wdev.make_router_tensor(cfg, l, dev) for l in range(1, n_mats)]
+    out = torch.empty((T, cfg.E), dtype=torch.float32, device=dev)
+    for i in range(3):
+        mv.router_logits(x, mats[i % n_mats], out=out)
+    torch.cuda.synchronize()
+    # events around each launch (the library's profiler), so host-side call
+    # overhead between launches is not counted as kernel time
+    mv.profile_begin(max_launches=iters + 8, classes=["router_logits"])
+    for i in range(iters):
+        mv.router_logits(x, mats[i % n_mats], out=out)
+    torch.cuda.synchronize()
+    rp = mv.profile_end()["router_logits"]
+    us = rp["ms"] * 1e3 / max(rp["launches"], 1)
+    nbytes = per + x.numel() * x.element_size() + out.numel() * 4
+    peak, peak_kind = peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del mats
+    torch.cuda.empty_cache()
+    return {"T": T, "H": cfg.H, "E": cfg.E, "w_dtype": "f32" if cfg.dtype == "f32" else "bf16",
+            "us_per_launch": us, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+            "frac_of_peak": gbs / peak, "peak_kind": peak_kind, "bound": "latency",
+            "timed": f"CUDA events around each of {iters} launches over {n_mats} distinct gate matrices "
+                     f"({n_mats * per / 2**20:.0f} MiB > L2)"}
 
 
 def ours(args, rank, ws, local):
@@ -289,6 +327,9 @@ def ours(args, rank, ws, local):
     torch.cuda.synchronize()
     prof = mv.profile_end()
 
+    # ---- router logits, timed alone (the step routes the given node logits).
+    router = router_measure(mv, cfg, wl, dev, stream)
+
     # ---- roofline of the dominant kernel (FFN gate/up), from pass B.
     gu_bytes = sum(n_unique) * gate_up_bytes(cfg) * args.steps
     gu_ms = gu["ms"]
@@ -373,6 +414,7 @@ def ours(args, rank, ws, local):
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms / args.steps,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "router_logits": router,
     }
     return result, wl, cfg
 

@@ -4,6 +4,7 @@
  * The library computes the data-parallel hot path of one speculative-decoding
  * verify step of a Mixture-of-Experts model:
  *   eco_select         EcoSpec cost-aware greedy draft selection
+ *   moe_router_logits  router (gate) logits x . W_r^T of the verify tokens
  *   moe_route          router top-k + softmax weights, optional S2-MoE reuse bias
  *   moe_union_permute  expert union of the verify tokens, per-expert token groups
  *   moe_verify_ffn     grouped SwiGLU expert FFN over the union + weighted combine
@@ -67,6 +68,41 @@ enum {
   MOE_DTYPE_E4M3_B128 = 2  /* FP8 E4M3 weights with one fp32 scale per 128x128 block;
                               bf16 activations                                              */
 };
+
+/* ---------------------------------------------------------------- router
+ * moe_router_logits -- the gate's score of every expert for every token.
+ *
+ * Defined by: S2-MoE write-up, background (each MoE layer holds E expert
+ * FFNs and a router/gate chooses each token's top-k of them) and EcoSpec
+ * write-up section 2 (S_l(x_t), the experts token t routes to at layer l, is
+ * a function of its hidden state x_t).  The gate is read as a bias-free
+ * linear layer:
+ *   logits[t, e] = sum_{h < H} x[t, h] * w_router[e, h]
+ * with fp32 products and fp32 accumulation in a fixed order, so repeated
+ * calls give identical bits.  The output is the input of moe_route.
+ *
+ *   x         [T, H] activations: cfg->x_dtype MOE_DTYPE_F32 or MOE_DTYPE_BF16
+ *             (16-bit patterns).  16-byte aligned.
+ *   w_router  [E, H] gate matrix: cfg->w_dtype MOE_DTYPE_F32 or
+ *             MOE_DTYPE_BF16.  16-byte aligned.
+ *   logits    [T, E] fp32 out.  4-byte aligned.
+ * Limits: 8 <= H <= 1048576 with H % 8 == 0, 1 <= E <= 1024,
+ * 0 <= T <= 65536 (T == 0 enqueues nothing and needs no pointers).
+ * Errors: MOE_ERR_ARG for a negative size, a NULL or misaligned pointer;
+ * MOE_ERR_UNSUPPORTED for sizes or dtypes outside the limits.  There are no
+ * device-side errors: NaN or Inf inputs propagate into the logits, and
+ * moe_route then flags MOE_DEV_NAN_LOGIT.
+ * Accuracy: each logit carries at most 8 * ceil(H / 1024) + 8 roundings in
+ * sequence, so |error| <= gamma_n * sum_h |x[t,h] * w_router[e,h]| with
+ * n = 8 * ceil(H / 1024) + 8 and gamma_n = n u / (1 - n u), u = 2^-24.
+ */
+typedef struct {
+  int32_t T, H, E;
+  int32_t x_dtype, w_dtype;
+} moe_router_cfg;
+
+int moe_router_logits(const void* x, const void* w_router, const moe_router_cfg* cfg,
+                      float* logits, void* stream);
 
 /* ---------------------------------------------------------------- routing
  * moe_route -- per token: top-k experts of the router logits and their weights.
@@ -313,10 +349,11 @@ int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* pare
  * max_launches pairs; later launches are not recorded).  moe_profile_end
  * synchronises those events (host blocking) and writes, per kernel class, the
  * summed milliseconds and the launch count.  Classes: 0 eco_select, 1 route,
- * 2 union/permute, 3 FFN prep, 4 FFN gate/up, 5 FFN down, 6 combine.
+ * 2 union/permute, 3 FFN prep, 4 FFN gate/up, 5 FFN down, 6 combine,
+ * 7 router logits.
  * Not for use under stream capture.
  */
-enum { MOE_PROF_CLASSES = 7 };
+enum { MOE_PROF_CLASSES = 8 };
 int moe_profile_begin(int32_t max_launches, int32_t class_mask);
 int moe_profile_end(float* ms_per_class, int32_t* launches_per_class, int32_t n_classes);
 

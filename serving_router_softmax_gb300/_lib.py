@@ -16,11 +16,16 @@ DEV_NAN_LOGIT, DEV_BAD_ID, DEV_DUP_ID, DEV_BAD_TREE, DEV_BAD_PROB, DEV_TIMEOUT, 
 DTYPE_F32, DTYPE_BF16, DTYPE_E4M3_B128 = 0, 1, 2
 LAYOUT_ROWMAJOR, LAYOUT_TILED = 0, 1
 PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up", "ffn_down",
-                "combine"]
+                "combine", "router_logits"]
 
-EXPORTED = ["moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
+EXPORTED = ["moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
             "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_profile_begin",
             "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version"]
+
+
+class RouterCfg(C.Structure):
+    _fields_ = [("T", C.c_int32), ("H", C.c_int32), ("E", C.c_int32), ("x_dtype", C.c_int32),
+                ("w_dtype", C.c_int32)]
 
 
 class RouteCfg(C.Structure):
@@ -62,6 +67,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib = C.CDLL(path)
     vp, i32, sz = C.c_void_p, C.c_int32, C.c_size_t
     P = C.POINTER
+    lib.moe_router_logits.argtypes = [vp, vp, P(RouterCfg), vp, vp]
+    lib.moe_router_logits.restype = C.c_int
     lib.moe_route.argtypes = [vp, vp, P(RouteCfg), vp, vp, vp, vp]
     lib.moe_route.restype = C.c_int
     lib.moe_union_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]

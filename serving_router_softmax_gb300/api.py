@@ -116,6 +116,36 @@ def pack_tiled(layer: ExpertLayer, stream=None) -> ExpertLayer:
 
 
 # ------------------------------------------------------------------ calls
+def _act_dtype(t: torch.Tensor, name: str) -> int:
+    if t.dtype == torch.float32:
+        return L.DTYPE_F32
+    if t.dtype in (torch.int16, torch.bfloat16):
+        return L.DTYPE_BF16
+    raise MoEError(f"{name}: expected float32, bfloat16 or int16 (bf16 bits), got {t.dtype}")
+
+
+def router_logits(x: torch.Tensor, w_router: torch.Tensor, out: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """Gate logits [T, E] fp32 = x [T, H] . w_router [E, H]^T (fp32 accumulation).
+
+    ``x`` and ``w_router`` are float32, bfloat16 or int16 holding bf16 bits."""
+    lib = L.load()
+    T, H = x.shape
+    E = w_router.shape[0]
+    if w_router.shape != (E, H):
+        raise MoEError(f"w_router: expected shape ({E}, {H}), got {tuple(w_router.shape)}")
+    for t, n in ((x, "x"), (w_router, "w_router")):
+        if not t.is_contiguous():
+            raise MoEError(f"{n} must be contiguous")
+    if out is None:
+        out = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    _need(out, torch.float32, (T, E), "out")
+    cfg = L.RouterCfg(T, H, E, _act_dtype(x, "x"), _act_dtype(w_router, "w_router"))
+    _check(lib.moe_router_logits(_ptr(x), _ptr(w_router), C.byref(cfg), _ptr(out), _stream(stream)),
+           "moe_router_logits")
+    return out
+
+
 def route(logits: torch.Tensor, k: int, w_conf: Optional[torch.Tensor] = None, cap: int = 0,
           alpha: float = 0.0, dev_err: Optional[torch.Tensor] = None, stream=None):
     """Top-k ids [T, k] int32 and weights [T, k] fp32 (optionally reuse-biased)."""

@@ -21,7 +21,7 @@ struct LaunchScope {
 };
 
 enum ProfClass { kProfEco = 0, kProfRoute = 1, kProfUnion = 2, kProfPrep = 3, kProfGateUp = 4,
-                 kProfDown = 5, kProfCombine = 6 };
+                 kProfDown = 5, kProfCombine = 6, kProfRouter = 7 };
 
 int sm_count();
 
@@ -118,6 +118,18 @@ int layer_head_launch(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, i
 int union_launch(const int32_t* ids, int T, int k, int E, int32_t* n_unique, int32_t* unique,
                  int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, int32_t* inv,
                  float* reuse_ratio, int32_t* dev_err, cudaStream_t s);
+
+// Router logits (optionally launched with programmatic dependent launch).
+struct RouterArgs {
+  const void* x;            // [T, H] fp32 or bf16 bits
+  const void* w_router;     // [E, H] fp32 or bf16 bits
+  moe_router_cfg cfg;
+  float* logits;            // [T, E]
+  cudaStream_t stream;
+  bool pdl;
+};
+int router_validate(const moe_router_cfg& c);
+int router_launch(const RouterArgs& a);
 
 struct EcoArgs {
   const float* P;

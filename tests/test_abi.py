@@ -28,7 +28,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["moe_route", "moe_union_permute", "moe_verify_ffn", "moe_verify_ffn_workspace",
+    for n in ["moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn", "moe_verify_ffn_workspace",
               "eco_select", "moe_verify_step", "moe_verify_step_workspace"]:
         assert n in names
 
@@ -53,6 +53,13 @@ def test_host_only_calls(lib):
                                                        ctypes.POINTER(L.EcoCfg)] + [ctypes.c_void_p] * 4
     assert lib.eco_select(None, None, None, 1, None, ctypes.byref(ecfg), None, None, None,
                           None) == L.MOE_ERR_UNSUPPORTED
+    rcfg = L.RouterCfg(2, 12, 4, L.DTYPE_BF16, L.DTYPE_BF16)  # H not a multiple of 8
+    lib.moe_router_logits.argtypes = [ctypes.c_void_p] * 2 + [ctypes.POINTER(L.RouterCfg)] + [ctypes.c_void_p] * 2
+    assert lib.moe_router_logits(None, None, ctypes.byref(rcfg), None, None) == L.MOE_ERR_UNSUPPORTED
+    rcfg = L.RouterCfg(0, 64, 4, L.DTYPE_BF16, L.DTYPE_F32)  # T = 0: nothing to do, no pointers needed
+    assert lib.moe_router_logits(None, None, ctypes.byref(rcfg), None, None) == L.MOE_OK
+    rcfg = L.RouterCfg(2, 64, 4, L.DTYPE_E4M3_B128, L.DTYPE_BF16)  # FP8 activations not accepted
+    assert lib.moe_router_logits(None, None, ctypes.byref(rcfg), None, None) == L.MOE_ERR_UNSUPPORTED
     lw = L.LayerWeights(100, 64, 8, 1, 0, None, None, None, None)  # H not a multiple of 64
     lib.moe_verify_ffn_workspace.argtypes = [ctypes.POINTER(L.LayerWeights), ctypes.c_int32, ctypes.c_int32]
     lib.moe_verify_ffn_workspace.restype = ctypes.c_size_t
