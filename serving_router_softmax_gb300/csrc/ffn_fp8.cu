@@ -7,7 +7,8 @@
 //   * A = E4M3 weights exactly as stored: 128 rows x 128 reduction bytes per
 //     k-block, TMA-loaded with the 128-byte swizzle.
 //   * B = activations as two E4M3 matrices per row: with a per-row scale s,
-//     hi = e4m3(x / s) and lo = e4m3((x / s - hi) * 16), so that
+//     a power of two that puts max |x| / s in [128, 256) (so the scaling is
+//     exact), hi = e4m3(x / s) and lo = e4m3((x / s - hi) * 16), so that
 //     x ~= s * (hi + lo / 16) with relative error near 2^-8.  hi and lo rows
 //     are stacked, so one MMA of N = 2 * np produces both partial products.
 //   * The weight block scale changes every 128 reduction elements, so every
@@ -18,8 +19,9 @@
 //   * gate/up writes h = silu(gate) * up quantized the same way, with one
 //     scale per (token, 128-row block of I), which is exactly one k-block of
 //     the down projection.
-// Stream-K partitioning over the layer's k-blocks, the last-arriver fixup of
-// split tiles and the fused weighted combine follow the bf16 kernel.
+// Stream-K partitioning over the layer's k-blocks and the last-arriver fixup
+// of split tiles follow the bf16 kernel; the weighted combine is its own
+// kernel afterwards.
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
@@ -39,7 +41,6 @@ constexpr int kNBMax = 16;         // TMEM promotion buffers (at most)
 constexpr int kMaxNM = 32;         // padded token columns handled by this path
 constexpr int kCombMax = 512;
 constexpr float kLoScale = 16.f;
-constexpr float kE4M3Max = 448.f;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 constexpr int kBarRegion = 512;    // mbarriers + flags of the CTA
 static_assert((2 * 12 + 2 * kNBMax + 1) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
@@ -127,6 +128,19 @@ __device__ __forceinline__ uint8_t float_to_e4m3(float v) {
 __device__ __forceinline__ void split_e4m3(float v, uint8_t& hi, uint8_t& lo) {
   hi = float_to_e4m3(v);
   lo = float_to_e4m3((v - e4m3_to_float(hi)) * kLoScale);
+}
+
+// Power-of-two scale s with amax / s in [128, 256), and 1/s: dividing by s is
+// then an exact multiplication.  Zero, NaN or tiny amax give s = 1.
+__device__ __forceinline__ void pow2_scale(float amax, float& s, float& inv_s) {
+  const int f = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+  if (!(amax > 0.f) || f < -119 || f > 127) {
+    s = 1.f;
+    inv_s = 1.f;
+    return;
+  }
+  s = __uint_as_float(static_cast<uint32_t>(f - 7 + 127) << 23);
+  inv_s = __uint_as_float(static_cast<uint32_t>(7 - f + 127) << 23);
 }
 
 template <bool kGateUp>
@@ -506,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (kGateUp) {
         // h = silu(gate) * up, quantized per (token, 128-row block) for the
-        // down projection: scale = max |h| over the block's rows / 448.
+        // down projection, with the power-of-two scale of max |h| over the
+        // block's rows.
         float h[kMaxNM];
 #pragma unroll
         for (int n = 0; n < kMaxNM; ++n) h[n] = (n < ti.ne && row_ok) ? silu_mul(ga[n], ua[n]) : 0.f;
@@ -524,9 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; n < kMaxNM; ++n) {
           if (n < ti.ne) {
             const float amax = fmaxf(fmaxf(s_red[n], s_red[kMaxNM + n]), fmaxf(s_red[2 * kMaxNM + n], s_red[3 * kMaxNM + n]));
-            const float sc = amax > 0.f ? amax / kE4M3Max : 1.f;
+            float sc, inv_sc;
+            pow2_scale(amax, sc, inv_sc);
             uint8_t hi, lo;
-            split_e4m3(h[n] / sc, hi, lo);
+            split_e4m3(h[n] * inv_sc, hi, lo);
             if (ti.prow_ok && row_ok) {
               p.hq_hi[(size_t)(ti.prow + n) * p.M + row] = hi;
               p.hq_lo[(size_t)(ti.prow + n) * p.M + row] = lo;
@@ -559,32 +575,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Padded group offsets, zeroed fixup counters and the quantized activations:
-// one warp per (token, slot) pair writes hi/lo E4M3 rows and the row scale.
-__global__ void __launch_bounds__(256) ffn_fp8_prep_kernel(
+// Padded group offsets, zeroed fixup counters and the quantized activations.
+// One CTA per token: it finds max |x| over the token's row, quantizes the row
+// once (power-of-two scale, hi/lo E4M3 pair) and writes it to every padded
+// row the token occupies, one per routed slot (found through inv).
+constexpr int kPrepThreads = 256;
+
+__global__ void __launch_bounds__(kPrepThreads) ffn_fp8_prep_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ x_rows, int x_rows_limit, int T, int k, int H,
     int cap, const int32_t* __restrict__ n_unique, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ perm_token, uint8_t* __restrict__ xq_hi, uint8_t* __restrict__ xq_lo,
+    const int32_t* __restrict__ inv, uint8_t* __restrict__ xq_hi, uint8_t* __restrict__ xq_lo,
     float* __restrict__ xscale, int32_t* __restrict__ poff, int32_t* __restrict__ counters, int n_counters,
     float* __restrict__ y, int32_t* dev_err) {
   __shared__ int32_t spoff[1025];
+  __shared__ int32_t soff[1025];  // offsets[0..U], for the group searches
+  __shared__ int32_t s_rr[16];
+  __shared__ float s_max[kPrepThreads / 32];
   __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
   const int TK = T * k;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x) counters[i] = 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = blockIdx.x * blockDim.x + tid; i < n_counters; i += gridDim.x * blockDim.x) counters[i] = 0;
   const int U = *n_unique;
-  if (threadIdx.x == 0) s_bad = 0;
+  if (tid == 0) s_bad = 0;
   __syncthreads();
   if (U < 1 || U > cap) {
-    if (U != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(dev_err, MOE_DEV_CAPACITY);
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * H;
+    if (U != 0 && blockIdx.x == 0 && tid == 0) flag_error(dev_err, MOE_DEV_CAPACITY);
+    for (long long i = blockIdx.x * (long long)blockDim.x + tid; i < (long long)T * H;
          i += (long long)gridDim.x * blockDim.x)
       y[i] = 0.f;
     return;
   }
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
+  if (warp == 0) {
     const int per = (U + 31) / 32;
     const int u0 = lane * per;
     int sum = 0;
@@ -592,6 +615,7 @@ __global__ void __launch_bounds__(256) ffn_fp8_prep_kernel(
       const int a = offsets[u], b = offsets[u + 1];
       if (a < 0 || b > TK || b - a < 1 || b - a > T) s_bad = 1;
       sum += ((b - a) + 15) & ~15;
+      soff[u] = a;
     }
     int ex = sum;
     for (int off = 1; off < 32; off <<= 1) {
@@ -605,44 +629,53 @@ __global__ void __launch_bounds__(256) ffn_fp8_prep_kernel(
     }
     if (lane == 31) {
       spoff[U] = ex;
+      soff[U] = offsets[U];
       if (offsets[U] != TK || offsets[0] != 0) s_bad = 1;
     }
   }
   __syncthreads();
   if (s_bad) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * H;
+    if (blockIdx.x == 0 && tid == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
+    for (long long i = blockIdx.x * (long long)blockDim.x + tid; i < (long long)T * H;
          i += (long long)gridDim.x * blockDim.x)
       y[i] = 0.f;
     return;
   }
   if (blockIdx.x == 0)
-    for (int u = threadIdx.x; u <= U; u += blockDim.x) poff[u] = spoff[u];
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int pp = gw; pp < TK; pp += nw) {
-    int lo = 0, hi = U - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (offsets[mid] <= pp) lo = mid;
-      else hi = mid - 1;
+    for (int u = tid; u <= U; u += blockDim.x) poff[u] = spoff[u];
+
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    // padded rows of the token's k slots (-1: invalid position)
+    if (tid < k) {
+      const int pp = inv[t * k + tid];
+      int rr = -1;
+      if (pp >= 0 && pp < TK) {
+        int lo = 0, hi = U - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (soff[mid] <= pp) lo = mid;
+          else hi = mid - 1;
+        }
+        rr = spoff[lo] + (pp - soff[lo]);
+      } else {
+        flag_error(dev_err, MOE_DEV_BAD_ID);
+      }
+      s_rr[tid] = rr;
     }
-    const int rr = spoff[lo] + (pp - offsets[lo]);
-    const int tok = perm_token[pp];
-    bool ok = tok >= 0 && tok < T;
-    int row = tok;
-    if (ok && x_rows) {
-      row = x_rows[tok];
+    int row = t;
+    bool ok = true;
+    if (x_rows) {
+      row = x_rows[t];
       ok = row >= 0 && row < x_rows_limit;
     }
     if (!ok) {
-      if (lane == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
+      if (tid == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
+      __syncthreads();
       continue;
     }
     const uint16_t* xr = x + (size_t)row * H;
     float amax = 0.f;
-    for (int c = lane * 8; c < H; c += 256) {
+    for (int c = tid * 8; c < H; c += kPrepThreads * 8) {
       const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -653,30 +686,38 @@ __global__ void __launch_bounds__(256) ffn_fp8_prep_kernel(
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    const float sc = amax > 0.f ? amax / kE4M3Max : 1.f;
-    for (int c = lane * 8; c < H; c += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-      uint32_t h0 = 0, h1 = 0, l0 = 0, l1 = 0;
+    if (lane == 0) s_max[warp] = amax;
+    __syncthreads();
+    amax = s_max[0];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
+    float sc, inv_sc;
+    pow2_scale(amax, sc, inv_sc);
+    for (int c = tid * 16; c < H; c += kPrepThreads * 16) {
+      const uint4 va = *reinterpret_cast<const uint4*>(xr + c);
+      const uint4 vb = *reinterpret_cast<const uint4*>(xr + c + 8);
+      const uint32_t wv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      uint32_t hw[4] = {0, 0, 0, 0}, lw[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
         uint8_t ha, la, hb, lb;
-        split_e4m3(__uint_as_float(wv[i] << 16) / sc, ha, la);
-        split_e4m3(__uint_as_float(wv[i] & 0xFFFF0000u) / sc, hb, lb);
-        const uint32_t hh = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 8);
-        const uint32_t ll = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 8);
-        if (i < 2) {
-          h0 |= hh << (16 * i);
-          l0 |= ll << (16 * i);
-        } else {
-          h1 |= hh << (16 * (i - 2));
-          l1 |= ll << (16 * (i - 2));
-        }
+        split_e4m3(__uint_as_float(wv[i] << 16) * inv_sc, ha, la);
+        split_e4m3(__uint_as_float(wv[i] & 0xFFFF0000u) * inv_sc, hb, lb);
+        const int sh = 16 * (i & 1);
+        hw[i >> 1] |= (static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 8)) << sh;
+        lw[i >> 1] |= (static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 8)) << sh;
       }
-      *reinterpret_cast<uint2*>(xq_hi + (size_t)rr * H + c) = make_uint2(h0, h1);
-      *reinterpret_cast<uint2*>(xq_lo + (size_t)rr * H + c) = make_uint2(l0, l1);
+      const uint4 qh = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      const uint4 ql = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      for (int j = 0; j < k; ++j) {
+        const int rr = s_rr[j];
+        if (rr < 0) continue;
+        *reinterpret_cast<uint4*>(xq_hi + (size_t)rr * H + c) = qh;
+        *reinterpret_cast<uint4*>(xq_lo + (size_t)rr * H + c) = ql;
+      }
     }
-    if (lane == 0) xscale[rr] = sc;
+    if (tid < k && s_rr[tid] >= 0) xscale[s_rr[tid]] = sc;
+    __syncthreads();  // s_rr and s_max are rewritten for the next token
   }
 }
 
@@ -857,13 +898,11 @@ int ffn_fp8_launch(const FfnArgs& a) {
 
   cudaStream_t s = a.stream;
   {
-    int blocks = (TK * 32 + 255) / 256;
-    if (blocks > g.G * 4) blocks = g.G * 4;
-    if (blocks < 1) blocks = 1;
+    const int blocks = T;  // one CTA per token (T <= kMaxNM)
     LaunchScope ls(kProfPrep, s);
-    if (launch_k(ffn_fp8_prep_kernel, dim3(blocks), dim3(256), 0, s, a.pdl_first,
+    if (launch_k(ffn_fp8_prep_kernel, dim3(blocks), dim3(kPrepThreads), 0, s, a.pdl_first,
                  static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, k, lw.H, cap, a.n_unique,
-                 a.offsets, a.perm_token, ws.xq_hi, ws.xq_lo, ws.xscale, ws.poff, cnt_gu, n_counters, a.y,
+                 a.offsets, a.inv, ws.xq_hi, ws.xq_lo, ws.xscale, ws.poff, cnt_gu, n_counters, a.y,
                  a.dev_err) != MOE_OK)
       return MOE_ERR_CUDA;
   }

@@ -274,6 +274,8 @@ __global__ void __launch_bounds__(256) down_simt_kernel(
 // y[t, :] = sum_j w[t, j] * o[inv[t*k + j], :], slots in order.  Shared by
 // all FFN paths; after the tensor-core down kernels it is launched with
 // programmatic dependent launch.
+constexpr int kCombK = 16;  // largest k (checked by ffn_validate)
+
 __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, int E,
                                                       const int32_t* __restrict__ n_unique,
                                                       const int32_t* __restrict__ inv,
@@ -292,18 +294,37 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, int E
     const int c = static_cast<int>(i - (long long)t * (H / 4)) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
-      for (int j = 0; j < k; ++j) {
-        int p = inv[t * k + j];
-        if (p < 0 || p >= TK) {
+      // All of the token's slot indices and weights, then all of its rows of
+      // o, are requested before the first use, so the loads overlap; the sum
+      // still runs in slot order.
+      int pj[kCombK];
+      float wj[kCombK];
+#pragma unroll
+      for (int j = 0; j < kCombK; ++j) {
+        pj[j] = -1;
+        wj[j] = 0.f;
+        if (j < k) {
+          pj[j] = inv[t * k + j];
+          wj[j] = w[t * k + j];
+        }
+      }
+      float4 v[kCombK];
+#pragma unroll
+      for (int j = 0; j < kCombK; ++j) {
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < k && pj[j] >= 0 && pj[j] < TK) v[j] = *reinterpret_cast<const float4*>(o + (size_t)pj[j] * H + c);
+      }
+#pragma unroll
+      for (int j = 0; j < kCombK; ++j) {
+        if (j >= k) break;
+        if (pj[j] < 0 || pj[j] >= TK) {
           flag_error(dev_err, MOE_DEV_BAD_ID);
           continue;
         }
-        float wj = w[t * k + j];
-        float4 v = *reinterpret_cast<const float4*>(o + (size_t)p * H + c);
-        acc.x = fmaf(wj, v.x, acc.x);
-        acc.y = fmaf(wj, v.y, acc.y);
-        acc.z = fmaf(wj, v.z, acc.z);
-        acc.w = fmaf(wj, v.w, acc.w);
+        acc.x = fmaf(wj[j], v[j].x, acc.x);
+        acc.y = fmaf(wj[j], v[j].y, acc.y);
+        acc.z = fmaf(wj[j], v[j].z, acc.z);
+        acc.w = fmaf(wj[j], v[j].w, acc.w);
       }
     }
     *reinterpret_cast<float4*>(y + (size_t)t * H + c) = acc;

@@ -486,6 +486,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
                                                        int32_t* __restrict__ counters, int n_counters,
                                                        float* __restrict__ y, int32_t* dev_err) {
   __shared__ int32_t spoff[1025];
+  __shared__ int32_t soff[1025];  // offsets[0..U], for the group searches
   __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
@@ -514,6 +515,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
       const int a = offsets[u], b = offsets[u + 1];
       if (a < 0 || b > TK || b - a < 1 || b - a > T) s_bad = 1;
       sum += ((b - a) + 15) & ~15;
+      soff[u] = a;
     }
     int ex = sum;
     for (int off = 1; off < 32; off <<= 1) {
@@ -527,6 +529,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
     }
     if (lane == 31) {
       spoff[U] = ex;
+      soff[U] = offsets[U];
       if (offsets[U] != TK || offsets[0] != 0) s_bad = 1;
     }
   }
@@ -543,7 +546,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
   // Gather the real token rows only (one 16-byte chunk per thread-iteration).
   // Pad rows of a group are left as they are: a pad row of the B operand only
   // feeds accumulator columns the epilogue never stores.
-  const int TKn = offsets[U];
+  const int TKn = soff[U];
   const int cpr = H / 8;  // chunks per row
   const long long chunks = (long long)TKn * cpr;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < chunks;
@@ -554,10 +557,10 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
     int lo = 0, hi = U - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (offsets[mid] <= pp) lo = mid;
+      if (soff[mid] <= pp) lo = mid;
       else hi = mid - 1;
     }
-    const int rr = spoff[lo] + (pp - offsets[lo]);
+    const int rr = spoff[lo] + (pp - soff[lo]);
     const int tok = perm_token[pp];
     bool ok = tok >= 0 && tok < T;
     int row = tok;

@@ -18,9 +18,14 @@ __global__ void __launch_bounds__(256) layer_head_kernel(RouteArgs ra, int32_t* 
                                                          int32_t* inv, float* reuse_ratio) {
   extern __shared__ __align__(16) uint8_t head_smem[];
   const moe_route_cfg& c = ra.cfg;
+  const int TK = c.T * c.k;
   const size_t bias_bytes = (routing::bias_view_bytes(c.T, c.E) + 15) & ~size_t(15);
+  const size_t union_bytes = (unions::union_view_bytes(c.E) + 15) & ~size_t(15);
   routing::BiasView bv = routing::carve_bias(head_smem, c.T, c.E);
   unions::UnionView uv = unions::carve_union(head_smem + bias_bytes, c.E);
+  // The routing result stays in shared memory for the union; a copy goes out.
+  int32_t* s_ids = reinterpret_cast<int32_t*>(head_smem + bias_bytes + union_bytes);
+  float* s_w = reinterpret_cast<float*>(s_ids + TK);
 
   // The logits rows are inputs, not results of the previous kernel: pull
   // them towards L2 while that kernel finishes.  (The row map may still be
@@ -39,12 +44,16 @@ __global__ void __launch_bounds__(256) layer_head_kernel(RouteArgs ra, int32_t* 
   pdl_trigger();
   if (c.use_bias)
     routing::route_bias_block<NPL>(ra.logits, ra.rows, ra.rows_limit, ra.w_conf, c.T, c.E, c.k, c.cap, c.alpha,
-                                   ra.ids, ra.w, ra.dev_err, bv);
+                                   s_ids, s_w, ra.dev_err, bv);
   else
-    routing::route_plain_warps<NPL>(ra.logits, ra.rows, ra.rows_limit, c.T, c.E, c.k, ra.ids, ra.w, ra.dev_err,
+    routing::route_plain_warps<NPL>(ra.logits, ra.rows, ra.rows_limit, c.T, c.E, c.k, s_ids, s_w, ra.dev_err,
                                     threadIdx.x >> 5, blockDim.x >> 5);
   __syncthreads();
-  unions::union_block(ra.ids, c.T, c.k, c.E, bv.member, uv, n_unique, unique, offsets, perm_token, perm_slot, inv,
+  for (int i = threadIdx.x; i < TK; i += blockDim.x) {
+    ra.ids[i] = s_ids[i];
+    ra.w[i] = s_w[i];
+  }
+  unions::union_block(s_ids, c.T, c.k, c.E, bv.member, uv, n_unique, unique, offsets, perm_token, perm_slot, inv,
                       reuse_ratio, ra.dev_err);
 }
 
@@ -52,7 +61,8 @@ template <int NPL>
 int launch_npl(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets, int32_t* perm_token,
                int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl) {
   const size_t smem = ((routing::bias_view_bytes(ra.cfg.T, ra.cfg.E) + 15) & ~size_t(15)) +
-                      unions::union_view_bytes(ra.cfg.E);
+                      ((unions::union_view_bytes(ra.cfg.E) + 15) & ~size_t(15)) +
+                      static_cast<size_t>(ra.cfg.T) * ra.cfg.k * 8;
   if (smem > 48 * 1024 && cudaFuncSetAttribute(layer_head_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return MOE_ERR_CUDA;

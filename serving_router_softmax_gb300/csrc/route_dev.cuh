@@ -5,7 +5,8 @@
 // per layer).  Reuse bias: S2-MoE write-up, component 2 (steps 1-3, Fig. 5).
 // One warp owns one token; each lane keeps ceil(E/32) logits in registers and
 // the top-k is k rounds of a warp-wide arg-max over a strict total order
-// (larger value, then lower id).
+// (larger value, then lower id).  Each round is two warp reductions
+// (redux.sync): the largest order key, then the lowest expert id holding it.
 #pragma once
 
 #include <cfloat>
@@ -19,9 +20,20 @@ namespace routing {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kMaxK = 16;
 
+// Order key of a non-NaN float: a larger value has a larger key, -0.0 and
+// +0.0 share one key, and no value maps to 0 (which marks "no entry").
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v + 0.0f);  // -0.0 -> +0.0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 template <int NPL>
 struct Row {
-  float v[NPL];
+  uint32_t key[NPL];  // order keys; 0 for entries past E
   uint32_t taken;
 };
 
@@ -34,43 +46,41 @@ __device__ __forceinline__ bool load_row(const float* __restrict__ row, int E, i
 #pragma unroll
   for (int j = 0; j < NPL; ++j) {
     int e = lane + 32 * j;
-    float x = -INFINITY;
+    uint32_t key = 0;
     if (e < E) {
-      x = row[e];
+      float x = row[e];
       nan |= (x != x);
       if (estar && ((estar[e >> 5] >> (e & 31)) & 1u)) x = __fadd_rn(x, lam);
+      key = order_key(x);
     }
-    r.v[j] = x;
+    r.key[j] = key;
   }
   r.taken = 0;
   return __any_sync(kFull, nan);
 }
 
-// One arg-max round over the not-yet-taken entries; every lane gets the result.
+// One arg-max round over the not-yet-taken entries; every lane gets the
+// result (bi = INT_MAX when nothing is left).  The lane's own entries are
+// scanned in ascending id order with a strict compare, so its candidate is
+// its lowest id among its largest keys; across lanes the lowest id among the
+// lanes holding the largest key wins.
 template <int NPL>
 __device__ __forceinline__ void argmax_round(Row<NPL>& r, int E, int lane, float& bv, int& bi) {
-  float lv = -INFINITY;
+  uint32_t lk = 0;
   int li = INT_MAX;
 #pragma unroll
   for (int j = 0; j < NPL; ++j) {
-    int e = lane + 32 * j;
-    if (e < E && !((r.taken >> j) & 1u) && topk_better(r.v[j], e, lv, li)) {
-      lv = r.v[j];
-      li = e;
+    if (!((r.taken >> j) & 1u) && r.key[j] > lk) {
+      lk = r.key[j];
+      li = lane + 32 * j;
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float ov = __shfl_xor_sync(kFull, lv, off);
-    int oi = __shfl_xor_sync(kFull, li, off);
-    if (topk_better(ov, oi, lv, li)) {
-      lv = ov;
-      li = oi;
-    }
-  }
-  if (li != INT_MAX && (li & 31) == lane) r.taken |= 1u << (li >> 5);
-  bv = lv;
-  bi = li;
+  const uint32_t mk = __reduce_max_sync(kFull, lk);
+  const uint32_t cand = (mk != 0 && lk == mk) ? static_cast<uint32_t>(li) : 0xFFFFFFFFu;
+  const uint32_t win = __reduce_min_sync(kFull, cand);
+  bi = mk != 0 ? static_cast<int>(win) : INT_MAX;
+  bv = mk != 0 ? key_value(mk) : -INFINITY;
+  if (bi != INT_MAX && (bi & 31) == lane) r.taken |= 1u << (bi >> 5);
 }
 
 // Top-k of a loaded row and softmax over the selected logits; writes the
@@ -240,26 +250,24 @@ __device__ __forceinline__ void route_bias_block(const float* __restrict__ logit
   if (!conf_bad && warp == 0) {
     uint32_t taken = 0;  // bit j: expert lane + 32 j
     for (int c = 0; c < cap; ++c) {
-      float lv = -INFINITY;
+      // largest g > 0 among the untaken experts, ties to the lower id (as argmax_round)
+      uint32_t lk = 0;
       int li = INT_MAX;
       for (int j = 0; j < EW; ++j) {
-        int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && sm.g[e] > 0.f && topk_better(sm.g[e], e, lv, li)) {
-          lv = sm.g[e];
-          li = e;
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && sm.g[e] > 0.f) {
+          const uint32_t key = order_key(sm.g[e]);
+          if (key > lk) {
+            lk = key;
+            li = e;
+          }
         }
       }
-      for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(kFull, lv, off);
-        int oi = __shfl_xor_sync(kFull, li, off);
-        if (topk_better(ov, oi, lv, li)) {
-          lv = ov;
-          li = oi;
-        }
-      }
-      if (li == INT_MAX) break;  // no expert left with g > 0
-      if ((li & 31) == lane) taken |= 1u << (li >> 5);
-      if (lane == 0) sm.estar[li >> 5] |= 1u << (li & 31);
+      const uint32_t mk = __reduce_max_sync(kFull, lk);
+      if (mk == 0) break;  // no expert left with g > 0
+      const uint32_t win = __reduce_min_sync(kFull, lk == mk ? static_cast<uint32_t>(li) : 0xFFFFFFFFu);
+      if (static_cast<int>(win & 31) == lane) taken |= 1u << (win >> 5);
+      if (lane == 0) sm.estar[win >> 5] |= 1u << (win & 31);
     }
   }
   __syncthreads();
