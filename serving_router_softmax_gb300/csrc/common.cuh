@@ -113,8 +113,11 @@ int route_launch(const RouteArgs& a);
 int union_validate(int T, int k, int E);
 
 // Fused route + union for one layer of the whole step (single CTA).
+// rows_ready: the row map was complete before the launch (it may be read
+// before the wait on the previous kernel).
 int layer_head_launch(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets,
-                      int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl);
+                      int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl,
+                      bool rows_ready);
 int union_launch(const int32_t* ids, int T, int k, int E, int32_t* n_unique, int32_t* unique,
                  int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, int32_t* inv,
                  float* reuse_ratio, int32_t* dev_err, cudaStream_t s);

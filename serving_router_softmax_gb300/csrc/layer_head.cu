@@ -1,89 +1,414 @@
 // Fused per-layer head of the verify step: routing (optionally with the
 // S2-MoE reuse bias) followed by the expert union and token permutation, in
-// one single-CTA launch.  Same arithmetic as moe_route + moe_union_permute
-// (route_dev.cuh, union_dev.cuh); launched with programmatic dependent launch
-// so that its launch overlaps the previous layer's last kernel.
+// one single-CTA launch.  Same arithmetic and outputs as moe_route followed by
+// moe_union_permute (EcoSpec write-up section 3.1 and section 2; S2-MoE
+// write-up component 2, steps 1-3, and challenge 2), laid out for latency:
+//   - shared state is cleared, and (once the row map is complete) each warp's
+//     logits row is loaded, before the wait on the previous kernel: the
+//     logits are step inputs, not results of that kernel;
+//   - the routing rounds record the union bookkeeping (token x expert bits,
+//     group sizes) as they select, so the union needs no scatter pass;
+//   - with the bias, warp 0 sums g_e and takes the top-cap experts in
+//     registers.
+// Launched with programmatic dependent launch, so its launch overlaps the
+// previous layer's last kernel.
 #include "common.cuh"
 #include "route_dev.cuh"
-#include "union_dev.cuh"
 
 namespace moe {
 namespace {
 
-// Shared memory is sized to T and E (a few KB in verify steps), so the head
-// can sit next to a running FFN CTA and start as soon as it is launched.
+using routing::kFull;
+using routing::Row;
+
+constexpr int kHeadThreads = 256;
+constexpr int kHeadWarps = kHeadThreads / 32;
+
+struct HeadSmem {
+  uint32_t* member;   // [T][EW] routed experts per token (union bookkeeping)
+  uint32_t* member0;  // [T][EW] unbiased top-k per token (bias only)
+  int32_t* count;     // [E] group sizes
+  int32_t* ustart;    // [E] first perm position of each expert's group
+  int32_t* ids;       // [T*k]
+  float* w;           // [T*k]
+  float* v1;          // [T] top-1 logit (bias only)
+  float* vk1;         // [T] (k+1)-th logit (bias only)
+  float* wc;          // [T] confidence weights (bias only)
+  uint32_t* estar;    // [EW] preferred experts (bias only)
+  uint8_t* bad;       // [T] 0 ok, 1 NaN logit, 2 row outside the node table
+  int* err;
+};
+
+__host__ __device__ inline size_t head_smem_bytes(int T, int E, int k) {
+  const int EW = (E + 31) / 32;
+  return 4 * (2 * static_cast<size_t>(T) * EW + 2 * static_cast<size_t>(E) + 2 * static_cast<size_t>(T) * k +
+              3 * static_cast<size_t>(T) + EW + 1) +
+         ((static_cast<size_t>(T) + 15) & ~size_t(15));
+}
+
+__device__ __forceinline__ HeadSmem carve(uint8_t* p, int T, int E, int k) {
+  const int EW = (E + 31) / 32;
+  HeadSmem s;
+  s.member = reinterpret_cast<uint32_t*>(p);
+  s.member0 = s.member + (size_t)T * EW;
+  s.count = reinterpret_cast<int32_t*>(s.member0 + (size_t)T * EW);
+  s.ustart = s.count + E;
+  s.ids = s.ustart + E;
+  s.w = reinterpret_cast<float*>(s.ids + (size_t)T * k);
+  s.v1 = s.w + (size_t)T * k;
+  s.vk1 = s.v1 + T;
+  s.wc = s.vk1 + T;
+  s.estar = reinterpret_cast<uint32_t*>(s.wc + T);
+  s.err = reinterpret_cast<int*>(s.estar + EW);
+  s.bad = reinterpret_cast<uint8_t*>(s.err + 1);
+  return s;
+}
+
+// Top-k of a loaded row, softmax over the selected logits, and the union
+// bookkeeping of the selected experts.  Lane j keeps slot j.
 template <int NPL>
-__global__ void __launch_bounds__(256) layer_head_kernel(RouteArgs ra, int32_t* n_unique, int32_t* unique,
-                                                         int32_t* offsets, int32_t* perm_token, int32_t* perm_slot,
-                                                         int32_t* inv, float* reuse_ratio) {
+__device__ __forceinline__ void select_token(Row<NPL>& r, int t, int E, int k, int EW, int lane, HeadSmem& sm) {
+  float mine_v = -INFINITY, m = 0.f;
+  int mine_i = -1;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float bv;
+    int bi;
+    routing::argmax_round(r, E, lane, bv, bi);
+    if (j == 0) m = bv;
+    if (lane == j) {
+      mine_v = bv;
+      mine_i = bi;
+    }
+  }
+  const float ex = lane < k ? expf(mine_v - m) : 0.f;
+  float s = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+  if (lane < k) {
+    sm.ids[t * k + lane] = mine_i;
+    sm.w[t * k + lane] = __fdiv_rn(ex, s);
+    // a token's k ids are distinct (each round excludes the earlier picks);
+    // k <= E is checked on the host, so every round finds an expert
+    if (mine_i >= 0 && mine_i < E) {
+      atomicOr(&sm.member[t * EW + (mine_i >> 5)], 1u << (mine_i & 31));
+      atomicAdd(&sm.count[mine_i], 1);
+    }
+  }
+}
+
+__device__ __forceinline__ void invalid_token(int t, int k, int lane, int bad, HeadSmem& sm, int32_t* dev_err) {
+  if (lane == 0) flag_error(dev_err, bad == 2 ? MOE_DEV_CAPACITY : MOE_DEV_NAN_LOGIT);
+  for (int j = lane; j < k; j += 32) {
+    sm.ids[t * k + j] = -1;
+    sm.w[t * k + j] = 0.f;
+  }
+  if (lane == 0) *sm.err = MOE_DEV_BAD_ID;  // the union is undefined without every token's ids
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, int32_t* n_unique, int32_t* unique,
+                                                                  int32_t* offsets, int32_t* perm_token,
+                                                                  int32_t* perm_slot, int32_t* inv,
+                                                                  float* reuse_ratio, int rows_ready) {
   extern __shared__ __align__(16) uint8_t head_smem[];
   const moe_route_cfg& c = ra.cfg;
-  const int TK = c.T * c.k;
-  const size_t bias_bytes = (routing::bias_view_bytes(c.T, c.E) + 15) & ~size_t(15);
-  const size_t union_bytes = (unions::union_view_bytes(c.E) + 15) & ~size_t(15);
-  routing::BiasView bv = routing::carve_bias(head_smem, c.T, c.E);
-  unions::UnionView uv = unions::carve_union(head_smem + bias_bytes, c.E);
-  // The routing result stays in shared memory for the union; a copy goes out.
-  int32_t* s_ids = reinterpret_cast<int32_t*>(head_smem + bias_bytes + union_bytes);
-  float* s_w = reinterpret_cast<float*>(s_ids + TK);
+  const int T = c.T, E = c.E, k = c.k, TK = T * k;
+  const int EW = (E + 31) >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  HeadSmem sm = carve(head_smem, T, E, k);
 
-  // The logits rows are inputs, not results of the previous kernel: pull
-  // them towards L2 while that kernel finishes.  (The row map may still be
-  // in flight for the first layer, so every index is bounds-checked first;
-  // a prefetch only moves data, it never changes results.)
-  {
-    const int lines = (c.E * 4 + 127) / 128;
-    for (int i = threadIdx.x; i < c.T * lines; i += blockDim.x) {
+  // ---- before the dependency wait: clear the bookkeeping, fetch the rows.
+  for (int i = threadIdx.x; i < 2 * T * EW; i += kHeadThreads) sm.member[i] = 0;  // member and member0
+  for (int e = threadIdx.x; e < E; e += kHeadThreads) sm.count[e] = 0;
+  for (int i = threadIdx.x; i < EW; i += kHeadThreads) sm.estar[i] = 0;
+  if (threadIdx.x == 0) *sm.err = 0;
+  // One token per warp keeps its row in registers through both passes.
+  const bool keep = T <= kHeadWarps;
+  Row<NPL> kept;
+  kept.taken = 0;
+  bool kept_nan = false, loaded = false;
+  int kept_bad = 0;
+  auto row_of = [&](int t, int& bad) -> long long {
+    const long long row = ra.rows ? ra.rows[t] : t;
+    bad = (ra.rows && (row < 0 || row >= ra.rows_limit)) ? 2 : 0;
+    return row;
+  };
+  if (keep && rows_ready) {
+    if (warp < T) {
+      const long long row = row_of(warp, kept_bad);
+      if (!kept_bad) kept_nan = routing::load_row<NPL>(ra.logits + row * E, E, lane, kept, nullptr, 0.f);
+      loaded = true;
+    }
+  } else {
+    // Warm L2 with bounds-checked addresses only: the row map may still be
+    // in flight (it is written by the kernel before the first layer's head),
+    // and a prefetch never changes results.
+    const int lines = (E * 4 + 127) / 128;
+    for (int i = threadIdx.x; i < T * lines; i += kHeadThreads) {
       const int t = i / lines;
       const long long row = ra.rows ? ra.rows[t] : t;
       if (row >= 0 && (!ra.rows || row < ra.rows_limit))
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(ra.logits + row * c.E + (i - t * lines) * 32));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(ra.logits + row * E + (i - t * lines) * 32));
     }
   }
   pdl_wait();
   pdl_trigger();
-  if (c.use_bias)
-    routing::route_bias_block<NPL>(ra.logits, ra.rows, ra.rows_limit, ra.w_conf, c.T, c.E, c.k, c.cap, c.alpha,
-                                   s_ids, s_w, ra.dev_err, bv);
-  else
-    routing::route_plain_warps<NPL>(ra.logits, ra.rows, ra.rows_limit, c.T, c.E, c.k, s_ids, s_w, ra.dev_err,
-                                    threadIdx.x >> 5, blockDim.x >> 5);
-  __syncthreads();
-  for (int i = threadIdx.x; i < TK; i += blockDim.x) {
-    ra.ids[i] = s_ids[i];
-    ra.w[i] = s_w[i];
+  if (keep && !loaded && warp < T) {
+    const long long row = row_of(warp, kept_bad);
+    if (!kept_bad) kept_nan = routing::load_row<NPL>(ra.logits + row * E, E, lane, kept, nullptr, 0.f);
   }
-  unions::union_block(s_ids, c.T, c.k, c.E, bv.member, uv, n_unique, unique, offsets, perm_token, perm_slot, inv,
-                      reuse_ratio, ra.dev_err);
+  int my_bad = 0;
+  if (c.use_bias) {
+    for (int t = threadIdx.x; t < T; t += kHeadThreads) {
+      const float cf = ra.w_conf[t];
+      sm.wc[t] = cf;
+      if (!(cf >= 0.f)) my_bad = 1;  // NaN or negative
+    }
+  }
+  __syncthreads();  // bookkeeping cleared
+
+  if (c.use_bias) {
+    // ---- pass 1: unbiased top-(k+1) -> TopK membership, l_(1), l_(k+1)
+    for (int t = warp; t < T; t += kHeadWarps) {
+      Row<NPL> r;
+      int bad = 0;
+      bool nan = false;
+      if (keep) {
+        r = kept;
+        bad = kept_bad;
+        nan = kept_nan;
+      } else {
+        const long long row = row_of(t, bad);
+        if (!bad) nan = routing::load_row<NPL>(ra.logits + row * E, E, lane, r, nullptr, 0.f);
+      }
+      if (!bad && nan) bad = 1;
+      if (lane == 0) sm.bad[t] = static_cast<uint8_t>(bad);
+      if (bad) continue;
+      for (int j = 0; j <= k; ++j) {
+        float bv;
+        int bi;
+        routing::argmax_round(r, E, lane, bv, bi);
+        if (lane == 0) {
+          if (j == 0) sm.v1[t] = bv;
+          if (j == k) sm.vk1[t] = bv;
+          if (j < k) sm.member0[t * EW + (bi >> 5)] |= 1u << (bi & 31);
+        }
+      }
+    }
+    const bool conf_bad = __syncthreads_or(my_bad) != 0;
+    if (conf_bad) {
+      if (threadIdx.x == 0) flag_error(ra.dev_err, MOE_DEV_BAD_PROB);
+      for (int i = threadIdx.x; i < TK; i += kHeadThreads) {
+        ra.ids[i] = -1;
+        ra.w[i] = 0.f;
+      }
+      if (threadIdx.x == 0) {
+        flag_error(ra.dev_err, MOE_DEV_BAD_ID);
+        *n_unique = 0;
+        *reuse_ratio = 0.f;
+        offsets[0] = 0;
+      }
+      return;
+    }
+    // ---- g_e (fp32, tokens in ascending order, plain adds) and E* = the
+    // top-cap experts by g among g > 0 (ties to the lower id), in warp 0.
+    if (warp == 0) {
+      uint32_t key[NPL];
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) {
+        const int e = lane + 32 * j;
+        float acc = 0.f;
+        if (e < E) {
+          for (int b = 0; b < T; ++b)
+            if (!sm.bad[b] && ((sm.member0[b * EW + (e >> 5)] >> (e & 31)) & 1u)) acc = __fadd_rn(acc, sm.wc[b]);
+        }
+        key[j] = acc > 0.f ? routing::order_key(acc) : 0u;
+      }
+      uint32_t words[NPL];  // E* bits this lane found, by word (lane 0 writes)
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) words[j] = 0;
+      for (int cc = 0; cc < c.cap; ++cc) {
+        uint32_t lk = 0;
+        int li = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) {
+          if (key[j] > lk) {
+            lk = key[j];
+            li = lane + 32 * j;
+          }
+        }
+        const uint32_t mk = __reduce_max_sync(kFull, lk);
+        if (mk == 0) break;  // no expert left with g > 0
+        const uint32_t win = __reduce_min_sync(kFull, lk == mk ? static_cast<uint32_t>(li) : 0xFFFFFFFFu);
+        if (static_cast<int>(win & 31) == lane) {
+#pragma unroll
+          for (int j = 0; j < NPL; ++j)
+            if (j == static_cast<int>(win >> 5)) key[j] = 0;
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < NPL; ++j)
+            if (j == static_cast<int>(win >> 5)) words[j] |= 1u << (win & 31);
+        }
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < NPL; ++j)
+          if (j < EW) sm.estar[j] = words[j];
+      }
+    }
+    __syncthreads();
+    // ---- pass 2: route the biased logits l' = l + lam_b on E*
+    for (int t = warp; t < T; t += kHeadWarps) {
+      if (sm.bad[t]) {
+        invalid_token(t, k, lane, sm.bad[t], sm, ra.dev_err);
+        continue;
+      }
+      const float lam = __fmul_rn(c.alpha, __fsub_rn(sm.v1[t], sm.vk1[t]));
+      Row<NPL> r;
+      if (keep) {
+        // from the kept keys: key_value(order_key(x)) == x up to the sign of
+        // zero, which no comparison or exponent sees
+        r = kept;
+        r.taken = 0;
+#pragma unroll
+        for (int j = 0; j < NPL; ++j) {
+          const int e = lane + 32 * j;
+          if (e < E && ((sm.estar[e >> 5] >> (e & 31)) & 1u))
+            r.key[j] = routing::order_key(__fadd_rn(routing::key_value(r.key[j]), lam));
+        }
+      } else {
+        int bad = 0;
+        const long long row = row_of(t, bad);
+        routing::load_row<NPL>(ra.logits + row * E, E, lane, r, sm.estar, lam);
+      }
+      select_token<NPL>(r, t, E, k, EW, lane, sm);
+    }
+  } else {
+    // ---- plain routing
+    for (int t = warp; t < T; t += kHeadWarps) {
+      Row<NPL> r;
+      int bad = 0;
+      bool nan = false;
+      if (keep) {
+        r = kept;
+        bad = kept_bad;
+        nan = kept_nan;
+      } else {
+        const long long row = row_of(t, bad);
+        if (!bad) nan = routing::load_row<NPL>(ra.logits + row * E, E, lane, r, nullptr, 0.f);
+      }
+      if (!bad && nan) bad = 1;
+      if (bad) {
+        invalid_token(t, k, lane, bad, sm, ra.dev_err);
+        continue;
+      }
+      select_token<NPL>(r, t, E, k, EW, lane, sm);
+    }
+  }
+  __syncthreads();
+
+  // ---- union: warp 0 scans the group sizes; the others publish ids and weights
+  const int err = *sm.err;
+  for (int i = threadIdx.x; i < TK; i += kHeadThreads) {
+    ra.ids[i] = sm.ids[i];
+    ra.w[i] = sm.w[i];
+  }
+  if (err) {
+    if (threadIdx.x == 0) {
+      flag_error(ra.dev_err, err);
+      *n_unique = 0;
+      *reuse_ratio = 0.f;
+      offsets[0] = 0;
+    }
+    return;
+  }
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int nz = 0, tok = 0;
+    for (int e = e0; e < e0 + per && e < E; ++e) {
+      const int cnt = sm.count[e];
+      nz += cnt > 0;
+      tok += cnt;
+    }
+    int nz_ex = nz, tok_ex = tok;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(kFull, nz_ex, off);
+      const int b = __shfl_up_sync(kFull, tok_ex, off);
+      if (lane >= off) {
+        nz_ex += a;
+        tok_ex += b;
+      }
+    }
+    nz_ex -= nz;
+    tok_ex -= tok;
+    for (int e = e0; e < e0 + per && e < E; ++e) {
+      const int cnt = sm.count[e];
+      if (cnt > 0) {
+        sm.ustart[e] = tok_ex;
+        unique[nz_ex] = e;
+        offsets[nz_ex] = tok_ex;
+        ++nz_ex;
+        tok_ex += cnt;
+      }
+    }
+    if (lane == 31) {
+      offsets[nz_ex] = tok_ex;  // == T*k
+      *n_unique = nz_ex;
+      *reuse_ratio = TK > 0 ? __fdiv_rn(static_cast<float>(nz_ex), static_cast<float>(TK)) : 0.f;
+    }
+  }
+  __syncthreads();
+  // ---- permutation: rank of token t in expert e's group = set bits of
+  // column e over tokens t' < t
+  for (int p = threadIdx.x; p < TK; p += kHeadThreads) {
+    const int t = p / k;
+    const int j = p - t * k;
+    const int e = sm.ids[p];
+    const int word = e >> 5;
+    const uint32_t bit = 1u << (e & 31);
+    int rank = 0;
+    for (int tt = 0; tt < t; ++tt) rank += (sm.member[tt * EW + word] & bit) ? 1 : 0;
+    const int pos = sm.ustart[e] + rank;
+    perm_token[pos] = t;
+    perm_slot[pos] = j;
+    inv[p] = pos;
+  }
 }
 
 template <int NPL>
 int launch_npl(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets, int32_t* perm_token,
-               int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl) {
-  const size_t smem = ((routing::bias_view_bytes(ra.cfg.T, ra.cfg.E) + 15) & ~size_t(15)) +
-                      ((unions::union_view_bytes(ra.cfg.E) + 15) & ~size_t(15)) +
-                      static_cast<size_t>(ra.cfg.T) * ra.cfg.k * 8;
+               int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl, bool rows_ready) {
+  const size_t smem = head_smem_bytes(ra.cfg.T, ra.cfg.E, ra.cfg.k);
   if (smem > 48 * 1024 && cudaFuncSetAttribute(layer_head_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return MOE_ERR_CUDA;
   LaunchScope ls(kProfRoute, ra.stream);
-  return launch_k(layer_head_kernel<NPL>, dim3(1), dim3(256), smem, ra.stream, pdl, ra, n_unique, unique, offsets,
-                  perm_token, perm_slot, inv, reuse_ratio);
+  return launch_k(layer_head_kernel<NPL>, dim3(1), dim3(kHeadThreads), smem, ra.stream, pdl, ra, n_unique, unique,
+                  offsets, perm_token, perm_slot, inv, reuse_ratio, rows_ready ? 1 : 0);
 }
 
 }  // namespace
 
-// T <= 256, E <= 1024 (checked by the step's validation).
+// T <= 256, E <= 1024, k <= 16 (checked by the step's validation).
 int layer_head_launch(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets,
-                      int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl) {
+                      int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl,
+                      bool rows_ready) {
   if (ra.cfg.T < 1 || ra.cfg.T > routing::kBiasMaxT || ra.cfg.E > 1024) return MOE_ERR_UNSUPPORTED;
   const int npl = (ra.cfg.E + 31) / 32;
-  if (npl <= 1) return launch_npl<1>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl);
-  if (npl <= 2) return launch_npl<2>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl);
-  if (npl <= 4) return launch_npl<4>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl);
-  if (npl <= 8) return launch_npl<8>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl);
-  if (npl <= 16) return launch_npl<16>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl);
-  return launch_npl<32>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl);
+  if (npl <= 1)
+    return launch_npl<1>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+  if (npl <= 2)
+    return launch_npl<2>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+  if (npl <= 4)
+    return launch_npl<4>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+  if (npl <= 8)
+    return launch_npl<8>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+  if (npl <= 16)
+    return launch_npl<16>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+  return launch_npl<32>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
 }
 
 }  // namespace moe

@@ -148,7 +148,7 @@ constexpr int kMaxEW = 32;  // 1024 experts / 32
 
 struct BiasSmem {
   uint32_t member[kBiasMaxT * kMaxEW];  // [t][EW] top-k membership bits
-  float v1[kBiasMaxT], vk1[kBiasMaxT];
+  float v1[kBiasMaxT], vk1[kBiasMaxT], wc[kBiasMaxT];
   uint8_t bad[kBiasMaxT];
   float g[1024];
   uint32_t estar[kMaxEW];
@@ -161,6 +161,7 @@ struct BiasView {
   uint32_t* member;  // [T][EW]
   float* v1;         // [T]
   float* vk1;        // [T]
+  float* wc;         // [T] confidence weights
   uint8_t* bad;      // [T]
   float* g;          // [E]
   uint32_t* estar;   // [EW]
@@ -168,14 +169,14 @@ struct BiasView {
 };
 
 __device__ __forceinline__ BiasView view_of(BiasSmem& sm) {
-  return BiasView{sm.member, sm.v1, sm.vk1, sm.bad, sm.g, sm.estar, &sm.conf_bad};
+  return BiasView{sm.member, sm.v1, sm.vk1, sm.wc, sm.bad, sm.g, sm.estar, &sm.conf_bad};
 }
 
 // Bytes of a BiasView carved by carve_bias (4-byte aligned pieces).
 __host__ __device__ inline size_t bias_view_bytes(int T, int E) {
   const int EW = (E + 31) / 32;
   const size_t Tb = (static_cast<size_t>(T) + 3) & ~size_t(3);
-  return 4 * (static_cast<size_t>(T) * EW + 2 * T + E + EW + 1) + Tb;
+  return 4 * (static_cast<size_t>(T) * EW + 3 * T + E + EW + 1) + Tb;
 }
 
 __device__ __forceinline__ BiasView carve_bias(uint8_t* p, int T, int E) {
@@ -184,7 +185,8 @@ __device__ __forceinline__ BiasView carve_bias(uint8_t* p, int T, int E) {
   v.member = reinterpret_cast<uint32_t*>(p);
   v.v1 = reinterpret_cast<float*>(v.member + (size_t)T * EW);
   v.vk1 = v.v1 + T;
-  v.g = v.vk1 + T;
+  v.wc = v.vk1 + T;
+  v.g = v.wc + T;
   v.estar = reinterpret_cast<uint32_t*>(v.g + E);
   v.conf_bad = reinterpret_cast<int*>(v.estar + EW);
   v.bad = reinterpret_cast<uint8_t*>(v.conf_bad + 1);
@@ -203,13 +205,18 @@ __device__ __forceinline__ void route_bias_block(const float* __restrict__ logit
   const int nwarps = blockDim.x >> 5;
   const int EW = (E + 31) >> 5;
 
-  if (threadIdx.x == 0) *sm.conf_bad = 0;
   for (int i = threadIdx.x; i < EW; i += blockDim.x) sm.estar[i] = 0;
-  __syncthreads();
+  int my_bad = 0;
   for (int t = threadIdx.x; t < T; t += blockDim.x) {
-    float c = w_conf[t];
-    if (!(c >= 0.f)) *sm.conf_bad = 1;  // NaN or negative
+    const float c = w_conf[t];
+    sm.wc[t] = c;
+    if (!(c >= 0.f)) my_bad = 1;  // NaN or negative
   }
+  // With at most one token per warp, the warp keeps its token's row in
+  // registers from the first pass to the second.
+  const bool keep = T <= nwarps;
+  Row<NPL> kept;
+  kept.taken = 0;
   // Pass 1: original top-(k+1) per token -> membership of TopK, l_(1), l_(k+1).
   for (int t = warp; t < T; t += nwarps) {
     const long long row = rows ? rows[t] : t;
@@ -222,6 +229,7 @@ __device__ __forceinline__ void route_bias_block(const float* __restrict__ logit
     bool nan = load_row<NPL>(logits + row * E, E, lane, r, nullptr, 0.f);
     if (lane == 0) sm.bad[t] = nan ? 1 : 0;
     if (nan) continue;
+    if (keep) kept = r;
     __syncwarp();
     for (int j = 0; j <= k; ++j) {
       float bv;
@@ -234,14 +242,13 @@ __device__ __forceinline__ void route_bias_block(const float* __restrict__ logit
       }
     }
   }
-  __syncthreads();
-  const bool conf_bad = *sm.conf_bad != 0;
+  const bool conf_bad = __syncthreads_or(my_bad) != 0;
   if (!conf_bad) {
     // Step 1: g_e = sum over tokens (ascending) of w_b for tokens whose top-k holds e.
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       float acc = 0.f;
       for (int b = 0; b < T; ++b)
-        if (!sm.bad[b] && ((sm.member[b * EW + (e >> 5)] >> (e & 31)) & 1u)) acc = __fadd_rn(acc, w_conf[b]);
+        if (!sm.bad[b] && ((sm.member[b * EW + (e >> 5)] >> (e & 31)) & 1u)) acc = __fadd_rn(acc, sm.wc[b]);
       sm.g[e] = acc;
     }
   }
@@ -289,9 +296,21 @@ __device__ __forceinline__ void route_bias_block(const float* __restrict__ logit
       continue;
     }
     const float lam = __fmul_rn(alpha, __fsub_rn(sm.v1[t], sm.vk1[t]));
-    const long long row = rows ? rows[t] : t;
     Row<NPL> r;
-    load_row<NPL>(logits + row * E, E, lane, r, sm.estar, lam);
+    if (keep) {
+      // l' = l + lam on E*, from the kept keys (key_value(order_key(x)) == x
+      // up to the sign of zero, which no comparison or exponent sees)
+      r = kept;
+      r.taken = 0;
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && ((sm.estar[e >> 5] >> (e & 31)) & 1u)) r.key[j] = order_key(__fadd_rn(key_value(r.key[j]), lam));
+      }
+    } else {
+      const long long row = rows ? rows[t] : t;
+      load_row<NPL>(logits + row * E, E, lane, r, sm.estar, lam);
+    }
     topk_softmax_write<NPL>(r, E, k, lane, ti, tw);
   }
 }

@@ -117,8 +117,10 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     RouteArgs ra{node_logits + static_cast<size_t>(l) * rows * c.E, ws.verify_rows, rows,
                  c.use_bias ? ws.verify_conf : nullptr, {c.T, c.E, c.k, c.use_bias, c.cap, c.alpha},
                  ws.ids, ws.w, dev_err, s};
+    // The verify rows come from the selection kernel, which the first layer's
+    // head follows directly; later heads may read them before their wait.
     if ((st = layer_head_launch(ra, n_unique + l, ws.unique, ws.offsets, ws.perm_token, ws.perm_slot, ws.inv,
-                                ws.ratio, true)) != MOE_OK)
+                                ws.ratio, true, l > 0)) != MOE_OK)
       return st;
     FfnArgs fa{static_cast<const char*>(node_x) + static_cast<size_t>(l) * rows * c.H * xelem,
                ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
