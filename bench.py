@@ -327,6 +327,26 @@ def ours(args, rank, ws, local):
     torch.cuda.synchronize()
     prof = mv.profile_end()
 
+    # ---- control path alone (selection + every layer's routing and union,
+    # the same kernels and launch chain as in the step, without the FFN).
+    plan = mv.VerifyPlan(spec, dev)
+
+    def one_plan():
+        plan(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+
+    for _ in range(3):
+        one_plan()
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    n_plan = min(args.steps, 100)
+    c0.record(stream)
+    for _ in range(n_plan):
+        one_plan()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    ctrl_ms = c0.elapsed_time(c1) / n_plan
+
     # ---- router logits, timed alone (the step routes the given node logits).
     router = router_measure(mv, cfg, wl, dev, stream)
 
@@ -408,7 +428,9 @@ def ours(args, rank, ws, local):
         "frac_of_8tbs_step": value / 8000.0 / ws,
         "roofline": roofline,
         "kernel_ms_per_step": {k: v["ms"] / n_c for k, v in prof.items()},
-        "control_path_frac": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))
+        "control_path_ms": ctrl_ms,
+        "control_path_frac": ctrl_ms / max(ms_step, 1e-9),
+        "control_path_frac_events": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))
         / n_c / max(ms_step, 1e-9),
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms / args.steps,

@@ -9,6 +9,7 @@
  *   moe_union_permute  expert union of the verify tokens, per-expert token groups
  *   moe_verify_ffn     grouped SwiGLU expert FFN over the union + weighted combine
  *   moe_verify_step    all of the above for L layers in one call
+ *   moe_verify_plan    the step's selection and per-layer routing/union only
  *
  * Conventions shared by every entry point
  *   - Every array argument is a DEVICE pointer owned by the caller, unless a
@@ -340,6 +341,39 @@ int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* pare
                     const float* node_logits, const void* node_x,
                     const moe_layer_weights* layers, int32_t* selected, int32_t* union_size,
                     int32_t* n_unique, float* y, void* workspace, size_t ws_bytes,
+                    int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------- plan
+ * moe_verify_plan -- the control path of one verify step, without the
+ * expert FFN: the selection of moe_verify_step and, for every layer, its
+ * routing (with the reuse bias when cfg->use_bias) and expert union, all
+ * written out.  For callers that schedule the expert FFN themselves (for
+ * example, to stage the union's experts before the layer runs) and for
+ * timing the control path on its own.
+ *
+ * Defined by: EcoSpec write-up section 2 (a round selects gamma nodes and
+ * verifies gamma+1 tokens; a layer's verify experts are the union of the
+ * tokens' routed experts) and sections 3.2-3.3; routing and bias as
+ * moe_route, union as moe_union_permute.
+ *
+ *   cfg            as moe_verify_step; H, I, dtype and layout are not read.
+ *   P, parent, own_fp, gamma_per_seq, node_logits   as moe_verify_step.
+ *   selected       [nseq, gamma_max] int32 out, union_size [nseq] int32 out.
+ *   verify_rows    [T] int32 out: node-table row of each verify token,
+ *                  sequence-major, each sequence's root first.
+ *   verify_conf    [T] fp32 out: path probability of each verify token
+ *                  (1 for roots); the bias's confidence weights.
+ *   ids, w         [L, T, k] out, as moe_route per layer.
+ *   n_unique       [L]; unique [L, cap]; offsets [L, cap + 1];
+ *   perm_token, perm_slot, inv [L, T*k]; reuse_ratio [L]: as
+ *                  moe_union_permute per layer, with cap = min(E, T*k).
+ * Needs no workspace.  Errors: as moe_verify_step's selection and routing.
+ */
+int moe_verify_plan(const moe_step_cfg* cfg, const float* P, const int32_t* parent,
+                    const uint32_t* own_fp, const int32_t* gamma_per_seq, const float* node_logits,
+                    int32_t* selected, int32_t* union_size, int32_t* verify_rows, float* verify_conf,
+                    int32_t* ids, float* w, int32_t* n_unique, int32_t* unique, int32_t* offsets,
+                    int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio,
                     int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------- timing

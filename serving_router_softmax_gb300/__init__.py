@@ -6,7 +6,7 @@ C ABI in ``include/moe_verify.h``); this package only marshals arguments.
 Importing it loads the library and raises if it has not been built.
 """
 from . import _lib
-from .api import (ExpertLayer, MoEError, StepSpec, VerifyStep, eco_select, ffn_workspace_bytes,  # noqa: F401
+from .api import (ExpertLayer, MoEError, StepSpec, VerifyPlan, VerifyStep, eco_select, ffn_workspace_bytes,  # noqa: F401
                   launch_count, new_dev_err, pack_tiled, profile_begin, profile_end, route, router_logits,
                   step_workspace_bytes,
                   union_permute, verify_ffn)

@@ -19,7 +19,7 @@ PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up
                 "combine", "router_logits"]
 
 EXPORTED = ["moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
-            "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_profile_begin",
+            "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_verify_plan", "moe_profile_begin",
             "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version"]
 
 
@@ -89,6 +89,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_verify_step.argtypes = [P(StepCfg), vp, vp, vp, vp, vp, vp, P(LayerWeights), vp, vp,
                                     vp, vp, vp, sz, vp, vp]
     lib.moe_verify_step.restype = C.c_int
+    lib.moe_verify_plan.argtypes = [P(StepCfg)] + [vp] * 19
+    lib.moe_verify_plan.restype = C.c_int
     lib.moe_profile_begin.argtypes = [i32, i32]
     lib.moe_profile_begin.restype = C.c_int
     lib.moe_profile_end.argtypes = [vp, vp, i32]

@@ -309,6 +309,44 @@ class VerifyStep:
         return self.y
 
 
+class VerifyPlan:
+    """The control path of a verify step (selection, then every layer's
+    routing and expert union) with its output tensors bound once."""
+
+    def __init__(self, spec: StepSpec, device="cuda"):
+        self.spec = spec
+        self.device = torch.device(device)
+        self._cfg = spec.struct()
+        d, i32, f32 = self.device, torch.int32, torch.float32
+        T, k, Lc = spec.T, spec.k, spec.L
+        cap = min(spec.E, T * k)
+        self.selected = torch.empty((spec.nseq, max(spec.gamma_max, 1)), dtype=i32, device=d)
+        self.union_size = torch.empty(spec.nseq, dtype=i32, device=d)
+        self.verify_rows = torch.empty(T, dtype=i32, device=d)
+        self.verify_conf = torch.empty(T, dtype=f32, device=d)
+        self.ids = torch.empty((Lc, T, k), dtype=i32, device=d)
+        self.w = torch.empty((Lc, T, k), dtype=f32, device=d)
+        self.n_unique = torch.empty(Lc, dtype=i32, device=d)
+        self.unique = torch.empty((Lc, cap), dtype=i32, device=d)
+        self.offsets = torch.empty((Lc, cap + 1), dtype=i32, device=d)
+        self.perm_token = torch.empty((Lc, T * k), dtype=i32, device=d)
+        self.perm_slot = torch.empty((Lc, T * k), dtype=i32, device=d)
+        self.inv = torch.empty((Lc, T * k), dtype=i32, device=d)
+        self.reuse_ratio = torch.empty(Lc, dtype=f32, device=d)
+        self.dev_err = torch.zeros(1, dtype=i32, device=d)
+
+    def __call__(self, P, parent, own_fp, gamma_per_seq, node_logits, stream=None):
+        lib = L.load()
+        _check(lib.moe_verify_plan(C.byref(self._cfg), _ptr(P), _ptr(parent), _ptr(own_fp), _ptr(gamma_per_seq),
+                                   _ptr(node_logits), _ptr(self.selected), _ptr(self.union_size),
+                                   _ptr(self.verify_rows), _ptr(self.verify_conf), _ptr(self.ids), _ptr(self.w),
+                                   _ptr(self.n_unique), _ptr(self.unique), _ptr(self.offsets),
+                                   _ptr(self.perm_token), _ptr(self.perm_slot), _ptr(self.inv),
+                                   _ptr(self.reuse_ratio), _ptr(self.dev_err), _stream(stream)),
+               "moe_verify_plan")
+        return self
+
+
 def profile_begin(max_launches: int = 65536, classes: Optional[Sequence[str]] = None):
     """Start event timing of the library's launches (all classes by default)."""
     names = L.PROF_CLASSES if classes is None else classes

@@ -8,8 +8,9 @@
 //     logits are step inputs, not results of that kernel;
 //   - the routing rounds record the union bookkeeping (token x expert bits,
 //     group sizes) as they select, so the union needs no scatter pass;
-//   - with the bias, warp 0 sums g_e and takes the top-cap experts in
-//     registers.
+//   - with the bias, g_e is one expert per thread and E* a rank test (an
+//     expert is in E* when fewer than cap experts beat it), with no serial
+//     selection rounds.
 // Launched with programmatic dependent launch, so its launch overlaps the
 // previous layer's last kernel.
 #include "common.cuh"
@@ -35,13 +36,15 @@ struct HeadSmem {
   float* vk1;         // [T] (k+1)-th logit (bias only)
   float* wc;          // [T] confidence weights (bias only)
   uint32_t* estar;    // [EW] preferred experts (bias only)
+  uint32_t* gkey;     // [E4] order keys of g_e, 0 where g_e <= 0 or e >= E (bias only; 16-byte aligned)
   uint8_t* bad;       // [T] 0 ok, 1 NaN logit, 2 row outside the node table
   int* err;
 };
 
 __host__ __device__ inline size_t head_smem_bytes(int T, int E, int k) {
   const int EW = (E + 31) / 32;
-  return 4 * (2 * static_cast<size_t>(T) * EW + 2 * static_cast<size_t>(E) + 2 * static_cast<size_t>(T) * k +
+  const size_t E4 = (static_cast<size_t>(E) + 3) & ~size_t(3);
+  return 4 * (E4 + 2 * static_cast<size_t>(T) * EW + 2 * static_cast<size_t>(E) + 2 * static_cast<size_t>(T) * k +
               3 * static_cast<size_t>(T) + EW + 1) +
          ((static_cast<size_t>(T) + 15) & ~size_t(15));
 }
@@ -49,7 +52,8 @@ __host__ __device__ inline size_t head_smem_bytes(int T, int E, int k) {
 __device__ __forceinline__ HeadSmem carve(uint8_t* p, int T, int E, int k) {
   const int EW = (E + 31) / 32;
   HeadSmem s;
-  s.member = reinterpret_cast<uint32_t*>(p);
+  s.gkey = reinterpret_cast<uint32_t*>(p);
+  s.member = s.gkey + ((E + 3) & ~3);
   s.member0 = s.member + (size_t)T * EW;
   s.count = reinterpret_cast<int32_t*>(s.member0 + (size_t)T * EW);
   s.ustart = s.count + E;
@@ -211,52 +215,38 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
       }
       return;
     }
-    // ---- g_e (fp32, tokens in ascending order, plain adds) and E* = the
-    // top-cap experts by g among g > 0 (ties to the lower id), in warp 0.
-    if (warp == 0) {
-      uint32_t key[NPL];
-#pragma unroll
-      for (int j = 0; j < NPL; ++j) {
-        const int e = lane + 32 * j;
-        float acc = 0.f;
-        if (e < E) {
-          for (int b = 0; b < T; ++b)
-            if (!sm.bad[b] && ((sm.member0[b * EW + (e >> 5)] >> (e & 31)) & 1u)) acc = __fadd_rn(acc, sm.wc[b]);
-        }
-        key[j] = acc > 0.f ? routing::order_key(acc) : 0u;
-      }
-      uint32_t words[NPL];  // E* bits this lane found, by word (lane 0 writes)
-#pragma unroll
-      for (int j = 0; j < NPL; ++j) words[j] = 0;
-      for (int cc = 0; cc < c.cap; ++cc) {
-        uint32_t lk = 0;
-        int li = INT_MAX;
-#pragma unroll
-        for (int j = 0; j < NPL; ++j) {
-          if (key[j] > lk) {
-            lk = key[j];
-            li = lane + 32 * j;
-          }
-        }
-        const uint32_t mk = __reduce_max_sync(kFull, lk);
-        if (mk == 0) break;  // no expert left with g > 0
-        const uint32_t win = __reduce_min_sync(kFull, lk == mk ? static_cast<uint32_t>(li) : 0xFFFFFFFFu);
-        if (static_cast<int>(win & 31) == lane) {
-#pragma unroll
-          for (int j = 0; j < NPL; ++j)
-            if (j == static_cast<int>(win >> 5)) key[j] = 0;
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int j = 0; j < NPL; ++j)
-            if (j == static_cast<int>(win >> 5)) words[j] |= 1u << (win & 31);
+    // ---- g_e (fp32, tokens in ascending order, plain adds), one expert per
+    // thread.  A token that does not hold e, or whose row was unusable, adds
+    // +0.0, which leaves every partial sum unchanged (sums are never -0.0).
+    const int E4 = (E + 3) & ~3;
+    for (int e = threadIdx.x; e < E4; e += kHeadThreads) {
+      float acc = 0.f;
+      if (e < E) {
+        for (int b = 0; b < T; ++b) {
+          const bool in = !sm.bad[b] && ((sm.member0[b * EW + (e >> 5)] >> (e & 31)) & 1u);
+          acc = __fadd_rn(acc, in ? sm.wc[b] : 0.f);
         }
       }
-      if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < NPL; ++j)
-          if (j < EW) sm.estar[j] = words[j];
+      sm.gkey[e] = acc > 0.f ? routing::order_key(acc) : 0u;
+    }
+    __syncthreads();
+    // ---- E* = the top-cap experts by g among g > 0 (ties to the lower id):
+    // expert e is in E* when fewer than cap experts beat it in that order.
+    for (int e = threadIdx.x; e < E; e += kHeadThreads) {
+      const uint32_t ke = sm.gkey[e];
+      if (ke == 0) continue;
+      int better = 0;
+      const uint4* g4 = reinterpret_cast<const uint4*>(sm.gkey);  // every thread reads the same word: broadcast
+#pragma unroll 4
+      for (int q4 = 0; q4 < E4 / 4; ++q4) {
+        const uint4 v = g4[q4];
+        const int q = 4 * q4;
+        better += (v.x > ke) || (v.x == ke && q < e);
+        better += (v.y > ke) || (v.y == ke && q + 1 < e);
+        better += (v.z > ke) || (v.z == ke && q + 2 < e);
+        better += (v.w > ke) || (v.w == ke && q + 3 < e);
       }
+      if (better < c.cap) atomicOr(&sm.estar[e >> 5], 1u << (e & 31));
     }
     __syncthreads();
     // ---- pass 2: route the biased logits l' = l + lam_b on E*

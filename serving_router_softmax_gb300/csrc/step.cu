@@ -57,6 +57,19 @@ size_t step_ws(const moe_step_cfg& c, void* base, StepWs* out) {
   return off;
 }
 
+// Selection and routing limits (the control path of the step).
+int plan_validate(const moe_step_cfg& c) {
+  if (c.L < 1 || c.nseq < 1 || c.T < 1) return MOE_ERR_ARG;
+  if (c.T < c.nseq) return MOE_ERR_ARG;
+  eco_cfg ec{c.N, c.W, c.gamma_max, c.mode, c.eps};
+  int st = eco_validate(ec, c.nseq);
+  if (st != MOE_OK) return st;
+  if (static_cast<long long>(c.L) * c.E > static_cast<long long>(c.W) * 32) return MOE_ERR_ARG;
+  moe_route_cfg rc{c.T, c.E, c.k, c.use_bias, c.cap, c.alpha};
+  if ((st = route_validate(rc, true)) != MOE_OK) return st;
+  return union_validate(c.T, c.k, c.E);
+}
+
 int step_validate(const moe_step_cfg& c) {
   if (c.L < 1 || c.nseq < 1 || c.T < 1) return MOE_ERR_ARG;
   if (c.T < c.nseq) return MOE_ERR_ARG;
@@ -129,4 +142,37 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     if ((st = ffn_launch(fa)) != MOE_OK) return st;
   }
   return MOE_OK;
+}
+
+extern "C" int moe_verify_plan(const moe_step_cfg* cfg, const float* P, const int32_t* parent,
+                               const uint32_t* own_fp, const int32_t* gamma_per_seq, const float* node_logits,
+                               int32_t* selected, int32_t* union_size, int32_t* verify_rows,
+                               float* verify_conf, int32_t* ids, float* w, int32_t* n_unique, int32_t* unique,
+                               int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, int32_t* inv,
+                               float* reuse_ratio, int32_t* dev_err, void* stream) {
+  using namespace moe;
+  if (!cfg) return MOE_ERR_ARG;
+  const moe_step_cfg& c = *cfg;
+  int st = plan_validate(c);
+  if (st != MOE_OK) return st;
+  if (!P || !parent || !own_fp || !node_logits || !union_size || !verify_rows || !verify_conf || !ids || !w ||
+      !n_unique || !unique || !offsets || !perm_token || !perm_slot || !inv || !reuse_ratio ||
+      (c.gamma_max > 0 && !selected))
+    return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EcoArgs ea{P, parent, own_fp, c.nseq, gamma_per_seq, {c.N, c.W, c.gamma_max, c.mode, c.eps},
+             selected, union_size, dev_err, verify_rows, verify_conf, c.T, s};
+  if ((st = eco_launch(ea)) != MOE_OK) return st;
+  const int rows = c.nseq * (c.N + 1);
+  const size_t TK = static_cast<size_t>(c.T) * c.k;
+  const size_t cap = static_cast<size_t>(c.E) < TK ? c.E : TK;
+  for (int l = 0; l < c.L; ++l) {
+    RouteArgs ra{node_logits + static_cast<size_t>(l) * rows * c.E, verify_rows, rows,
+                 c.use_bias ? verify_conf : nullptr, {c.T, c.E, c.k, c.use_bias, c.cap, c.alpha},
+                 ids + l * TK, w + l * TK, dev_err, s};
+    if ((st = layer_head_launch(ra, n_unique + l, unique + l * cap, offsets + l * (cap + 1), perm_token + l * TK,
+                                perm_slot + l * TK, inv + l * TK, reuse_ratio + l, true, l > 0)) != MOE_OK)
+      return st;
+  }
+  return check_launch();
 }

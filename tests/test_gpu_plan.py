@@ -1,0 +1,105 @@
+"""GPU parity of moe_verify_plan (the step's selection and per-layer routing
+and union, written out) against the oracle, at small and full sizes."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import serving_router_softmax_gb300 as m
+    return m
+
+
+def plan_for(mv, cfg):
+    from workload import device as wdev
+    from workload import gen
+    wl = gen.make_workload(cfg)
+    t = wdev.workload_tensors(wl, "cuda")
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap, alpha=cfg.alpha)
+    plan = mv.VerifyPlan(spec)
+    plan(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+    torch.cuda.synchronize()
+    return wl, plan
+
+
+def check_against_oracle(wl, plan):
+    from oracle import moe_layer as ml
+    from oracle import verify_step as vs
+    cfg = wl.cfg
+    assert int(plan.dev_err.item()) == 0
+    sels, sizes = vs.run_selection(wl)
+    sel = plan.selected.cpu().numpy()
+    for s in range(cfg.nseq):
+        assert sel[s, : wl.gamma[s]].tolist() == sels[s]
+    assert plan.union_size.cpu().tolist() == sizes
+    rows = vs.verify_rows(wl.parent.shape[0], sels)
+    conf = vs.token_conf(wl.P, sels)
+    assert plan.verify_rows.cpu().tolist() == list(rows)
+    assert np.array_equal(plan.verify_conf.cpu().numpy(), conf)
+    ids, w = plan.ids.cpu().numpy(), plan.w.cpu().numpy()
+    cap = min(cfg.E, wl.T * cfg.k)
+    for l in range(cfg.L):
+        lg = wl.logits[l].reshape(-1, cfg.E)[rows]
+        if cfg.use_bias:
+            lg = ml.reuse_bias(lg, conf, cfg.k, cfg.cap, cfg.alpha)
+        rid, rw = ml.route(lg, cfg.k)
+        assert np.array_equal(ids[l], rid), f"layer {l} ids"
+        np.testing.assert_allclose(w[l], rw, rtol=2e-6, atol=1e-7)
+        up = ml.union_permute(rid, cfg.E)
+        U = up["n_unique"]
+        assert int(plan.n_unique[l]) == U
+        assert plan.unique[l, :U].cpu().tolist() == up["unique"].tolist()
+        assert plan.offsets[l, : U + 1].cpu().tolist() == up["offsets"].tolist()
+        assert plan.perm_token[l].cpu().tolist() == up["perm_token"].tolist()
+        assert plan.perm_slot[l].cpu().tolist() == up["perm_slot"].tolist()
+        assert plan.inv[l].cpu().tolist() == up["inv"].tolist()
+        assert float(plan.reuse_ratio[l]) == float(np.float32(up["reuse_ratio"]))
+        assert U <= cap
+
+
+SMALL = [dict(name="plan_bf16"), dict(name="plan_bias", use_bias=True, cap=8, alpha=0.25),
+         dict(name="plan_batched", nseq=4, ragged=True, tau=0.1),
+         dict(name="plan_batched_bias", nseq=4, ragged=True, tau=0.1, use_bias=True, cap=6, alpha=0.5),
+         dict(name="plan_static", mode=1)]
+
+
+@pytest.mark.parametrize("kw", SMALL, ids=[d["name"] for d in SMALL])
+def test_plan_small_matches_oracle(mv, kw):
+    from workload import gen
+    kw = dict(kw)
+    cfg = gen.small_case(kw.pop("name"), L=3, **kw)
+    wl, plan = plan_for(mv, cfg)
+    check_against_oracle(wl, plan)
+
+
+@pytest.mark.parametrize("name", ["qwen3_235b_like", "gpt_oss_120b_like", "deepseek_v3_like",
+                                  "batched_qwen_like"])
+def test_plan_full_size_matches_oracle(mv, name):
+    from workload import CONFIGS
+    wl, plan = plan_for(mv, CONFIGS[name])
+    check_against_oracle(wl, plan)
+
+
+def test_plan_matches_the_step_unions(mv):
+    """The plan's per-layer union sizes are the ones the whole step reports."""
+    from workload import device as wdev
+    from workload import gen
+    cfg = gen.small_case("plan_vs_step", L=2, use_bias=True, cap=8, alpha=0.25)
+    wl, plan = plan_for(mv, cfg)
+    t = wdev.workload_tensors(wl, "cuda")
+    layers = []
+    for l in range(cfg.L):
+        gu, dn, sgu, sdn = wdev.make_layer_tensors(cfg, l, "cuda")
+        layers.append(mv.ExpertLayer(gu, dn, cfg.dtype, sgu, sdn))
+    step = mv.VerifyStep(plan.spec, layers)
+    step(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    torch.cuda.synchronize()
+    assert step.n_unique.cpu().tolist() == plan.n_unique.cpu().tolist()
