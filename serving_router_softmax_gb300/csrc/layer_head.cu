@@ -138,6 +138,15 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
     bad = (ra.rows && (row < 0 || row >= ra.rows_limit)) ? 2 : 0;
     return row;
   };
+  int my_bad = 0;
+  auto load_conf = [&]() {
+    for (int t = threadIdx.x; t < T; t += kHeadThreads) {
+      const float cf = ra.w_conf[t];
+      sm.wc[t] = cf;
+      if (!(cf >= 0.f)) my_bad = 1;  // NaN or negative
+    }
+  };
+  if (rows_ready && c.use_bias) load_conf();
   if (keep && rows_ready) {
     if (warp < T) {
       const long long row = row_of(warp, kept_bad);
@@ -162,14 +171,7 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
     const long long row = row_of(warp, kept_bad);
     if (!kept_bad) kept_nan = routing::load_row<NPL>(ra.logits + row * E, E, lane, kept, nullptr, 0.f);
   }
-  int my_bad = 0;
-  if (c.use_bias) {
-    for (int t = threadIdx.x; t < T; t += kHeadThreads) {
-      const float cf = ra.w_conf[t];
-      sm.wc[t] = cf;
-      if (!(cf >= 0.f)) my_bad = 1;  // NaN or negative
-    }
-  }
+  if (c.use_bias && !rows_ready) load_conf();
   __syncthreads();  // bookkeeping cleared
 
   if (c.use_bias) {
