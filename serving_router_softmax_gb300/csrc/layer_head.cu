@@ -26,45 +26,51 @@ constexpr int kHeadThreads = 256;
 constexpr int kHeadWarps = kHeadThreads / 32;
 
 struct HeadSmem {
+  int32_t* count;     // [EP] group sizes, EP = 32 * ceil(E / 32) (16-byte aligned, zero past E)
+  int32_t* ustart;    // [E] first perm position of each expert's group
+  uint32_t* cand_key; // [E] experts with g_e > 0: order keys ... (bias only)
+  int32_t* cand_e;    // [E] ... and ids, in arbitrary order
   uint32_t* member;   // [T][EW] routed experts per token (union bookkeeping)
   uint32_t* member0;  // [T][EW] unbiased top-k per token (bias only)
-  int32_t* count;     // [E] group sizes
-  int32_t* ustart;    // [E] first perm position of each expert's group
   int32_t* ids;       // [T*k]
   float* w;           // [T*k]
   float* v1;          // [T] top-1 logit (bias only)
   float* vk1;         // [T] (k+1)-th logit (bias only)
   float* wc;          // [T] confidence weights (bias only)
+  float* vw;          // [T] the weight a token adds to g_e: wc, or 0 if its row is unusable
   uint32_t* estar;    // [EW] preferred experts (bias only)
-  uint32_t* gkey;     // [E4] order keys of g_e, 0 where g_e <= 0 or e >= E (bias only; 16-byte aligned)
   uint8_t* bad;       // [T] 0 ok, 1 NaN logit, 2 row outside the node table
   int* err;
+  int* ncand;
 };
 
 __host__ __device__ inline size_t head_smem_bytes(int T, int E, int k) {
   const int EW = (E + 31) / 32;
-  const size_t E4 = (static_cast<size_t>(E) + 3) & ~size_t(3);
-  return 4 * (E4 + 2 * static_cast<size_t>(T) * EW + 2 * static_cast<size_t>(E) + 2 * static_cast<size_t>(T) * k +
-              3 * static_cast<size_t>(T) + EW + 1) +
+  const size_t EP = 32 * static_cast<size_t>(EW);
+  return 4 * (EP + 3 * static_cast<size_t>(E) + 2 * static_cast<size_t>(T) * EW + 2 * static_cast<size_t>(T) * k +
+              4 * static_cast<size_t>(T) + EW + 2) +
          ((static_cast<size_t>(T) + 15) & ~size_t(15));
 }
 
 __device__ __forceinline__ HeadSmem carve(uint8_t* p, int T, int E, int k) {
   const int EW = (E + 31) / 32;
   HeadSmem s;
-  s.gkey = reinterpret_cast<uint32_t*>(p);
-  s.member = s.gkey + ((E + 3) & ~3);
+  s.count = reinterpret_cast<int32_t*>(p);
+  s.ustart = s.count + 32 * EW;
+  s.cand_key = reinterpret_cast<uint32_t*>(s.ustart + E);
+  s.cand_e = reinterpret_cast<int32_t*>(s.cand_key + E);
+  s.member = reinterpret_cast<uint32_t*>(s.cand_e + E);
   s.member0 = s.member + (size_t)T * EW;
-  s.count = reinterpret_cast<int32_t*>(s.member0 + (size_t)T * EW);
-  s.ustart = s.count + E;
-  s.ids = s.ustart + E;
+  s.ids = reinterpret_cast<int32_t*>(s.member0 + (size_t)T * EW);
   s.w = reinterpret_cast<float*>(s.ids + (size_t)T * k);
   s.v1 = s.w + (size_t)T * k;
   s.vk1 = s.v1 + T;
   s.wc = s.vk1 + T;
-  s.estar = reinterpret_cast<uint32_t*>(s.wc + T);
+  s.vw = s.wc + T;
+  s.estar = reinterpret_cast<uint32_t*>(s.vw + T);
   s.err = reinterpret_cast<int*>(s.estar + EW);
-  s.bad = reinterpret_cast<uint8_t*>(s.err + 1);
+  s.ncand = s.err + 1;
+  s.bad = reinterpret_cast<uint8_t*>(s.ncand + 1);
   return s;
 }
 
@@ -124,9 +130,12 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
 
   // ---- before the dependency wait: clear the bookkeeping, fetch the rows.
   for (int i = threadIdx.x; i < 2 * T * EW; i += kHeadThreads) sm.member[i] = 0;  // member and member0
-  for (int e = threadIdx.x; e < E; e += kHeadThreads) sm.count[e] = 0;
+  for (int e = threadIdx.x; e < 32 * EW; e += kHeadThreads) sm.count[e] = 0;
   for (int i = threadIdx.x; i < EW; i += kHeadThreads) sm.estar[i] = 0;
-  if (threadIdx.x == 0) *sm.err = 0;
+  if (threadIdx.x == 0) {
+    *sm.err = 0;
+    *sm.ncand = 0;
+  }
   // One token per warp keeps its row in registers through both passes.
   const bool keep = T <= kHeadWarps;
   Row<NPL> kept;
@@ -189,7 +198,10 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
         if (!bad) nan = routing::load_row<NPL>(ra.logits + row * E, E, lane, r, nullptr, 0.f);
       }
       if (!bad && nan) bad = 1;
-      if (lane == 0) sm.bad[t] = static_cast<uint8_t>(bad);
+      if (lane == 0) {
+        sm.bad[t] = static_cast<uint8_t>(bad);
+        sm.vw[t] = bad ? 0.f : sm.wc[t];
+      }
       if (bad) continue;
       for (int j = 0; j <= k; ++j) {
         float bv;
@@ -218,37 +230,41 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
       return;
     }
     // ---- g_e (fp32, tokens in ascending order, plain adds), one expert per
-    // thread.  A token that does not hold e, or whose row was unusable, adds
-    // +0.0, which leaves every partial sum unchanged (sums are never -0.0).
-    const int E4 = (E + 3) & ~3;
-    for (int e = threadIdx.x; e < E4; e += kHeadThreads) {
+    // thread.  A token that does not hold e, or whose row was unusable (vw =
+    // 0), adds +0.0, which leaves every partial sum unchanged (sums are never
+    // -0.0).  Experts with g_e > 0 (at most T*k of them) become candidates.
+    for (int e = threadIdx.x; e < E; e += kHeadThreads) {
+      const int we = e >> 5;
+      const uint32_t bit = 1u << (e & 31);
       float acc = 0.f;
-      if (e < E) {
-        for (int b = 0; b < T; ++b) {
-          const bool in = !sm.bad[b] && ((sm.member0[b * EW + (e >> 5)] >> (e & 31)) & 1u);
-          acc = __fadd_rn(acc, in ? sm.wc[b] : 0.f);
-        }
+#pragma unroll 4
+      for (int b = 0; b < T; ++b) acc = __fadd_rn(acc, (sm.member0[b * EW + we] & bit) ? sm.vw[b] : 0.f);
+      if (acc > 0.f) {
+        const int i = atomicAdd(sm.ncand, 1);
+        sm.cand_key[i] = routing::order_key(acc);
+        sm.cand_e[i] = e;
       }
-      sm.gkey[e] = acc > 0.f ? routing::order_key(acc) : 0u;
     }
     __syncthreads();
     // ---- E* = the top-cap experts by g among g > 0 (ties to the lower id):
-    // expert e is in E* when fewer than cap experts beat it in that order.
-    for (int e = threadIdx.x; e < E; e += kHeadThreads) {
-      const uint32_t ke = sm.gkey[e];
-      if (ke == 0) continue;
-      int better = 0;
-      const uint4* g4 = reinterpret_cast<const uint4*>(sm.gkey);  // every thread reads the same word: broadcast
-#pragma unroll 4
-      for (int q4 = 0; q4 < E4 / 4; ++q4) {
-        const uint4 v = g4[q4];
-        const int q = 4 * q4;
-        better += (v.x > ke) || (v.x == ke && q < e);
-        better += (v.y > ke) || (v.y == ke && q + 1 < e);
-        better += (v.z > ke) || (v.z == ke && q + 2 < e);
-        better += (v.w > ke) || (v.w == ke && q + 3 < e);
+    // a candidate is in E* when fewer than cap candidates beat it in that
+    // order (the candidates' order in the list does not matter).
+    {
+      const int nc = *sm.ncand;
+      for (int i = threadIdx.x; i < nc; i += kHeadThreads) {
+        const uint32_t ke = sm.cand_key[i];
+        const int e = sm.cand_e[i];
+        int b0 = 0, b1 = 0;
+        int q = 0;
+        for (; q + 1 < nc; q += 2) {
+          const uint32_t k0 = sm.cand_key[q], k1 = sm.cand_key[q + 1];
+          const int e0 = sm.cand_e[q], e1 = sm.cand_e[q + 1];
+          b0 += (k0 > ke) || (k0 == ke && e0 < e);
+          b1 += (k1 > ke) || (k1 == ke && e1 < e);
+        }
+        if (q < nc) b0 += (sm.cand_key[q] > ke) || (sm.cand_key[q] == ke && sm.cand_e[q] < e);
+        if (b0 + b1 < c.cap) atomicOr(&sm.estar[e >> 5], 1u << (e & 31));
       }
-      if (better < c.cap) atomicOr(&sm.estar[e >> 5], 1u << (e & 31));
     }
     __syncthreads();
     // ---- pass 2: route the biased logits l' = l + lam_b on E*
@@ -317,13 +333,34 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
     return;
   }
   if (warp == 0) {
-    const int per = (E + 31) / 32;
+    // lane l scans experts [l * per, l * per + per); the group sizes are read
+    // as 16-byte vectors when per allows (no bank conflicts)
+    const int per = EW;
     const int e0 = lane * per;
+    int cv[NPL];
+    bool vec = false;
+    if constexpr (NPL >= 4) vec = (per & 3) == 0;
+    if (vec) {
+      if constexpr (NPL >= 4) {
+#pragma unroll
+        for (int i = 0; i < NPL; i += 4) {
+          int4 v = make_int4(0, 0, 0, 0);
+          if (i < per) v = *reinterpret_cast<const int4*>(sm.count + e0 + i);
+          cv[i] = v.x;
+          cv[i + 1] = v.y;
+          cv[i + 2] = v.z;
+          cv[i + 3] = v.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) cv[i] = i < per ? sm.count[e0 + i] : 0;
+    }
     int nz = 0, tok = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e) {
-      const int cnt = sm.count[e];
-      nz += cnt > 0;
-      tok += cnt;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      nz += cv[i] > 0;
+      tok += cv[i];
     }
     int nz_ex = nz, tok_ex = tok;
     for (int off = 1; off < 32; off <<= 1) {
@@ -336,14 +373,15 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
     }
     nz_ex -= nz;
     tok_ex -= tok;
-    for (int e = e0; e < e0 + per && e < E; ++e) {
-      const int cnt = sm.count[e];
-      if (cnt > 0) {
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = e0 + i;
+      if (cv[i] > 0) {  // zero past per and past E
         sm.ustart[e] = tok_ex;
         unique[nz_ex] = e;
         offsets[nz_ex] = tok_ex;
         ++nz_ex;
-        tok_ex += cnt;
+        tok_ex += cv[i];
       }
     }
     if (lane == 31) {
