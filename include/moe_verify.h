@@ -10,6 +10,7 @@
  *   moe_verify_ffn     grouped SwiGLU expert FFN over the union + weighted combine
  *   moe_verify_step    all of the above for L layers in one call
  *   moe_verify_plan    the step's selection and per-layer routing/union only
+ *   s2_expand          S2-MoE utility-driven draft expansion
  *
  * Conventions shared by every entry point
  *   - Every array argument is a DEVICE pointer owned by the caller, unless a
@@ -343,6 +344,42 @@ int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* pare
                     int32_t* n_unique, float* y, void* workspace, size_t ws_bytes,
                     int32_t* dev_err, void* stream);
 
+/* ---------------------------------------------------------------- S2-MoE expansion
+ * s2_expand -- routing-aware adaptive speculative expansion: which draft
+ * tokens are worth verifying, judged by the experts they would add.
+ *
+ * Defined by: S2-MoE write-up, component 1.  Adding draft token i to the
+ * selected set S costs |E_i minus the union of E_j over j in S| * T_exp plus
+ * the draft cost C_draft; its utility is p_i * T_AR over that cost; every
+ * candidate with utility >= 1 is taken, until none qualifies.  Readings used:
+ * on a draft tree a node is a candidate once its parent is selected (the
+ * root's children always are), so the selection is prefix-closed; the
+ * selected set does not depend on the order candidates are examined in (it
+ * is the least fixed point of a monotone rule); U_i >= 1 is evaluated as
+ * p_i * T_AR >= n_new * T_exp + C_draft in fp64 with that operation order.
+ *
+ *   P          [nseq, N] fp32 path probability of each draft node (p_i).
+ *   parent     [nseq, N] int32, breadth-first order: -1 or an index < t.
+ *   own_fp     [nseq, N, W] uint32: node's own predicted footprint, bit
+ *              l*E + e for expert e of layer l.
+ *   cfg        N, W and the cost model T_AR, T_exp, C_draft (finite, >= 0,
+ *              any consistent time unit).
+ *   selected   [nseq, N] int32 out: selected node indices in ascending
+ *              order, then -1.
+ *   n_selected [nseq] int32 out; union_size [nseq] int32 out: bits set in
+ *              the union of the selected footprints.
+ * Limits: 1 <= N <= 1024, 1 <= W <= 4096, N*W <= 40960.  Device errors:
+ * MOE_DEV_BAD_TREE, MOE_DEV_BAD_PROB (that sequence selects nothing).
+ */
+typedef struct {
+  int32_t N, W;
+  float T_AR, T_exp, C_draft;
+} s2_cfg;
+
+int s2_expand(const float* P, const int32_t* parent, const uint32_t* own_fp, int32_t nseq,
+              const s2_cfg* cfg, int32_t* selected, int32_t* n_selected, int32_t* union_size,
+              int32_t* dev_err, void* stream);
+
 /* ---------------------------------------------------------------- plan
  * moe_verify_plan -- the control path of one verify step, without the
  * expert FFN: the selection of moe_verify_step and, for every layer, its
@@ -384,10 +421,10 @@ int moe_verify_plan(const moe_step_cfg* cfg, const float* P, const int32_t* pare
  * synchronises those events (host blocking) and writes, per kernel class, the
  * summed milliseconds and the launch count.  Classes: 0 eco_select, 1 route,
  * 2 union/permute, 3 FFN prep, 4 FFN gate/up, 5 FFN down, 6 combine,
- * 7 router logits.
+ * 7 router logits, 8 S2-MoE expansion.
  * Not for use under stream capture.
  */
-enum { MOE_PROF_CLASSES = 8 };
+enum { MOE_PROF_CLASSES = 9 };
 int moe_profile_begin(int32_t max_launches, int32_t class_mask);
 int moe_profile_end(float* ms_per_class, int32_t* launches_per_class, int32_t n_classes);
 

@@ -7,7 +7,7 @@ Importing it loads the library and raises if it has not been built.
 """
 from . import _lib
 from .api import (ExpertLayer, MoEError, StepSpec, VerifyPlan, VerifyStep, eco_select, ffn_workspace_bytes,  # noqa: F401
-                  launch_count, new_dev_err, pack_tiled, profile_begin, profile_end, route, router_logits,
+                  launch_count, new_dev_err, pack_tiled, profile_begin, profile_end, route, router_logits, s2_expand,
                   step_workspace_bytes,
                   union_permute, verify_ffn)
 

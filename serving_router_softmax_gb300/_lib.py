@@ -16,11 +16,16 @@ DEV_NAN_LOGIT, DEV_BAD_ID, DEV_DUP_ID, DEV_BAD_TREE, DEV_BAD_PROB, DEV_TIMEOUT, 
 DTYPE_F32, DTYPE_BF16, DTYPE_E4M3_B128 = 0, 1, 2
 LAYOUT_ROWMAJOR, LAYOUT_TILED = 0, 1
 PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up", "ffn_down",
-                "combine", "router_logits"]
+                "combine", "router_logits", "s2_expand"]
 
-EXPORTED = ["moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
+EXPORTED = ["s2_expand", "moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
             "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_verify_plan", "moe_profile_begin",
             "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version"]
+
+
+class S2Cfg(C.Structure):
+    _fields_ = [("N", C.c_int32), ("W", C.c_int32), ("T_AR", C.c_float), ("T_exp", C.c_float),
+                ("C_draft", C.c_float)]
 
 
 class RouterCfg(C.Structure):
@@ -67,6 +72,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib = C.CDLL(path)
     vp, i32, sz = C.c_void_p, C.c_int32, C.c_size_t
     P = C.POINTER
+    lib.s2_expand.argtypes = [vp, vp, vp, i32, P(S2Cfg), vp, vp, vp, vp, vp]
+    lib.s2_expand.restype = C.c_int
     lib.moe_router_logits.argtypes = [vp, vp, P(RouterCfg), vp, vp]
     lib.moe_router_logits.restype = C.c_int
     lib.moe_route.argtypes = [vp, vp, P(RouteCfg), vp, vp, vp, vp]

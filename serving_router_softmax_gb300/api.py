@@ -347,6 +347,26 @@ class VerifyPlan:
         return self
 
 
+def s2_expand(P: torch.Tensor, parent: torch.Tensor, own_fp: torch.Tensor, T_AR: float, T_exp: float,
+              C_draft: float = 0.0, dev_err: Optional[torch.Tensor] = None, stream=None):
+    """S2-MoE utility expansion per sequence: (selected [nseq, N] ascending
+    then -1, n_selected [nseq], union_size [nseq])."""
+    lib = L.load()
+    nseq, N = P.shape
+    W = own_fp.shape[-1]
+    _need(P, torch.float32, (nseq, N), "P")
+    _need(parent, torch.int32, (nseq, N), "parent")
+    _need(own_fp, torch.int32, (nseq, N, W), "own_fp")
+    dev = P.device
+    selected = torch.empty((nseq, N), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(nseq, dtype=torch.int32, device=dev)
+    usize = torch.empty(nseq, dtype=torch.int32, device=dev)
+    cfg = L.S2Cfg(N, W, T_AR, T_exp, C_draft)
+    _check(lib.s2_expand(_ptr(P), _ptr(parent), _ptr(own_fp), nseq, C.byref(cfg), _ptr(selected), _ptr(n_sel),
+                         _ptr(usize), _ptr(dev_err), _stream(stream)), "s2_expand")
+    return selected, n_sel, usize
+
+
 def profile_begin(max_launches: int = 65536, classes: Optional[Sequence[str]] = None):
     """Start event timing of the library's launches (all classes by default)."""
     names = L.PROF_CLASSES if classes is None else classes

@@ -21,7 +21,7 @@ struct LaunchScope {
 };
 
 enum ProfClass { kProfEco = 0, kProfRoute = 1, kProfUnion = 2, kProfPrep = 3, kProfGateUp = 4,
-                 kProfDown = 5, kProfCombine = 6, kProfRouter = 7 };
+                 kProfDown = 5, kProfCombine = 6, kProfRouter = 7, kProfS2 = 8 };
 
 int sm_count();
 
