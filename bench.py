@@ -198,6 +198,76 @@ def gate_up_bytes(cfg):
     return b
 
 
+def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
+    """The verify-cost model of the S2-MoE write-up (Fig. 6), checked on this
+    GPU: the whole step at several draft budgets and both selection modes,
+    step time fitted against the total expert union (T_exp = slope, R^2,
+    MAPE); then s2_expand on the workload's trees with that T_exp, T_AR = the
+    measured step with no draft token (one autoregressive token: the root
+    alone) and C_draft = 0."""
+    import torch
+    from workload import gen
+    from workload import device as wdev
+
+    pts = []
+    for mode in (0, 1):
+        for g in (0, 1, 2, 3, 4, 6, 8):
+            c2 = cfg.replace(gamma=g, mode=mode, ragged=False)
+            wl2 = gen.make_workload(c2)
+            t2 = wdev.workload_tensors(wl2, dev)
+            spec = mv.StepSpec(L=c2.L, nseq=c2.nseq, N=wl2.parent.shape[0], W=c2.W, E=c2.E, k=c2.k, H=c2.H,
+                               I=c2.I, dtype=c2.dtype, T=wl2.T, gamma_max=int(wl2.gamma.max()), mode=mode,
+                               eps=c2.eps, use_bias=c2.use_bias, cap=c2.cap, alpha=c2.alpha, layout=layout)
+            step = mv.VerifyStep(spec, layers, dev)
+
+            def one():
+                step(t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"], t2["x"])
+
+            for _ in range(3):
+                one()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                one()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            pts.append({"gamma": g, "mode": "marginal" if mode == 0 else "static", "tokens": int(wl2.T),
+                        "union_experts": int(step.n_unique.sum().item()),
+                        "ms": e0.elapsed_time(e1) / steps})
+            del step
+    x = np.array([p["union_experts"] for p in pts], dtype=np.float64)
+    y = np.array([p["ms"] for p in pts], dtype=np.float64) * 1e3  # us
+    A = np.stack([np.ones_like(x), x], axis=1)
+    (a, b), *_ = np.linalg.lstsq(A, y, rcond=None)
+    pred = a + b * x
+    r2 = 1.0 - float(np.sum((y - pred) ** 2) / np.sum((y - y.mean()) ** 2))
+    mape = float(np.mean(np.abs(pred - y) / y))
+    model = {"points": pts, "T_exp_us": float(b), "intercept_us": float(a), "r2": r2, "mape": mape,
+             "fit": "step_us = intercept + T_exp * (sum over layers of unique experts)"}
+
+    # S2-MoE expansion on the workload's own trees with the calibrated cost.
+    wl = gen.make_workload(cfg)
+    t = wdev.workload_tensors(wl, dev)
+    T_exp = float(b)
+    T_AR = 1e3 * next(p["ms"] for p in pts if p["gamma"] == 0)
+    sel, n_sel, usize = mv.s2_expand(t["P"], t["parent"], t["own_fp"], T_AR, T_exp, 0.0)
+    for _ in range(3):
+        mv.s2_expand(t["P"], t["parent"], t["own_fp"], T_AR, T_exp, 0.0)
+    torch.cuda.synchronize()
+    mv.profile_begin(max_launches=128, classes=["s2_expand"])
+    for _ in range(100):
+        mv.s2_expand(t["P"], t["parent"], t["own_fp"], T_AR, T_exp, 0.0)
+    torch.cuda.synchronize()
+    sp = mv.profile_end()["s2_expand"]
+    expansion = {"T_AR_us": T_AR, "T_exp_us": T_exp, "C_draft_us": 0.0,
+                 "selected_per_seq": n_sel.cpu().tolist(), "predicted_union_experts": usize.cpu().tolist(),
+                 "draft_nodes": int(wl.parent.shape[0]),
+                 "us_per_call": sp["ms"] * 1e3 / max(sp["launches"], 1)}
+    return model, expansion
+
+
 def router_measure(mv, cfg, wl, dev, stream, iters=200):
     """Gate logits of the step's verify tokens (T x H activations against one
     layer's E x H gate), timed with CUDA events over back-to-back launches that
@@ -347,6 +417,11 @@ def ours(args, rank, ws, local):
     torch.cuda.synchronize()
     ctrl_ms = c0.elapsed_time(c1) / n_plan
 
+    # ---- verify-cost model check and S2-MoE expansion (rank 0 only).
+    cost_model, expansion = (None, None)
+    if rank == 0 and not args.layers and not args.experts:
+        cost_model, expansion = cost_model_and_expansion(mv, cfg, layers, layout, dev, stream)
+
     # ---- router logits, timed alone (the step routes the given node logits).
     router = router_measure(mv, cfg, wl, dev, stream)
 
@@ -437,6 +512,8 @@ def ours(args, rank, ws, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "router_logits": router,
+        "cost_model": cost_model,
+        "s2_expand": expansion,
     }
     return result, wl, cfg
 
