@@ -23,9 +23,19 @@ Readings where the page is silent:
 * Scores are compared exactly: P is an fp32 number and eps a power of two, so
   every score is a rational number; we compare them with Python Fractions.
 
+* Batch (``select_batch_global``; the page's batch ablation in section 4.3
+  gives no algorithm): one buffer B shared by all sequences of the batch, and
+  one greedy over the forest of their draft trees with the budget
+  sum(gamma_i) and at most ``cap`` nodes per sequence.  Each sequence's depth
+  is an outcome of the greedy (confident sequences whose experts overlap get
+  more nodes), in the spirit of the width-vs-depth note's confidence gating.
+  Ties go to the lower (sequence, node) index.
+
 Parity: pinned (tests/test_oracle_eco.py: hand-worked trees, static mode equal
 to a sort by static score, prefix closure, union bookkeeping, aggregate
-marginal-vs-static comparison over seeded trees).
+marginal-vs-static comparison over seeded trees; batch mode: one sequence
+equals the per-sequence greedy, a hand-worked batch, budget and cap
+bookkeeping).
 """
 from __future__ import annotations
 
@@ -105,3 +115,49 @@ def select_batch(P: np.ndarray, parent: np.ndarray, own_fp: np.ndarray, E: int,
         sels.append(sel)
         sizes.append(len(B))
     return sels, sizes
+
+
+def select_batch_global(P: np.ndarray, parent: np.ndarray, own_fp: np.ndarray, E: int,
+                        gamma: Sequence[int], eps: float, cap: int):
+    """Batch-global marginal selection (see the module notes).
+
+    Returns (per-sequence selected lists in selection order, per-sequence
+    union sizes of their own selected trajectories, batch union size |B|).
+    """
+    nseq, n = P.shape
+    par = [int(p) for p in parent]
+    trajs = []
+    for s in range(nseq):
+        own = [footprint_set(own_fp[s, t], E) for t in range(n)]
+        trajs.append(trajectory_footprints(par, own))
+    eps_q = Fraction(eps)
+    Pq = [[Fraction(float(np.float32(p))) for p in P[s]] for s in range(nseq)]
+    cap = min(cap, n)
+    budget = sum(min(max(int(g), 0), n) for g in gamma)
+    sels: List[List[int]] = [[] for _ in range(nseq)]
+    chosen = set()
+    B: Set = set()
+    for _ in range(budget):
+        best, best_score = None, None
+        for s in range(nseq):
+            if len(sels[s]) >= cap:
+                continue
+            for t in range(n):
+                if (s, t) in chosen:
+                    continue
+                score = Pq[s][t] / (len(trajs[s][t] - B) + eps_q)
+                if best is None or score > best_score:
+                    best, best_score = (s, t), score
+        if best is None:
+            break
+        s, t = best
+        sels[s].append(t)
+        chosen.add(best)
+        B |= trajs[s][t]
+    sizes = []
+    for s in range(nseq):
+        U: Set = set()
+        for t in sels[s]:
+            U |= trajs[s][t]
+        sizes.append(len(U))
+    return sels, sizes, len(B)

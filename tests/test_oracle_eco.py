@@ -165,3 +165,94 @@ def test_marginal_not_worse_than_static_on_aggregate():
 def test_footprint_set_roundtrip():
     fp = bitsets([[(0, 0), (1, 15), (2, 31), (3, 0)]], 4, 32)[0]
     assert eco.footprint_set(fp, 32) == {(0, 0), (1, 15), (2, 31), (3, 0)}
+
+
+# ------------------------------------------------------------ batch-global mode
+def test_batch_global_one_sequence_is_the_per_sequence_greedy():
+    rng = np.random.default_rng(50)
+    for _ in range(100):
+        parent, P, fp = random_tree(rng)
+        g = int(rng.integers(0, 15))
+        sels, sizes = eco.select_batch(P[None], parent, fp[None], 16, [g], 2.0 ** -10, 0)
+        bs, bsz, bu = eco.select_batch_global(P[None], parent, fp[None], 16, [g], 2.0 ** -10, 14)
+        assert bs == sels and bsz == sizes and bu == sizes[0]
+
+
+def test_batch_global_hand_example():
+    # sequence A: a0 (P .9, 3 experts) -> a1 (P .8, 2 more); sequence B: b0 (P .6,
+    # 1 expert) -> b1 (P .5, 1 more).  Budget 2 (gamma 1 + 1), cap 2.
+    # Per sequence: A takes a0, B takes b0: union {1,2,3,6}.
+    # Batch: b0 scores .6/1 > a0 .9/3; then b1 (cost 1, .5) beats a0 (.3):
+    # depth vector (0, 2), union {6, 7}.
+    E = 16
+    parent = np.array([-1, 0])
+    P = np.array([[0.9, 0.8], [0.6, 0.5]], dtype=np.float32)
+    fp = np.stack([bitsets([[(0, 1), (0, 2), (0, 3)], [(0, 4), (0, 5)]], 1, E),
+                   bitsets([[(0, 6)], [(0, 7)]], 1, E)])
+    sels, sizes = eco.select_batch(P, parent, fp, E, [1, 1], 2.0 ** -10, 0)
+    assert sels == [[0], [0]] and sizes == [3, 1]
+    bs, bsz, bu = eco.select_batch_global(P, parent, fp, E, [1, 1], 2.0 ** -10, 2)
+    assert bs == [[], [0, 1]] and bsz == [0, 2] and bu == 2
+    # a cap of one node per sequence forces the second pick into A
+    bs, bsz, bu = eco.select_batch_global(P, parent, fp, E, [1, 1], 2.0 ** -10, 1)
+    assert bs == [[0], [0]] and bu == 4
+
+
+def test_batch_global_budget_cap_prefix_and_unions():
+    rng = np.random.default_rng(51)
+    for _ in range(60):
+        trees = [random_tree(rng) for _ in range(3)]
+        parent = trees[0][0]
+        P = np.stack([tr[1] for tr in trees])
+        fp = np.stack([tr[2] for tr in trees])
+        gam = [int(x) for x in rng.integers(0, 7, size=3)]
+        cap = int(rng.integers(1, 15))
+        bs, bsz, bu = eco.select_batch_global(P, parent, fp, 16, gam, 2.0 ** -10, cap)
+        assert sum(len(x) for x in bs) == min(sum(gam), 3 * min(cap, 14))
+        U = set()
+        for s in range(3):
+            assert len(bs[s]) <= cap
+            own = [eco.footprint_set(fp[s, t], 16) for t in range(14)]
+            traj = eco.trajectory_footprints(list(parent), own)
+            seen, Us = set(), set()
+            for t in bs[s]:
+                assert parent[t] < 0 or parent[t] in seen
+                seen.add(t)
+                Us |= traj[t]
+            assert len(Us) == bsz[s]
+            U |= Us
+        assert len(U) == bu
+
+
+def test_batch_global_union_not_larger_on_aggregate():
+    """Sharing B across the batch lets the greedy buy experts once for several
+    sequences; over seeded batches of four trees with one budget, the batch
+    union is smaller on average than the union of per-sequence selections."""
+    rng = np.random.default_rng(52)
+    ub, up = [], []
+    for _ in range(150):
+        trees = [random_tree(rng, L=2, E=16, k=2) for _ in range(4)]
+        parent = trees[0][0]
+        P = np.stack([tr[1] for tr in trees])
+        fp = np.stack([tr[2] for tr in trees])
+        sels, _ = eco.select_batch(P, parent, fp, 16, [4] * 4, 2.0 ** -10, 0)
+        U = set()
+        for s in range(4):
+            own = [eco.footprint_set(fp[s, t], 16) for t in range(14)]
+            traj = eco.trajectory_footprints(list(parent), own)
+            for t in sels[s]:
+                U |= traj[t]
+        up.append(len(U))
+        _, _, bu = eco.select_batch_global(P, parent, fp, 16, [4] * 4, 2.0 ** -10, 14)
+        ub.append(bu)
+    assert np.mean(ub) < np.mean(up)
+
+
+def test_batch_global_ties_go_to_the_lower_sequence():
+    E = 16
+    parent = np.array([-1, 0])
+    P = np.array([[0.5, 0.25], [0.5, 0.25]], dtype=np.float32)
+    one = bitsets([[(0, 1)], [(0, 2)]], 1, E)
+    fp = np.stack([one, one])
+    bs, bsz, bu = eco.select_batch_global(P, parent, fp, E, [1, 0], 2.0 ** -10, 2)
+    assert bs == [[0], []] and bu == 1
