@@ -276,6 +276,12 @@ int moe_verify_ffn_noalloc(const void* x, int32_t T, int32_t k, const moe_layer_
  * S(t) = P(t) / (|E_traj(t) \ B| + eps); greedy: take the argmax, add it to
  * S, B |= E_traj(best), until gamma nodes are chosen; prefix consistency).
  * mode 1 is the static ablation of section 4.3: denominator |E_traj(t)|.
+ * mode 2 is batch-global: one buffer B shared by all nseq sequences and one
+ * greedy over the forest of their trees, with the budget
+ * sum(min(gamma_i, N)) and at most min(gamma_max, N) nodes per sequence, so
+ * each sequence's depth is decided by the scores (the write-up's batch
+ * ablation, section 4.3, gives no algorithm; this is the plainest batch form
+ * of section 3.3).  Ties go to the lower (sequence, node) index.
  *
  *   P        [nseq, N] fp32 path probabilities (product of draft
  *            probabilities from the root), finite and >= 0.
@@ -287,13 +293,15 @@ int moe_verify_ffn_noalloc(const void* x, int32_t T, int32_t k, const moe_layer_
  *   gamma_per_seq [nseq] int32 per-sequence budget in [0, gamma_max], or
  *            NULL for gamma_max everywhere.  Budgets above N select all nodes.
  *   selected [nseq, gamma_max] int32 out: chosen nodes in selection order;
- *            unused slots are -1.
- *   union_size [nseq] int32 out: |B| after the last round.
+ *            unused slots are -1 (in mode 2 a sequence's count is whatever
+ *            the greedy gave it).
+ *   union_size [nseq] int32 out: |B| after the last round (mode 2: the
+ *            union of that sequence's own selected trajectories).
  * Scores are compared exactly: a beats b when
  * P_a * (c_b + eps) > P_b * (c_a + eps), computed in fp64 (exact under the
  * limits below); equal scores go to the lower node index.
  * Limits: eps = 2^-s with 0 <= s <= 20; W*32*2^s < 2^29; 1 <= N <= 1024;
- * 1 <= W <= 4096; N*W <= 40960.
+ * 1 <= W <= 4096; N*W <= 40960; mode 2: nseq*N <= 1024, nseq*N*W <= 40960.
  * Device errors: MOE_DEV_BAD_TREE, MOE_DEV_BAD_PROB (that sequence's
  * selected = -1, union_size = 0).
  */

@@ -55,10 +55,16 @@ def token_conf(P: np.ndarray, sels: List[List[int]]) -> np.ndarray:
     return np.array(out, dtype=np.float32)
 
 
-def run_selection(wl, mode: Optional[int] = None):
+def run_selection(wl, mode: Optional[int] = None, cap: Optional[int] = None):
+    """Per-sequence selection (modes 0, 1) or batch-global (mode 2, with at
+    most ``cap`` nodes per sequence; default the largest gamma_i)."""
     cfg = wl.cfg
-    return eco.select_batch(wl.P, wl.parent, wl.own_fp, cfg.E, wl.gamma, cfg.eps,
-                            cfg.mode if mode is None else mode)
+    mode = cfg.mode if mode is None else mode
+    if mode == 2:
+        cap = int(np.max(wl.gamma)) if cap is None else cap
+        sels, sizes, _ = eco.select_batch_global(wl.P, wl.parent, wl.own_fp, cfg.E, wl.gamma, cfg.eps, cap)
+        return sels, sizes
+    return eco.select_batch(wl.P, wl.parent, wl.own_fp, cfg.E, wl.gamma, cfg.eps, mode)
 
 
 def run_step(wl, experts_for_layer, layers: Optional[Sequence[int]] = None,

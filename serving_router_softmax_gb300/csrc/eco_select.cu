@@ -13,6 +13,14 @@
 // Scores are compared by cross-multiplication in fp64, which is exact because
 // P is fp32 (24-bit significand) and c + eps = c + 2^-s has at most 29
 // significant bits (checked on the host).
+//
+// mode 2 (batch-global): one CTA over the forest of all sequences' trees, one
+// buffer B shared by the batch and one greedy with the budget sum(gamma_i) and
+// at most min(gamma_max, N) nodes per sequence; each sequence's depth is an
+// outcome of the greedy.  The EcoSpec write-up's batch ablation (section 4.3)
+// gives no algorithm; this is the plainest batch form of section 3.3, and it
+// turns the confidence gating of the width-vs-depth note into a by-product of
+// the score.  Ties go to the lower (sequence, node) index.
 #include "common.cuh"
 
 namespace moe {
@@ -196,12 +204,181 @@ __global__ void __launch_bounds__(512) eco_kernel(
   }
 }
 
+__global__ void __launch_bounds__(512) eco_batch_kernel(
+    const float* __restrict__ P, const int32_t* __restrict__ parent, const uint32_t* __restrict__ own_fp,
+    const int32_t* __restrict__ gamma_per_seq, int N, int W, int nseq, int gamma_max, double eps,
+    int32_t* __restrict__ selected, int32_t* __restrict__ union_size, int32_t* dev_err,
+    int32_t* __restrict__ verify_rows, float* __restrict__ verify_conf, int T_expected) {
+  extern __shared__ uint32_t smem[];
+  const int G = nseq * N;
+  uint32_t* traj = smem;               // [G][W]
+  uint32_t* B = traj + (size_t)G * W;  // [W]
+  __shared__ int32_t cost[kMaxN];
+  __shared__ uint8_t chosen[kMaxN];
+  __shared__ int16_t par_s[kMaxN];     // parent as a global node index (-1: root)
+  __shared__ int16_t depth_s[kMaxN];
+  __shared__ int16_t cnt[kMaxN];       // nodes taken per sequence
+  __shared__ int bad, best_g, max_depth, budget;
+  pdl_trigger();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int cap = gamma_max < N ? gamma_max : N;
+
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const int s = g / N, t = g - s * N;
+    const int p = parent[g];
+    if (p < -1 || p >= t) atomicOr(&bad, MOE_DEV_BAD_TREE);
+    const float pt = P[g];
+    if (!(pt >= 0.f) || pt == INFINITY) atomicOr(&bad, MOE_DEV_BAD_PROB);
+    par_s[g] = static_cast<int16_t>(p < 0 ? -1 : s * N + p);
+    chosen[g] = 0;
+  }
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int gs = gamma_per_seq ? gamma_per_seq[s] : gamma_max;
+    if (gs < 0 || gs > gamma_max) atomicOr(&bad, MOE_DEV_BAD_TREE);
+    cnt[s] = 0;
+  }
+  for (int w = threadIdx.x; w < W; w += blockDim.x) B[w] = 0;
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) flag_error(dev_err, bad);
+    for (int i = threadIdx.x; i < nseq * gamma_max; i += blockDim.x) selected[i] = -1;
+    for (int s = threadIdx.x; s < nseq; s += blockDim.x) union_size[s] = 0;
+    if (verify_rows) {
+      // every token points at its sequence's root row (keeps the gathers in bounds)
+      if (threadIdx.x == 0) {
+        int tok = 0;
+        for (int s = 0; s < nseq && tok < T_expected; ++s) {
+          int gs = gamma_per_seq ? gamma_per_seq[s] : gamma_max;
+          gs = gs < 0 ? 0 : (gs > N ? N : gs);
+          for (int q = 0; q <= gs && tok < T_expected; ++q, ++tok) {
+            verify_rows[tok] = s * (N + 1);
+            verify_conf[tok] = 1.f;
+          }
+        }
+      }
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    int b = 0;
+    for (int s = 0; s < nseq; ++s) {
+      int gs = gamma_per_seq ? gamma_per_seq[s] : gamma_max;
+      b += gs < N ? gs : N;
+    }
+    budget = b;
+  }
+
+  // Trajectory footprints, level by level over the forest.
+  for (int i = threadIdx.x; i < G * W; i += blockDim.x) traj[i] = own_fp[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int maxd = 0;
+    for (int g = 0; g < G; ++g) {
+      const int p = par_s[g];
+      const int d = p < 0 ? 0 : depth_s[p] + 1;
+      depth_s[g] = static_cast<int16_t>(d);
+      maxd = d > maxd ? d : maxd;
+    }
+    max_depth = maxd;
+  }
+  __syncthreads();
+  for (int d = 1; d <= max_depth; ++d) {
+    for (int i = threadIdx.x; i < G * W; i += blockDim.x) {
+      const int g = i / W;
+      if (depth_s[g] == d) traj[i] |= traj[(size_t)par_s[g] * W + (i - g * W)];
+    }
+    __syncthreads();
+  }
+
+  for (int r = 0; r < budget; ++r) {
+    for (int g = warp; g < G; g += nwarps) {
+      int c = 0;
+      if (!chosen[g] && cnt[g / N] < cap) {
+        const uint32_t* tt = traj + (size_t)g * W;
+        for (int w = lane; w < W; w += 32) c += __popc(tt[w] & ~B[w]);
+        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+      }
+      if (lane == 0) cost[g] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float bp = 0.f;
+      int bc = 0, bi = -1;
+      for (int g = lane; g < G; g += 32) {
+        if (chosen[g] || cnt[g / N] >= cap) continue;
+        if (bi < 0 || score_better(P[g], cost[g], g, bp, bc, bi, eps)) {
+          bp = P[g];
+          bc = cost[g];
+          bi = g;
+        }
+      }
+      for (int off = 16; off > 0; off >>= 1) {
+        const float op = __shfl_xor_sync(0xFFFFFFFFu, bp, off);
+        const int oc = __shfl_xor_sync(0xFFFFFFFFu, bc, off);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+        if (oi >= 0 && (bi < 0 || score_better(op, oc, oi, bp, bc, bi, eps))) {
+          bp = op;
+          bc = oc;
+          bi = oi;
+        }
+      }
+      if (lane == 0) {
+        best_g = bi;
+        if (bi >= 0) {
+          const int s = bi / N;
+          chosen[bi] = 1;
+          selected[(size_t)s * gamma_max + cnt[s]] = bi - s * N;
+          cnt[s] = static_cast<int16_t>(cnt[s] + 1);
+        }
+      }
+    }
+    __syncthreads();
+    if (best_g < 0) break;
+    const uint32_t* tb = traj + (size_t)best_g * W;
+    for (int w = threadIdx.x; w < W; w += blockDim.x) B[w] |= tb[w];
+    __syncthreads();
+  }
+
+  // Unused slots, per-sequence unions of their own selections.
+  for (int i = threadIdx.x; i < nseq * gamma_max; i += blockDim.x) {
+    const int s = i / gamma_max, j = i - s * gamma_max;
+    if (j >= cnt[s]) selected[i] = -1;
+  }
+  for (int s = warp; s < nseq; s += nwarps) {
+    int c = 0;
+    for (int w = lane; w < W; w += 32) {
+      uint32_t u = 0;
+      for (int j = 0; j < cnt[s]; ++j) u |= traj[(size_t)(s * N + selected[(size_t)s * gamma_max + j]) * W + w];
+      c += __popc(u);
+    }
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+    if (lane == 0) union_size[s] = c;
+  }
+  if (verify_rows && threadIdx.x == 0) {
+    int tok = 0;
+    for (int s = 0; s < nseq; ++s) {
+      for (int q = 0; q <= cnt[s]; ++q, ++tok) {
+        if (tok >= T_expected) continue;
+        const int node = q == 0 ? -1 : selected[(size_t)s * gamma_max + q - 1];
+        verify_rows[tok] = s * (N + 1) + (q == 0 ? 0 : 1 + node);
+        verify_conf[tok] = q == 0 ? 1.f : P[(size_t)s * N + node];
+      }
+    }
+    if (tok != T_expected) flag_error(dev_err, MOE_DEV_CAPACITY);
+  }
+}
+
 }  // namespace
 
 int eco_validate(const eco_cfg& c, int nseq) {
   if (nseq < 0 || c.N < 1 || c.N > kMaxN || c.W < 1 || c.W > kMaxW) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(c.N) * c.W > kMaxNW) return MOE_ERR_UNSUPPORTED;
-  if (c.gamma_max < 0 || (c.mode != 0 && c.mode != 1)) return MOE_ERR_ARG;
+  if (c.gamma_max < 0 || c.mode < 0 || c.mode > 2) return MOE_ERR_ARG;
+  if (c.mode == 2 && (static_cast<long long>(nseq) * c.N > kMaxN ||
+                      static_cast<long long>(nseq) * c.N * c.W > kMaxNW))
+    return MOE_ERR_UNSUPPORTED;
   // eps must be 2^-s, 0 <= s <= 20, and W*32 * 2^s < 2^29 so that c + eps is
   // exact in <= 29 bits and P * (c + eps) is exact in fp64.
   int s = -1;
@@ -216,6 +393,18 @@ int eco_validate(const eco_cfg& c, int nseq) {
 int eco_launch(const EcoArgs& a) {
   if (a.nseq == 0) return MOE_OK;
   const auto& c = a.cfg;
+  if (c.mode == 2) {
+    const size_t smem = (static_cast<size_t>(a.nseq) * c.N * c.W + c.W) * sizeof(uint32_t);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(eco_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    LaunchScope ls(kProfEco, a.stream);
+    eco_batch_kernel<<<1, 512, smem, a.stream>>>(a.P, a.parent, a.own_fp, a.gamma, c.N, c.W, a.nseq, c.gamma_max,
+                                                  static_cast<double>(c.eps), a.selected, a.union_size, a.dev_err,
+                                                  a.verify_rows, a.verify_conf, a.T_expected);
+    return check_launch();
+  }
   size_t smem = (static_cast<size_t>(c.N) * c.W + c.W) * sizeof(uint32_t);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(eco_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -187,7 +187,9 @@ def check_step(wl, got, ref, tol, sample_tokens=None):
     cfg = wl.cfg
     assert got["dev_err"] == 0
     for s in range(cfg.nseq):
-        assert got["selected"][s, : wl.gamma[s]].tolist() == ref["selected"][s]
+        n = len(ref["selected"][s])  # gamma_s, or what the batch-global greedy gave it
+        assert got["selected"][s, :n].tolist() == ref["selected"][s]
+        assert (got["selected"][s, n:] == -1).all()
     assert got["union_size"] == ref["union_size"]
     # union size of every layer, from oracle routing on all layers
     from oracle import verify_step as ovs
@@ -220,6 +222,20 @@ def test_step_small_shapes_full_compare(mv, name, layout):
     """Every workload's routing/selection structure at reduced H/I: all outputs compared."""
     from workload import CONFIGS
     cfg = CONFIGS[name].replace(**SMALL[name])
+    wl, got, ref = run_step(mv, cfg, layout=layout)
+    check_step(wl, got, ref, TOL[cfg.dtype])
+
+
+@pytest.mark.parametrize("layout", ["rowmajor", "tiled"])
+@pytest.mark.parametrize("bias", [False, True])
+def test_step_batch_global_selection(mv, layout, bias):
+    """Batch-global selection (one buffer over the batch, per-sequence depth
+    decided by the greedy) through the whole step."""
+    from workload import CONFIGS
+    kw = dict(L=2, H=512, I=256, mode=2)
+    if bias:
+        kw.update(use_bias=True, cap=8, alpha=0.25)
+    cfg = CONFIGS["batched_qwen_like"].replace(**kw)
     wl, got, ref = run_step(mv, cfg, layout=layout)
     check_step(wl, got, ref, TOL[cfg.dtype])
 

@@ -213,3 +213,64 @@ def test_eco_bad_tree_flags(mv):
     mv.eco_select(cuda(P), cuda(par), cuda(fp), 2, dev_err=dev_err)
     torch.cuda.synchronize()
     assert dev_err.item() & 0x10
+
+
+@pytest.mark.parametrize("cfgname", ["qwen3_235b_like", "batched_qwen_like", "deepseek_v3_like"])
+def test_eco_batch_global_matches_oracle(mv, cfgname):
+    from oracle import eco_select as oeco
+    from workload import CONFIGS, make_workload
+    rng = np.random.default_rng(11)
+    for seed in range(3):
+        cfg = CONFIGS[cfgname].replace(seed=200 + seed, L=min(CONFIGS[cfgname].L, 4))
+        wl = make_workload(cfg)
+        nseq, N = wl.P.shape
+        for cap in [int(wl.gamma.max()), N]:
+            gam = wl.gamma.copy()
+            par = np.tile(wl.parent, (nseq, 1)).astype(np.int32)
+            sel, usz = mv.eco_select(cuda(wl.P), cuda(par), cuda(wl.own_fp.view(np.int32)), cap,
+                                     gamma_per_seq=cuda(gam), eps=cfg.eps, mode=2)
+            rsel, rsz, _ = oeco.select_batch_global(wl.P, wl.parent, wl.own_fp, cfg.E, gam, cfg.eps, cap)
+            s_np = sel.cpu().numpy()
+            for s in range(nseq):
+                assert s_np[s, : len(rsel[s])].tolist() == rsel[s]
+                assert np.all(s_np[s, len(rsel[s]):] == -1)
+            assert usz.cpu().tolist() == rsz
+
+
+def test_eco_batch_global_random_forests(mv):
+    from oracle import eco_select as oeco
+    rng = np.random.default_rng(12)
+    for nseq, N, W, cap in [(4, 14, 8, 6), (8, 30, 4, 10), (16, 60, 2, 20), (2, 500, 16, 40)]:
+        parent = np.array([-1 if t < 2 else int(rng.integers(0, t)) for t in range(N)], dtype=np.int32)
+        P = np.zeros((nseq, N), dtype=np.float32)
+        for s in range(nseq):
+            for t in range(N):
+                base = np.float32(1) if parent[t] < 0 else P[s, parent[t]]
+                P[s, t] = np.float32(base * np.float32(rng.uniform(0.05, 1.0)))
+        fp = rng.integers(0, 2 ** 32, size=(nseq, N, W), dtype=np.uint64).astype(np.uint32)
+        fp &= rng.integers(0, 2 ** 32, size=(nseq, N, W), dtype=np.uint64).astype(np.uint32)
+        gam = rng.integers(0, cap + 1, size=nseq).astype(np.int32)
+        par = np.tile(parent, (nseq, 1)).astype(np.int32)
+        sel, usz = mv.eco_select(cuda(P), cuda(par), cuda(fp.view(np.int32)), cap, gamma_per_seq=cuda(gam),
+                                 eps=2.0 ** -10, mode=2)
+        rsel, rsz, _ = oeco.select_batch_global(P, parent, fp, 32 * W, gam, 2.0 ** -10, cap)
+        s_np = sel.cpu().numpy()
+        for s in range(nseq):
+            assert s_np[s, : len(rsel[s])].tolist() == rsel[s]
+        assert usz.cpu().tolist() == rsz
+
+
+def test_eco_batch_global_hand_example(mv):
+    # the oracle pin's batch: the greedy gives sequence A nothing and B two nodes
+    E = 16
+    parent = np.array([[-1, 0], [-1, 0]], dtype=np.int32)
+    P = np.array([[0.9, 0.8], [0.6, 0.5]], dtype=np.float32)
+    fp = np.zeros((2, 2, 1), dtype=np.uint32)
+    for t, bits in enumerate([[1, 2, 3], [4, 5]]):
+        for b in bits:
+            fp[0, t, 0] |= np.uint32(1 << b)
+    fp[1, 0, 0] = np.uint32(1 << 6)
+    fp[1, 1, 0] = np.uint32(1 << 7)
+    sel, usz = mv.eco_select(cuda(P), cuda(parent), cuda(fp.view(np.int32)), 2,
+                             gamma_per_seq=cuda(np.array([1, 1], dtype=np.int32)), eps=2.0 ** -10, mode=2)
+    assert sel.cpu().tolist() == [[-1, -1], [0, 1]] and usz.cpu().tolist() == [0, 2]

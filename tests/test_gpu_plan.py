@@ -38,7 +38,8 @@ def check_against_oracle(wl, plan):
     sels, sizes = vs.run_selection(wl)
     sel = plan.selected.cpu().numpy()
     for s in range(cfg.nseq):
-        assert sel[s, : wl.gamma[s]].tolist() == sels[s]
+        assert sel[s, : len(sels[s])].tolist() == sels[s]
+        assert (sel[s, len(sels[s]):] == -1).all()
     assert plan.union_size.cpu().tolist() == sizes
     rows = vs.verify_rows(wl.parent.shape[0], sels)
     conf = vs.token_conf(wl.P, sels)
@@ -68,7 +69,9 @@ def check_against_oracle(wl, plan):
 SMALL = [dict(name="plan_bf16"), dict(name="plan_bias", use_bias=True, cap=8, alpha=0.25),
          dict(name="plan_batched", nseq=4, ragged=True, tau=0.1),
          dict(name="plan_batched_bias", nseq=4, ragged=True, tau=0.1, use_bias=True, cap=6, alpha=0.5),
-         dict(name="plan_static", mode=1)]
+         dict(name="plan_static", mode=1),
+         dict(name="plan_batch_global", nseq=4, ragged=True, tau=0.1, mode=2),
+         dict(name="plan_batch_global_bias", nseq=3, mode=2, use_bias=True, cap=6, alpha=0.5)]
 
 
 @pytest.mark.parametrize("kw", SMALL, ids=[d["name"] for d in SMALL])
