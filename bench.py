@@ -210,13 +210,19 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
     from workload import device as wdev
 
     pts = []
-    for mode in (0, 1):
+    # 0 marginal, 1 static, 2 batch-global (batches only), 3 confidence only:
+    # the marginal greedy with empty predicted footprints takes the top-gamma
+    # nodes by path probability, the selection of a confidence-driven drafter.
+    modes = (0, 1, 2, 3) if cfg.nseq > 1 else (0, 1, 3)
+    for mode in modes:
         for g in (0, 1, 2, 3, 4, 6, 8):
-            c2 = cfg.replace(gamma=g, mode=mode, ragged=False)
+            c2 = cfg.replace(gamma=g, mode=0 if mode == 3 else mode, ragged=False)
             wl2 = gen.make_workload(c2)
             t2 = wdev.workload_tensors(wl2, dev)
+            if mode == 3:
+                t2["own_fp"].zero_()
             spec = mv.StepSpec(L=c2.L, nseq=c2.nseq, N=wl2.parent.shape[0], W=c2.W, E=c2.E, k=c2.k, H=c2.H,
-                               I=c2.I, dtype=c2.dtype, T=wl2.T, gamma_max=int(wl2.gamma.max()), mode=mode,
+                               I=c2.I, dtype=c2.dtype, T=wl2.T, gamma_max=int(wl2.gamma.max()), mode=c2.mode,
                                eps=c2.eps, use_bias=c2.use_bias, cap=c2.cap, alpha=c2.alpha, layout=layout)
             step = mv.VerifyStep(spec, layers, dev)
 
@@ -233,7 +239,8 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
                 one()
             e1.record(stream)
             torch.cuda.synchronize()
-            pts.append({"gamma": g, "mode": "marginal" if mode == 0 else "static", "tokens": int(wl2.T),
+            pts.append({"gamma": g, "mode": ["marginal", "static", "batch_global", "confidence"][mode],
+                        "tokens": int(wl2.T),
                         "union_experts": int(step.n_unique.sum().item()),
                         "ms": e0.elapsed_time(e1) / steps})
             del step
