@@ -244,6 +244,34 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
                         "union_experts": int(step.n_unique.sum().item()),
                         "ms": e0.elapsed_time(e1) / steps})
             del step
+    # Predictor mismatch: marginal selection at gamma = 4 from footprints of
+    # an imperfect predictor (top-K accuracy a), verified against the true
+    # routing; the union is what the step actually loads.
+    mism = []
+    for acc in (1.0, 0.93, 0.82, 0.5):
+        c2 = cfg.replace(gamma=4, mode=0, ragged=False)
+        wl2 = gen.make_workload(c2)
+        t2 = wdev.workload_tensors(wl2, dev)
+        if acc < 1.0:
+            t2["own_fp"] = torch.from_numpy(gen.perturbed_footprints(wl2, acc).view(np.int32).copy()).to(dev)
+        spec = mv.StepSpec(L=c2.L, nseq=c2.nseq, N=wl2.parent.shape[0], W=c2.W, E=c2.E, k=c2.k, H=c2.H, I=c2.I,
+                           dtype=c2.dtype, T=wl2.T, gamma_max=int(wl2.gamma.max()), mode=0, eps=c2.eps,
+                           use_bias=c2.use_bias, cap=c2.cap, alpha=c2.alpha, layout=layout)
+        step = mv.VerifyStep(spec, layers, dev)
+        for _ in range(3):
+            step(t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"], t2["x"])
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step(t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"], t2["x"])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mism.append({"topk_accuracy": acc, "union_experts": int(step.n_unique.sum().item()),
+                     "ms": e0.elapsed_time(e1) / steps})
+        del step
+
     x = np.array([p["union_experts"] for p in pts], dtype=np.float64)
     y = np.array([p["ms"] for p in pts], dtype=np.float64) * 1e3  # us
     A = np.stack([np.ones_like(x), x], axis=1)
@@ -251,7 +279,8 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
     pred = a + b * x
     r2 = 1.0 - float(np.sum((y - pred) ** 2) / np.sum((y - y.mean()) ** 2))
     mape = float(np.mean(np.abs(pred - y) / y))
-    model = {"points": pts, "T_exp_us": float(b), "intercept_us": float(a), "r2": r2, "mape": mape,
+    model = {"points": pts, "predictor_mismatch": mism, "T_exp_us": float(b), "intercept_us": float(a),
+             "r2": r2, "mape": mape,
              "fit": "step_us = intercept + T_exp * (sum over layers of unique experts)"}
 
     # S2-MoE expansion on the workload's own trees with the calibrated cost.

@@ -67,3 +67,24 @@ def test_expert_slice_regeneration():
     full = ch.fill_host(gen.weight_kind(cfg), keys["gate_up"], 0, cfg.E * 2 * cfg.I * cfg.H)
     full = full.reshape(cfg.E, 2 * cfg.I, cfg.H)
     assert np.array_equal(full[3], w3["gate_up"])
+
+
+def test_perturbed_footprints_accuracy_and_shape():
+    import numpy as np
+    from workload import gen
+    cfg = gen.small_case("perturb", L=3, E=32, k=4, seed=4)
+    wl = gen.make_workload(cfg)
+    assert np.array_equal(gen.perturbed_footprints(wl, 1.0), wl.own_fp)
+    for acc in (0.93, 0.82, 0.5, 0.0):
+        fp = gen.perturbed_footprints(wl, acc, seed=1)
+        kept = tot = 0
+        for s in range(wl.P.shape[0]):
+            for t in range(wl.P.shape[1]):
+                for l in range(cfg.L):
+                    lo, hi = l * cfg.E, (l + 1) * cfg.E
+                    pred = {b - lo for b in range(lo, hi) if (fp[s, t, b // 32] >> (b % 32)) & 1}
+                    true = {b - lo for b in range(lo, hi) if (wl.own_fp[s, t, b // 32] >> (b % 32)) & 1}
+                    assert len(pred) == cfg.k  # still k distinct experts per layer
+                    kept += len(pred & true)
+                    tot += cfg.k
+        assert abs(kept / tot - acc) < 0.08

@@ -284,6 +284,32 @@ def make_workload(cfg: MoEConfig) -> Workload:
                     logits=logits, x=x, weight_seed=cfg.seed)
 
 
+def perturbed_footprints(wl: Workload, accuracy: float, seed: int = 0) -> np.ndarray:
+    """Predicted footprints of an imperfect expert predictor: each of a node's
+    k predicted experts per layer is kept with probability ``accuracy``, else
+    replaced by a uniformly drawn expert outside the node's true top-k (so the
+    top-K accuracy, the share of predicted experts that are real, is
+    ``accuracy`` in expectation).  Input construction for the mismatch study;
+    the true routing (the logits) is unchanged."""
+    cfg = wl.cfg
+    L, E, k = cfg.L, cfg.E, cfg.k
+    nseq, N = wl.P.shape
+    rng = np.random.default_rng([cfg.seed, 0xF00D, seed, int(round(accuracy * 1e6))])
+    out = np.zeros_like(wl.own_fp)
+    for s in range(nseq):
+        for t in range(N):
+            for l in range(L):
+                top = np.argsort(-wl.logits[l, s, t + 1], kind="stable")[:k]
+                others = np.setdiff1d(np.arange(E), top)
+                keep = rng.random(k) < accuracy
+                repl = rng.choice(others, size=int((~keep).sum()), replace=False)
+                pred = np.concatenate([top[keep], repl])
+                for e in pred:
+                    bit = l * E + int(e)
+                    out[s, t, bit // 32] |= np.uint32(1 << (bit % 32))
+    return out
+
+
 def small_case(name: str = "small_bf16", **kw) -> MoEConfig:
     """Shapes the oracle finishes in seconds that still span several 128-row
     tiles and a ragged tail; used by the parity tests."""
