@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-residency", action="store_true", help="skip the expert-residency measurement")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of the workload (recorded in config)")
     ap.add_argument("--experts", type=int, default=0,
@@ -304,6 +305,137 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
     return model, expansion
 
 
+def host_mem_available():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def residency_measure(mv, cfg, layers, layout, dev, stream, n_layers=2, steps=10):
+    """Expert-level residency (S2-MoE write-up, system implementation): the
+    first n_layers layers of the workload with every expert in page-locked
+    Grace memory and a profiled hot list resident in HBM; each step stages
+    its union's cold experts over NVLink-C2C (moe_stage_experts inside the
+    step).  Hot lists come from the routing counts of a calibration workload
+    (another seed), not the timed one.  Reported per hot fraction: step time,
+    staging time and bytes, the staging kernel's link rate; plus the copy
+    engine's host->device rate over the same link and the cold-expert cost
+    fitted from the step times."""
+    import torch
+    from workload import gen
+    from workload import device as wdev
+
+    c2 = cfg.replace(L=min(n_layers, cfg.L))
+    ebytes = None
+    host = None
+    need = c2.L * c2.E * expert_bytes(c2)
+    if host_mem_available() < 2 * need:
+        return {"skipped": f"needs {2 * need / 2**30:.1f} GiB of free host memory"}
+    host = mv.HostExperts(layers[:c2.L])
+    ebytes = host.gate_up_bytes + host.down_bytes
+
+    # Copy-engine reference over the same link: one 1 GiB pinned -> device copy.
+    src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    best = None
+    for _ in range(5):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        dst.copy_(src, non_blocking=True)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ms = a0.elapsed_time(a1)
+        best = ms if best is None else min(best, ms)
+    ce_gbs = (1 << 30) / (best / 1e3) / 1e9
+    del src, dst
+
+    # Offline profiling: routing counts of a calibration workload.
+    cal = cfg.replace(L=c2.L, seed=cfg.seed + 1000)
+    wl_cal = gen.make_workload(cal)
+    t_cal = wdev.workload_tensors(wl_cal, dev)
+    spec_cal = mv.StepSpec(L=cal.L, nseq=cal.nseq, N=wl_cal.parent.shape[0], W=cal.W, E=cal.E, k=cal.k,
+                           H=cal.H, I=cal.I, dtype=cal.dtype, T=wl_cal.T, gamma_max=int(wl_cal.gamma.max()),
+                           mode=cal.mode, eps=cal.eps, use_bias=cal.use_bias, cap=cal.cap, alpha=cal.alpha,
+                           layout=layout)
+    plan_cal = mv.VerifyPlan(spec_cal, dev)
+    plan_cal(t_cal["P"], t_cal["parent"], t_cal["own_fp"], t_cal["gamma"], t_cal["logits"])
+    torch.cuda.synchronize()
+    counts = []
+    for l in range(cal.L):
+        ids = plan_cal.ids[l].reshape(-1).long()
+        counts.append(torch.bincount(ids[ids >= 0], minlength=cal.E).cpu())
+
+    wl2 = gen.make_workload(c2)
+    t2 = wdev.workload_tensors(wl2, dev)
+    spec = mv.StepSpec(L=c2.L, nseq=c2.nseq, N=wl2.parent.shape[0], W=c2.W, E=c2.E, k=c2.k, H=c2.H, I=c2.I,
+                       dtype=c2.dtype, T=wl2.T, gamma_max=int(wl2.gamma.max()), mode=c2.mode, eps=c2.eps,
+                       use_bias=c2.use_bias, cap=c2.cap, alpha=c2.alpha, layout=layout)
+    plan = mv.VerifyPlan(spec, dev)
+    plan(t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"])
+    torch.cuda.synchronize()
+    n_unique = plan.n_unique.cpu()
+    unique = [plan.unique[l][:int(n_unique[l])].cpu() for l in range(c2.L)]
+    args = (t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"], t2["x"])
+
+    def timed(step):
+        for _ in range(3):
+            step(*args)
+        torch.cuda.synchronize()
+        if int(step.dev_err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(step.dev_err.item())}")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step(*args)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mv.profile_begin(max_launches=steps * c2.L + 16, classes=["stage_experts"])
+        for _ in range(steps):
+            step(*args)
+        torch.cuda.synchronize()
+        st = mv.profile_end()["stage_experts"]
+        return e0.elapsed_time(e1) / steps, st["ms"] / steps
+
+    base = mv.VerifyStep(spec, layers[:c2.L], dev)
+    resident_ms, _ = timed(base)
+    y_ref = base.y.clone()
+    del base
+    cap_union = min(c2.E, wl2.T * c2.k)
+    pts = []
+    for frac in (1.0, 0.75, 0.5, 0.25, 0.0):
+        n_hot = int(round(frac * c2.E))
+        hot = [mv.hot_from_counts(counts[l], n_hot) for l in range(c2.L)]
+        pool = mv.ExpertPool(host, hot, n_stage=min(c2.E - n_hot, cap_union), device=dev)
+        step = mv.VerifyStep(spec, pool.layers, dev)
+        ms, stage_ms = timed(step)
+        same = bool(torch.equal(step.y, y_ref))
+        cold = sum(int((pool.home_slot[l].cpu()[unique[l].long()] == -1).sum()) for l in range(c2.L))
+        pts.append({"hot_frac": frac, "n_hot": n_hot, "n_stage": pool.n_stage,
+                    "device_gb": pool.n_slots * ebytes / 1e9, "cold_experts_per_step": cold,
+                    "staged_gb_per_step": cold * ebytes / 1e9, "ms_per_step": ms,
+                    "stage_ms_per_step": stage_ms,
+                    "stage_gbs": (cold * ebytes / 1e9) / (stage_ms / 1e3) if cold and stage_ms > 0 else None,
+                    "output_equals_resident": same})
+        del step, pool
+        torch.cuda.empty_cache()
+    x = np.array([p["cold_experts_per_step"] for p in pts], dtype=np.float64)
+    y = np.array([p["ms_per_step"] for p in pts], dtype=np.float64) * 1e3
+    A = np.stack([np.ones_like(x), x], axis=1)
+    (a, b), *_ = np.linalg.lstsq(A, y, rcond=None)
+    pred = a + b * x
+    r2 = 1.0 - float(np.sum((y - pred) ** 2) / max(np.sum((y - y.mean()) ** 2), 1e-30))
+    return {"layers": c2.L, "expert_mb": ebytes / 1e6, "union_experts": [int(v) for v in n_unique],
+            "resident_ms_per_step": resident_ms, "copy_engine_h2d_gbs": ce_gbs, "points": pts,
+            "T_cold_us": float(b), "intercept_us": float(a), "r2": r2,
+            "fit": "step_us = intercept + T_cold * (cold experts staged per step)",
+            "T_cold_us_at_copy_engine_rate": ebytes / (ce_gbs * 1e9) * 1e6,
+            "hot_list": "per layer, the most routed experts of a calibration workload (seed + 1000)"}
+
+
 def router_measure(mv, cfg, wl, dev, stream, iters=200):
     """Gate logits of the step's verify tokens (T x H activations against one
     layer's E x H gate), timed with CUDA events over back-to-back launches that
@@ -461,6 +593,11 @@ def ours(args, rank, ws, local):
     # ---- router logits, timed alone (the step routes the given node logits).
     router = router_measure(mv, cfg, wl, dev, stream)
 
+    # ---- expert residency with on-demand staging from Grace memory (rank 0 only).
+    residency = None
+    if rank == 0 and not args.layers and not args.experts and not args.no_residency:
+        residency = residency_measure(mv, cfg, layers, layout, dev, stream)
+
     # ---- roofline of the dominant kernel (FFN gate/up), from pass B.
     gu_bytes = sum(n_unique) * gate_up_bytes(cfg) * args.steps
     gu_ms = gu["ms"]
@@ -550,6 +687,7 @@ def ours(args, rank, ws, local):
         "router_logits": router,
         "cost_model": cost_model,
         "s2_expand": expansion,
+        "residency": residency,
     }
     return result, wl, cfg
 

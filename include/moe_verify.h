@@ -10,6 +10,7 @@
  *   moe_verify_ffn     grouped SwiGLU expert FFN over the union + weighted combine
  *   moe_verify_step    all of the above for L layers in one call
  *   moe_verify_plan    the step's selection and per-layer routing/union only
+ *   moe_stage_experts  copies a layer's cold experts of the union from host memory
  *   s2_expand          S2-MoE utility-driven draft expansion
  *
  * Conventions shared by every entry point
@@ -62,6 +63,9 @@ enum {
 #define MOE_DEV_BAD_PROB  0x10  /* a path probability / confidence weight is NaN or negative    */
 #define MOE_DEV_TIMEOUT   0x20  /* a bounded device-side wait gave up                            */
 #define MOE_DEV_CAPACITY  0x40  /* a count exceeded the capacity the caller sized buffers for   */
+/* With an expert pool, an expert whose slot_of entry is outside [0, n_slots)
+ * is reported by the FFN as MOE_DEV_BAD_ID; its weights are not read and the
+ * outputs of the tokens routed to it are not valid. */
 
 /* Weight storage types. */
 enum {
@@ -188,8 +192,54 @@ int moe_union_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E,
  *
  * Pointers must be 16-byte aligned.  Limits: H and I multiples of 64
  * (of 128 for FP8), E <= 1024.
+ *
+ * Expert residency (optional, `pool` != NULL): w_gate_up / w_down then hold
+ * pool->n_slots expert slots in the layout above (slot s where expert s
+ * would be) instead of all E experts, and expert e of the union is read from
+ * slot pool->slot_of[e].  FP8 block scales stay indexed by expert id (all E
+ * experts, resident).  See moe_stage_experts.
  */
 enum { MOE_LAYOUT_ROWMAJOR = 0, MOE_LAYOUT_TILED = 1 };
+
+/*
+ * moe_expert_pool -- expert-level residency of one layer on a Grace-Blackwell
+ * node: hot experts live in HBM, cold ones in the Grace (host) memory and are
+ * copied over NVLink-C2C into HBM staging slots when a step's union needs
+ * them.
+ *
+ * Defined by: S2-MoE write-up, "system implementation: expert-level
+ * offloading in llama.cpp" (non-expert parameters and frequently activated
+ * experts stay in device memory; any other expert is fetched on demand, from
+ * host memory on a platform with separate CPU and GPU memory; the hot list
+ * comes from offline profiling of activation frequencies).  The write-up
+ * gives no algorithm for the fetch; this library's reading: the union of the
+ * layer (known only on the device) decides, a kernel copies the cold experts
+ * of the union into staging slots, in union order, without a host round trip.
+ *
+ *   n_slots       expert slots in the layer's device buffers (1..65536).
+ *   stage_first, n_stage
+ *                 slots stage_first .. stage_first+n_stage-1 are staging
+ *                 slots (n_stage may be 0).  Several layers may point at the
+ *                 same buffers and share one staging range: every layer's
+ *                 staging starts after the previous layer's FFN finished.
+ *   home_slot     device [E] int32: the slot holding resident expert e
+ *                 (in [0, n_slots), outside the staging range), or -1 for
+ *                 a cold expert.
+ *   host_gate_up, host_down
+ *                 all E experts in the layer's layout (the sizes of an
+ *                 un-pooled layer), in page-locked host memory the device
+ *                 can address (cudaHostAlloc / cudaHostRegister), 16-byte
+ *                 aligned.  May be NULL when n_stage is 0.
+ *   slot_of       device [E] int32: written by moe_stage_experts for the
+ *                 experts of the union; read by the FFN for the same experts.
+ */
+typedef struct {
+  int32_t n_slots, stage_first, n_stage;
+  const int32_t* home_slot;
+  const void* host_gate_up;
+  const void* host_down;
+  int32_t* slot_of;
+} moe_expert_pool;
 
 typedef struct {
   int32_t H, I, E, dtype, layout;
@@ -197,6 +247,7 @@ typedef struct {
   const void* w_down;
   const float* scales_gate_up;
   const float* scales_down;
+  const moe_expert_pool* pool;  /* HOST pointer, read during the call only; NULL: all E resident */
 } moe_layer_weights;
 
 /* Bytes of the tiled copies of one layer's bf16 or FP8 weights (gate/up and down,
@@ -204,12 +255,40 @@ typedef struct {
  * or 0 if the layer cannot be tiled. */
 size_t moe_tiled_bytes(const moe_layer_weights* lw, size_t* gate_up_bytes, size_t* down_bytes);
 
-/* Packs one layer's row-major bf16 or FP8 weights (src->layout must be ROWMAJOR)
+/* Packs one layer's row-major bf16 or FP8 weights (src->layout must be ROWMAJOR, src->pool NULL)
  * into the MOE_LAYOUT_TILED layout at dst_gate_up / dst_down (caller-owned
  * device buffers of the sizes moe_tiled_bytes reports, 16-byte aligned, not
  * overlapping src).  FP8 scales are not copied: the tiled layer points at
  * the same scale tensors.  A load-time step; enqueued on `stream`. */
 int moe_pack_tiled(const moe_layer_weights* src, void* dst_gate_up, void* dst_down, void* stream);
+
+/* Bytes of one expert's gate/up and down weights in the layer's layout
+ * (the size of one pool slot); returns their sum, 0 for an invalid layer. */
+size_t moe_expert_bytes(const moe_layer_weights* lw, size_t* gate_up_bytes, size_t* down_bytes);
+
+/*
+ * moe_stage_experts -- makes every expert of a layer's union available in
+ * the layer's device pool (lw->pool must be set).
+ *
+ * For u < *n_unique, expert e = unique[u]: if home_slot[e] >= 0 then
+ * slot_of[e] = home_slot[e]; otherwise e is the c-th cold expert of the
+ * union (c counted in union order from 0), slot_of[e] = stage_first + c, and its
+ * gate/up and down weights are copied from host_gate_up / host_down into
+ * that slot of w_gate_up / w_down.  The copy reads host memory with plain
+ * 16-byte loads over NVLink-C2C (no bulk-tensor copies touch host memory)
+ * and runs on the device: the host never sees the union.  Call it after the
+ * union is written and before moe_verify_ffn on the same stream;
+ * moe_verify_step does so itself for every layer that has a pool.
+ *
+ *   n_unique, unique   as written by moe_union_permute (device).
+ *   n_staged           device int32 out, optional: cold experts copied.
+ * Device errors: MOE_DEV_CAPACITY (more cold experts than staging slots:
+ * the excess are not copied and their slot_of is -1, so the FFN flags them),
+ * MOE_DEV_BAD_ID (an id outside [0, E), or a home slot that is neither -1
+ * nor a slot outside the staging range: that expert's slot_of is -1).
+ */
+int moe_stage_experts(const moe_layer_weights* lw, const int32_t* n_unique, const int32_t* unique,
+                      int32_t* n_staged, int32_t* dev_err, void* stream);
 
 /* Bytes of workspace moe_verify_ffn needs for T tokens with top-k routing. */
 size_t moe_verify_ffn_workspace(const moe_layer_weights* lw, int32_t T, int32_t k);
@@ -429,10 +508,10 @@ int moe_verify_plan(const moe_step_cfg* cfg, const float* P, const int32_t* pare
  * synchronises those events (host blocking) and writes, per kernel class, the
  * summed milliseconds and the launch count.  Classes: 0 eco_select, 1 route,
  * 2 union/permute, 3 FFN prep, 4 FFN gate/up, 5 FFN down, 6 combine,
- * 7 router logits, 8 S2-MoE expansion.
+ * 7 router logits, 8 S2-MoE expansion, 9 expert staging.
  * Not for use under stream capture.
  */
-enum { MOE_PROF_CLASSES = 9 };
+enum { MOE_PROF_CLASSES = 10 };
 int moe_profile_begin(int32_t max_launches, int32_t class_mask);
 int moe_profile_end(float* ms_per_class, int32_t* launches_per_class, int32_t n_classes);
 

@@ -1,14 +1,15 @@
 """GB300-native MoE speculative-verify hot path (router, reuse bias, expert
-union, grouped SwiGLU expert FFN, EcoSpec draft selection).
+union, grouped SwiGLU expert FFN, EcoSpec draft selection, S2-MoE expansion,
+expert residency with on-demand staging from host memory).
 
 The computation lives in ``libmoeverify.so`` (hand-written CUDA for sm_103a,
 C ABI in ``include/moe_verify.h``); this package only marshals arguments.
 Importing it loads the library and raises if it has not been built.
 """
 from . import _lib
-from .api import (ExpertLayer, MoEError, StepSpec, VerifyPlan, VerifyStep, eco_select, ffn_workspace_bytes,  # noqa: F401
-                  launch_count, new_dev_err, pack_tiled, profile_begin, profile_end, route, router_logits, s2_expand,
-                  step_workspace_bytes,
-                  union_permute, verify_ffn)
+from .api import (ExpertLayer, ExpertPool, MoEError, StepSpec, VerifyPlan, VerifyStep, eco_select,  # noqa: F401
+                  expert_bytes, ffn_workspace_bytes, hot_from_counts, HostExperts, launch_count, new_dev_err, pack_tiled,
+                  profile_begin, profile_end, route, router_logits, s2_expand, stage_experts,
+                  step_workspace_bytes, union_permute, verify_ffn)
 
 _lib.load()

@@ -16,11 +16,12 @@ DEV_NAN_LOGIT, DEV_BAD_ID, DEV_DUP_ID, DEV_BAD_TREE, DEV_BAD_PROB, DEV_TIMEOUT, 
 DTYPE_F32, DTYPE_BF16, DTYPE_E4M3_B128 = 0, 1, 2
 LAYOUT_ROWMAJOR, LAYOUT_TILED = 0, 1
 PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up", "ffn_down",
-                "combine", "router_logits", "s2_expand"]
+                "combine", "router_logits", "s2_expand", "stage_experts"]
 
 EXPORTED = ["s2_expand", "moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
             "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_verify_plan", "moe_profile_begin",
-            "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version"]
+            "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version", "moe_expert_bytes",
+            "moe_stage_experts"]
 
 
 class S2Cfg(C.Structure):
@@ -38,10 +39,17 @@ class RouteCfg(C.Structure):
                 ("cap", C.c_int32), ("alpha", C.c_float)]
 
 
+class ExpertPool(C.Structure):
+    _fields_ = [("n_slots", C.c_int32), ("stage_first", C.c_int32), ("n_stage", C.c_int32),
+                ("home_slot", C.c_void_p), ("host_gate_up", C.c_void_p), ("host_down", C.c_void_p),
+                ("slot_of", C.c_void_p)]
+
+
 class LayerWeights(C.Structure):
     _fields_ = [("H", C.c_int32), ("I", C.c_int32), ("E", C.c_int32), ("dtype", C.c_int32),
                 ("layout", C.c_int32), ("w_gate_up", C.c_void_p), ("w_down", C.c_void_p),
-                ("scales_gate_up", C.c_void_p), ("scales_down", C.c_void_p)]
+                ("scales_gate_up", C.c_void_p), ("scales_down", C.c_void_p),
+                ("pool", C.POINTER(ExpertPool))]
 
 
 class EcoCfg(C.Structure):
@@ -84,6 +92,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_tiled_bytes.restype = sz
     lib.moe_pack_tiled.argtypes = [P(LayerWeights), vp, vp, vp]
     lib.moe_pack_tiled.restype = C.c_int
+    lib.moe_expert_bytes.argtypes = [P(LayerWeights), P(sz), P(sz)]
+    lib.moe_expert_bytes.restype = sz
+    lib.moe_stage_experts.argtypes = [P(LayerWeights), vp, vp, vp, vp, vp]
+    lib.moe_stage_experts.restype = C.c_int
     lib.moe_verify_ffn_workspace.argtypes = [P(LayerWeights), i32, i32]
     lib.moe_verify_ffn_workspace.restype = sz
     lib.moe_verify_ffn.argtypes = [vp, i32, i32, P(LayerWeights), vp, vp, vp, vp, vp, vp, vp, vp,

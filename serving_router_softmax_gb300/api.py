@@ -75,6 +75,7 @@ class ExpertLayer:
     scales_down: Optional[torch.Tensor] = None
     layout: str = "rowmajor"
     dims: Optional[tuple] = None
+    pool: Optional[L.ExpertPool] = None  # expert residency (see ExpertPool); None: all E experts resident
 
     @property
     def E(self):
@@ -91,7 +92,125 @@ class ExpertLayer:
     def struct(self) -> L.LayerWeights:
         return L.LayerWeights(self.H, self.I, self.E, DTYPES[self.dtype], LAYOUTS[self.layout],
                               _ptr(self.gate_up), _ptr(self.down), _ptr(self.scales_gate_up),
-                              _ptr(self.scales_down))
+                              _ptr(self.scales_down), C.pointer(self.pool) if self.pool is not None else None)
+
+
+def expert_bytes(layer: ExpertLayer):
+    """(gate/up, down) bytes of one expert of the layer in its layout (one pool slot)."""
+    gu, dn = C.c_size_t(0), C.c_size_t(0)
+    st = layer.struct()
+    if L.load().moe_expert_bytes(C.byref(st), C.byref(gu), C.byref(dn)) == 0:
+        raise MoEError("invalid layer")
+    return gu.value, dn.value
+
+
+def hot_from_counts(counts: torch.Tensor, n_hot: int) -> List[int]:
+    """Hot list from profiled activation counts [E]: the n_hot largest counts, equal counts to the
+    lower expert id; returned in ascending id order."""
+    E = counts.numel()
+    if not 0 <= n_hot <= E:
+        raise MoEError("n_hot outside [0, E]")
+    order = torch.sort(-counts.to(torch.int64).cpu(), stable=True).indices[:n_hot]
+    return sorted(int(e) for e in order)
+
+
+class HostExperts:
+    """All E experts of every layer of a stack in page-locked host (Grace) memory, in the layers'
+    layout (one row of ``gate_up[l]`` / ``down[l]`` per expert).  FP8 block scales stay on the
+    device (they are indexed by expert id and always resident)."""
+
+    def __init__(self, full_layers: List[ExpertLayer]):
+        if not full_layers:
+            raise MoEError("no layers")
+        ref = full_layers[0]
+        self.H, self.I, self.E, self.dtype, self.layout = ref.H, ref.I, ref.E, ref.dtype, ref.layout
+        self.gate_up_bytes, self.down_bytes = expert_bytes(ref)
+        self.scales = []
+        self.gate_up, self.down = [], []
+        for lay in full_layers:
+            if (lay.H, lay.I, lay.E, lay.dtype, lay.layout) != (self.H, self.I, self.E, self.dtype, self.layout):
+                raise MoEError("all layers share one shape")
+            if lay.pool is not None:
+                raise MoEError("expected fully resident layers")
+            for src, dst, nb in ((lay.gate_up, self.gate_up, self.gate_up_bytes),
+                                 (lay.down, self.down, self.down_bytes)):
+                h = torch.empty((self.E, nb), dtype=torch.uint8, pin_memory=True)
+                h.copy_(src.contiguous().view(torch.uint8).reshape(self.E, nb))
+                dst.append(h)
+            self.scales.append((lay.scales_gate_up, lay.scales_down))
+
+    @property
+    def L(self) -> int:
+        return len(self.gate_up)
+
+
+class ExpertPool:
+    """Expert-level residency for a stack of layers on one Grace-Blackwell GPU.
+
+    Every layer keeps all E experts in page-locked host (Grace) memory
+    (``HostExperts``).  One pair of device buffers holds, for layer l, its
+    hot experts in slots l * n_hot + j (hot[l][j], ascending ids), followed
+    by n_stage staging slots that all layers share; a layer's cold experts of
+    the union are copied there over NVLink-C2C by moe_stage_experts
+    (moe_verify_step does it for every pooled layer).  ``layers`` gives the
+    ExpertLayer views to pass to verify_ffn / VerifyStep.
+    """
+
+    def __init__(self, host, hot: Sequence[Sequence[int]], n_stage: int, device=None):
+        if not isinstance(host, HostExperts):
+            host = HostExperts(list(host))
+        if len(hot) != host.L:
+            raise MoEError("one hot list per layer required")
+        n_hot = len(hot[0])
+        if any(len(h) != n_hot for h in hot):
+            raise MoEError("every layer needs the same number of hot experts")
+        if n_stage < 0:
+            raise MoEError("n_stage < 0")
+        dev = torch.device(device) if device is not None else (
+            host.scales[0][0].device if host.scales[0][0] is not None else torch.device("cuda"))
+        self.host = host
+        self.n_hot, self.n_stage, self.L = n_hot, n_stage, host.L
+        self.n_slots = self.L * n_hot + n_stage
+        self.stage_first = self.L * n_hot
+        gu_b, dn_b = host.gate_up_bytes, host.down_bytes
+        self.gate_up_bytes, self.down_bytes = gu_b, dn_b
+        self.pool_gate_up = torch.empty((max(self.n_slots, 1), gu_b), dtype=torch.uint8, device=dev)
+        self.pool_down = torch.empty((max(self.n_slots, 1), dn_b), dtype=torch.uint8, device=dev)
+        self.host_gate_up, self.host_down = host.gate_up, host.down
+        self.home_slot, self.slot_of = [], []
+        self.layers: List[ExpertLayer] = []
+        for l, hl in enumerate(hot):
+            hl = sorted(int(e) for e in hl)
+            if len(set(hl)) != len(hl) or any(e < 0 or e >= host.E for e in hl):
+                raise MoEError("hot list: distinct ids in [0, E)")
+            home = torch.full((host.E,), -1, dtype=torch.int32)
+            for j, e in enumerate(hl):
+                s_ = l * n_hot + j
+                home[e] = s_
+                self.pool_gate_up[s_].copy_(host.gate_up[l][e])
+                self.pool_down[s_].copy_(host.down[l][e])
+            home = home.to(dev)
+            slot_of = torch.full((host.E,), -1, dtype=torch.int32, device=dev)
+            st = L.ExpertPool(self.n_slots, self.stage_first, n_stage, home.data_ptr(),
+                              host.gate_up[l].data_ptr(), host.down[l].data_ptr(), slot_of.data_ptr())
+            self.home_slot.append(home)
+            self.slot_of.append(slot_of)
+            sgu, sdn = host.scales[l]
+            self.layers.append(ExpertLayer(self.pool_gate_up, self.pool_down, host.dtype, sgu, sdn,
+                                           layout=host.layout, dims=(host.H, host.I, host.E), pool=st))
+
+    def resident_bytes(self) -> int:
+        return self.n_slots * (self.gate_up_bytes + self.down_bytes)
+
+
+def stage_experts(layer: ExpertLayer, union: Dict[str, torch.Tensor], n_staged: Optional[torch.Tensor] = None,
+                  dev_err: Optional[torch.Tensor] = None, stream=None):
+    """Copies the union's cold experts of a pooled layer into its staging slots (moe_stage_experts)."""
+    if layer.pool is None:
+        raise MoEError("layer has no expert pool")
+    st = layer.struct()
+    _check(L.load().moe_stage_experts(C.byref(st), _ptr(union["n_unique"]), _ptr(union["unique"]),
+                                      _ptr(n_staged), _ptr(dev_err), _stream(stream)), "moe_stage_experts")
 
 
 def pack_tiled(layer: ExpertLayer, stream=None) -> ExpertLayer:

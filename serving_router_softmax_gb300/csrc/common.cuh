@@ -21,7 +21,7 @@ struct LaunchScope {
 };
 
 enum ProfClass { kProfEco = 0, kProfRoute = 1, kProfUnion = 2, kProfPrep = 3, kProfGateUp = 4,
-                 kProfDown = 5, kProfCombine = 6, kProfRouter = 7, kProfS2 = 8 };
+                 kProfDown = 5, kProfCombine = 6, kProfRouter = 7, kProfS2 = 8, kProfStage = 9 };
 
 int sm_count();
 
@@ -71,6 +71,19 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits_rn(float f) {
   return static_cast<uint16_t>(u >> 16);
 }
 
+// Expert slots held by a layer's weight buffers, and the expert -> slot table
+// (NULL when every expert sits at its own index).
+inline int weight_slots(const moe_layer_weights& lw) { return lw.pool ? lw.pool->n_slots : lw.E; }
+inline const int32_t* slot_table(const moe_layer_weights& lw) { return lw.pool ? lw.pool->slot_of : nullptr; }
+
+// Slot of expert e (a valid id) in the weight buffers, -1 if the table holds
+// a value outside [0, n_slots).
+__device__ __forceinline__ int weight_slot(const int32_t* slot_of, int n_slots, int e) {
+  if (!slot_of) return e;
+  const int s = slot_of[e];
+  return s >= 0 && s < n_slots ? s : -1;
+}
+
 // Host-side FFN internals shared by the standalone call and the whole step.
 struct FfnArgs {
   const void* x;            // [*, H] activations (fp32 or bf16 bits)
@@ -94,6 +107,12 @@ struct FfnArgs {
 size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_validate(const moe_layer_weights& lw, int T, int k);
 int ffn_launch(const FfnArgs& a);
+
+// Expert staging (layers with an expert pool).
+bool expert_bytes(const moe_layer_weights& lw, size_t* gate_up, size_t* down);
+int stage_validate(const moe_layer_weights& lw);
+int stage_launch(const moe_layer_weights& lw, const int32_t* n_unique, const int32_t* unique, int32_t* n_staged,
+                 int32_t* dev_err, cudaStream_t s, bool pdl);
 
 // Route internals (optional row map into a node table, optional confidence map).
 struct RouteArgs {

@@ -46,6 +46,17 @@ int ffn_validate(const moe_layer_weights& lw, int T, int k) {
   if ((reinterpret_cast<uintptr_t>(lw.w_gate_up) | reinterpret_cast<uintptr_t>(lw.w_down)) & 15)
     return MOE_ERR_ARG;
   if (lw.dtype == MOE_DTYPE_E4M3_B128 && (!lw.scales_gate_up || !lw.scales_down)) return MOE_ERR_ARG;
+  if (lw.pool) {
+    const moe_expert_pool& pl = *lw.pool;
+    if (pl.n_slots < 1 || pl.n_slots > 65536 || pl.stage_first < 0 || pl.n_stage < 0 ||
+        pl.stage_first > pl.n_slots - pl.n_stage || !pl.slot_of)
+      return MOE_ERR_ARG;
+    // Tile-block indices of the slots must stay within int range.
+    const long long blocks_gu = static_cast<long long>((lw.I + 127) / 128) * (lw.H / 64);
+    const long long blocks_d = static_cast<long long>((lw.H + 127) / 128) * (lw.I / 64);
+    const long long mb = blocks_gu > blocks_d ? blocks_gu : blocks_d;
+    if (pl.n_slots * mb >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  }
   return MOE_OK;
 }
 

@@ -72,10 +72,12 @@ struct Fp8Params {
   const float* w;
   float* y;
   int32_t* dev_err;
+  const int32_t* slot_of;  // expert -> weight slot (NULL: identity); block scales stay per expert id
+  int n_slots;
 };
 
 struct Tile {
-  int u, m, e, ne, np, prow, off;
+  int u, m, e, ws, ne, np, prow, off;  // ws: the expert's slot in the weight buffers
   bool ok, prow_ok;
 };
 
@@ -89,6 +91,8 @@ __device__ __forceinline__ Tile tile_info(const Fp8Params& p, int U, int t, bool
   ti.np = (ti.ne + 15) & ~15;
   ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
           ti.off + ti.ne <= p.T * p.k;
+  ti.ws = ti.ok ? weight_slot(p.slot_of, p.n_slots, ti.e) : -1;
+  ti.ok = ti.ok && ti.ws >= 0;
   ti.prow = with_prow ? p.poff[ti.u] : -1;
   ti.prow_ok = with_prow && ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
   return ti;
@@ -266,14 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * 2 * ti.np * 128;
           tc::mbar_arrive_expect_tx(&full[stage], tx);
           if (p.tiled) {
-            const int blk = (ti.e * MT + ti.m) * KB + kb;
+            const int blk = (ti.ws * MT + ti.m) * KB + kb;
             if (kGateUp || nq == 2)
               tc::tma_load_3d(sA, &tmA0, 0, 0, blk, &full[stage], polA);
             else
               tc::tma_load_3d(sA, &tmA1, 0, 0, blk, &full[stage], polA);
           } else {
-            tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
-            if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+            tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.ws, &full[stage], polA);
+            if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.ws, &full[stage], polA);
           }
           if (dep_done) {
             issue_b(t, kb, nq, stage);
@@ -853,7 +857,7 @@ int ffn_fp8_launch(const FfnArgs& a) {
   int32_t* cnt_d = cnt_gu + static_cast<size_t>(cap) * g.MT_gu;
   int32_t* done = cnt_d + static_cast<size_t>(cap) * g.MT_d;
 
-  const uint64_t H = lw.H, I = lw.I, E = lw.E;
+  const uint64_t H = lw.H, I = lw.I, E = weight_slots(lw);  // E: expert slots in the buffers
   const uint64_t KBg = H / kBK, KBd = I / kBK;
   CUtensorMap tm_g, tm_u, tm_xh, tm_xl, tm_wd, tm_wd1, tm_hh, tm_hl;
   if (lw.layout == MOE_LAYOUT_TILED) {
@@ -930,6 +934,8 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.w = a.w;
   fp.y = a.y;
   fp.dev_err = a.dev_err;
+  fp.slot_of = slot_table(lw);
+  fp.n_slots = weight_slots(lw);
 
   // gate/up
   fp.M = lw.I;

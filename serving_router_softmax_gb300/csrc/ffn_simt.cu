@@ -118,6 +118,7 @@ template <int DT>
 __global__ void __launch_bounds__(256) gateup_simt_kernel(
     const void* __restrict__ x, const int32_t* __restrict__ x_rows, int x_rows_limit, int T, int k,
     int H, int I, int E, const void* __restrict__ wgu, const float* __restrict__ sgu,
+    const int32_t* __restrict__ slot_of, int n_slots,
     const int32_t* __restrict__ n_unique, const int32_t* __restrict__ unique,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_token, void* __restrict__ h,
     int32_t* dev_err) {
@@ -137,11 +138,12 @@ __global__ void __launch_bounds__(256) gateup_simt_kernel(
     const int i = static_cast<int>(it - (long long)u * I);
     const int e = unique[u];
     const int o0 = offsets[u], o1 = offsets[u + 1];
-    if (e < 0 || e >= E || o0 < 0 || o1 > TK || o0 > o1) {
+    const int ws = e >= 0 && e < E ? weight_slot(slot_of, n_slots, e) : -1;
+    if (ws < 0 || o0 < 0 || o1 > TK || o0 > o1) {
       if (lane == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
       continue;
     }
-    const char* grow = reinterpret_cast<const char*>(wgu) + ((size_t)e * 2 * I + i) * H * EB;
+    const char* grow = reinterpret_cast<const char*>(wgu) + ((size_t)ws * 2 * I + i) * H * EB;
     const char* urow = grow + (size_t)I * H * EB;
     for (int c0 = o0; c0 < o1; c0 += kTokChunk) {
       const int nt = min(kTokChunk, o1 - c0);
@@ -210,6 +212,7 @@ __global__ void __launch_bounds__(256) gateup_simt_kernel(
 template <int DT>
 __global__ void __launch_bounds__(256) down_simt_kernel(
     int T, int k, int H, int I, int E, const void* __restrict__ wd, const float* __restrict__ sd,
+    const int32_t* __restrict__ slot_of, int n_slots,
     const int32_t* __restrict__ n_unique, const int32_t* __restrict__ unique,
     const int32_t* __restrict__ offsets, const void* __restrict__ h, float* __restrict__ o,
     int32_t* dev_err) {
@@ -231,11 +234,12 @@ __global__ void __launch_bounds__(256) down_simt_kernel(
     const int r = static_cast<int>(it - (long long)u * H);
     const int e = unique[u];
     const int o0 = offsets[u], o1 = offsets[u + 1];
-    if (e < 0 || e >= E || o0 < 0 || o1 > TK || o0 > o1) {
+    const int ws = e >= 0 && e < E ? weight_slot(slot_of, n_slots, e) : -1;
+    if (ws < 0 || o0 < 0 || o1 > TK || o0 > o1) {
       if (lane == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
       continue;
     }
-    const char* row = reinterpret_cast<const char*>(wd) + ((size_t)e * H + r) * I * EB;
+    const char* row = reinterpret_cast<const char*>(wd) + ((size_t)ws * H + r) * I * EB;
     for (int c0 = o0; c0 < o1; c0 += kTokChunk) {
       const int nt = min(kTokChunk, o1 - c0);
       float acc[kTokChunk];
@@ -343,6 +347,7 @@ int ffn_simt_launch(const FfnArgs& a, const FfnWorkspace& ws) {
       LaunchScope ls(kProfGateUp, s);                                                                 \
       gateup_simt_kernel<DT><<<blocks, 256, 0, s>>>(a.x, a.x_rows, a.x_rows_limit, a.T, a.k, lw.H,     \
                                                     lw.I, lw.E, lw.w_gate_up, lw.scales_gate_up,      \
+                                                    slot_table(lw), weight_slots(lw),                 \
                                                     a.n_unique, a.unique, a.offsets, a.perm_token,    \
                                                     ws.h, a.dev_err);                                 \
     }                                                                                                 \
@@ -350,7 +355,8 @@ int ffn_simt_launch(const FfnArgs& a, const FfnWorkspace& ws) {
     {                                                                                                 \
       LaunchScope ls(kProfDown, s);                                                                   \
       down_simt_kernel<DT><<<blocks, 256, 0, s>>>(a.T, a.k, lw.H, lw.I, lw.E, lw.w_down,              \
-                                                  lw.scales_down, a.n_unique, a.unique, a.offsets,    \
+                                                  lw.scales_down, slot_table(lw), weight_slots(lw),   \
+                                                  a.n_unique, a.unique, a.offsets,                    \
                                                   ws.h, ws.o, a.dev_err);                             \
     }                                                                                                 \
     if (check_launch() != MOE_OK) return MOE_ERR_CUDA;                                                \

@@ -74,10 +74,12 @@ struct TcParams {
   const float* w;
   float* y;          // [T][M] (down)
   int32_t* dev_err;
+  const int32_t* slot_of;  // expert -> weight slot (NULL: identity)
+  int n_slots;
 };
 
 struct Tile {
-  int u, m, e, ne, np, prow, off;
+  int u, m, e, ws, ne, np, prow, off;  // ws: the expert's slot in the weight buffers
   bool ok, prow_ok;
 };
 
@@ -96,6 +98,8 @@ __device__ __forceinline__ Tile tile_info(const TcParams& p, int U, int t) {
   ti.prow = p.poff[ti.u];
   ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
           ti.off + ti.ne <= p.T * p.k;
+  ti.ws = ti.ok ? weight_slot(p.slot_of, p.n_slots, ti.e) : -1;
+  ti.ok = ti.ok && ti.ws >= 0;
   ti.prow_ok = ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
   return ti;
 }
@@ -113,6 +117,8 @@ __device__ __forceinline__ Tile tile_core(const TcParams& p, int U, int t) {
   ti.prow = -1;
   ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
           ti.off + ti.ne <= p.T * p.k;
+  ti.ws = ti.ok ? weight_slot(p.slot_of, p.n_slots, ti.e) : -1;
+  ti.ok = ti.ok && ti.ws >= 0;
   ti.prow_ok = false;
   return ti;
 }
@@ -194,9 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // Under programmatic dependent launch the weights of the first S stages
-    // are requested before the previous kernel has finished (they depend only
-    // on the expert union, complete by then); their token operand follows
-    // once griddepcontrol.wait returns.
+    // are requested before the previous kernel has finished.  They depend
+    // only on the expert union, its slot table and staged weights, all written
+    // before the prep kernel's own griddepcontrol.wait returned (prep starts
+    // this grid only after that wait); their token operand follows once
+    // griddepcontrol.wait returns here.
     if (tc::elect_one()) {
       const uint64_t polA = tc::policy_evict_first();
       const uint64_t polB = tc::policy_evict_last();
@@ -246,14 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Tile-packed weights: block (e, m, kb) is contiguous.  gate/up:
             // one 256-row box holds the gate tile then the up tile; down: one
             // box of nq consecutive 16 KB k-blocks.
-            const int blk = (ti.e * MT + ti.m) * KB + kb;
+            const int blk = (ti.ws * MT + ti.m) * KB + kb;
             if (kGateUp || nq == 2)
               tc::tma_load_3d(sA, &tmA0, 0, 0, blk, &full[stage], polA);
             else
               tc::tma_load_3d(sA, &tmA1, 0, 0, blk, &full[stage], polA);
           } else {
-            tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
-            if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.e, &full[stage], polA);
+            tc::tma_load_3d(sA, &tmA0, kb * kBK, ti.m * kBM, ti.ws, &full[stage], polA);
+            if (kGateUp) tc::tma_load_3d(sA + kABytes, &tmA1, kb * kBK, ti.m * kBM, ti.ws, &full[stage], polA);
           }
           if (dep_done) {
             issue_b(t, kb, nq, stage);
@@ -694,7 +702,7 @@ int ffn_tc_launch(const FfnArgs& a) {
 
   // Tensor maps (host-side encoding only; nothing is enqueued).
   CUtensorMap tm_g, tm_u, tm_x, tm_wd, tm_wd1, tm_h;
-  const uint64_t H = lw.H, I = lw.I, E = lw.E;
+  const uint64_t H = lw.H, I = lw.I, E = weight_slots(lw);  // E: expert slots in the buffers
   const uint64_t KBg = H / kBK, KBd = I / kBK;
   if (lw.layout == MOE_LAYOUT_TILED) {
     {
@@ -765,6 +773,8 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.w = a.w;
   tp.y = a.y;
   tp.dev_err = a.dev_err;
+  tp.slot_of = slot_table(lw);
+  tp.n_slots = weight_slots(lw);
   tp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
   tp.pdl = 1;
 

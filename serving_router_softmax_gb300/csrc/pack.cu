@@ -87,7 +87,7 @@ extern "C" size_t moe_tiled_bytes(const moe_layer_weights* lw, size_t* gate_up_b
 
 extern "C" int moe_pack_tiled(const moe_layer_weights* src, void* dst_gate_up, void* dst_down, void* stream) {
   using namespace moe;
-  if (!src || src->layout != MOE_LAYOUT_ROWMAJOR) return MOE_ERR_ARG;
+  if (!src || src->layout != MOE_LAYOUT_ROWMAJOR || src->pool) return MOE_ERR_ARG;
   size_t gu = 0, dn = 0;
   if (!tiled_sizes(*src, &gu, &dn)) return MOE_ERR_UNSUPPORTED;
   if (!src->w_gate_up || !src->w_down || !dst_gate_up || !dst_down) return MOE_ERR_ARG;

@@ -127,4 +127,4 @@ extern "C" const char* moe_status_str(int status) {
 
 extern "C" uint64_t moe_launch_count(void) { return moe::g_launches.load(); }
 
-extern "C" int moe_version(void) { return 100; }
+extern "C" int moe_version(void) { return 101; }

@@ -115,6 +115,7 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     if (lw.H != c.H || lw.I != c.I || lw.E != c.E || lw.dtype != c.dtype || lw.layout != c.layout)
       return MOE_ERR_ARG;
     if ((st = ffn_validate(lw, c.T, c.k)) != MOE_OK) return st;
+    if (lw.pool && (st = stage_validate(lw)) != MOE_OK) return st;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StepWs ws;
@@ -134,6 +135,12 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     // head follows directly; later heads may read them before their wait.
     if ((st = layer_head_launch(ra, n_unique + l, ws.unique, ws.offsets, ws.perm_token, ws.perm_slot, ws.inv,
                                 ws.ratio, true, l > 0)) != MOE_OK)
+      return st;
+    // Expert residency: the union's cold experts are staged into HBM before
+    // the FFN's prep kernel, whose wait then covers the copies (the FFN's
+    // weight loads may start right after prep's wait).
+    if (layers[l].pool &&
+        (st = stage_launch(layers[l], n_unique + l, ws.unique, nullptr, dev_err, s, true)) != MOE_OK)
       return st;
     FfnArgs fa{static_cast<const char*>(node_x) + static_cast<size_t>(l) * rows * c.H * xelem,
                ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
