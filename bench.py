@@ -42,6 +42,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-residency", action="store_true", help="skip the expert-residency measurement")
+    ap.add_argument("--residency", action="store_true",
+                    help="run the expert-residency measurement even on a --layers/--experts profiling run")
+    ap.add_argument("--residency-fracs", default="1,0.75,0.5,0.25,0",
+                    help="hot fractions of the residency sweep (comma-separated)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of the workload (recorded in config)")
     ap.add_argument("--experts", type=int, default=0,
@@ -315,7 +319,82 @@ def host_mem_available():
     return 0
 
 
-def residency_measure(mv, cfg, layers, layout, dev, stream, n_layers=2, steps=10):
+def residency_expansion(mv, cfg, layout, dev, expansion, T_cold, hot_frac=0.5):
+    """S2-MoE expansion priced for residency: every layer keeps its hot_frac
+    most routed experts (from a calibration workload) resident, a new cold
+    expert costs T_cold (measured) on top of T_exp.  Compared with the plain
+    expansion on the same trees: nodes taken, predicted union and its cold
+    part (host-side bookkeeping of the outputs)."""
+    import torch
+    from workload import gen
+    from workload import device as wdev
+
+    cal = cfg.replace(seed=cfg.seed + 1000)
+    wl_cal = gen.make_workload(cal)
+    t_cal = wdev.workload_tensors(wl_cal, dev)
+    spec_cal = mv.StepSpec(L=cal.L, nseq=cal.nseq, N=wl_cal.parent.shape[0], W=cal.W, E=cal.E, k=cal.k,
+                           H=cal.H, I=cal.I, dtype=cal.dtype, T=wl_cal.T, gamma_max=int(wl_cal.gamma.max()),
+                           mode=cal.mode, eps=cal.eps, use_bias=cal.use_bias, cap=cal.cap, alpha=cal.alpha,
+                           layout=layout)
+    plan = mv.VerifyPlan(spec_cal, dev)
+    plan(t_cal["P"], t_cal["parent"], t_cal["own_fp"], t_cal["gamma"], t_cal["logits"])
+    torch.cuda.synchronize()
+    n_hot = int(round(hot_frac * cfg.E))
+    cold_bits = np.zeros(cfg.W, dtype=np.uint32)
+    for l in range(cfg.L):
+        ids = plan.ids[l].reshape(-1).long()
+        hot = set(mv.hot_from_counts(torch.bincount(ids[ids >= 0], minlength=cfg.E).cpu(), n_hot))
+        for e in range(cfg.E):
+            if e not in hot:
+                b = l * cfg.E + e
+                cold_bits[b // 32] |= np.uint32(1 << (b % 32))
+    wl = gen.make_workload(cfg)
+    t = wdev.workload_tensors(wl, dev)
+    cold_t = torch.from_numpy(cold_bits.view(np.int32).copy()).to(dev)
+
+    def is_cold(l, e):
+        b = l * cfg.E + e
+        return bool((int(cold_bits[b // 32]) >> (b % 32)) & 1)
+
+    # T_AR under the same residency: the measured all-resident step with no
+    # draft token plus T_cold for every cold expert the root tokens route to.
+    c0 = cfg.replace(gamma=0, ragged=False)
+    wl0 = gen.make_workload(c0)
+    t0 = wdev.workload_tensors(wl0, dev)
+    spec0 = mv.StepSpec(L=c0.L, nseq=c0.nseq, N=wl0.parent.shape[0], W=c0.W, E=c0.E, k=c0.k, H=c0.H, I=c0.I,
+                        dtype=c0.dtype, T=wl0.T, gamma_max=0, mode=c0.mode, eps=c0.eps, use_bias=c0.use_bias,
+                        cap=c0.cap, alpha=c0.alpha, layout=layout)
+    plan0 = mv.VerifyPlan(spec0, dev)
+    plan0(t0["P"], t0["parent"], t0["own_fp"], t0["gamma"], t0["logits"])
+    torch.cuda.synchronize()
+    nu0 = plan0.n_unique.cpu().tolist()
+    root_cold = sum(is_cold(l, int(e)) for l in range(cfg.L) for e in plan0.unique[l][:nu0[l]].cpu().tolist())
+    T_AR = expansion["T_AR_us"] + T_cold * root_cold
+    out = {"hot_frac": hot_frac, "T_cold_us": T_cold, "T_exp_us": expansion["T_exp_us"],
+           "T_AR_resident_us": expansion["T_AR_us"], "root_cold_experts": root_cold, "T_AR_us": T_AR,
+           "T_AR": "all-resident step with no draft token + T_cold * cold experts of the root tokens"}
+    for name, kw in (("plain", {}), ("residency_aware", {"T_cold": T_cold, "cold_fp": cold_t})):
+        sel, n_sel, _ = mv.s2_expand(t["P"], t["parent"], t["own_fp"], T_AR, expansion["T_exp_us"], 0.0, **kw)
+        sel, n_sel = sel.cpu().numpy(), n_sel.cpu().tolist()
+        unions, colds = [], []
+        for s_ in range(cfg.nseq):
+            u = np.zeros(cfg.W, dtype=np.uint32)
+            for node in sel[s_, :n_sel[s_]]:
+                u |= wl.own_fp[s_][node]
+            unions.append(int(sum(bin(int(w)).count("1") for w in u)))
+            colds.append(int(sum(bin(int(w)).count("1") for w in (u & cold_bits))))
+        gains = [float(sum(np.float64(wl.P[s_][node]) for node in sel[s_, :n_sel[s_]])) * T_AR
+                 for s_ in range(cfg.nseq)]
+        out[name] = {"selected_per_seq": n_sel, "predicted_union_experts": unions,
+                     "predicted_cold_experts": colds,
+                     "predicted_gain_us": gains,
+                     "predicted_cost_us": [unions[i] * expansion["T_exp_us"] + colds[i] * T_cold
+                                           for i in range(cfg.nseq)]}
+    return out
+
+
+def residency_measure(mv, cfg, layers, layout, dev, stream, expansion=None, n_layers=2, steps=10,
+                      fracs=(1.0, 0.75, 0.5, 0.25, 0.0)):
     """Expert-level residency (S2-MoE write-up, system implementation): the
     first n_layers layers of the workload with every expert in page-locked
     Grace memory and a profiled hot list resident in HBM; each step stages
@@ -330,8 +409,6 @@ def residency_measure(mv, cfg, layers, layout, dev, stream, n_layers=2, steps=10
     from workload import device as wdev
 
     c2 = cfg.replace(L=min(n_layers, cfg.L))
-    ebytes = None
-    host = None
     need = c2.L * c2.E * expert_bytes(c2)
     if host_mem_available() < 2 * need:
         return {"skipped": f"needs {2 * need / 2**30:.1f} GiB of free host memory"}
@@ -406,7 +483,7 @@ def residency_measure(mv, cfg, layers, layout, dev, stream, n_layers=2, steps=10
     del base
     cap_union = min(c2.E, wl2.T * c2.k)
     pts = []
-    for frac in (1.0, 0.75, 0.5, 0.25, 0.0):
+    for frac in fracs:
         n_hot = int(round(frac * c2.E))
         hot = [mv.hot_from_counts(counts[l], n_hot) for l in range(c2.L)]
         pool = mv.ExpertPool(host, hot, n_stage=min(c2.E - n_hot, cap_union), device=dev)
@@ -422,18 +499,21 @@ def residency_measure(mv, cfg, layers, layout, dev, stream, n_layers=2, steps=10
                     "output_equals_resident": same})
         del step, pool
         torch.cuda.empty_cache()
-    x = np.array([p["cold_experts_per_step"] for p in pts], dtype=np.float64)
-    y = np.array([p["ms_per_step"] for p in pts], dtype=np.float64) * 1e3
+    x = np.array([0.0] + [p["cold_experts_per_step"] for p in pts], dtype=np.float64)
+    y = np.array([resident_ms] + [p["ms_per_step"] for p in pts], dtype=np.float64) * 1e3
     A = np.stack([np.ones_like(x), x], axis=1)
     (a, b), *_ = np.linalg.lstsq(A, y, rcond=None)
     pred = a + b * x
     r2 = 1.0 - float(np.sum((y - pred) ** 2) / max(np.sum((y - y.mean()) ** 2), 1e-30))
-    return {"layers": c2.L, "expert_mb": ebytes / 1e6, "union_experts": [int(v) for v in n_unique],
-            "resident_ms_per_step": resident_ms, "copy_engine_h2d_gbs": ce_gbs, "points": pts,
-            "T_cold_us": float(b), "intercept_us": float(a), "r2": r2,
-            "fit": "step_us = intercept + T_cold * (cold experts staged per step)",
-            "T_cold_us_at_copy_engine_rate": ebytes / (ce_gbs * 1e9) * 1e6,
-            "hot_list": "per layer, the most routed experts of a calibration workload (seed + 1000)"}
+    res = {"layers": c2.L, "expert_mb": ebytes / 1e6, "union_experts": [int(v) for v in n_unique],
+           "resident_ms_per_step": resident_ms, "copy_engine_h2d_gbs": ce_gbs, "points": pts,
+           "T_cold_us": float(b), "intercept_us": float(a), "r2": r2,
+           "fit": "step_us = intercept + T_cold * (cold experts staged per step)",
+           "T_cold_us_at_copy_engine_rate": ebytes / (ce_gbs * 1e9) * 1e6,
+           "hot_list": "per layer, the most routed experts of a calibration workload (seed + 1000)"}
+    if expansion is not None:
+        res["s2_expand"] = residency_expansion(mv, cfg, layout, dev, expansion, float(b))
+    return res
 
 
 def router_measure(mv, cfg, wl, dev, stream, iters=200):
@@ -595,8 +675,9 @@ def ours(args, rank, ws, local):
 
     # ---- expert residency with on-demand staging from Grace memory (rank 0 only).
     residency = None
-    if rank == 0 and not args.layers and not args.experts and not args.no_residency:
-        residency = residency_measure(mv, cfg, layers, layout, dev, stream)
+    if rank == 0 and not args.no_residency and (args.residency or (not args.layers and not args.experts)):
+        fracs = tuple(float(v) for v in args.residency_fracs.split(","))
+        residency = residency_measure(mv, cfg, layers, layout, dev, stream, expansion, fracs=fracs)
 
     # ---- roofline of the dominant kernel (FFN gate/up), from pass B.
     gu_bytes = sum(n_unique) * gate_up_bytes(cfg) * args.steps

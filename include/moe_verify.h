@@ -443,14 +443,23 @@ int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* pare
  * root's children always are), so the selection is prefix-closed; the
  * selected set does not depend on the order candidates are examined in (it
  * is the least fixed point of a monotone rule); U_i >= 1 is evaluated as
- * p_i * T_AR >= n_new * T_exp + C_draft in fp64 with that operation order.
+ * p_i * T_AR >= n_new * T_exp + C_draft in fp64 with that operation order
+ * (with the cold-expert term below when cold_fp is given).
  *
  *   P          [nseq, N] fp32 path probability of each draft node (p_i).
  *   parent     [nseq, N] int32, breadth-first order: -1 or an index < t.
  *   own_fp     [nseq, N, W] uint32: node's own predicted footprint, bit
  *              l*E + e for expert e of layer l.
- *   cfg        N, W and the cost model T_AR, T_exp, C_draft (finite, >= 0,
- *              any consistent time unit).
+ *   cfg        N, W and the cost model T_AR, T_exp, C_draft, T_cold
+ *              (finite, >= 0, any consistent time unit).
+ *   cfg->cold_fp  optional DEVICE [W] uint32 mask of the experts that are
+ *              not resident (bit l*E + e; see moe_expert_pool), or NULL.
+ *              The write-up calibrates the expert cost from the expert's
+ *              bytes and the bandwidth it is moved at; with expert residency
+ *              a cold expert is moved twice (host link, then HBM), so each
+ *              new expert that is also cold adds T_cold:
+ *              cost = (n_new * T_exp + n_new_cold * T_cold) + C_draft, in
+ *              fp64 in that order.  NULL (or T_cold = 0) gives the plain rule.
  *   selected   [nseq, N] int32 out: selected node indices in ascending
  *              order, then -1.
  *   n_selected [nseq] int32 out; union_size [nseq] int32 out: bits set in
@@ -460,7 +469,8 @@ int moe_verify_step(const moe_step_cfg* cfg, const float* P, const int32_t* pare
  */
 typedef struct {
   int32_t N, W;
-  float T_AR, T_exp, C_draft;
+  float T_AR, T_exp, C_draft, T_cold;
+  const uint32_t* cold_fp;
 } s2_cfg;
 
 int s2_expand(const float* P, const int32_t* parent, const uint32_t* own_fp, int32_t nseq,

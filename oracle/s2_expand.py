@@ -29,6 +29,12 @@ Readings where the page is silent (the CUDA path applies the same ones):
   (utility +inf: the node is taken).
 * A NaN or negative P, or a parent outside [-1, t), is an error: nothing is
   selected.
+* Expert residency (the write-up's system implementation offloads experts
+  and calibrates the expert cost from the expert's bytes and the bandwidth
+  it is moved at): with a set of non-resident (cold) experts, every new
+  expert that is also cold adds T_cold, the time to bring it over the host
+  link: cost = (n_new * T_exp + n_new_cold * T_cold) + C_draft, in fp64 in
+  that order.  No cold set, or T_cold = 0, gives the plain rule.
 
 Parity: pinned (tests/test_oracle_s2.py: a hand-worked tree, the T_exp = 0
 closed form (a plain confidence threshold), order independence against a
@@ -36,7 +42,7 @@ simultaneous-update iteration, prefix closure and the union bookkeeping).
 """
 from __future__ import annotations
 
-from typing import List, Sequence, Tuple
+from typing import List, Optional, Sequence, Set, Tuple
 
 import numpy as np
 
@@ -48,8 +54,11 @@ class S2Error(ValueError):
 
 
 def s2_expand(P: Sequence[float], parent: Sequence[int], own_fp: np.ndarray, E: int, T_AR: float,
-              T_exp: float, C_draft: float) -> Tuple[List[int], int]:
-    """Selected nodes (ascending) and the size of the union of their footprints."""
+              T_exp: float, C_draft: float, T_cold: float = 0.0,
+              cold: Optional[Set[Tuple[int, int]]] = None) -> Tuple[List[int], int]:
+    """Selected nodes (ascending) and the size of the union of their footprints.
+
+    cold: the (layer, expert) pairs that are not resident (None: all resident)."""
     N = len(parent)
     for t in range(N):
         if not (-1 <= parent[t] < t):
@@ -60,6 +69,8 @@ def s2_expand(P: Sequence[float], parent: Sequence[int], own_fp: np.ndarray, E: 
     t_ar = np.float64(np.float32(T_AR))
     t_exp = np.float64(np.float32(T_exp))
     c_draft = np.float64(np.float32(C_draft))
+    t_cold = np.float64(np.float32(T_cold))
+    cold = set() if cold is None else set(cold)
     gain = [np.float64(np.float32(P[t])) * t_ar for t in range(N)]
     chosen = [False] * N
     B = set()
@@ -71,8 +82,10 @@ def s2_expand(P: Sequence[float], parent: Sequence[int], own_fp: np.ndarray, E: 
                 continue
             if parent[i] >= 0 and not chosen[parent[i]]:
                 continue
-            n_new = len(own[i] - B)
-            cost = np.float64(n_new) * t_exp + c_draft
+            new = own[i] - B
+            n_new = len(new)
+            n_cold = len(new & cold)
+            cost = (np.float64(n_new) * t_exp + np.float64(n_cold) * t_cold) + c_draft
             if gain[i] >= cost:
                 chosen[i] = True
                 B |= own[i]
@@ -81,11 +94,12 @@ def s2_expand(P: Sequence[float], parent: Sequence[int], own_fp: np.ndarray, E: 
 
 
 def s2_expand_batch(P: np.ndarray, parent: Sequence[int], own_fp: np.ndarray, E: int, T_AR: float,
-                    T_exp: float, C_draft: float):
+                    T_exp: float, C_draft: float, T_cold: float = 0.0,
+                    cold: Optional[Set[Tuple[int, int]]] = None):
     """Independent expansion per sequence: P [nseq, N], own_fp [nseq, N, W]."""
     sels, sizes = [], []
     for s in range(P.shape[0]):
-        sel, size = s2_expand(P[s], parent, own_fp[s], E, T_AR, T_exp, C_draft)
+        sel, size = s2_expand(P[s], parent, own_fp[s], E, T_AR, T_exp, C_draft, T_cold, cold)
         sels.append(sel)
         sizes.append(size)
     return sels, sizes

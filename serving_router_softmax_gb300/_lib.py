@@ -26,7 +26,7 @@ EXPORTED = ["s2_expand", "moe_router_logits", "moe_route", "moe_union_permute", 
 
 class S2Cfg(C.Structure):
     _fields_ = [("N", C.c_int32), ("W", C.c_int32), ("T_AR", C.c_float), ("T_exp", C.c_float),
-                ("C_draft", C.c_float)]
+                ("C_draft", C.c_float), ("T_cold", C.c_float), ("cold_fp", C.c_void_p)]
 
 
 class RouterCfg(C.Structure):

@@ -467,9 +467,12 @@ class VerifyPlan:
 
 
 def s2_expand(P: torch.Tensor, parent: torch.Tensor, own_fp: torch.Tensor, T_AR: float, T_exp: float,
-              C_draft: float = 0.0, dev_err: Optional[torch.Tensor] = None, stream=None):
+              C_draft: float = 0.0, dev_err: Optional[torch.Tensor] = None, stream=None,
+              T_cold: float = 0.0, cold_fp: Optional[torch.Tensor] = None):
     """S2-MoE utility expansion per sequence: (selected [nseq, N] ascending
-    then -1, n_selected [nseq], union_size [nseq])."""
+    then -1, n_selected [nseq], union_size [nseq]).  ``cold_fp`` [W] int32
+    marks non-resident experts (bit l*E + e); each new cold expert costs
+    T_cold on top of T_exp."""
     lib = L.load()
     nseq, N = P.shape
     W = own_fp.shape[-1]
@@ -480,7 +483,9 @@ def s2_expand(P: torch.Tensor, parent: torch.Tensor, own_fp: torch.Tensor, T_AR:
     selected = torch.empty((nseq, N), dtype=torch.int32, device=dev)
     n_sel = torch.empty(nseq, dtype=torch.int32, device=dev)
     usize = torch.empty(nseq, dtype=torch.int32, device=dev)
-    cfg = L.S2Cfg(N, W, T_AR, T_exp, C_draft)
+    if cold_fp is not None:
+        _need(cold_fp, torch.int32, (W,), "cold_fp")
+    cfg = L.S2Cfg(N, W, T_AR, T_exp, C_draft, T_cold, _ptr(cold_fp))
     _check(lib.s2_expand(_ptr(P), _ptr(parent), _ptr(own_fp), nseq, C.byref(cfg), _ptr(selected), _ptr(n_sel),
                          _ptr(usize), _ptr(dev_err), _stream(stream)), "s2_expand")
     return selected, n_sel, usize

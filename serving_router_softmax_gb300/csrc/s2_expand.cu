@@ -16,6 +16,11 @@
 // U_i >= 1 is evaluated as p_i * T_AR >= n_new * T_exp + C_draft in fp64 with
 // that operation order (both products exact, the addition rounded once).
 //
+// Expert residency: the write-up prices an expert by its bytes over the
+// bandwidth it is moved at.  With a mask of non-resident experts, a new expert
+// that is also cold costs T_cold more (it crosses the host link before HBM):
+// cost = (n_new * T_exp + n_new_cold * T_cold) + C_draft.
+//
 // One CTA per sequence; footprints live in shared memory as bitsets.
 #include <cmath>
 
@@ -30,12 +35,14 @@ constexpr int kS2MaxNW = 40960;  // N*W words of footprint bitsets (160 KB)
 
 __global__ void __launch_bounds__(512) s2_kernel(const float* __restrict__ P, const int32_t* __restrict__ parent,
                                                  const uint32_t* __restrict__ own_fp, int N, int W, double t_ar,
-                                                 double t_exp, double c_draft, int32_t* __restrict__ selected,
+                                                 double t_exp, double c_draft, double t_cold,
+                                                 const uint32_t* __restrict__ cold_fp, int32_t* __restrict__ selected,
                                                  int32_t* __restrict__ n_selected, int32_t* __restrict__ union_size,
                                                  int32_t* dev_err) {
   extern __shared__ uint32_t smem[];
   uint32_t* fp = smem;               // [N][W] own footprints
   uint32_t* B = fp + (size_t)N * W;  // [W] union of the selected footprints
+  uint32_t* cold = B + W;            // [W] non-resident experts (when cold_fp is given)
   __shared__ uint8_t chosen[kS2MaxN];
   __shared__ uint8_t take[kS2MaxN];
   __shared__ int16_t par_s[kS2MaxN];
@@ -59,7 +66,10 @@ __global__ void __launch_bounds__(512) s2_kernel(const float* __restrict__ P, co
     chosen[t] = 0;
   }
   for (int i = threadIdx.x; i < N * W; i += blockDim.x) fp[i] = own[i];
-  for (int w = threadIdx.x; w < W; w += blockDim.x) B[w] = 0;
+  for (int w = threadIdx.x; w < W; w += blockDim.x) {
+    B[w] = 0;
+    cold[w] = cold_fp ? cold_fp[w] : 0u;
+  }
   __syncthreads();
   if (bad) {
     if (threadIdx.x == 0) {
@@ -76,18 +86,27 @@ __global__ void __launch_bounds__(512) s2_kernel(const float* __restrict__ P, co
   for (int round = 0; round <= N; ++round) {
     for (int t = warp; t < N; t += nwarps) {
       const bool cand = !chosen[t] && (par_s[t] < 0 || chosen[par_s[t]]);
-      int c = 0;
+      int c = 0, cc = 0;
       if (cand) {
         const uint32_t* ft = fp + (size_t)t * W;
-        for (int w = lane; w < W; w += 32) c += __popc(ft[w] & ~B[w]);
+        for (int w = lane; w < W; w += 32) {
+          const uint32_t nw = ft[w] & ~B[w];
+          c += __popc(nw);
+          cc += __popc(nw & cold[w]);
+        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+        for (int off = 16; off > 0; off >>= 1) {
+          c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+          cc += __shfl_xor_sync(0xFFFFFFFFu, cc, off);
+        }
       }
       if (lane == 0) {
         bool tk = false;
         if (cand) {
           const double gain = __dmul_rn(static_cast<double>(Ps[t]), t_ar);
-          const double cost = __dadd_rn(__dmul_rn(static_cast<double>(c), t_exp), c_draft);
+          const double moved = __dadd_rn(__dmul_rn(static_cast<double>(c), t_exp),
+                                         __dmul_rn(static_cast<double>(cc), t_cold));
+          const double cost = __dadd_rn(moved, c_draft);
           tk = gain >= cost;
         }
         take[t] = tk ? 1 : 0;
@@ -144,12 +163,12 @@ extern "C" int s2_expand(const float* P, const int32_t* parent, const uint32_t* 
   if (c.N < 1 || c.N > kS2MaxN || c.W < 1 || c.W > kS2MaxW ||
       static_cast<long long>(c.N) * c.W > kS2MaxNW)
     return MOE_ERR_UNSUPPORTED;
-  if (!std::isfinite(c.T_AR) || !std::isfinite(c.T_exp) || !std::isfinite(c.C_draft) || c.T_AR < 0.f ||
-      c.T_exp < 0.f || c.C_draft < 0.f)
+  if (!std::isfinite(c.T_AR) || !std::isfinite(c.T_exp) || !std::isfinite(c.C_draft) || !std::isfinite(c.T_cold) ||
+      c.T_AR < 0.f || c.T_exp < 0.f || c.C_draft < 0.f || c.T_cold < 0.f)
     return MOE_ERR_ARG;
   if (nseq == 0) return MOE_OK;
   if (!P || !parent || !own_fp || !selected || !n_selected || !union_size) return MOE_ERR_ARG;
-  const size_t smem = (static_cast<size_t>(c.N) * c.W + c.W) * sizeof(uint32_t);
+  const size_t smem = (static_cast<size_t>(c.N) * c.W + 2 * static_cast<size_t>(c.W)) * sizeof(uint32_t);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(s2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
           cudaSuccess)
@@ -158,7 +177,8 @@ extern "C" int s2_expand(const float* P, const int32_t* parent, const uint32_t* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LaunchScope ls(kProfS2, s);
   s2_kernel<<<nseq, threads, smem, s>>>(P, parent, own_fp, c.N, c.W, static_cast<double>(c.T_AR),
-                                        static_cast<double>(c.T_exp), static_cast<double>(c.C_draft), selected,
-                                        n_selected, union_size, dev_err);
+                                        static_cast<double>(c.T_exp), static_cast<double>(c.C_draft),
+                                        static_cast<double>(c.T_cold), c.cold_fp, selected, n_selected, union_size,
+                                        dev_err);
   return check_launch();
 }

@@ -15,19 +15,24 @@ def mv():
     return m
 
 
-def run(mv, P, parent, own_fp, T_AR, T_exp, C, dev_err=None):
+def run(mv, P, parent, own_fp, T_AR, T_exp, C, dev_err=None, T_cold=0.0, cold_bits=None):
     Pt = torch.from_numpy(np.ascontiguousarray(P, dtype=np.float32)).cuda()
     par = torch.from_numpy(np.ascontiguousarray(np.tile(parent, (P.shape[0], 1)), dtype=np.int32)).cuda()
     fp = torch.from_numpy(np.ascontiguousarray(own_fp).view(np.int32)).cuda()
-    sel, n, u = mv.s2_expand(Pt, par, fp, T_AR, T_exp, C, dev_err=dev_err)
+    cold = None
+    if cold_bits is not None:
+        cold = torch.from_numpy(np.ascontiguousarray(cold_bits, dtype=np.uint32).view(np.int32)).cuda()
+    sel, n, u = mv.s2_expand(Pt, par, fp, T_AR, T_exp, C, dev_err=dev_err, T_cold=T_cold, cold_fp=cold)
     torch.cuda.synchronize()
     return sel.cpu().numpy(), n.cpu().tolist(), u.cpu().tolist()
 
 
-def check(mv, P, parent, own_fp, E, T_AR, T_exp, C):
+def check(mv, P, parent, own_fp, E, T_AR, T_exp, C, T_cold=0.0, cold_bits=None):
     from oracle import s2_expand as s2
-    sel, n, u = run(mv, P, parent, own_fp, T_AR, T_exp, C)
-    want, sizes = s2.s2_expand_batch(P, parent, own_fp, E, T_AR, T_exp, C)
+    from oracle.eco_select import footprint_set
+    sel, n, u = run(mv, P, parent, own_fp, T_AR, T_exp, C, T_cold=T_cold, cold_bits=cold_bits)
+    cold = None if cold_bits is None else footprint_set(cold_bits, E)
+    want, sizes = s2.s2_expand_batch(P, parent, own_fp, E, T_AR, T_exp, C, T_cold, cold)
     for s in range(P.shape[0]):
         assert n[s] == len(want[s])
         assert sel[s, : n[s]].tolist() == want[s]
@@ -104,3 +109,41 @@ def test_s2_errors(mv):
     with pytest.raises(mv.MoEError):
         run(mv, np.array([[0.5]], dtype=np.float32), np.array([-1]), np.zeros((1, 1, 1), np.uint32), 1.0,
             float("inf"), 0.0)
+
+
+def test_s2_hand_example_cold(mv):
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "s2_expand_hand.json")))
+    fp = np.zeros((1, len(g["own"]), 1), dtype=np.uint32)
+    for t, s in enumerate(g["own"]):
+        for b in s:
+            fp[0, t, 0] |= np.uint32(1 << b)
+    P = np.array([g["P"]], dtype=np.float32)
+    cc, c2 = g["cold_cases"], g["second_case"]
+    cold = np.zeros(1, dtype=np.uint32)
+    for b in cc["cold"]:
+        cold[0] |= np.uint32(1 << b)
+    for case in cc["cases"]:
+        sel, n, u = run(mv, P, np.array(g["parent"]), fp, g["T_AR"], c2["T_exp"], c2["C_draft"],
+                        T_cold=case["T_cold"], cold_bits=cold)
+        assert sel[0, : n[0]].tolist() == case["selected"] and u[0] == case["union_size"]
+
+
+@pytest.mark.parametrize("name", ["qwen3_235b_like", "deepseek_v3_like", "batched_qwen_like"])
+def test_s2_workload_trees_with_cold_experts(mv, name):
+    """Residency-aware expansion: a hot list per layer (the most frequent experts of the
+    workload's own footprints), every other expert cold at a surcharge T_cold."""
+    from workload import CONFIGS, gen
+    cfg = CONFIGS[name]
+    wl = gen.make_workload(cfg)
+    rng = np.random.default_rng(11 + len(name))
+    for frac in (0.0, 0.25, 0.5, 0.9):
+        cold = (rng.random(cfg.L * cfg.E) >= frac)
+        bits = np.zeros(cfg.W, dtype=np.uint32)
+        for b in np.nonzero(cold)[0]:
+            bits[b // 32] |= np.uint32(1 << (b % 32))
+        for T_AR, T_exp, C, T_cold in [(200.0, 1.0, 0.5, 30.0), (2000.0, 1.0, 0.0, 30.0),
+                                       (float(rng.uniform(10, 5000)), float(rng.uniform(0, 4)),
+                                        float(rng.uniform(0, 4)), float(rng.uniform(0, 100)))]:
+            check(mv, wl.P, wl.parent, wl.own_fp, cfg.E, T_AR, T_exp, C, T_cold=T_cold, cold_bits=bits)

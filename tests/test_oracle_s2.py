@@ -136,3 +136,82 @@ def test_utility_exactly_one_is_taken():
     assert sel == [0] and size == 2
     sel, _ = s2.s2_expand([0.5], [-1], fp, 8, 4.0, 0.5, 1.0 + 2.0 ** -20)
     assert sel == []
+
+
+# ---------------------------------------------------------------- cold experts (residency)
+def cold_set(bits, E):
+    return {(b // E, b % E) for b in bits}
+
+
+def test_hand_example_with_cold_experts():
+    g = json.load(open(os.path.join(GOLD, "s2_expand_hand.json")))
+    fp = bits_of(g["own"], 1)
+    cc = g["cold_cases"]
+    c2 = g["second_case"]
+    for case in cc["cases"]:
+        sel, size = s2.s2_expand(g["P"], g["parent"], fp, g["E"], g["T_AR"], c2["T_exp"], c2["C_draft"],
+                                 case["T_cold"], cold_set(cc["cold"], g["E"]))
+        assert sel == case["selected"] and size == case["union_size"], case["T_cold"]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_all_cold_equals_a_dearer_expert(seed):
+    # every expert cold: n_new * T_exp + n_new * T_cold == n_new * (T_exp + T_cold)
+    # exactly for dyadic costs, so the selection is the plain one at T_exp + T_cold
+    cfg, wl = random_trees(1, seed)
+    every = {(l, e) for l in range(cfg.L) for e in range(cfg.E)}
+    rng = np.random.default_rng(seed)
+    for _ in range(10):
+        T_exp = float(rng.integers(0, 32)) / 16
+        T_cold = float(rng.integers(0, 64)) / 16
+        C = float(rng.integers(0, 16)) / 16
+        T_AR = float(rng.integers(1, 200))
+        got = s2.s2_expand(wl.P[0], wl.parent, wl.own_fp[0], cfg.E, T_AR, T_exp, C, T_cold, every)
+        assert got == s2.s2_expand(wl.P[0], wl.parent, wl.own_fp[0], cfg.E, T_AR, T_exp + T_cold, C)
+        # nothing cold (or no set): the surcharge never applies
+        plain = s2.s2_expand(wl.P[0], wl.parent, wl.own_fp[0], cfg.E, T_AR, T_exp, C)
+        assert s2.s2_expand(wl.P[0], wl.parent, wl.own_fp[0], cfg.E, T_AR, T_exp, C, T_cold, set()) == plain
+        assert s2.s2_expand(wl.P[0], wl.parent, wl.own_fp[0], cfg.E, T_AR, T_exp, C, T_cold, None) == plain
+
+
+def jacobi_cold(P, parent, own, T_AR, T_exp, C, T_cold, cold):
+    N = len(parent)
+    f = lambda v: np.float64(np.float32(v))  # noqa: E731
+    gain = [f(P[t]) * f(T_AR) for t in range(N)]
+    chosen = [False] * N
+    B = set()
+    while True:
+        take = []
+        for i in range(N):
+            if chosen[i] or (parent[i] >= 0 and not chosen[parent[i]]):
+                continue
+            new = own[i] - B
+            cost = (np.float64(len(new)) * f(T_exp) + np.float64(len(new & cold)) * f(T_cold)) + f(C)
+            if gain[i] >= cost:
+                take.append(i)
+        if not take:
+            return [t for t in range(N) if chosen[t]], len(B)
+        for i in take:
+            chosen[i] = True
+            B |= own[i]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cold_order_independent_and_monotone(seed):
+    cfg, wl = random_trees(1, seed)
+    from oracle.eco_select import footprint_set
+    rng = np.random.default_rng(100 + seed)
+    own = [footprint_set(wl.own_fp[0][t], cfg.E) for t in range(len(wl.parent))]
+    for _ in range(10):
+        cold = {(l, e) for l in range(cfg.L) for e in range(cfg.E) if rng.random() < 0.5}
+        T_AR, T_exp, C = float(rng.uniform(1, 200)), float(rng.uniform(0, 3)), float(rng.uniform(0, 2))
+        prev = None
+        for T_cold in [0.0, 0.5, 1.0, 3.0, 10.0, 1e9]:
+            got = s2.s2_expand(wl.P[0], wl.parent, wl.own_fp[0], cfg.E, T_AR, T_exp, C, T_cold, cold)
+            assert got == jacobi_cold(wl.P[0], wl.parent, own, T_AR, T_exp, C, T_cold, cold)
+            if prev is not None:
+                assert set(got[0]) <= set(prev)  # a dearer cold expert never adds nodes
+            prev = got[0]
+            # selected nodes never bring a cold expert worth more than their gain alone
+            for t in got[0]:
+                assert np.float64(np.float32(wl.P[0][t])) * np.float64(np.float32(T_AR)) >= np.float64(np.float32(C))
