@@ -7,12 +7,15 @@
 // the static-cost ablation of section 4.3 (denominator |E_traj(t)|).
 //
 // Design: one CTA per sequence.  Path footprints E_traj are built once in
-// shared memory as bitsets (parent index < child index, so one breadth-first
-// pass suffices); every round each warp popcounts (E_traj(t) & ~B) for its
-// nodes, warp 0 takes the exact arg-max and all threads OR the winner into B.
-// Scores are compared by cross-multiplication in fp64, which is exact because
-// P is fp32 (24-bit significand) and c + eps = c + 2^-s has at most 29
-// significant bits (checked on the host).
+// shared memory as bitsets (parent index < child index, so one in-order pass
+// per bitset word suffices); every round each warp popcounts (E_traj(t) & ~B)
+// for its nodes, warp 0 takes the exact arg-max and all threads OR the winner
+// into B.  Scores are compared exactly by cross-multiplication in integers:
+// with eps = 2^-s, P_a / (c_a + eps) > P_b / (c_b + eps) iff
+// P_a * X_b > P_b * X_a with X = c * 2^s + 1 < 2^29 (checked on the host), and
+// P = m * 2^e with a 24-bit integer m, so each side is an integer below 2^53
+// times a power of two.  (GB300's fp64 pipe is narrow: the same comparison in
+// fp64 cost about 300 cycles per operation in the arg-max chain.)
 //
 // mode 2 (batch-global): one CTA over the forest of all sequences' trees, one
 // buffer B shared by the batch and one greedy with the budget sum(gamma_i) and
@@ -30,30 +33,90 @@ constexpr int kMaxN = 1024;
 constexpr int kMaxW = 4096;
 constexpr int kMaxNW = 40960;  // N*W words of trajectory bitsets (160 KB)
 
+// A node's score P / (c + 2^-s) as exact integers: P = m * 2^e, X = c * 2^s + 1.
+struct Score {
+  uint32_t m;  // significand of P (< 2^24)
+  int e;       // exponent of P
+  uint32_t x;  // c * 2^s + 1 (< 2^29)
+  int i;       // node index, -1 for none
+};
+
+__device__ __forceinline__ Score make_score(float p, int c, int eps_shift, int i) {
+  const uint32_t u = __float_as_uint(p);  // p >= 0 and finite (validated)
+  const uint32_t ex = (u >> 23) & 0xFFu, fr = u & 0x7FFFFFu;
+  Score sc;
+  sc.m = ex ? (fr | 0x800000u) : fr;
+  sc.e = ex ? static_cast<int>(ex) - 150 : -149;
+  sc.x = (static_cast<uint32_t>(c) << eps_shift) + 1u;
+  sc.i = i;
+  return sc;
+}
+
+// Sign of A * 2^ea - B * 2^eb for A, B < 2^54.
+__device__ __forceinline__ int cmp_pow2(uint64_t A, int ea, uint64_t B, int eb) {
+  if (A == 0 || B == 0) return static_cast<int>(A != 0) - static_cast<int>(B != 0);
+  const int la = 63 - __clzll(static_cast<long long>(A)) + ea;  // position of the leading bit
+  const int lb = 63 - __clzll(static_cast<long long>(B)) + eb;
+  if (la != lb) return la > lb ? 1 : -1;
+  // Equal leading positions: the shift keeps the shifted value at the other's bit length.
+  if (ea >= eb)
+    A <<= (ea - eb);
+  else
+    B <<= (eb - ea);
+  return A > B ? 1 : (A < B ? -1 : 0);
+}
+
 // a beats b: P_a / (c_a + eps) > P_b / (c_b + eps), ties -> lower index.
-__device__ __forceinline__ bool score_better(float pa, int ca, int ia, float pb, int cb, int ib,
-                                             double eps) {
-  double lhs = static_cast<double>(pa) * (static_cast<double>(cb) + eps);
-  double rhs = static_cast<double>(pb) * (static_cast<double>(ca) + eps);
-  return lhs > rhs || (lhs == rhs && ia < ib);
+__device__ __forceinline__ bool score_better(const Score& a, const Score& b) {
+  const int c = cmp_pow2(static_cast<uint64_t>(a.m) * b.x, a.e, static_cast<uint64_t>(b.m) * a.x, b.e);
+  return c > 0 || (c == 0 && a.i < b.i);
+}
+
+__device__ __forceinline__ Score shfl_score(const Score& a, int off) {
+  Score o;
+  o.m = __shfl_xor_sync(0xFFFFFFFFu, a.m, off);
+  o.e = __shfl_xor_sync(0xFFFFFFFFu, a.e, off);
+  o.x = __shfl_xor_sync(0xFFFFFFFFu, a.x, off);
+  o.i = __shfl_xor_sync(0xFFFFFFFFu, a.i, off);
+  return o;
+}
+
+__device__ __forceinline__ Score shfl_score_from(const Score& a, int src) {
+  Score o;
+  o.m = __shfl_sync(0xFFFFFFFFu, a.m, src);
+  o.e = __shfl_sync(0xFFFFFFFFu, a.e, src);
+  o.x = __shfl_sync(0xFFFFFFFFu, a.x, src);
+  o.i = __shfl_sync(0xFFFFFFFFu, a.i, src);
+  return o;
+}
+
+// E_traj(t) = own(t) | E_traj(parent(t)) over nodes 0..G-1 (parent < child):
+// one thread per bitset word walks the nodes in order, so every parent is
+// final before its children read it.  No barriers between tree levels.
+__device__ __forceinline__ void close_paths(uint32_t* traj, const int16_t* par, int G, int W) {
+  for (int w = threadIdx.x; w < W; w += blockDim.x) {
+    for (int g = 0; g < G; ++g) {
+      const int p = par[g];
+      if (p >= 0) traj[(size_t)g * W + w] |= traj[(size_t)p * W + w];
+    }
+  }
 }
 
 __global__ void __launch_bounds__(512) eco_kernel(
     const float* __restrict__ P, const int32_t* __restrict__ parent,
     const uint32_t* __restrict__ own_fp, const int32_t* __restrict__ gamma_per_seq, int N, int W,
-    int gamma_max, int mode, double eps, int32_t* __restrict__ selected,
+    int gamma_max, int mode, int eps_shift, int fast_key, int32_t* __restrict__ selected,
     int32_t* __restrict__ union_size, int32_t* dev_err, int32_t* __restrict__ verify_rows,
     float* __restrict__ verify_conf, int T_expected, int nseq) {
   extern __shared__ uint32_t smem[];
   uint32_t* traj = smem;                 // [N][W]
   uint32_t* B = traj + (size_t)N * W;    // [W]
   __shared__ int32_t cost[kMaxN];
-  __shared__ uint8_t chosen[kMaxN];
+  __shared__ float pf[kMaxN];     // P
+  __shared__ uint32_t pm[kMaxN];  // P = pm * 2^pe (exact split of the fp32 value)
+  __shared__ int16_t pe[kMaxN];
   __shared__ int bad;
-  __shared__ int best_s;
   __shared__ int16_t par_s[kMaxN];
-  __shared__ int16_t depth_s[kMaxN];
-  __shared__ int max_depth;
 
   pdl_trigger();  // the first layer's head may launch while selection runs
   const int s = blockIdx.x;
@@ -69,12 +132,19 @@ __global__ void __launch_bounds__(512) eco_kernel(
 
   if (threadIdx.x == 0) bad = 0;
   __syncthreads();
+  // One pass: own footprints (the trajectories' start), then validation,
+  // parents and the split of P, behind a single barrier.
+  for (int i = threadIdx.x; i < N * W; i += blockDim.x) traj[i] = own[i];
   for (int t = threadIdx.x; t < N; t += blockDim.x) {
     int p = par[t];
     if (p < -1 || p >= t) atomicOr(&bad, MOE_DEV_BAD_TREE);
     float pt = Ps[t];
     if (!(pt >= 0.f) || pt == INFINITY) atomicOr(&bad, MOE_DEV_BAD_PROB);
-    chosen[t] = 0;
+    par_s[t] = static_cast<int16_t>(p < -1 || p >= t ? -1 : p);
+    const Score sc = make_score(pt >= 0.f ? pt : 0.f, 0, 0, t);
+    pf[t] = pt;
+    pm[t] = sc.m;
+    pe[t] = static_cast<int16_t>(sc.e);
   }
   if (threadIdx.x == 0 && (gamma < 0 || gamma > gamma_max)) atomicOr(&bad, MOE_DEV_BAD_TREE);
   for (int w = threadIdx.x; w < W; w += blockDim.x) B[w] = 0;
@@ -110,72 +180,75 @@ __global__ void __launch_bounds__(512) eco_kernel(
   }
   if (gamma > N) gamma = N;
 
-  // E_traj(t) = own(t) | E_traj(parent(t)).  Own footprints come in with one
-  // coalesced pass; the ORs then run level by level (one barrier per tree
-  // level), deepest level last.
-  for (int i = threadIdx.x; i < N * W; i += blockDim.x) traj[i] = own[i];
-  for (int t = threadIdx.x; t < N; t += blockDim.x) par_s[t] = static_cast<int16_t>(par[t]);
+  close_paths(traj, par_s, N, W);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int maxd = 0;
-    for (int t = 0; t < N; ++t) {
-      const int p = par_s[t];
-      const int d = p < 0 ? 0 : depth_s[p] + 1;
-      depth_s[t] = static_cast<int16_t>(d);
-      maxd = d > maxd ? d : maxd;
-    }
-    max_depth = maxd;
-  }
-  __syncthreads();
-  for (int d = 1; d <= max_depth; ++d) {
-    for (int i = threadIdx.x; i < N * W; i += blockDim.x) {
-      const int t = i / W;
-      if (depth_s[t] == d) traj[i] |= traj[(size_t)par_s[t] * W + (i - t * W)];
-    }
-    __syncthreads();
-  }
 
+  // Rounds.  Every warp computes the same arg-max from the shared costs, so
+  // the winner needs no broadcast barrier: two barriers per round.  Lane l
+  // tracks in `taken` (bit j) whether node l + 32 j was chosen; the copies
+  // agree across warps.
+  //
+  // Arg-max: when every X = c * 2^s + 1 is below 2^24 (fast_key, checked on
+  // the host) X and P are exact fp32 values, so the correctly rounded quotient
+  // key = P / X never decreases as the exact score grows: the winner is among
+  // the nodes holding the largest key, which a single warp max finds.  Only a
+  // tie in the key needs the exact comparison.
+  uint32_t taken = 0;
   for (int r = 0; r < gamma; ++r) {
     // Costs: |E_traj(t) \ B| (marginal) or |E_traj(t)| (static).
     for (int t = warp; t < N; t += nwarps) {
+      const bool ch = (__shfl_sync(0xFFFFFFFFu, taken, t & 31) >> (t >> 5)) & 1u;
       int c = 0;
-      if (!chosen[t]) {
+      if (!ch) {
         const uint32_t* tt = traj + (size_t)t * W;
+#pragma unroll 4
         for (int w = lane; w < W; w += 32) c += __popc(mode == 0 ? (tt[w] & ~B[w]) : tt[w]);
-        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
       }
       if (lane == 0) cost[t] = c;
     }
     __syncthreads();
-    if (warp == 0) {
-      float bp = 0.f;
-      int bc = 0, bi = -1;
-      for (int t = lane; t < N; t += 32) {
-        if (chosen[t]) continue;
-        if (bi < 0 || score_better(Ps[t], cost[t], t, bp, bc, bi, eps)) {
-          bp = Ps[t];
-          bc = cost[t];
-          bi = t;
+    Score best{0u, 0, 1u, -1};
+    uint32_t best_key = 0;  // key bits + 1 (0: none); keys are >= +0.0
+    for (int t = lane, j = 0; t < N; t += 32, ++j) {
+      if ((taken >> j) & 1u) continue;
+      Score sc;
+      sc.m = pm[t];
+      sc.e = pe[t];
+      sc.x = (static_cast<uint32_t>(cost[t]) << eps_shift) + 1u;
+      sc.i = t;
+      if (fast_key) {
+        const uint32_t kb = __float_as_uint(__fdiv_rn(pf[t], static_cast<float>(sc.x))) + 1u;
+        if (kb > best_key || (kb == best_key && score_better(sc, best))) {
+          best = sc;
+          best_key = kb;
         }
-      }
-      for (int off = 16; off > 0; off >>= 1) {
-        float op = __shfl_xor_sync(0xFFFFFFFFu, bp, off);
-        int oc = __shfl_xor_sync(0xFFFFFFFFu, bc, off);
-        int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        if (oi >= 0 && (bi < 0 || score_better(op, oc, oi, bp, bc, bi, eps))) {
-          bp = op;
-          bc = oc;
-          bi = oi;
-        }
-      }
-      if (lane == 0) {
-        best_s = bi;
-        chosen[bi] = 1;
-        sel[r] = bi;
+      } else if (best.i < 0 || score_better(sc, best)) {
+        best = sc;
       }
     }
-    __syncthreads();
-    const uint32_t* tb = traj + (size_t)best_s * W;
+    if (fast_key) {
+      const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, best_key);
+      uint32_t cand = __ballot_sync(0xFFFFFFFFu, best_key == kmax && best.i >= 0);
+      Score b = shfl_score_from(best, __ffs(cand) - 1);
+      cand &= cand - 1;
+      while (cand) {  // lanes whose keys tie: exact comparison (rare)
+        const Score o = shfl_score_from(best, __ffs(cand) - 1);
+        if (score_better(o, b)) b = o;
+        cand &= cand - 1;
+      }
+      best = b;
+    } else {
+      for (int off = 16; off > 0; off >>= 1) {
+        const Score o = shfl_score(best, off);
+        if (o.i >= 0 && (best.i < 0 || score_better(o, best))) best = o;
+      }
+    }
+    const int bi = best.i;  // >= 0: gamma <= N leaves an unchosen node every round
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (threadIdx.x == 0) sel[r] = bi;
+    // B |= E_traj(best); the arg-max above reads no B, so this needs no barrier before it.
+    const uint32_t* tb = traj + (size_t)bi * W;
     for (int w = threadIdx.x; w < W; w += blockDim.x) B[w] |= tb[w];
     __syncthreads();
   }
@@ -206,7 +279,7 @@ __global__ void __launch_bounds__(512) eco_kernel(
 
 __global__ void __launch_bounds__(512) eco_batch_kernel(
     const float* __restrict__ P, const int32_t* __restrict__ parent, const uint32_t* __restrict__ own_fp,
-    const int32_t* __restrict__ gamma_per_seq, int N, int W, int nseq, int gamma_max, double eps,
+    const int32_t* __restrict__ gamma_per_seq, int N, int W, int nseq, int gamma_max, int eps_shift,
     int32_t* __restrict__ selected, int32_t* __restrict__ union_size, int32_t* dev_err,
     int32_t* __restrict__ verify_rows, float* __restrict__ verify_conf, int T_expected) {
   extern __shared__ uint32_t smem[];
@@ -216,9 +289,8 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
   __shared__ int32_t cost[kMaxN];
   __shared__ uint8_t chosen[kMaxN];
   __shared__ int16_t par_s[kMaxN];     // parent as a global node index (-1: root)
-  __shared__ int16_t depth_s[kMaxN];
   __shared__ int16_t cnt[kMaxN];       // nodes taken per sequence
-  __shared__ int bad, best_g, max_depth, budget;
+  __shared__ int bad, best_g, budget;
   pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int cap = gamma_max < N ? gamma_max : N;
@@ -231,9 +303,10 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
     if (p < -1 || p >= t) atomicOr(&bad, MOE_DEV_BAD_TREE);
     const float pt = P[g];
     if (!(pt >= 0.f) || pt == INFINITY) atomicOr(&bad, MOE_DEV_BAD_PROB);
-    par_s[g] = static_cast<int16_t>(p < 0 ? -1 : s * N + p);
+    par_s[g] = static_cast<int16_t>(p < 0 || p >= t ? -1 : s * N + p);
     chosen[g] = 0;
   }
+  for (int i = threadIdx.x; i < G * W; i += blockDim.x) traj[i] = own_fp[i];
   for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
     const int gs = gamma_per_seq ? gamma_per_seq[s] : gamma_max;
     if (gs < 0 || gs > gamma_max) atomicOr(&bad, MOE_DEV_BAD_TREE);
@@ -270,27 +343,9 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
     budget = b;
   }
 
-  // Trajectory footprints, level by level over the forest.
-  for (int i = threadIdx.x; i < G * W; i += blockDim.x) traj[i] = own_fp[i];
+  // Trajectory footprints over the forest (a parent precedes its children).
+  close_paths(traj, par_s, G, W);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int maxd = 0;
-    for (int g = 0; g < G; ++g) {
-      const int p = par_s[g];
-      const int d = p < 0 ? 0 : depth_s[p] + 1;
-      depth_s[g] = static_cast<int16_t>(d);
-      maxd = d > maxd ? d : maxd;
-    }
-    max_depth = maxd;
-  }
-  __syncthreads();
-  for (int d = 1; d <= max_depth; ++d) {
-    for (int i = threadIdx.x; i < G * W; i += blockDim.x) {
-      const int g = i / W;
-      if (depth_s[g] == d) traj[i] |= traj[(size_t)par_s[g] * W + (i - g * W)];
-    }
-    __syncthreads();
-  }
 
   for (int r = 0; r < budget; ++r) {
     for (int g = warp; g < G; g += nwarps) {
@@ -304,27 +359,18 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
     }
     __syncthreads();
     if (warp == 0) {
-      float bp = 0.f;
-      int bc = 0, bi = -1;
+      Score best{0u, 0, 1u, -1};
       for (int g = lane; g < G; g += 32) {
         if (chosen[g] || cnt[g / N] >= cap) continue;
-        if (bi < 0 || score_better(P[g], cost[g], g, bp, bc, bi, eps)) {
-          bp = P[g];
-          bc = cost[g];
-          bi = g;
-        }
+        const Score sc = make_score(P[g], cost[g], eps_shift, g);
+        if (best.i < 0 || score_better(sc, best)) best = sc;
       }
       for (int off = 16; off > 0; off >>= 1) {
-        const float op = __shfl_xor_sync(0xFFFFFFFFu, bp, off);
-        const int oc = __shfl_xor_sync(0xFFFFFFFFu, bc, off);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        if (oi >= 0 && (bi < 0 || score_better(op, oc, oi, bp, bc, bi, eps))) {
-          bp = op;
-          bc = oc;
-          bi = oi;
-        }
+        const Score o = shfl_score(best, off);
+        if (o.i >= 0 && (best.i < 0 || score_better(o, best))) best = o;
       }
       if (lane == 0) {
+        const int bi = best.i;
         best_g = bi;
         if (bi >= 0) {
           const int s = bi / N;
@@ -372,6 +418,13 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
 
 }  // namespace
 
+// s with eps == 2^-s (0 <= s <= 20), or -1.
+int eps_shift(float eps) {
+  for (int q = 0; q <= 20; ++q)
+    if (eps == static_cast<float>(1.0 / static_cast<double>(1u << q))) return q;
+  return -1;
+}
+
 int eco_validate(const eco_cfg& c, int nseq) {
   if (nseq < 0 || c.N < 1 || c.N > kMaxN || c.W < 1 || c.W > kMaxW) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(c.N) * c.W > kMaxNW) return MOE_ERR_UNSUPPORTED;
@@ -379,11 +432,9 @@ int eco_validate(const eco_cfg& c, int nseq) {
   if (c.mode == 2 && (static_cast<long long>(nseq) * c.N > kMaxN ||
                       static_cast<long long>(nseq) * c.N * c.W > kMaxNW))
     return MOE_ERR_UNSUPPORTED;
-  // eps must be 2^-s, 0 <= s <= 20, and W*32 * 2^s < 2^29 so that c + eps is
-  // exact in <= 29 bits and P * (c + eps) is exact in fp64.
-  int s = -1;
-  for (int q = 0; q <= 20; ++q)
-    if (c.eps == static_cast<float>(1.0 / static_cast<double>(1u << q))) s = q;
+  // eps must be 2^-s, 0 <= s <= 20, and W*32 * 2^s < 2^29 so that
+  // X = c * 2^s + 1 fits in 29 bits and P's significand times X in 53.
+  const int s = eps_shift(c.eps);
   if (s < 0) return MOE_ERR_UNSUPPORTED;
   if (static_cast<double>(c.W) * 32.0 * static_cast<double>(1u << s) >= 536870912.0)
     return MOE_ERR_UNSUPPORTED;
@@ -401,7 +452,7 @@ int eco_launch(const EcoArgs& a) {
       return MOE_ERR_CUDA;
     LaunchScope ls(kProfEco, a.stream);
     eco_batch_kernel<<<1, 512, smem, a.stream>>>(a.P, a.parent, a.own_fp, a.gamma, c.N, c.W, a.nseq, c.gamma_max,
-                                                  static_cast<double>(c.eps), a.selected, a.union_size, a.dev_err,
+                                                  eps_shift(c.eps), a.selected, a.union_size, a.dev_err,
                                                   a.verify_rows, a.verify_conf, a.T_expected);
     return check_launch();
   }
@@ -413,7 +464,8 @@ int eco_launch(const EcoArgs& a) {
   int threads = c.W >= 256 || c.N >= 16 ? 512 : 256;
   LaunchScope ls(kProfEco, a.stream);
   eco_kernel<<<a.nseq, threads, smem, a.stream>>>(a.P, a.parent, a.own_fp, a.gamma, c.N, c.W,
-                                                  c.gamma_max, c.mode, static_cast<double>(c.eps),
+                                                  c.gamma_max, c.mode, eps_shift(c.eps),
+                                                  (static_cast<long long>(c.W) * 32) << eps_shift(c.eps) < (1ll << 24) - 1,
                                                   a.selected, a.union_size, a.dev_err,
                                                   a.verify_rows, a.verify_conf, a.T_expected,
                                                   a.nseq);

@@ -71,7 +71,13 @@ SMALL = [dict(name="plan_bf16"), dict(name="plan_bias", use_bias=True, cap=8, al
          dict(name="plan_batched_bias", nseq=4, ragged=True, tau=0.1, use_bias=True, cap=6, alpha=0.5),
          dict(name="plan_static", mode=1),
          dict(name="plan_batch_global", nseq=4, ragged=True, tau=0.1, mode=2),
-         dict(name="plan_batch_global_bias", nseq=3, mode=2, use_bias=True, cap=6, alpha=0.5)]
+         dict(name="plan_batch_global_bias", nseq=3, mode=2, use_bias=True, cap=6, alpha=0.5),
+         # the head's biased pass ranks the candidates (unbiased top-k | E*) when lam_b >= 0 and there
+         # are at most 32 of them; otherwise it runs the k rounds over every expert
+         dict(name="plan_bias_neg_alpha", use_bias=True, cap=8, alpha=-0.5),
+         dict(name="plan_bias_zero_alpha", use_bias=True, cap=8, alpha=0.0),
+         dict(name="plan_bias_big_cap", E=64, k=6, use_bias=True, cap=40, alpha=0.25),
+         dict(name="plan_bias_wide", E=256, k=8, use_bias=True, cap=16, alpha=1.0)]
 
 
 @pytest.mark.parametrize("kw", SMALL, ids=[d["name"] for d in SMALL])
@@ -106,3 +112,22 @@ def test_plan_matches_the_step_unions(mv):
     step(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
     torch.cuda.synchronize()
     assert step.n_unique.cpu().tolist() == plan.n_unique.cpu().tolist()
+
+
+@pytest.mark.parametrize("alpha", [0.25, 2.0])
+def test_plan_bias_with_tied_logits(mv, alpha):
+    """Logits on a coarse grid: many equal values, so the lower-id rule decides
+    in both the unbiased and the biased top-k."""
+    from workload import gen
+    cfg = gen.small_case("plan_bias_ties", L=3, E=32, k=4, use_bias=True, cap=6, alpha=alpha)
+    wl = gen.make_workload(cfg)
+    wl.logits = (np.round(wl.logits * 2.0) / 2.0).astype(np.float32)
+    from workload import device as wdev
+    t = wdev.workload_tensors(wl, "cuda")
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, use_bias=True, cap=cfg.cap, alpha=cfg.alpha)
+    plan = mv.VerifyPlan(spec)
+    plan(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+    torch.cuda.synchronize()
+    check_against_oracle(wl, plan)
