@@ -291,7 +291,7 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
     # S2-MoE expansion on the workload's own trees with the calibrated cost.
     wl = gen.make_workload(cfg)
     t = wdev.workload_tensors(wl, dev)
-    T_exp = float(b)
+    T_exp = max(float(b), 0.0)  # a least-squares slope; never negative as a cost
     T_AR = 1e3 * next(p["ms"] for p in pts if p["gamma"] == 0)
     sel, n_sel, usize = mv.s2_expand(t["P"], t["parent"], t["own_fp"], T_AR, T_exp, 0.0)
     for _ in range(3):
@@ -512,7 +512,7 @@ def residency_measure(mv, cfg, layers, layout, dev, stream, expansion=None, n_la
            "T_cold_us_at_copy_engine_rate": ebytes / (ce_gbs * 1e9) * 1e6,
            "hot_list": "per layer, the most routed experts of a calibration workload (seed + 1000)"}
     if expansion is not None:
-        res["s2_expand"] = residency_expansion(mv, cfg, layout, dev, expansion, float(b))
+        res["s2_expand"] = residency_expansion(mv, cfg, layout, dev, expansion, max(float(b), 0.0))
     return res
 
 
