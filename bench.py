@@ -623,6 +623,24 @@ def ours(args, rank, ws, local):
     value = total_bytes / (ms_total / 1e3) / 1e9
     tokens = sum_over_ranks(wl.T * args.steps, ws)
 
+    # ---- the same step replayed from a CUDA graph (no host launch work per step).
+    graph_ms = None
+    try:
+        g = step.capture(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+        g.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / args.steps
+        del g
+    except RuntimeError as exc:  # capture unsupported: report it, keep the eager numbers
+        graph_ms = f"unavailable: {exc}"
+
     # ---- pass B: the same K steps with CUDA events around the dominant
     # kernel only (FFN gate/up), on the stream it runs on.
     mv.profile_begin(max_launches=args.steps * cfg.L + 16, classes=["ffn_gate_up"])
@@ -757,6 +775,7 @@ def ours(args, rank, ws, local):
         "frac_of_8tbs_step": value / 8000.0 / ws,
         "roofline": roofline,
         "kernel_ms_per_step": {k: v["ms"] / n_c for k, v in prof.items()},
+        "graph_ms_per_step": graph_ms,
         "control_path_ms": ctrl_ms,
         "control_path_frac": ctrl_ms / max(ms_step, 1e-9),
         "control_path_frac_events": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))

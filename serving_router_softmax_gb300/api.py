@@ -427,6 +427,23 @@ class VerifyStep:
                "moe_verify_step")
         return self.y
 
+    def capture(self, P, parent, own_fp, gamma_per_seq, node_logits, node_x, steps: int = 1):
+        """Records `steps` verify steps on these input tensors into a CUDA graph and returns it;
+        `graph.replay()` then runs them with no host launch work.  The inputs are read at replay
+        time, so new values are copied into the same tensors between replays.  The step makes no
+        allocation and no host synchronisation, which is what makes it capturable."""
+        args = (P, parent, own_fp, gamma_per_seq, node_logits, node_x)
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self(*args)  # warm-up outside the capture (one-time attribute setup)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(steps):
+                self(*args)
+        return graph
+
 
 class VerifyPlan:
     """The control path of a verify step (selection, then every layer's

@@ -258,3 +258,42 @@ def test_step_full_size_sampled(mv, name):
     layout = "tiled" if cfg.dtype in ("bf16", "e4m3") else "rowmajor"  # as the bench runs it
     wl, got, ref = run_step(mv, cfg, sample_tokens=tokens, sample_layers=layers, layout=layout)
     check_step(wl, got, ref, TOL[cfg.dtype], sample_tokens=tokens)
+
+
+def test_step_in_a_cuda_graph(mv):
+    """The whole step is capturable: replaying a CUDA graph of it gives the eager
+    step's outputs bit for bit, also after new inputs are copied into the captured
+    tensors."""
+    from workload import CONFIGS, gen
+    from workload import device as wdev
+    cfg = CONFIGS["batched_qwen_like"].replace(L=2, H=512, I=256, use_bias=True, cap=8, alpha=0.25)
+    wl = gen.make_workload(cfg)
+    layers = [make_layer(mv, cfg, l, "tiled") for l in range(cfg.L)]
+    t = wdev.workload_tensors(wl)
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, use_bias=True, cap=cfg.cap, alpha=cfg.alpha, layout="tiled")
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    eager = mv.VerifyStep(spec, layers)
+    y0 = eager(*args).clone()
+    sel0 = eager.selected.clone()
+    torch.cuda.synchronize()
+    assert eager.dev_err.item() == 0
+    step = mv.VerifyStep(spec, layers)
+    g = step.capture(*args)
+    step.y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    assert torch.equal(step.y, y0) and torch.equal(step.selected, sel0)
+    # new inputs of the same shape: logits and hidden states of another seed
+    wl2 = gen.make_workload(cfg.replace(seed=cfg.seed + 7))
+    t2 = wdev.workload_tensors(wl2)
+    for k_ in ("P", "own_fp", "logits", "x"):
+        t[k_].copy_(t2[k_])
+    g.replay()
+    y_eager = eager(*args)
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0 and eager.dev_err.item() == 0
+    assert torch.equal(step.y, y_eager) and torch.equal(step.selected, eager.selected)
+    assert not torch.equal(y_eager, y0)

@@ -185,3 +185,71 @@ def test_step_with_pools_matches_resident_step(mv):
     assert pstep.dev_err.item() == 0
     assert torch.equal(pstep.n_unique, nu_res)
     assert torch.equal(y_pool, y_res)
+
+
+def _host_mem_available():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def test_step_with_pool_full_size_layer(mv):
+    """One Qwen3-235B-like layer at full size (128 experts of 37.7 MB, tiled), half resident by a
+    calibration profile: the pooled step equals the resident step bit for bit, and the staged
+    bytes of the union's cold experts equal the host copy."""
+    from oracle import residency as R
+    from workload import CONFIGS, gen
+    from workload import device as wdev
+    cfg = CONFIGS["qwen3_235b_like"].replace(L=1)
+    need = cfg.E * 3 * cfg.H * cfg.I * 2
+    if _host_mem_available() < 3 * need:
+        pytest.skip("not enough free host memory for the page-locked expert copy")
+    free, _ = torch.cuda.mem_get_info()
+    if free < 3 * need:
+        pytest.skip("not enough free device memory")
+    layers = [make_layer(mv, cfg, 0, "tiled")]
+    wl = gen.make_workload(cfg)
+    t = wdev.workload_tensors(wl)
+    spec = mv.StepSpec(L=1, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H, I=cfg.I,
+                       dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode, eps=cfg.eps,
+                       layout="tiled")
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    step = mv.VerifyStep(spec, layers)
+    y_res = step(*args).clone()
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    # calibration profile: routing of another seed's workload
+    cal = cfg.replace(seed=cfg.seed + 1000)
+    wl_cal = gen.make_workload(cal)
+    plan = mv.VerifyPlan(mv.StepSpec(L=1, nseq=cal.nseq, N=wl_cal.parent.shape[0], W=cal.W, E=cal.E, k=cal.k,
+                                     H=cal.H, I=cal.I, dtype=cal.dtype, T=wl_cal.T,
+                                     gamma_max=int(wl_cal.gamma.max()), mode=cal.mode, eps=cal.eps,
+                                     layout="tiled"))
+    tc = wdev.workload_tensors(wl_cal)
+    plan(tc["P"], tc["parent"], tc["own_fp"], tc["gamma"], tc["logits"])
+    torch.cuda.synchronize()
+    hot = [R.hot_experts(R.activation_counts(plan.ids[0].cpu().numpy(), cfg.E), cfg.E // 2)]
+    pool = mv.ExpertPool(layers, hot, n_stage=min(cfg.E // 2, wl.T * cfg.k))
+    pstep = mv.VerifyStep(spec, pool.layers)
+    y_pool = pstep(*args)
+    torch.cuda.synchronize()
+    assert pstep.dev_err.item() == 0
+    assert torch.equal(y_pool, y_res)
+    U = int(pstep.n_unique[0].item())
+    plan2 = mv.VerifyPlan(spec)
+    plan2(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+    torch.cuda.synchronize()
+    unique = plan2.unique[0][:U].cpu().numpy()
+    slot_ref, staged, errors = R.stage_plan(unique, pool.home_slot[0].cpu().numpy(), pool.n_slots,
+                                            pool.stage_first, pool.n_stage)
+    assert errors == [] and len(staged) > 0
+    slot_of = pool.slot_of[0].cpu().numpy()
+    assert {int(e): int(slot_of[e]) for e in unique} == slot_ref
+    for c, e in enumerate(staged[:3]):
+        s = pool.stage_first + c
+        assert torch.equal(pool.pool_gate_up[s].cpu(), pool.host_gate_up[0][e])
+        assert torch.equal(pool.pool_down[s].cpu(), pool.host_down[0][e])
