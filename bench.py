@@ -75,24 +75,32 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(v, ws):
+def _reduce(v, ws, op_name):
     if ws == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    # NCCL reduces device tensors; gloo (the CPU tests of this path) host tensors.
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=getattr(dist.ReduceOp, op_name))
     return float(t.item())
+
+
+def max_over_ranks(v, ws):
+    return _reduce(v, ws, "MAX")
 
 
 def sum_over_ranks(v, ws):
-    if ws == 1:
-        return v
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(v, ws, "SUM")
+
+
+def job_throughput(bytes_local, ms_local, ws):
+    """Whole-job GB/s of independent replicas: the bytes every rank moved over
+    the slowest rank's time; returns (GB/s, that time in ms)."""
+    ms_total = max_over_ranks(ms_local, ws)
+    total = sum_over_ranks(bytes_local, ws)
+    return total / (ms_total / 1e3) / 1e9, ms_total
 
 
 def peaks():
@@ -617,10 +625,9 @@ def ours(args, rank, ws, local):
     barrier(ws)
     launches = mv.launch_count() - launches0
     ms_local = e0.elapsed_time(e1)
-    ms_total = max_over_ranks(ms_local, ws)
+    value, ms_total = job_throughput(bytes_step * args.steps, ms_local, ws)
     ms_step = ms_total / args.steps
     total_bytes = sum_over_ranks(bytes_step * args.steps, ws)
-    value = total_bytes / (ms_total / 1e3) / 1e9
     tokens = sum_over_ranks(wl.T * args.steps, ws)
 
     # ---- the same step replayed from a CUDA graph (no host launch work per step).
