@@ -33,6 +33,9 @@
 // MOE_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 #include "ffn_internal.cuh"
 #include "tc_ptx.cuh"
@@ -59,6 +62,7 @@ struct TcParams {
   int KS;            // k-blocks per pipeline stage (1, or 2 for tiled down)
   int stages;
   int pdl;           // launched with programmatic dependent launch
+  int stall;         // test hook: the producer issues nothing, so the bounded waits run out
   int acc_stages;
   uint32_t tmem_cols;
   const int32_t* n_unique;
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         npend = 0;
         dep_done = true;
       };
-      for (long long x = s0; x < s1 && !*abort_flag;) {
+      for (long long x = p.stall ? s1 : s0; x < s1 && !*abort_flag;) {
         const int t = static_cast<int>(x / KU);
         const int u0 = static_cast<int>(x - (long long)t * KU);
         const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
@@ -777,6 +781,12 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.n_slots = weight_slots(lw);
   tp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
   tp.pdl = 1;
+  // Test hook for the failure path (no fault is involved): with
+  // MOE_TEST_STALL=gate_up the gate/up producer issues no copies, every CTA's
+  // bounded wait runs out after its budget, and the launch reports
+  // MOE_DEV_TIMEOUT with the context intact.
+  const char* stall = std::getenv("MOE_TEST_STALL");
+  const bool stall_gu = stall && std::strcmp(stall, "gate_up") == 0;
 
   // gate/up
   tp.KS = 1;
@@ -787,6 +797,7 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.tmem_cols = pow2_cols(tp.acc_stages * 2 * g.NM);
   tp.tile_cnt = cnt_gu;
   tp.done_cnt = nullptr;
+  tp.stall = stall_gu ? 1 : 0;
   if (cudaFuncSetAttribute(ffn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_gu)) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -806,6 +817,7 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.tmem_cols = pow2_cols(tp.acc_stages * g.NM);
   tp.tile_cnt = cnt_d;
   tp.done_cnt = done;
+  tp.stall = 0;
   if (cudaFuncSetAttribute(ffn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_d)) != cudaSuccess)
     return MOE_ERR_CUDA;
