@@ -39,7 +39,6 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kNBMax = 16;         // TMEM promotion buffers (at most)
 constexpr int kMaxNM = 32;         // padded token columns handled by this path
-constexpr int kCombMax = 512;
 constexpr float kLoScale = 16.f;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 constexpr int kBarRegion = 512;    // mbarriers + flags of the CTA
@@ -67,10 +66,6 @@ struct Fp8Params {
   float* o;             // down output [T*k][M]
   float* partials;      // [grid][2][2*NM][128]
   int32_t* tile_cnt;
-  int32_t* done_cnt;
-  const int32_t* inv;
-  const float* w;
-  float* y;
   int32_t* dev_err;
   const int32_t* slot_of;  // expert -> weight slot (NULL: identity); block scales stay per expert id
   int n_slots;
@@ -169,9 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* issued = bcast + 1;
   volatile int* consumed = issued + 1;
   // Barrier/flag block (at most 2*12 + 9 mbarriers + 5 words) then the combine's staging.
-  int32_t* s_inv = reinterpret_cast<int32_t*>(base + (size_t)S * stageBytes + kBarRegion);
-  float* s_w = reinterpret_cast<float*>(s_inv + kCombMax);
-  float* s_red = s_w + kCombMax;  // [4 warps][kMaxNM] column maxima
+  float* s_red = reinterpret_cast<float*>(base + (size_t)S * stageBytes + kBarRegion);  // [4 warps][kMaxNM] column maxima
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -762,7 +755,7 @@ struct Fp8Geom {
 };
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kSmemExtra = 1024 + kBarRegion + 8 * kCombMax + 4 * 4 * kMaxNM;
+constexpr size_t kSmemExtra = 1024 + kBarRegion + 4 * 4 * kMaxNM;
 
 Fp8Geom fp8_geom(const moe_layer_weights& lw, int T, int k) {
   Fp8Geom g;
@@ -826,7 +819,7 @@ Fp8Ws fp8_carve(const moe_layer_weights& lw, int T, int k, void* base) {
   w.o = reinterpret_cast<float*>(take(static_cast<size_t>(TK) * lw.H * 4));
   w.partials = reinterpret_cast<float*>(take(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4));
   w.poff = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cap + 1) * 4));
-  w.counters = reinterpret_cast<int32_t*>(take((static_cast<size_t>(cap) * (g.MT_gu + g.MT_d) + g.MT_d) * 4));
+  w.counters = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cap) * (g.MT_gu + g.MT_d) * 4));
   w.bytes = static_cast<size_t>(p - p0);
   return w;
 }
@@ -852,10 +845,9 @@ int ffn_fp8_launch(const FfnArgs& a) {
   const int cap = lw.E < TK ? lw.E : TK;
   Fp8Geom g = fp8_geom(lw, T, k);
   Fp8Ws ws = fp8_carve(lw, T, k, a.ws);
-  const int n_counters = cap * (g.MT_gu + g.MT_d) + g.MT_d;
+  const int n_counters = cap * (g.MT_gu + g.MT_d);
   int32_t* cnt_gu = ws.counters;
   int32_t* cnt_d = cnt_gu + static_cast<size_t>(cap) * g.MT_gu;
-  int32_t* done = cnt_d + static_cast<size_t>(cap) * g.MT_d;
 
   const uint64_t H = lw.H, I = lw.I, E = weight_slots(lw);  // E: expert slots in the buffers
   const uint64_t KBg = H / kBK, KBd = I / kBK;
@@ -930,9 +922,6 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.hscale = ws.hscale;
   fp.o = ws.o;
   fp.partials = ws.partials;
-  fp.inv = a.inv;
-  fp.w = a.w;
-  fp.y = a.y;
   fp.dev_err = a.dev_err;
   fp.slot_of = slot_table(lw);
   fp.n_slots = weight_slots(lw);
@@ -948,7 +937,6 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.scale_rows = 2 * lw.I / 128;
   fp.bscale = ws.xscale;
   fp.tile_cnt = cnt_gu;
-  fp.done_cnt = nullptr;
   if (cudaFuncSetAttribute(ffn_fp8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_gu)) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -969,7 +957,6 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.scale_rows = lw.H / 128;
   fp.bscale = ws.hscale;
   fp.tile_cnt = cnt_d;
-  fp.done_cnt = done;
   if (cudaFuncSetAttribute(ffn_fp8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_d)) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -24,8 +24,7 @@
 // evenly (stream-K).  A tile cut between CTAs is finished by the last CTA to
 // arrive (atomic counter, no waiting), which sums the fp32 partials of all
 // contributors in CTA order, so results do not depend on timing.  The down
-// kernel also counts finished tiles per 128-row block of y; the CTA that
-// completes a block does the weighted combine for it.
+// weighted combine is its own kernel afterwards.
 //
 // Roles per CTA (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
 // issues MMAs, warps 2-5 drain accumulators (TMEM lane quarter = warp % 4).
@@ -49,7 +48,6 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
-constexpr int kCombMax = 512;     // (token, slot) pairs whose inv/w the down epilogue keeps in smem
 constexpr int kBarRegion = 512;   // mbarriers + flags of the CTA
 static_assert((2 * 12 + 5) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
 
@@ -73,10 +71,6 @@ struct TcParams {
   float* o;          // down output, [T*k][M] fp32 (perm order)
   float* partials;   // [grid][2][2*NM][128] fp32
   int32_t* tile_cnt; // [cap * MT]
-  int32_t* done_cnt; // [MT] (down)
-  const int32_t* inv;
-  const float* w;
-  float* y;          // [T][M] (down)
   int32_t* dev_err;
   const int32_t* slot_of;  // expert -> weight slot (NULL: identity)
   int n_slots;
@@ -151,8 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* issued = bcast + 1;
   volatile int* consumed = issued + 1;
   // Barrier/flag block (at most 2*12 + 9 mbarriers + 5 words) then the combine's staging.
-  int32_t* s_inv = reinterpret_cast<int32_t*>(base + (size_t)S * stageBytes + kBarRegion);
-  float* s_w = reinterpret_cast<float*>(s_inv + kCombMax);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -628,7 +620,7 @@ struct TcGeom {
 };
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kSmemExtra = 1024 /*align*/ + kBarRegion /*barriers & flags*/ + 8 * kCombMax /*combine inv/w*/;
+constexpr size_t kSmemExtra = 1024 /*align*/ + kBarRegion /*barriers & flags*/;
 
 TcGeom tc_geom(const moe_layer_weights& lw, int T, int k) {
   TcGeom g;
@@ -679,7 +671,7 @@ size_t ffn_tc_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
   b += align_up(static_cast<size_t>(TK) * lw.H * 4, 256);                     // O
   b += align_up(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4, 256);       // partials
   b += align_up(static_cast<size_t>(cap + 1) * 4, 256);                       // poff
-  b += align_up((static_cast<size_t>(cap) * (g.MT_gu + g.MT_d) + g.MT_d) * 4, 256);  // counters
+  b += align_up(static_cast<size_t>(cap) * (g.MT_gu + g.MT_d) * 4, 256);  // fix-up counters
   return b;
 }
 
@@ -701,8 +693,7 @@ int ffn_tc_launch(const FfnArgs& a) {
   p += align_up(static_cast<size_t>(cap + 1) * 4, 256);
   int32_t* cnt_gu = reinterpret_cast<int32_t*>(p);
   int32_t* cnt_d = cnt_gu + static_cast<size_t>(cap) * g.MT_gu;
-  int32_t* done = cnt_d + static_cast<size_t>(cap) * g.MT_d;
-  const int n_counters = cap * (g.MT_gu + g.MT_d) + g.MT_d;
+  const int n_counters = cap * (g.MT_gu + g.MT_d);
 
   // Tensor maps (host-side encoding only; nothing is enqueued).
   CUtensorMap tm_g, tm_u, tm_x, tm_wd, tm_wd1, tm_h;
@@ -773,9 +764,6 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.hp = hp;
   tp.o = o;
   tp.partials = partials;
-  tp.inv = a.inv;
-  tp.w = a.w;
-  tp.y = a.y;
   tp.dev_err = a.dev_err;
   tp.slot_of = slot_table(lw);
   tp.n_slots = weight_slots(lw);
@@ -796,7 +784,6 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.acc_stages = 2 * 2 * g.NM <= 512 ? 2 : 1;
   tp.tmem_cols = pow2_cols(tp.acc_stages * 2 * g.NM);
   tp.tile_cnt = cnt_gu;
-  tp.done_cnt = nullptr;
   tp.stall = stall_gu ? 1 : 0;
   if (cudaFuncSetAttribute(ffn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_gu)) != cudaSuccess)
@@ -816,7 +803,6 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.acc_stages = 2 * g.NM <= 512 ? 2 : 1;
   tp.tmem_cols = pow2_cols(tp.acc_stages * g.NM);
   tp.tile_cnt = cnt_d;
-  tp.done_cnt = done;
   tp.stall = 0;
   if (cudaFuncSetAttribute(ffn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_d)) != cudaSuccess)
