@@ -317,6 +317,51 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
     return model, expansion
 
 
+def reuse_bias_sweep(mv, cfg, layers, layout, dev, stream, steps=20):
+    """S2-MoE reuse-aware gating on the bench's workload: the whole step with
+    the bias off and at alpha in {0.1, 0.25, 0.5, 1} (cap = the workload's, or
+    8), reporting the mean union per layer, the reuse ratio and the step time.
+    The bias only re-ranks experts inside E* (a subset of the unbiased union),
+    so the union can only shrink; what it costs in routing fidelity is the
+    write-up's accuracy question, out of scope here."""
+    import torch
+    from workload import gen
+    from workload import device as wdev
+    cap = cfg.cap if cfg.use_bias else 8
+    pts = []
+    for alpha in (None, 0.1, 0.25, 0.5, 1.0):
+        c2 = cfg.replace(use_bias=alpha is not None, cap=cap, alpha=alpha if alpha is not None else 0.25)
+        wl2 = gen.make_workload(c2)
+        t2 = wdev.workload_tensors(wl2, dev)
+        spec = mv.StepSpec(L=c2.L, nseq=c2.nseq, N=wl2.parent.shape[0], W=c2.W, E=c2.E, k=c2.k, H=c2.H,
+                           I=c2.I, dtype=c2.dtype, T=wl2.T, gamma_max=int(wl2.gamma.max()), mode=c2.mode,
+                           eps=c2.eps, use_bias=c2.use_bias, cap=c2.cap, alpha=c2.alpha, layout=layout)
+        step = mv.VerifyStep(spec, layers, dev)
+        args = (t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"], t2["x"])
+        for _ in range(3):
+            step(*args)
+        torch.cuda.synchronize()
+        if int(step.dev_err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(step.dev_err.item())}")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step(*args)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        nu = step.n_unique.cpu().tolist()
+        plan = mv.VerifyPlan(spec, dev)
+        plan(t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"])
+        torch.cuda.synchronize()
+        pts.append({"alpha": alpha, "cap": cap if alpha is not None else None,
+                    "union_per_layer": sum(nu) / len(nu),
+                    "reuse_ratio": float(plan.reuse_ratio.mean().item()),
+                    "ms_per_step": e0.elapsed_time(e1) / steps})
+        del step, plan
+    return {"points": pts, "tokens": int(gen.make_workload(cfg).T),
+            "note": "alpha None = bias off; union and time at the workload's own draft tree"}
+
+
 def host_mem_available():
     try:
         for line in open("/proc/meminfo"):
@@ -698,6 +743,11 @@ def ours(args, rank, ws, local):
     # ---- router logits, timed alone (the step routes the given node logits).
     router = router_measure(mv, cfg, wl, dev, stream)
 
+    # ---- S2-MoE reuse-bias sweep (rank 0 only).
+    bias_sweep = None
+    if rank == 0 and not args.layers and not args.experts:
+        bias_sweep = reuse_bias_sweep(mv, cfg, layers, layout, dev, stream)
+
     # ---- expert residency with on-demand staging from Grace memory (rank 0 only).
     residency = None
     if rank == 0 and not args.no_residency and (args.residency or (not args.layers and not args.experts)):
@@ -795,6 +845,7 @@ def ours(args, rank, ws, local):
         "cost_model": cost_model,
         "s2_expand": expansion,
         "residency": residency,
+        "reuse_bias": bias_sweep,
     }
     return result, wl, cfg
 
