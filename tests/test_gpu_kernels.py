@@ -150,6 +150,28 @@ def test_eco_golden_trees(mv):
             assert usz.item() == ex["union"]
 
 
+def test_eco_rounded_scores_tie_but_exact_scores_do_not(mv):
+    """The selection kernel compares scores P / (c + eps) through the correctly
+    rounded fp32 quotient P / X, X = c * 2^s + 1 (eps = 2^-s), and falls back to
+    the exact comparison only on equal quotients.  With eps = 1/2: node 0 has
+    P = 1 and one new expert (X = 3), node 1 has P = fl32(1/3) > 1/3 and none
+    (X = 1).  Both quotients round to fl32(1/3), but exactly
+    P_1 * X_0 = 3 * fl32(1/3) > 1 = P_0 * X_1, so node 1 wins, not the lower
+    index."""
+    from oracle import eco_select as oeco
+    p1 = float(np.float32(1.0 / 3.0))
+    P = np.array([[1.0, p1]], dtype=np.float32)
+    par = np.array([[-1, -1]], dtype=np.int32)
+    fp = _bits([[(0, 3)], []], 1, 16)[None]
+    # the quotients the kernel's key uses round to the same value
+    assert np.float32(np.float32(1.0) / np.float32(3.0)) == np.float32(np.float32(p1) / np.float32(1.0))
+    sel, usz = mv.eco_select(cuda(P), cuda(par), cuda(fp.view(np.int32)), 1, eps=0.5)
+    torch.cuda.synchronize()
+    rsel, _ = oeco.select_batch(P, np.array([-1, -1]), fp, 16, np.array([1]), 0.5, 0)
+    assert rsel[0] == [1]
+    assert sel[0].cpu().tolist() == [1] and usz.item() == 0
+
+
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("cfgname", ["toy", "qwen3_235b_like", "deepseek_v3_like", "batched_qwen_like"])
 def test_eco_matches_oracle_on_workload_trees(mv, mode, cfgname):
