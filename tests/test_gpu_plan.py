@@ -131,3 +131,27 @@ def test_plan_bias_with_tied_logits(mv, alpha):
     plan(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
     torch.cuda.synchronize()
     check_against_oracle(wl, plan)
+
+
+def test_plan_fuzz_small_configs(mv):
+    """Randomised control-path configurations (experts, top-k, batch, selection
+    mode, bias settings) against the oracle: selection, routing and unions."""
+    from workload import gen
+    rng = np.random.default_rng(2024)
+    for trial in range(24):
+        E = int(rng.choice([8, 16, 40, 64, 128, 200, 256, 300]))
+        k = int(rng.integers(1, min(8, E - 1) + 1))
+        L = int(rng.integers(1, 4))
+        nseq = int(rng.integers(1, 4))
+        mode = int(rng.choice([0, 1, 2])) if nseq > 1 else int(rng.choice([0, 1]))
+        use_bias = bool(rng.integers(0, 2))
+        kw = dict(L=L, E=E, k=k, nseq=nseq, mode=mode, c=float(rng.uniform(0.0, 0.1)),
+                  rho=float(rng.uniform(0.2, 0.9)), seed=int(rng.integers(0, 1 << 20)))
+        if nseq > 1:
+            kw.update(ragged=bool(rng.integers(0, 2)), tau=0.1)
+        if use_bias:
+            kw.update(use_bias=True, cap=int(rng.integers(1, min(E, 24) + 1)),
+                      alpha=float(rng.choice([-0.5, 0.0, 0.1, 0.25, 1.0, 3.0])))
+        cfg = gen.small_case(f"fuzz{trial}", **kw)
+        wl, plan = plan_for(mv, cfg)
+        check_against_oracle(wl, plan)
