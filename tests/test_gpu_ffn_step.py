@@ -299,3 +299,37 @@ def test_step_in_a_cuda_graph(mv):
     assert step.dev_err.item() == 0 and eager.dev_err.item() == 0
     assert torch.equal(step.y, y_eager) and torch.equal(step.selected, eager.selected)
     assert not torch.equal(y_eager, y0)
+
+
+def test_ffn_fuzz_shapes(mv):
+    """Random FFN shapes, dtypes and layouts against the oracle: ragged tiles
+    (H, I not multiples of 128), token groups of every size, all kernel paths."""
+    from oracle import moe_layer as ml
+    from workload import gen
+    rng = np.random.default_rng(77)
+    for trial in range(16):
+        dtype = str(rng.choice(["bf16", "bf16", "e4m3", "f32"]))
+        mult = 128 if dtype == "e4m3" else 64
+        H = mult * int(rng.integers(1, 7))
+        I = mult * int(rng.integers(1, 6))
+        E = int(rng.choice([4, 9, 16, 33, 64]))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.choice([1, 2, 5, 13, 24, 40])) if dtype != "e4m3" else int(rng.choice([1, 3, 5, 17, 32, 40]))
+        layout = "tiled" if dtype != "f32" and rng.integers(0, 2) else "rowmajor"
+        if dtype == "e4m3" and T > 32:
+            layout = "rowmajor"  # the CUDA-core FP8 path reads row-major weights
+        cfg = gen.MoEConfig(f"ffnfuzz{trial}", L=1, H=H, E=E, k=k, I=I, dtype=dtype, seed=1000 + trial)
+        layer = make_layer(mv, cfg, 0, layout)
+        lg = (rng.standard_normal((T, E)) - 0.2 * rng.permutation(E)).astype(np.float32)
+        xs = rng.standard_normal((T, H)).astype(np.float32)
+        x_host = xs if dtype == "f32" else gen.bf16_bits_rne(xs)
+        x_dev = cuda(xs) if dtype == "f32" else cuda(x_host.view(np.int16))
+        dev_err = mv.new_dev_err()
+        ids, w = mv.route(cuda(lg), k, dev_err=dev_err)
+        up = mv.union_permute(ids, E, dev_err=dev_err)
+        y = mv.verify_ffn(x_dev, k, layer, up, w, dev_err=dev_err)
+        torch.cuda.synchronize()
+        assert dev_err.item() == 0, (trial, dtype, H, I, E, k, T, layout)
+        ref = ml.layer_forward(lg, x_decode(cfg)(x_host), k, E, host_experts(cfg, 0))
+        err = rowwise_err(y.cpu().numpy().astype(np.float64), ref["y"])
+        assert err < TOL[dtype], (trial, dtype, H, I, E, k, T, layout, err)
