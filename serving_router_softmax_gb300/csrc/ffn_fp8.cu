@@ -15,7 +15,11 @@
 //     k-block is multiplied into its own TMEM buffer (up to 16 in rotation, as
 //     many as fit in the 512 columns) and the
 //     epilogue warps promote it: acc += w_scale * s * (d_hi + d_lo / 16), in
-//     fp32 registers.
+//     fp32 registers.  In the down projection the buffers go in pairs: one
+//     commit and one barrier round trip per two k-blocks (there the
+//     per-k-block synchronisation, not the tensor pipe, is the tighter
+//     resource at these small N; gate/up, with half as many buffers, keeps
+//     one k-block per barrier).
 //   * gate/up writes h = silu(gate) * up quantized the same way, with one
 //     scale per (token, 128-row block of I), which is exactly one k-block of
 //     the down projection.
@@ -147,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ffn_fp8_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
                    const Fp8Params p) {
+  constexpr int kGroup = kGateUp ? 1 : 2;  // k-blocks per TMEM barrier
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int aBytes = kGateUp ? 2 * kABytes : p.KS * kABytes;
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < p.NB; ++b) {
+    for (int b = 0; b < p.NB / kGroup; ++b) {  // one group of TMEM buffers per barrier
       tc::mbar_init(&tfull[b], 1);
       tc::mbar_init(&tempty[b], kEpiThreads);
     }
@@ -297,8 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tc::elect_one()) {
       int stage = 0;
       uint32_t phase = 0;
-      int kc = 0;               // k-blocks issued (selects the TMEM buffer)
-      uint32_t tphase = 0;      // bit b: phase parity of buffer b
+      const int nbp = p.NB / kGroup;  // buffer groups
+      int pc = 0;               // groups committed (selects the group)
+      int pb = 0;               // current group
+      uint32_t tphase = 0;      // bit b: phase parity of group b
       int n_consumed = 0;
       bool stop = false;
       for (long long x = s0; x < s1 && !stop;) {
@@ -309,6 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile ti = tile_info(p, U, t, false);
         if (!ti.ok) continue;
         const uint32_t idesc = idesc_e4m3_f32(kBM, 2 * ti.np);
+        // Groups are kGroup consecutive k-blocks counted from the segment's
+        // first k-block; the epilogue walks the same groups.
+        const int kb_first = u0 * p.KS;
+        const int kb_end = u1 * p.KS < KB ? u1 * p.KS : KB;
         for (int uu = u0; uu < u1 && !stop; ++uu) {
           if (!tc::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetNs)) {
             *abort_flag = 1;
@@ -321,15 +332,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t aAddr = tc::smem_u32(base + (size_t)stage * stageBytes);
           const uint32_t bAddr = aAddr + aBytes;
           for (int q = 0; q < nq; ++q) {
-            const int b = kc % p.NB;
-            if (!tc::mbar_wait_bounded(&tempty[b], ((tphase >> b) & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
-              *abort_flag = 1;
-              flag_error(p.dev_err, MOE_DEV_TIMEOUT);
-              stop = true;
-              break;
+            const int kb = uu * p.KS + q;
+            const int half = (kb - kb_first) % kGroup;
+            if (half == 0) {
+              pb = pc % nbp;
+              if (!tc::mbar_wait_bounded(&tempty[pb], ((tphase >> pb) & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
+                *abort_flag = 1;
+                flag_error(p.dev_err, MOE_DEV_TIMEOUT);
+                stop = true;
+                break;
+              }
+              tc::tc_fence_after();
             }
-            tc::tc_fence_after();
-            const uint32_t d0 = tmem_base + b * buf_cols;
+            const uint32_t d0 = tmem_base + (kGroup * pb + half) * buf_cols;
             const uint32_t aq = aAddr + (kGateUp ? 0 : q * kABytes);
             const uint32_t bq = bAddr + q * bStride;
 #pragma unroll
@@ -339,9 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_e4m3(d0, tc::smem_desc_sw128(aq + kk * 32), bdesc, idesc, accum);
               if (kGateUp) mma_e4m3(d0 + 2 * p.NM, tc::smem_desc_sw128(aq + kABytes + kk * 32), bdesc, idesc, accum);
             }
-            tc::mma_commit(&tfull[b]);
-            tphase ^= 1u << b;
-            ++kc;
+            if (half == kGroup - 1 || kb + 1 == kb_end) {
+              tc::mma_commit(&tfull[pb]);
+              tphase ^= 1u << pb;
+              ++pc;
+            }
           }
           if (stop) break;
           tc::mma_commit(&empty[stage]);
@@ -364,8 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::griddep_wait();
     const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
     const int KBs = p.K / 128;  // scale blocks along K (== KB)
-    int kc = 0;
-    uint32_t tphase = 0;
+    const int nbp = p.NB / kGroup;  // TMEM buffer groups
+    int pc = 0;                 // groups consumed
+    uint32_t tphase = 0;        // bit b: phase parity of group b
     bool stop = false;
     for (long long x = s0; x < s1 && !stop;) {
       const int t = static_cast<int>(x / KU);
@@ -409,30 +427,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
       }
-      for (int kb = kb_first; kb < kb_end; ++kb) {
-        const int b = kc % p.NB;
-        // Scales of this k-block are requested before waiting for its MMAs,
-        // so their latency hides behind the wait.
-        const float sg = __ldg(&wsg[kb]);
-        const float su = kGateUp ? __ldg(&wsu[kb]) : 0.f;
-        if (!kGateUp) {
-          const float* src = p.bscale + (size_t)kb * p.hs_stride + prow0;
+      // Promotes one k-block's buffer: acc += w_scale * s_row * (hi + lo / 16).
+      auto promote = [&](uint32_t tb, float sg, float su, const float* sb_row) {
 #pragma unroll
-          for (int cc = 0; cc < kMaxNM / 16; ++cc)
-            if (cc < ti.np / 16) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(src + cc * 16 + q * 4));
-                sbr[cc * 16 + q * 4] = v.x;
-                sbr[cc * 16 + q * 4 + 1] = v.y;
-                sbr[cc * 16 + q * 4 + 2] = v.z;
-                sbr[cc * 16 + q * 4 + 3] = v.w;
-              }
+        for (int cc = 0; cc < kMaxNM / 16; ++cc) {
+          if (cc < ti.np / 16) {
+            float gh[16], gl[16], uh[16], ul[16];
+            tc::tmem_ld16(tb + cc * 16, gh);
+            tc::tmem_ld16(tb + ti.np + cc * 16, gl);
+            if (kGateUp) {
+              tc::tmem_ld16(tb + 2 * p.NM + cc * 16, uh);
+              tc::tmem_ld16(tb + 2 * p.NM + ti.np + cc * 16, ul);
             }
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = cc * 16 + j;
+              const float sb = sb_row[n];
+              ga[n] = fmaf(sg * sb, fmaf(gl[j], 1.f / kLoScale, gh[j]), ga[n]);
+              if (kGateUp) ua[n] = fmaf(su * sb, fmaf(ul[j], 1.f / kLoScale, uh[j]), ua[n]);
+            }
+          }
+        }
+      };
+      auto load_row_scales = [&](int kb, float* dst) {  // down: per (k-block, row)
+        const float* src = p.bscale + (size_t)kb * p.hs_stride + prow0;
+#pragma unroll
+        for (int cc = 0; cc < kMaxNM / 16; ++cc)
+          if (cc < ti.np / 16) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 v = __ldg(reinterpret_cast<const float4*>(src + cc * 16 + q * 4));
+              dst[cc * 16 + q * 4] = v.x;
+              dst[cc * 16 + q * 4 + 1] = v.y;
+              dst[cc * 16 + q * 4 + 2] = v.z;
+              dst[cc * 16 + q * 4 + 3] = v.w;
+            }
+          }
+      };
+      for (int kb = kb_first; kb < kb_end; kb += kGroup) {
+        const bool two = kGroup == 2 && kb + 1 < kb_end;
+        const int pb = pc % nbp;
+        // Scales of both k-blocks are requested before waiting for their
+        // MMAs, so their latency hides behind the wait.
+        const float sg0 = __ldg(&wsg[kb]);
+        const float su0 = kGateUp ? __ldg(&wsu[kb]) : 0.f;
+        const float sg1 = two ? __ldg(&wsg[kb + 1]) : 0.f;
+        const float su1 = kGateUp && two ? __ldg(&wsu[kb + 1]) : 0.f;
+        float sbr1[kMaxNM];
+        if (!kGateUp) {
+          load_row_scales(kb, sbr);
+          if (two) load_row_scales(kb + 1, sbr1);
         }
         // Warp-uniform wait: a warp that gives up keeps walking the same
         // loop (skipping the arithmetic) so every later barrier is reached.
-        bool ok = tc::mbar_wait_bounded(&tfull[b], (tphase >> b) & 1u, abort_flag, kWaitBudgetNs);
+        bool ok = tc::mbar_wait_bounded(&tfull[pb], (tphase >> pb) & 1u, abort_flag, kWaitBudgetNs);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok && lane == 0) {
           *abort_flag = 1;
@@ -440,32 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
           tc::tc_fence_after();
-          const uint32_t tb = tmem_base + lane_off + b * buf_cols;
-#pragma unroll
-          for (int cc = 0; cc < kMaxNM / 16; ++cc) {
-            if (cc < ti.np / 16) {
-              float gh[16], gl[16], uh[16], ul[16];
-              tc::tmem_ld16(tb + cc * 16, gh);
-              tc::tmem_ld16(tb + ti.np + cc * 16, gl);
-              if (kGateUp) {
-                tc::tmem_ld16(tb + 2 * p.NM + cc * 16, uh);
-                tc::tmem_ld16(tb + 2 * p.NM + ti.np + cc * 16, ul);
-              }
-              tc::tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int n = cc * 16 + j;
-                const float sb = sbr[n];
-                ga[n] = fmaf(sg * sb, fmaf(gl[j], 1.f / kLoScale, gh[j]), ga[n]);
-                if (kGateUp) ua[n] = fmaf(su * sb, fmaf(ul[j], 1.f / kLoScale, uh[j]), ua[n]);
-              }
-            }
-          }
+          const uint32_t tb = tmem_base + lane_off + kGroup * pb * buf_cols;
+          promote(tb, sg0, su0, sbr);
+          if (two) promote(tb + buf_cols, sg1, su1, kGateUp ? sbr : sbr1);
         }
         tc::tc_fence_before();
-        tc::mbar_arrive(&tempty[b]);
-        tphase ^= 1u << b;
-        ++kc;
+        tc::mbar_arrive(&tempty[pb]);
+        tphase ^= 1u << pb;
+        ++pc;
       }
       tc::named_bar_sync(1, kEpiThreads);
       if (*abort_flag) {
