@@ -407,7 +407,10 @@ int eco_select(const float* P, const int32_t* parent, const uint32_t* own_fp, in
  *               layer; row 0 of each sequence is the root token.
  *   node_x      [L, nseq, N+1, H] layer inputs of every tree node (fp32 or
  *               bf16 bits, by dtype).
- *   layers      HOST array of L moe_layer_weights (same H, I, E, dtype).
+ *   layers      HOST array of L moe_layer_weights (same H, I, E, dtype).  A
+ *               layer with an expert pool has its union's cold experts
+ *               staged (moe_stage_experts) between its routing and its FFN;
+ *               layers may share one staging range.
  *   selected, union_size: as eco_select.
  *   n_unique    [L] int32 out: union size per layer.
  *   y           [L, T, H] fp32 out.
