@@ -253,3 +253,31 @@ def test_step_with_pool_full_size_layer(mv):
         s = pool.stage_first + c
         assert torch.equal(pool.pool_gate_up[s].cpu(), pool.host_gate_up[0][e])
         assert torch.equal(pool.pool_down[s].cpu(), pool.host_down[0][e])
+
+
+def test_pooled_step_in_a_cuda_graph(mv):
+    """Staging runs inside a captured step: replays equal the eager pooled step."""
+    from oracle import residency as R
+    from workload import CONFIGS, gen
+    from workload import device as wdev
+    cfg = CONFIGS["qwen3_235b_like"].replace(L=2, H=256, I=192, E=32, k=4)
+    wl = gen.make_workload(cfg)
+    t = wdev.workload_tensors(wl)
+    layers = [make_layer(mv, cfg, l, "tiled") for l in range(cfg.L)]
+    hot = [R.hot_experts(np.arange(32)[::-1].copy(), 8) for _ in range(cfg.L)]
+    pool = mv.ExpertPool(layers, hot, n_stage=24)
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), layout="tiled")
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    eager = mv.VerifyStep(spec, pool.layers)
+    y0 = eager(*args).clone()
+    torch.cuda.synchronize()
+    assert eager.dev_err.item() == 0
+    step = mv.VerifyStep(spec, pool.layers)
+    g = step.capture(*args)
+    step.y.zero_()
+    pool.pool_gate_up[pool.stage_first:].zero_()  # the replay must stage the cold experts again
+    g.replay()
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    assert torch.equal(step.y, y0)
