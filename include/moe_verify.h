@@ -304,7 +304,9 @@ size_t moe_verify_ffn_workspace(const moe_layer_weights* lw, int32_t T, int32_t 
  *
  *   x        [T, H] activations: fp32 for MOE_DTYPE_F32, bf16 bits otherwise.
  *   n_unique, unique, offsets, perm_token, inv: as written by
- *            moe_union_permute for the same ids.
+ *            moe_union_permute for the same ids (each expert's group lists
+ *            its tokens in ascending order; with bf16 weights and T <= 32 a
+ *            group that does not ascend raises MOE_DEV_BAD_ID).
  *   w        [T, k] fp32 routing weights.
  *   y        [T, H] fp32 out.  The combine sums slots j = 0..k-1 in order.
  * Arithmetic: fp32 accumulation.  bf16 weights: tensor cores on bf16

@@ -645,11 +645,7 @@ __global__ void __launch_bounds__(kPrepThreads) ffn_fp8_prep_kernel(
       sum += ((b - a) + 15) & ~15;
       soff[u] = a;
     }
-    int ex = sum;
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, ex, off);
-      if (lane >= off) ex += v;
-    }
+    int ex = warp_inclusive_sum(sum, lane);
     ex -= sum;
     for (int u = u0; u < u0 + per && u < U; ++u) {
       spoff[u] = ex;

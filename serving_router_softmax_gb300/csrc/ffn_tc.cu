@@ -55,7 +55,9 @@ struct TcParams {
   int T, k, E, cap;
   int M, K;          // rows of each expert matrix, reduction length
   int NM;            // max padded token columns (multiple of 16, <= 256)
-  int Rmax;          // rows of Xp / Hp
+  int Rmax;          // rows of Xp
+  int Rh;            // rows of Hp
+  int dense;         // token-dense gate/up (see ffn_tc_dense)
   int tiled;         // weights in the tile-packed layout (else row-major)
   int KS;            // k-blocks per pipeline stage (1, or 2 for tiled down)
   int stages;
@@ -66,6 +68,7 @@ struct TcParams {
   const int32_t* n_unique;
   const int32_t* unique;
   const int32_t* offsets;
+  const int32_t* perm_token;
   const int32_t* poff;
   uint16_t* hp;      // gate/up output, [R_pad_max][M] bf16
   float* o;          // down output, [T*k][M] fp32 (perm order)
@@ -93,17 +96,18 @@ __device__ __forceinline__ Tile tile_info(const TcParams& p, int U, int t) {
   ti.off = p.offsets[ti.u];
   ti.ne = p.offsets[ti.u + 1] - ti.off;
   ti.np = (ti.ne + 15) & ~15;
-  ti.prow = p.poff[ti.u];
+  ti.prow = p.dense ? ti.u * p.NM : p.poff[ti.u];
   ti.ok = ti.e >= 0 && ti.e < p.E && ti.ne >= 1 && ti.ne <= p.T && ti.np <= p.NM && ti.off >= 0 &&
           ti.off + ti.ne <= p.T * p.k;
   ti.ws = ti.ok ? weight_slot(p.slot_of, p.n_slots, ti.e) : -1;
   ti.ok = ti.ok && ti.ws >= 0;
-  ti.prow_ok = ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
+  ti.prow_ok = ti.prow >= 0 && ti.prow + ti.np <= p.Rh;
   return ti;
 }
 
 // The part of tile_info that does not depend on the padded group offsets
-// (written by the kernel that runs just before gate/up).
+// (written by the kernel that runs just before gate/up).  In the token-dense
+// gate/up every tile's B operand is the same NM rows, so np is NM there.
 __device__ __forceinline__ Tile tile_core(const TcParams& p, int U, int t) {
   Tile ti;
   ti.m = t / U;
@@ -122,6 +126,26 @@ __device__ __forceinline__ Tile tile_core(const TcParams& p, int U, int t) {
 }
 
 __device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+
+// Tokens of a tile's expert as a bit mask over the T <= 32 token columns.
+// The group lists its tokens in ascending order (the union's layout), so a
+// token's row in the expert's Hp block is the number of its group's tokens
+// below it.  All 32 lanes of a warp take part (ne <= T <= 32): lane r reads
+// the group's r-th token (group_token, issued before the accumulator wait so
+// that the load overlaps it), then group_mask combines the lanes.  Returns
+// false for a group that is not strictly ascending or names a token outside
+// [0, T).
+__device__ __forceinline__ int group_token(const TcParams& p, const Tile& ti, int lane) {
+  return lane < ti.ne ? p.perm_token[ti.off + lane] : 0;
+}
+
+__device__ __forceinline__ bool group_mask(const TcParams& p, const Tile& ti, int lane, int tok, uint32_t& mask) {
+  const bool mine = lane < ti.ne;
+  const int prev = __shfl_up_sync(0xFFFFFFFFu, tok, 1);
+  const bool ok = !mine || (tok >= 0 && tok < p.T && (lane == 0 || tok > prev));
+  mask = __reduce_or_sync(0xFFFFFFFFu, (mine && tok >= 0 && tok < 32) ? 1u << tok : 0u);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
 
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -213,9 +237,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool dep_done = !p.pdl;
       if (dep_done) tc::griddep_launch_dependents();
       auto issue_b = [&](int t, int kb, int nq, int st) {
+        uint8_t* sB = base + (size_t)st * stageBytes + aBytes;
+        if (kGateUp && p.dense) {
+          // all NM token rows in one box; rows past T are filled with zeros
+          for (int q = 0; q < nq; ++q) tc::tma_load_2d(sB + q * bStride, &tmB, (kb + q) * kBK, 0, &full[st], polB);
+          return;
+        }
         const Tile ti = tile_info(p, U, t);
         const int prow = ti.prow_ok ? ti.prow : 0;  // bad offsets: load something in bounds, epilogue skips
-        uint8_t* sB = base + (size_t)st * stageBytes + aBytes;
         for (int q = 0; q < nq; ++q)
           for (int j = 0; j < ti.np / 16; ++j)
             tc::tma_load_2d(sB + q * bStride + j * 2048, &tmB, (kb + q) * kBK, prow + 16 * j, &full[st], polB);
@@ -244,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb = uu * p.KS;
           const int nq = KB - kb < p.KS ? KB - kb : p.KS;
           uint8_t* sA = base + (size_t)stage * stageBytes;
-          const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * ti.np * 128;
+          const int nb = (kGateUp && p.dense) ? p.NM : ti.np;  // B rows
+          const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * nb * 128;
           tc::mbar_arrive_expect_tx(&full[stage], tx);
           if (p.tiled) {
             // Tile-packed weights: block (e, m, kb) is contiguous.  gate/up:
@@ -302,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tc_fence_after();
         const uint32_t d0 = tmem_base + acc * acc_cols;
-        const uint32_t idesc = tc::idesc_bf16_f32(kBM, ti.np);
+        const uint32_t idesc = tc::idesc_bf16_f32(kBM, (kGateUp && p.dense) ? p.NM : ti.np);
         for (int uu = u0; uu < u1; ++uu) {
           if (!tc::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitBudgetNs)) {
             *abort_flag = 1;
@@ -364,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (kGateUp && !ti.prow_ok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+      const int gtok = (kGateUp && p.dense) ? group_token(p, ti, lane) : 0;
       // Every epilogue thread waits; the outcome is made uniform through a
       // shared vote so that no thread is left behind at a named barrier.
       if (!tc::mbar_wait_bounded(&accf[acc], acc_phase[acc], abort_flag, kWaitBudgetNs)) {
@@ -373,29 +404,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::named_bar_sync(1, kEpiThreads);
       if (*abort_flag) break;
       tc::tc_fence_after();
+      uint32_t mask = 0;
+      bool hp_ok = ti.prow_ok;
+      if (kGateUp && p.dense) {
+        const bool mok = group_mask(p, ti, lane, gtok, mask);
+        if (!mok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+        hp_ok = hp_ok && mok;
+      }
       const bool whole = u0 == 0 && u1 == KU;
       const int row = ti.m * kBM + r;
       const bool row_ok = row < p.M;
       const uint32_t tacc = tmem_base + lane_off + acc * acc_cols;
       float* P = p.partials + ((size_t)c * 2 + (t == first_tile_c ? 0 : 1)) * (size_t)(2 * p.NM * 128);
-      for (int cc = 0; cc < ti.np / 16; ++cc) {
+      // Result column n: gate/up writes h to Hp (token-dense: column n is
+      // token n, stored at its rank in the expert's group), down writes o.
+      auto put = [&](int n, float gv, float vv) {
+        if (!row_ok) return;
+        if (kGateUp) {
+          if (p.dense) {
+            if (hp_ok && n < 32 && ((mask >> n) & 1u))
+              p.hp[(size_t)(ti.prow + __popc(mask & ((1u << n) - 1u))) * p.M + row] =
+                  float_to_bf16_bits_rn(silu_mul(gv, vv));
+          } else if (n < ti.ne && hp_ok) {
+            p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(gv, vv));
+          }
+        } else if (n < ti.ne) {
+          p.o[(size_t)(ti.off + n) * p.M + row] = gv;
+        }
+      };
+      const int ncols = (kGateUp && p.dense) ? p.NM : ti.np;
+      for (int cc = 0; cc < ncols / 16; ++cc) {
         float g[16], v[16];
         tc::tmem_ld16(tacc + cc * 16, g);
         if (kGateUp) tc::tmem_ld16(tacc + p.NM + cc * 16, v);
         tc::tmem_ld_wait();
         if (whole) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = cc * 16 + j;
-            if (n < ti.ne && row_ok) {
-              if (kGateUp) {
-                if (ti.prow_ok)
-                  p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
-              } else {
-                p.o[(size_t)(ti.off + n) * p.M + row] = g[j];
-              }
-            }
-          }
+          for (int j = 0; j < 16; ++j) put(cc * 16 + j, g[j], kGateUp ? v[j] : 0.f);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -429,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (arrived == cl - cf) {
           __threadfence();
           finished = true;
-          for (int cc = 0; cc < ti.np / 16; ++cc) {
+          for (int cc = 0; cc < ncols / 16; ++cc) {
             float g[16], v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) g[j] = v[j] = 0.f;
@@ -443,17 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = cc * 16 + j;
-              if (n < ti.ne && row_ok) {
-                if (kGateUp) {
-                  if (ti.prow_ok)
-                    p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(g[j], v[j]));
-                } else {
-                  p.o[(size_t)(ti.off + n) * p.M + row] = g[j];
-                }
-              }
-            }
+            for (int j = 0; j < 16; ++j) put(cc * 16 + j, g[j], kGateUp ? v[j] : 0.f);
           }
         }
       }
@@ -521,11 +556,7 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
       sum += ((b - a) + 15) & ~15;
       soff[u] = a;
     }
-    int ex = sum;
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, ex, off);
-      if (lane >= off) ex += v;
-    }
+    int ex = warp_inclusive_sum(sum, lane);
     ex -= sum;
     for (int u = u0; u < u0 + per && u < U; ++u) {
       spoff[u] = ex;
@@ -580,6 +611,35 @@ __global__ void __launch_bounds__(256) ffn_prep_kernel(const uint16_t* __restric
   }
 }
 
+// Token-dense prep (T <= 32): copies the T token rows into Xp rows 0..T-1 and
+// zeroes the fix-up counters.  Neither depends on the union; the work still
+// follows the wait, so that it never competes with the latency-bound head
+// kernel it follows, and it hides behind the gate/up kernel's first weight
+// loads (that grid starts at this one's trigger).
+__global__ void __launch_bounds__(256) ffn_prep_dense_kernel(const uint16_t* __restrict__ x,
+                                                             const int32_t* __restrict__ x_rows,
+                                                             int x_rows_limit, int T, int H,
+                                                             uint16_t* __restrict__ xp,
+                                                             int32_t* __restrict__ counters, int n_counters,
+                                                             int32_t* dev_err) {
+  pdl_wait();
+  pdl_trigger();
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long nth = (long long)gridDim.x * blockDim.x;
+  for (long long i = tid; i < n_counters; i += nth) counters[i] = 0;
+  const int cpr = H / 8;  // 16-byte chunks per row
+  for (long long i = tid; i < (long long)T * cpr; i += nth) {
+    const int t = static_cast<int>(i / cpr);
+    const int ch = static_cast<int>(i - (long long)t * cpr);
+    const long long row = x_rows ? x_rows[t] : t;
+    if (row >= 0 && (!x_rows || row < x_rows_limit))
+      *reinterpret_cast<uint4*>(xp + (size_t)t * H + ch * 8) =
+          *reinterpret_cast<const uint4*>(x + (size_t)row * H + ch * 8);
+    else
+      flag_error(dev_err, MOE_DEV_BAD_ID);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -614,7 +674,8 @@ bool make_tmap(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims
 }
 
 struct TcGeom {
-  int NM, MT_gu, MT_d, Rmax, G, KS_d;
+  int NM, MT_gu, MT_d, Rmax, Rh, G, KS_d;
+  int dense;  // token-dense gate/up: every tile multiplies all T tokens
   int stages_gu, stages_d;
   size_t smem_gu, smem_d;
 };
@@ -631,6 +692,12 @@ TcGeom tc_geom(const moe_layer_weights& lw, int T, int k) {
   g.MT_gu = (lw.I + kBM - 1) / kBM;
   g.MT_d = (lw.H + kBM - 1) / kBM;
   g.Rmax = TK + 15 * cap;
+  // With at most 32 tokens the MMA's N covers every token at once (16 or 32
+  // columns, the width a single group would already pad to), so gate/up
+  // reads the T token rows directly and the prep kernel needs no union; Hp
+  // then holds NM rows per unique expert.
+  g.dense = T <= 32 ? 1 : 0;
+  g.Rh = g.dense && cap * g.NM > g.Rmax ? cap * g.NM : g.Rmax;
   g.G = sm_count();
   g.KS_d = lw.layout == MOE_LAYOUT_TILED ? 2 : 1;
   const size_t b = static_cast<size_t>(g.NM) * 128;
@@ -667,7 +734,7 @@ size_t ffn_tc_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
   const int cap = lw.E < TK ? lw.E : TK;
   size_t b = 0;
   b += align_up(static_cast<size_t>(g.Rmax) * lw.H * 2, 256);                 // Xp
-  b += align_up(static_cast<size_t>(g.Rmax) * lw.I * 2, 256);                 // Hp
+  b += align_up(static_cast<size_t>(g.Rh) * lw.I * 2, 256);                   // Hp
   b += align_up(static_cast<size_t>(TK) * lw.H * 4, 256);                     // O
   b += align_up(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4, 256);       // partials
   b += align_up(static_cast<size_t>(cap + 1) * 4, 256);                       // poff
@@ -684,7 +751,7 @@ int ffn_tc_launch(const FfnArgs& a) {
   uint16_t* xp = reinterpret_cast<uint16_t*>(p);
   p += align_up(static_cast<size_t>(g.Rmax) * lw.H * 2, 256);
   uint16_t* hp = reinterpret_cast<uint16_t*>(p);
-  p += align_up(static_cast<size_t>(g.Rmax) * lw.I * 2, 256);
+  p += align_up(static_cast<size_t>(g.Rh) * lw.I * 2, 256);
   float* o = reinterpret_cast<float*>(p);
   p += align_up(static_cast<size_t>(TK) * lw.H * 4, 256);
   float* partials = reinterpret_cast<float*>(p);
@@ -726,19 +793,34 @@ int ffn_tc_launch(const FfnArgs& a) {
       tm_wd1 = tm_wd;
     }
   }
-  {
+  if (g.dense) {
+    // the T token rows; the box's rows past T read as zeros
+    uint64_t dims[2] = {H, static_cast<uint64_t>(T)}, str[1] = {H * 2};
+    uint32_t box[2] = {kBK, static_cast<uint32_t>(g.NM)};
+    if (!make_tmap(&tm_x, xp, 2, dims, str, box)) return MOE_ERR_CUDA;
+  } else {
     uint64_t dims[2] = {H, static_cast<uint64_t>(g.Rmax)}, str[1] = {H * 2};
     uint32_t box[2] = {kBK, 16};
     if (!make_tmap(&tm_x, xp, 2, dims, str, box)) return MOE_ERR_CUDA;
   }
   {
-    uint64_t dims[2] = {I, static_cast<uint64_t>(g.Rmax)}, str[1] = {I * 2};
+    uint64_t dims[2] = {I, static_cast<uint64_t>(g.Rh)}, str[1] = {I * 2};
     uint32_t box[2] = {kBK, 16};
     if (!make_tmap(&tm_h, hp, 2, dims, str, box)) return MOE_ERR_CUDA;
   }
 
   cudaStream_t s = a.stream;
-  {
+  if (g.dense) {
+    const long long chunks = static_cast<long long>(T) * (lw.H / 8);
+    const long long work = chunks > n_counters ? chunks : n_counters;
+    int blocks = static_cast<int>((work + 255) / 256);
+    if (blocks > g.G) blocks = g.G;
+    LaunchScope ls(kProfPrep, s);
+    if (launch_k(ffn_prep_dense_kernel, dim3(blocks), dim3(256), 0, s, a.pdl_first,
+                 static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, lw.H, xp, cnt_gu, n_counters,
+                 a.dev_err) != MOE_OK)
+      return MOE_ERR_CUDA;
+  } else {
     long long chunks = static_cast<long long>(TK) * (lw.H / 8);  // real rows only
     int blocks = static_cast<int>((chunks + 255) / 256);
     if (blocks > g.G * 4) blocks = g.G * 4;
@@ -757,6 +839,9 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.cap = cap;
   tp.NM = g.NM;
   tp.Rmax = g.Rmax;
+  tp.Rh = g.Rh;
+  tp.dense = g.dense;
+  tp.perm_token = a.perm_token;
   tp.n_unique = a.n_unique;
   tp.unique = a.unique;
   tp.offsets = a.offsets;

@@ -203,16 +203,26 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
         sm.vw[t] = bad ? 0.f : sm.wc[t];
       }
       if (bad) continue;
+      // The round results stay in registers (lane j keeps the j-th id) and
+      // reach shared memory after the rounds, so that no lane branches off
+      // between the warp reductions.
+      float v1 = 0.f, vk1 = 0.f;
+      int mine = -1;
+      __syncwarp();
+#pragma unroll 1
       for (int j = 0; j <= k; ++j) {
         float bv;
         int bi;
         routing::argmax_round(r, E, lane, bv, bi);
-        if (lane == 0) {
-          if (j == 0) sm.v1[t] = bv;
-          if (j == k) sm.vk1[t] = bv;
-          if (j < k) sm.member0[t * EW + (bi >> 5)] |= 1u << (bi & 31);
-        }
+        v1 = j == 0 ? bv : v1;
+        vk1 = bv;
+        mine = (lane == j && j < k) ? bi : mine;
       }
+      if (lane == 0) {
+        sm.v1[t] = v1;
+        sm.vk1[t] = vk1;
+      }
+      if (mine >= 0 && mine < E) atomicOr(&sm.member0[t * EW + (mine >> 5)], 1u << (mine & 31));
     }
     const bool conf_bad = __syncthreads_or(my_bad) != 0;
     if (conf_bad) {
@@ -363,14 +373,7 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
       tok += cv[i];
     }
     int nz_ex = nz, tok_ex = tok;
-    for (int off = 1; off < 32; off <<= 1) {
-      const int a = __shfl_up_sync(kFull, nz_ex, off);
-      const int b = __shfl_up_sync(kFull, tok_ex, off);
-      if (lane >= off) {
-        nz_ex += a;
-        tok_ex += b;
-      }
-    }
+    warp_inclusive_sum2(nz_ex, tok_ex, lane);
     nz_ex -= nz;
     tok_ex -= tok;
 #pragma unroll

@@ -89,14 +89,7 @@ __device__ __forceinline__ void union_block(const int32_t* __restrict__ ids, int
       tok += us.count[e];
     }
     int nz_ex = nz, tok_ex = tok;  // inclusive -> exclusive scan
-    for (int off = 1; off < 32; off <<= 1) {
-      int a = __shfl_up_sync(0xFFFFFFFFu, nz_ex, off);
-      int b = __shfl_up_sync(0xFFFFFFFFu, tok_ex, off);
-      if (lane >= off) {
-        nz_ex += a;
-        tok_ex += b;
-      }
-    }
+    warp_inclusive_sum2(nz_ex, tok_ex, lane);
     nz_ex -= nz;
     tok_ex -= tok;
     for (int e = e0; e < e0 + per && e < E; ++e) {

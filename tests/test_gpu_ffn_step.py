@@ -333,3 +333,43 @@ def test_ffn_fuzz_shapes(mv):
         ref = ml.layer_forward(lg, x_decode(cfg)(x_host), k, E, host_experts(cfg, 0))
         err = rowwise_err(y.cpu().numpy().astype(np.float64), ref["y"])
         assert err < TOL[dtype], (trial, dtype, H, I, E, k, T, layout, err)
+
+
+@pytest.mark.parametrize("T", [5, 24, 40])
+def test_ffn_group_order_checked(mv, T):
+    """A union whose token group does not ascend (the union's layout) is
+    flagged, not silently mis-scattered.  T <= 32 runs the token-dense
+    gate/up, which places each token by its rank in the group; T = 40 runs
+    the padded-group path, which reads the group in stored order and so
+    needs no order (it must stay clean)."""
+    from workload import gen
+    H, I, E, k = 256, 192, 8, 4
+    cfg = gen.MoEConfig("order", L=1, H=H, E=E, k=k, I=I, dtype="bf16", seed=3)
+    layer = make_layer(mv, cfg, 0, "tiled")
+    rng = np.random.default_rng(T)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    x_dev = cuda(gen.bf16_bits_rne(rng.standard_normal((T, H)).astype(np.float32)).view(np.int16))
+    dev_err = mv.new_dev_err()
+    ids, w = mv.route(cuda(lg), k, dev_err=dev_err)
+    up = mv.union_permute(ids, E, dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert dev_err.item() == 0
+    off = up["offsets"].cpu().numpy()
+    U = int(up["n_unique"].item())
+    g = next(u for u in range(U) if off[u + 1] - off[u] >= 2)
+    pt = up["perm_token"].clone()
+    a, b = int(off[g]), int(off[g]) + 1
+    pt[a], pt[b] = up["perm_token"][b].item(), up["perm_token"][a].item()
+    inv = up["inv"].clone()
+    for p in (a, b):  # keep inv consistent with the swapped positions
+        t = int(pt[p].item())
+        for j in range(k):
+            if int(ids[t, j].item()) == int(up["unique"][g].item()):
+                inv[t * k + j] = p
+    bad = dict(up, perm_token=pt, inv=inv)
+    mv.verify_ffn(x_dev, k, layer, bad, w, dev_err=dev_err)
+    torch.cuda.synchronize()
+    if T <= 32:
+        assert dev_err.item() & mv._lib.DEV_BAD_ID
+    else:
+        assert dev_err.item() == 0
