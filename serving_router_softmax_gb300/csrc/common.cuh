@@ -51,6 +51,13 @@ int launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaS
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Store with release semantics at GPU scope: writes this thread made, or
+// observed through a barrier, before it are visible to a reader that
+// acquires the stored value.
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void flag_error(int32_t* dev_err, int32_t bits) {
   if (dev_err) atomicOr(dev_err, bits);
 }
@@ -129,10 +136,36 @@ struct FfnArgs {
   int32_t* dev_err;
   cudaStream_t stream;
   bool pdl_first;           // the first FFN kernel may start before the caller's previous kernel ends
+  // Whole step, bf16 tensor-core layers with T <= 32 and resident weights:
+  // the layer-head kernel already copied the token rows and zeroed the
+  // fix-up counters (no prep kernel), and publishes ready_value in
+  // ready_flag once the union is written (see TcParams::ready_flag).
+  bool head_prepared;
+  int32_t* ready_flag;
+  int32_t ready_value;
 };
 size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_validate(const moe_layer_weights& lw, int T, int k);
 int ffn_launch(const FfnArgs& a);
+
+// Work of the bf16 tensor-core FFN's prep kernel that the layer-head kernel
+// can take over (token-dense layers, T <= 32, resident weights): copy the T
+// token rows of x (through the row map) into xd and zero n_counters fix-up
+// counters.  The head then also publishes the union to the gate/up kernel
+// through ready_flag.  ffn_head_prep returns false when the layer does not
+// qualify; the pointers lie in the FFN workspace `ws`.
+struct HeadPrep {
+  const uint16_t* x;        // [rows, H] bf16 bits
+  const int32_t* x_rows;    // token t uses row x_rows[t]
+  int32_t x_rows_limit;
+  int32_t H;
+  uint16_t* xd;             // [T, H]
+  int32_t* counters;
+  int32_t n_counters;
+  int32_t* ready_flag;      // written ready_value (release) once the union is out
+  int32_t ready_value;
+};
+bool ffn_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp);
 
 // Expert staging (layers with an expert pool).
 bool expert_bytes(const moe_layer_weights& lw, size_t* gate_up, size_t* down);
@@ -160,9 +193,11 @@ int union_validate(int T, int k, int E);
 // Fused route + union for one layer of the whole step (single CTA).
 // rows_ready: the row map was complete before the launch (it may be read
 // before the wait on the previous kernel).
+// hp (optional): the FFN prep work and union handshake of HeadPrep, done by
+// extra CTAs of the same launch (CTA 0 routes).
 int layer_head_launch(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets,
                       int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl,
-                      bool rows_ready);
+                      bool rows_ready, const HeadPrep* hp = nullptr);
 int union_launch(const int32_t* ids, int T, int k, int E, int32_t* n_unique, int32_t* unique,
                  int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, int32_t* inv,
                  float* reuse_ratio, int32_t* dev_err, cudaStream_t s);
@@ -195,6 +230,10 @@ struct EcoArgs {
   float* verify_conf;
   int32_t T_expected;
   cudaStream_t stream;
+  // Whole step: the FFN's union-ready word, cleared here at the start of
+  // every step (so that a value left by an interrupted step is never taken
+  // for a fresh one).  NULL: nothing to clear.
+  int32_t* ready_flag;
 };
 int eco_validate(const eco_cfg& c, int nseq);
 int eco_launch(const EcoArgs& a);

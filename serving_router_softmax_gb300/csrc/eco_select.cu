@@ -107,8 +107,9 @@ __global__ void __launch_bounds__(512) eco_kernel(
     const uint32_t* __restrict__ own_fp, const int32_t* __restrict__ gamma_per_seq, int N, int W,
     int gamma_max, int mode, int eps_shift, int fast_key, int32_t* __restrict__ selected,
     int32_t* __restrict__ union_size, int32_t* dev_err, int32_t* __restrict__ verify_rows,
-    float* __restrict__ verify_conf, int T_expected, int nseq) {
+    float* __restrict__ verify_conf, int T_expected, int nseq, int32_t* ready_flag) {
   extern __shared__ uint32_t smem[];
+  if (ready_flag && blockIdx.x == 0 && threadIdx.x == 0) *ready_flag = 0;
   uint32_t* traj = smem;                 // [N][W]
   uint32_t* B = traj + (size_t)N * W;    // [W]
   __shared__ int32_t cost[kMaxN];
@@ -281,8 +282,9 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
     const float* __restrict__ P, const int32_t* __restrict__ parent, const uint32_t* __restrict__ own_fp,
     const int32_t* __restrict__ gamma_per_seq, int N, int W, int nseq, int gamma_max, int eps_shift,
     int32_t* __restrict__ selected, int32_t* __restrict__ union_size, int32_t* dev_err,
-    int32_t* __restrict__ verify_rows, float* __restrict__ verify_conf, int T_expected) {
+    int32_t* __restrict__ verify_rows, float* __restrict__ verify_conf, int T_expected, int32_t* ready_flag) {
   extern __shared__ uint32_t smem[];
+  if (ready_flag && threadIdx.x == 0) *ready_flag = 0;
   const int G = nseq * N;
   uint32_t* traj = smem;               // [G][W]
   uint32_t* B = traj + (size_t)G * W;  // [W]
@@ -453,7 +455,7 @@ int eco_launch(const EcoArgs& a) {
     LaunchScope ls(kProfEco, a.stream);
     eco_batch_kernel<<<1, 512, smem, a.stream>>>(a.P, a.parent, a.own_fp, a.gamma, c.N, c.W, a.nseq, c.gamma_max,
                                                   eps_shift(c.eps), a.selected, a.union_size, a.dev_err,
-                                                  a.verify_rows, a.verify_conf, a.T_expected);
+                                                  a.verify_rows, a.verify_conf, a.T_expected, a.ready_flag);
     return check_launch();
   }
   size_t smem = (static_cast<size_t>(c.N) * c.W + c.W) * sizeof(uint32_t);
@@ -468,7 +470,7 @@ int eco_launch(const EcoArgs& a) {
                                                   (static_cast<long long>(c.W) * 32) << eps_shift(c.eps) < (1ll << 24) - 1,
                                                   a.selected, a.union_size, a.dev_err,
                                                   a.verify_rows, a.verify_conf, a.T_expected,
-                                                  a.nseq);
+                                                  a.nseq, a.ready_flag);
   return check_launch();
 }
 

@@ -60,6 +60,10 @@ int ffn_validate(const moe_layer_weights& lw, int T, int k) {
   return MOE_OK;
 }
 
+bool ffn_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp) {
+  return ffn_tc_head_prep(lw, T, k, ws, hp);
+}
+
 int ffn_launch(const FfnArgs& a) {
   if (a.T == 0) return MOE_OK;
   if (a.ws_bytes < ffn_workspace_bytes(a.lw, a.T, a.k) || !a.ws) return MOE_ERR_WORKSPACE;

@@ -19,6 +19,7 @@ int combine_launch(const FfnArgs& a, const float* o, bool pdl);
 bool ffn_tc_supported(const moe_layer_weights& lw, int T, int k);
 size_t ffn_tc_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_tc_launch(const FfnArgs& a);
+bool ffn_tc_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp);
 
 // Tensor-core path (FP8 E4M3 weights with 128 x 128 block scales).
 bool ffn_fp8_supported(const moe_layer_weights& lw, int T, int k);

@@ -48,6 +48,7 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+constexpr uint64_t kReadyBudgetNs = 100000ull;     // 100 us for the union handshake
 constexpr int kBarRegion = 512;   // mbarriers + flags of the CTA
 static_assert((2 * 12 + 5) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
 
@@ -75,6 +76,15 @@ struct TcParams {
   float* partials;   // [grid][2][2*NM][128] fp32
   int32_t* tile_cnt; // [cap * MT]
   int32_t* dev_err;
+  // Union-ready handshake with the layer-head kernel that gate/up follows
+  // directly (NULL: a prep kernel sits between them and the union is
+  // complete before gate/up starts).  gate/up waits (bounded) until the head
+  // has published ready_value in ready_flag before reading the union ahead
+  // of its dependency wait.  down (whose union is always complete before it
+  // starts) clears ready_clear once gate/up has finished.
+  int32_t* ready_flag;
+  int32_t ready_value;
+  int32_t* ready_clear;
   const int32_t* slot_of;  // expert -> weight slot (NULL: identity)
   int n_slots;
 };
@@ -202,20 +212,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int U = *p.n_unique;
-  const bool valid = U >= 1 && U <= p.cap;
-  if (!valid && blockIdx.x == 0 && threadIdx.x == 0 && U != 0) flag_error(p.dev_err, MOE_DEV_CAPACITY);
   const int MT = (p.M + kBM - 1) / kBM;
   const int KB = p.K / kBK;
   const int KU = (KB + p.KS - 1) / p.KS;  // pipeline units (stages) per tile
-  const long long total = valid ? (long long)U * MT * KU : 0;
-  // Partition over at most `total` CTAs so that every range is non-empty and
-  // the CTAs sharing a tile are exactly the consecutive owners of its k-blocks.
-  const int G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
   const int c = blockIdx.x;
-  const long long s0 = c < G ? total * c / G : total;
-  const long long s1 = c < G ? total * (c + 1) / G : total;
   const int acc_cols = nA * p.NM;
+  int U = 0, G = 0;
+  long long total = 0, s0 = 0, s1 = 0;
+  // Reads the union size and partitions the layer's pipeline units over at
+  // most `total` CTAs, so that every range is non-empty and the CTAs sharing
+  // a tile are exactly the consecutive owners of its k-blocks.  Each role
+  // calls it once the union is visible to it.
+  auto load_partition = [&]() {
+    U = *p.n_unique;
+    const bool valid = U >= 1 && U <= p.cap;
+    total = valid ? (long long)U * MT * KU : 0;
+    G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
+    s0 = c < G ? total * c / G : total;
+    s1 = c < G ? total * (c + 1) / G : total;
+  };
+  if (!p.ready_flag) load_partition();  // complete before this grid started
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -236,6 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int npend = 0;
       bool dep_done = !p.pdl;
       if (dep_done) tc::griddep_launch_dependents();
+      if (p.ready_flag) {
+        // The union comes from the kernel this grid follows directly: read
+        // it early only once the head has published it (acquire), else
+        // (bounded wait ran out) after the dependency wait.
+        if (dep_done || !tc::wait_flag_acquire(p.ready_flag, p.ready_value, kReadyBudgetNs)) {
+          if (!dep_done) {
+            tc::griddep_wait();
+            tc::griddep_launch_dependents();
+            dep_done = true;
+          }
+        }
+        load_partition();
+      }
       auto issue_b = [&](int t, int kb, int nq, int st) {
         uint8_t* sB = base + (size_t)st * stageBytes + aBytes;
         if (kGateUp && p.dense) {
@@ -311,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     tc::griddep_wait();
+    if (p.ready_flag) load_partition();
     if (tc::elect_one()) {
       int stage = 0;
       uint32_t phase = 0;
@@ -380,6 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int etid = threadIdx.x - 64;  // 0..127
     tc::griddep_wait();
+    if (p.ready_flag) load_partition();
+    if (etid == 0 && blockIdx.x == 0 && U != 0 && !(U >= 1 && U <= p.cap)) flag_error(p.dev_err, MOE_DEV_CAPACITY);
+    // down: gate/up has finished, so no CTA still reads the handshake word
+    if (!kGateUp && p.ready_clear && etid == 0 && blockIdx.x == 0) *p.ready_clear = 0;
     int acc = 0;
     uint32_t acc_phase[2] = {0, 0};
     const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
@@ -742,6 +776,25 @@ size_t ffn_tc_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
   return b;
 }
 
+bool ffn_tc_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp) {
+  if (!ffn_tc_supported(lw, T, k) || lw.pool) return false;
+  const TcGeom g = tc_geom(lw, T, k);
+  if (!g.dense) return false;
+  const int TK = T * k;
+  const int cap = lw.E < TK ? lw.E : TK;
+  char* p = static_cast<char*>(ws);
+  hp->xd = reinterpret_cast<uint16_t*>(p);
+  p += align_up(static_cast<size_t>(g.Rmax) * lw.H * 2, 256);
+  p += align_up(static_cast<size_t>(g.Rh) * lw.I * 2, 256);
+  p += align_up(static_cast<size_t>(TK) * lw.H * 4, 256);
+  p += align_up(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4, 256);
+  p += align_up(static_cast<size_t>(cap + 1) * 4, 256);
+  hp->counters = reinterpret_cast<int32_t*>(p);
+  hp->n_counters = cap * (g.MT_gu + g.MT_d);
+  hp->H = lw.H;
+  return true;
+}
+
 int ffn_tc_launch(const FfnArgs& a) {
   const auto& lw = a.lw;
   const int T = a.T, k = a.k, TK = T * k;
@@ -810,7 +863,9 @@ int ffn_tc_launch(const FfnArgs& a) {
   }
 
   cudaStream_t s = a.stream;
-  if (g.dense) {
+  if (a.head_prepared) {
+    // the layer-head kernel copied the token rows and zeroed the counters
+  } else if (g.dense) {
     const long long chunks = static_cast<long long>(T) * (lw.H / 8);
     const long long work = chunks > n_counters ? chunks : n_counters;
     int blocks = static_cast<int>((work + 255) / 256);
@@ -842,6 +897,9 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.Rh = g.Rh;
   tp.dense = g.dense;
   tp.perm_token = a.perm_token;
+  tp.ready_flag = a.head_prepared ? a.ready_flag : nullptr;
+  tp.ready_value = a.ready_value;
+  tp.ready_clear = nullptr;
   tp.n_unique = a.n_unique;
   tp.unique = a.unique;
   tp.offsets = a.offsets;
@@ -889,6 +947,8 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.tmem_cols = pow2_cols(tp.acc_stages * g.NM);
   tp.tile_cnt = cnt_d;
   tp.stall = 0;
+  tp.ready_clear = tp.ready_flag;
+  tp.ready_flag = nullptr;
   if (cudaFuncSetAttribute(ffn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_d)) != cudaSuccess)
     return MOE_ERR_CUDA;

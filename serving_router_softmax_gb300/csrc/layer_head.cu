@@ -10,7 +10,12 @@
 //     group sizes) as they select, so the union needs no scatter pass;
 //   - with the bias, g_e is one expert per thread and E* a rank test (an
 //     expert is in E* when fewer than cap experts beat it), with no serial
-//     selection rounds.
+//     selection rounds;
+//   - optionally (bf16 tensor-core layers with T <= 32), extra CTAs copy the
+//     token rows for the FFN and zero its fix-up counters, and CTA 0
+//     publishes the union to the gate/up kernel (release store) as soon as
+//     it is written, so that kernel can start its weight stream while this
+//     one finishes the permutation.
 // Launched with programmatic dependent launch, so its launch overlaps the
 // previous layer's last kernel.
 #include "common.cuh"
@@ -120,8 +125,31 @@ template <int NPL>
 __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, int32_t* n_unique, int32_t* unique,
                                                                   int32_t* offsets, int32_t* perm_token,
                                                                   int32_t* perm_slot, int32_t* inv,
-                                                                  float* reuse_ratio, int rows_ready) {
+                                                                  float* reuse_ratio, int rows_ready,
+                                                                  HeadPrep hp) {
   extern __shared__ __align__(16) uint8_t head_smem[];
+  if (blockIdx.x > 0) {
+    // ---- FFN prep CTAs.  When this grid starts, the previous layer's FFN
+    // kernels have finished (the kernel it follows starts it only after its
+    // own wait), so the token rows and counters are free to overwrite; only
+    // the row map may still be in flight (first layer).
+    if (!rows_ready) pdl_wait();
+    const long long nth = (long long)(gridDim.x - 1) * blockDim.x;
+    const long long tid = (long long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+    for (long long i = tid; i < hp.n_counters; i += nth) hp.counters[i] = 0;
+    const int cpr = hp.H / 8;  // 16-byte chunks per row
+    for (long long i = tid; i < (long long)ra.cfg.T * cpr; i += nth) {
+      const int t = static_cast<int>(i / cpr);
+      const int ch = static_cast<int>(i - (long long)t * cpr);
+      const long long row = hp.x_rows[t];
+      if (row >= 0 && row < hp.x_rows_limit)
+        *reinterpret_cast<uint4*>(hp.xd + (size_t)t * hp.H + ch * 8) =
+            *reinterpret_cast<const uint4*>(hp.x + (size_t)row * hp.H + ch * 8);
+      else
+        flag_error(ra.dev_err, MOE_DEV_BAD_ID);
+    }
+    return;
+  }
   const moe_route_cfg& c = ra.cfg;
   const int T = c.T, E = c.E, k = c.k, TK = T * k;
   const int EW = (E + 31) >> 5;
@@ -236,6 +264,7 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
         *n_unique = 0;
         *reuse_ratio = 0.f;
         offsets[0] = 0;
+        if (hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);
       }
       return;
     }
@@ -339,6 +368,7 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
       *n_unique = 0;
       *reuse_ratio = 0.f;
       offsets[0] = 0;
+      if (hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);
     }
     return;
   }
@@ -392,6 +422,10 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
       *n_unique = nz_ex;
       *reuse_ratio = TK > 0 ? __fdiv_rn(static_cast<float>(nz_ex), static_cast<float>(TK)) : 0.f;
     }
+    // The union (n_unique, unique, offsets) is out: publish it.  The warp
+    // barrier orders every lane's stores before lane 0's release.
+    __syncwarp();
+    if (lane == 0 && hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);
   }
   __syncthreads();
   // ---- permutation: rank of token t in expert e's group = set bits of
@@ -413,14 +447,25 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
 
 template <int NPL>
 int launch_npl(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets, int32_t* perm_token,
-               int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl, bool rows_ready) {
+               int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl, bool rows_ready,
+               const HeadPrep* hp) {
   const size_t smem = head_smem_bytes(ra.cfg.T, ra.cfg.E, ra.cfg.k);
   if (smem > 48 * 1024 && cudaFuncSetAttribute(layer_head_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)) != cudaSuccess)
     return MOE_ERR_CUDA;
+  HeadPrep h{};
+  int grid = 1;
+  if (hp) {
+    h = *hp;
+    const long long chunks = static_cast<long long>(ra.cfg.T) * (h.H / 8);
+    const long long work = chunks > h.n_counters ? chunks : h.n_counters;
+    long long extra = (work + kHeadThreads - 1) / kHeadThreads;
+    if (extra > 32) extra = 32;
+    grid = 1 + static_cast<int>(extra);
+  }
   LaunchScope ls(kProfRoute, ra.stream);
-  return launch_k(layer_head_kernel<NPL>, dim3(1), dim3(kHeadThreads), smem, ra.stream, pdl, ra, n_unique, unique,
-                  offsets, perm_token, perm_slot, inv, reuse_ratio, rows_ready ? 1 : 0);
+  return launch_k(layer_head_kernel<NPL>, dim3(grid), dim3(kHeadThreads), smem, ra.stream, pdl, ra, n_unique, unique,
+                  offsets, perm_token, perm_slot, inv, reuse_ratio, rows_ready ? 1 : 0, h);
 }
 
 }  // namespace
@@ -428,20 +473,21 @@ int launch_npl(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t*
 // T <= 256, E <= 1024, k <= 16 (checked by the step's validation).
 int layer_head_launch(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets,
                       int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl,
-                      bool rows_ready) {
+                      bool rows_ready, const HeadPrep* hp) {
+  if (hp && (!hp->x || !hp->x_rows || !hp->xd || !hp->counters || hp->H % 8)) return MOE_ERR_ARG;
   if (ra.cfg.T < 1 || ra.cfg.T > routing::kBiasMaxT || ra.cfg.E > 1024) return MOE_ERR_UNSUPPORTED;
   const int npl = (ra.cfg.E + 31) / 32;
   if (npl <= 1)
-    return launch_npl<1>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+    return launch_npl<1>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready, hp);
   if (npl <= 2)
-    return launch_npl<2>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+    return launch_npl<2>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready, hp);
   if (npl <= 4)
-    return launch_npl<4>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+    return launch_npl<4>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready, hp);
   if (npl <= 8)
-    return launch_npl<8>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+    return launch_npl<8>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready, hp);
   if (npl <= 16)
-    return launch_npl<16>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
-  return launch_npl<32>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready);
+    return launch_npl<16>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready, hp);
+  return launch_npl<32>(ra, n_unique, unique, offsets, perm_token, perm_slot, inv, reuse_ratio, pdl, rows_ready, hp);
 }
 
 }  // namespace moe

@@ -4,6 +4,9 @@
 // EcoSpec write-up, section 2: a round drafts a tree, selects gamma nodes and
 // verifies gamma+1 tokens in one target forward; in every MoE layer the
 // verify tokens route to their top-k experts and the union is loaded once.
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 
 namespace moe {
@@ -20,6 +23,7 @@ struct StepWs {
   int32_t* perm_slot;
   int32_t* inv;
   float* ratio;
+  int32_t* ready;  // union-ready word of the head -> gate/up handshake
   void* ffn;
   size_t ffn_bytes;
 };
@@ -35,7 +39,7 @@ size_t step_ws(const moe_step_cfg& c, void* base, StepWs* out) {
   };
   size_t o_rows = take(T * 4), o_conf = take(T * 4), o_ids = take(TK * 4), o_w = take(TK * 4);
   size_t o_u = take(cap * 4), o_off = take((cap + 1) * 4), o_pt = take(TK * 4), o_ps = take(TK * 4);
-  size_t o_inv = take(TK * 4), o_ratio = take(4);
+  size_t o_inv = take(TK * 4), o_ratio = take(4), o_ready = take(4);
   moe_layer_weights lw{c.H, c.I, c.E, c.dtype, c.layout, nullptr, nullptr, nullptr, nullptr};
   size_t fb = ffn_workspace_bytes(lw, c.T, c.k);
   size_t o_ffn = take(fb);
@@ -51,6 +55,7 @@ size_t step_ws(const moe_step_cfg& c, void* base, StepWs* out) {
     out->perm_slot = reinterpret_cast<int32_t*>(b + o_ps);
     out->inv = reinterpret_cast<int32_t*>(b + o_inv);
     out->ratio = reinterpret_cast<float*>(b + o_ratio);
+    out->ready = reinterpret_cast<int32_t*>(b + o_ready);
     out->ffn = b + o_ffn;
     out->ffn_bytes = fb;
   }
@@ -122,19 +127,37 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
   step_ws(c, workspace, &ws);
 
   EcoArgs ea{P, parent, own_fp, c.nseq, gamma_per_seq, {c.N, c.W, c.gamma_max, c.mode, c.eps},
-             selected, union_size, dev_err, ws.verify_rows, ws.verify_conf, c.T, s};
+             selected, union_size, dev_err, ws.verify_rows, ws.verify_conf, c.T, s, ws.ready};
   if ((st = eco_launch(ea)) != MOE_OK) return st;
 
+  // Test hook for the handshake's fallback (no fault is involved): with
+  // MOE_TEST_STALL=ready_flag the heads never publish the union, so every
+  // gate/up launch waits out its bounded handshake and reads the union after
+  // its dependency wait instead; results are unchanged.
+  const char* stall = std::getenv("MOE_TEST_STALL");
+  const bool stall_ready = stall && std::strcmp(stall, "ready_flag") == 0;
   const int rows = c.nseq * (c.N + 1);
   const size_t xelem = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
   for (int l = 0; l < c.L; ++l) {
     RouteArgs ra{node_logits + static_cast<size_t>(l) * rows * c.E, ws.verify_rows, rows,
                  c.use_bias ? ws.verify_conf : nullptr, {c.T, c.E, c.k, c.use_bias, c.cap, c.alpha},
                  ws.ids, ws.w, dev_err, s};
+    const char* xl = static_cast<const char*>(node_x) + static_cast<size_t>(l) * rows * c.H * xelem;
+    // bf16 tensor-core layers with T <= 32 and resident weights: the head
+    // also does the FFN's prep work and hands the union to gate/up directly.
+    HeadPrep hp{};
+    const bool head_prep = ffn_head_prep(layers[l], c.T, c.k, ws.ffn, &hp);
+    if (head_prep) {
+      hp.x = reinterpret_cast<const uint16_t*>(xl);
+      hp.x_rows = ws.verify_rows;
+      hp.x_rows_limit = rows;
+      hp.ready_flag = stall_ready ? nullptr : ws.ready;
+      hp.ready_value = l + 1;
+    }
     // The verify rows come from the selection kernel, which the first layer's
     // head follows directly; later heads may read them before their wait.
     if ((st = layer_head_launch(ra, n_unique + l, ws.unique, ws.offsets, ws.perm_token, ws.perm_slot, ws.inv,
-                                ws.ratio, true, l > 0)) != MOE_OK)
+                                ws.ratio, true, l > 0, head_prep ? &hp : nullptr)) != MOE_OK)
       return st;
     // Expert residency: the union's cold experts are staged into HBM before
     // the FFN's prep kernel, whose wait then covers the copies (the FFN's
@@ -142,10 +165,9 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     if (layers[l].pool &&
         (st = stage_launch(layers[l], n_unique + l, ws.unique, nullptr, dev_err, s, true)) != MOE_OK)
       return st;
-    FfnArgs fa{static_cast<const char*>(node_x) + static_cast<size_t>(l) * rows * c.H * xelem,
-               ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
+    FfnArgs fa{xl, ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
                ws.perm_token, ws.inv, ws.w, y + static_cast<size_t>(l) * c.T * c.H, ws.ffn,
-               ws.ffn_bytes, dev_err, s, true};
+               ws.ffn_bytes, dev_err, s, true, head_prep, ws.ready, l + 1};
     if ((st = ffn_launch(fa)) != MOE_OK) return st;
   }
   return MOE_OK;

@@ -66,6 +66,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Waits until the word at `flag` holds `value`, reading it with acquire
+// semantics at GPU scope, so that the writes its publisher made before the
+// matching release are visible afterwards.  Gives up after `budget_ns` and
+// returns false.
+__device__ __forceinline__ bool wait_flag_acquire(const int32_t* flag, int32_t value, uint64_t budget_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == value) return true;
+    if (globaltimer_ns() - t0 > budget_ns) return false;
+    __nanosleep(64);
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

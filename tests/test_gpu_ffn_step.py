@@ -373,3 +373,36 @@ def test_ffn_group_order_checked(mv, T):
         assert dev_err.item() & mv._lib.DEV_BAD_ID
     else:
         assert dev_err.item() == 0
+
+
+@pytest.mark.parametrize("name", ["qwen3_235b_like", "gpt_oss_120b_like", "batched_qwen_like"])
+def test_step_union_handshake_fallback(mv, name, monkeypatch):
+    """bf16 layers with T <= 32 hand each layer's union from the head kernel
+    to the gate/up kernel through a release/acquire word, so gate/up can read
+    it before its dependency wait.  With the test hook the heads never
+    publish: every gate/up waits out its bounded handshake (100 us) and reads
+    the union after its dependency wait.  The step must give the same
+    outputs bit for bit, with no error flagged."""
+    from workload import CONFIGS, gen
+    from workload import device as wdev
+    cfg = CONFIGS[name].replace(**SMALL[name])
+    wl = gen.make_workload(cfg)
+    layers = [make_layer(mv, cfg, l, "tiled") for l in range(cfg.L)]
+    t = wdev.workload_tensors(wl)
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap, alpha=cfg.alpha, layout="tiled")
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    step = mv.VerifyStep(spec, layers)
+    y0 = step(*args).clone()
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    monkeypatch.setenv("MOE_TEST_STALL", "ready_flag")
+    y1 = step(*args).clone()
+    torch.cuda.synchronize()
+    monkeypatch.delenv("MOE_TEST_STALL")
+    assert step.dev_err.item() == 0
+    assert torch.equal(y0, y1)
+    y2 = step(*args)
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0 and torch.equal(y0, y2)
