@@ -286,32 +286,41 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int H, int E
                                                       const float* __restrict__ w,
                                                       const float* __restrict__ o,
                                                       float* __restrict__ y, int32_t* dev_err) {
+  const int TK = T * k;
+  const long long total = (long long)T * (H / 4);
+  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  // All of an item's slot indices and weights, then all of its rows of o,
+  // are requested before the first use, so the loads overlap; the sum still
+  // runs in slot order.  The union size, indices and weights come from the
+  // routing kernels, which finished before the down projection this kernel
+  // follows started (only o is that kernel's result), so the first item's
+  // are read before the wait.
+  int pj[kCombK];
+  float wj[kCombK];
+  auto load_slots = [&](long long i) {
+    const int t = static_cast<int>(i / (H / 4));
+#pragma unroll
+    for (int j = 0; j < kCombK; ++j) {
+      pj[j] = -1;
+      wj[j] = 0.f;
+      if (j < k) {
+        pj[j] = inv[t * k + j];
+        wj[j] = w[t * k + j];
+      }
+    }
+  };
+  const int U = *n_unique;
+  const bool valid = U > 0 && U <= min(E, TK);
+  if (valid && i0 < total) load_slots(i0);
   pdl_wait();
   pdl_trigger();
-  const int TK = T * k;
-  int U = *n_unique;
-  const bool valid = U > 0 && U <= min(E, TK);
-  const long long total = (long long)T * (H / 4);
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
+  for (long long i = i0; i < total; i += stride) {
     const int t = static_cast<int>(i / (H / 4));
     const int c = static_cast<int>(i - (long long)t * (H / 4)) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
-      // All of the token's slot indices and weights, then all of its rows of
-      // o, are requested before the first use, so the loads overlap; the sum
-      // still runs in slot order.
-      int pj[kCombK];
-      float wj[kCombK];
-#pragma unroll
-      for (int j = 0; j < kCombK; ++j) {
-        pj[j] = -1;
-        wj[j] = 0.f;
-        if (j < k) {
-          pj[j] = inv[t * k + j];
-          wj[j] = w[t * k + j];
-        }
-      }
+      if (i != i0) load_slots(i);
       float4 v[kCombK];
 #pragma unroll
       for (int j = 0; j < kCombK; ++j) {

@@ -79,8 +79,9 @@ struct TcParams {
   // Union-ready handshake with the layer-head kernel that gate/up follows
   // directly (NULL: a prep kernel sits between them and the union is
   // complete before gate/up starts).  gate/up waits (bounded) until the head
-  // has published ready_value in ready_flag before reading the union ahead
-  // of its dependency wait.  down (whose union is always complete before it
+  // has published ready_value in the low 16 bits of ready_flag (the union
+  // size in the high bits) before reading the union ahead of its dependency
+  // wait.  down (whose union is always complete before it
   // starts) clears ready_clear once gate/up has finished.
   int32_t* ready_flag;
   int32_t ready_value;
@@ -223,14 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // most `total` CTAs, so that every range is non-empty and the CTAs sharing
   // a tile are exactly the consecutive owners of its k-blocks.  Each role
   // calls it once the union is visible to it.
-  auto load_partition = [&]() {
-    U = *p.n_unique;
+  auto partition = [&](int u) {
+    U = u;
     const bool valid = U >= 1 && U <= p.cap;
     total = valid ? (long long)U * MT * KU : 0;
     G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
     s0 = c < G ? total * c / G : total;
     s1 = c < G ? total * (c + 1) / G : total;
   };
+  auto load_partition = [&]() { partition(*p.n_unique); };
   if (!p.ready_flag) load_partition();  // complete before this grid started
 
   if (warp == 0) {
@@ -256,14 +258,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The union comes from the kernel this grid follows directly: read
         // it early only once the head has published it (acquire), else
         // (bounded wait ran out) after the dependency wait.
-        if (dep_done || !tc::wait_flag_acquire(p.ready_flag, p.ready_value, kReadyBudgetNs)) {
+        // The head publishes the union size with it (bits 16..31), which
+        // saves one dependent read before the first weight load.
+        int32_t word = 0;
+        if (!dep_done && tc::wait_flag_acquire(p.ready_flag, p.ready_value, kReadyBudgetNs, &word)) {
+          partition(static_cast<int>(static_cast<uint32_t>(word) >> 16));
+        } else {
           if (!dep_done) {
             tc::griddep_wait();
             tc::griddep_launch_dependents();
             dep_done = true;
           }
+          load_partition();
         }
-        load_partition();
       }
       auto issue_b = [&](int t, int kb, int nq, int st) {
         uint8_t* sB = base + (size_t)st * stageBytes + aBytes;

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
         *n_unique = 0;
         *reuse_ratio = 0.f;
         offsets[0] = 0;
-        if (hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);
+        if (hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);  // union size 0
       }
       return;
     }
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
       *n_unique = 0;
       *reuse_ratio = 0.f;
       offsets[0] = 0;
-      if (hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);
+      if (hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);  // union size 0
     }
     return;
   }
@@ -422,10 +422,12 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
       *n_unique = nz_ex;
       *reuse_ratio = TK > 0 ? __fdiv_rn(static_cast<float>(nz_ex), static_cast<float>(TK)) : 0.f;
     }
-    // The union (n_unique, unique, offsets) is out: publish it.  The warp
-    // barrier orders every lane's stores before lane 0's release.
+    // The union (n_unique, unique, offsets) is out: publish it, with its size
+    // in the high 16 bits (U <= min(E, T*k) <= 1024).  The warp barrier
+    // orders every lane's stores before lane 0's release.
     __syncwarp();
-    if (lane == 0 && hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value);
+    const int u_total = __shfl_sync(kFull, nz_ex, 31);
+    if (lane == 0 && hp.ready_flag) st_release_gpu(hp.ready_flag, hp.ready_value | (u_total << 16));
   }
   __syncthreads();
   // ---- permutation: rank of token t in expert e's group = set bits of

@@ -152,7 +152,7 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
       hp.x_rows = ws.verify_rows;
       hp.x_rows_limit = rows;
       hp.ready_flag = stall_ready ? nullptr : ws.ready;
-      hp.ready_value = l + 1;
+      hp.ready_value = l % 65535 + 1;  // nonzero, 16 bits, differs from the previous layer's
     }
     // The verify rows come from the selection kernel, which the first layer's
     // head follows directly; later heads may read them before their wait.
@@ -167,7 +167,7 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
       return st;
     FfnArgs fa{xl, ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
                ws.perm_token, ws.inv, ws.w, y + static_cast<size_t>(l) * c.T * c.H, ws.ffn,
-               ws.ffn_bytes, dev_err, s, true, head_prep, ws.ready, l + 1};
+               ws.ffn_bytes, dev_err, s, true, head_prep, ws.ready, l % 65535 + 1};
     if ((st = ffn_launch(fa)) != MOE_OK) return st;
   }
   return MOE_OK;

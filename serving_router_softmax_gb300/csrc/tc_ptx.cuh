@@ -66,16 +66,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// Waits until the word at `flag` holds `value`, reading it with acquire
-// semantics at GPU scope, so that the writes its publisher made before the
-// matching release are visible afterwards.  Gives up after `budget_ns` and
-// returns false.
-__device__ __forceinline__ bool wait_flag_acquire(const int32_t* flag, int32_t value, uint64_t budget_ns) {
+// Waits until the low 16 bits of the word at `flag` hold `value`, reading it
+// with acquire semantics at GPU scope, so that the writes its publisher made
+// before the matching release are visible afterwards; *word gets the whole
+// word.  Gives up after `budget_ns` and returns false.
+__device__ __forceinline__ bool wait_flag_acquire(const int32_t* flag, int32_t value, uint64_t budget_ns,
+                                                  int32_t* word) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     int32_t v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v == value) return true;
+    *word = v;
+    if ((v & 0xFFFF) == value) return true;
     if (globaltimer_ns() - t0 > budget_ns) return false;
     __nanosleep(64);
   }
