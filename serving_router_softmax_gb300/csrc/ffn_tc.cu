@@ -60,6 +60,8 @@ struct TcParams {
   int Rh;            // rows of Hp
   int dense;         // token-dense gate/up (see ffn_tc_dense)
   int tiled;         // weights in the tile-packed layout (else row-major)
+  int tail_rows;     // tiled: rows loaded for the last M-tile when M % 128 leaves it
+                     // partly padding (multiple of 8, < 128), else 0
   int KS;            // k-blocks per pipeline stage (1, or 2 for tiled down)
   int stages;
   int pdl;           // launched with programmatic dependent launch
@@ -161,7 +163,8 @@ __device__ __forceinline__ bool group_mask(const TcParams& p, const Tile& ti, in
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                  const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+                  const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmT,
+                  const TcParams p) {
   constexpr int nA = kGateUp ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -202,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch_desc(&tmA0);
     if (kGateUp) tc::tma_prefetch_desc(&tmA1);
+    if (p.tail_rows) tc::tma_prefetch_desc(&tmT);
     tc::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
@@ -310,14 +314,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nq = KB - kb < p.KS ? KB - kb : p.KS;
           uint8_t* sA = base + (size_t)stage * stageBytes;
           const int nb = (kGateUp && p.dense) ? p.NM : ti.np;  // B rows
-          const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * nb * 128;
+          // The last M-tile of a matrix whose rows stop short of it reads only
+          // its real rows (the tile-packed layout stores the rest as zeros);
+          // the MMA still runs 128 rows and the epilogue drops rows past M.
+          const bool tail = p.tiled && p.tail_rows && ti.m == MT - 1;
+          const int a_rows = tail ? p.tail_rows : kBM;
+          const uint32_t tx = (kGateUp ? 2 : nq) * a_rows * 128 + nq * nb * 128;
           tc::mbar_arrive_expect_tx(&full[stage], tx);
           if (p.tiled) {
             // Tile-packed weights: block (e, m, kb) is contiguous.  gate/up:
             // one 256-row box holds the gate tile then the up tile; down: one
             // box of nq consecutive 16 KB k-blocks.
             const int blk = (ti.ws * MT + ti.m) * KB + kb;
-            if (kGateUp || nq == 2)
+            if (tail) {
+              if (kGateUp) {
+                tc::tma_load_3d(sA, &tmT, 0, 0, blk, &full[stage], polA);
+                tc::tma_load_3d(sA + kABytes, &tmT, 0, kBM, blk, &full[stage], polA);
+              } else {
+                for (int q = 0; q < nq; ++q)
+                  tc::tma_load_3d(sA + q * kABytes, &tmT, 0, 0, blk + q, &full[stage], polA);
+              }
+            } else if (kGateUp || nq == 2)
               tc::tma_load_3d(sA, &tmA0, 0, 0, blk, &full[stage], polA);
             else
               tc::tma_load_3d(sA, &tmA1, 0, 0, blk, &full[stage], polA);
@@ -823,7 +840,14 @@ int ffn_tc_launch(const FfnArgs& a) {
   const int n_counters = cap * (g.MT_gu + g.MT_d);
 
   // Tensor maps (host-side encoding only; nothing is enqueued).
-  CUtensorMap tm_g, tm_u, tm_x, tm_wd, tm_wd1, tm_h;
+  CUtensorMap tm_g, tm_u, tm_x, tm_wd, tm_wd1, tm_h, tm_gt, tm_dt;
+  // rows of the last M-tile worth loading (tiled layout): M - 128 (MT - 1), up to a multiple of 8
+  auto tail_of = [](uint64_t M) -> int {
+    const int r = static_cast<int>(M % kBM);
+    return r == 0 ? 0 : ((r + 7) & ~7) < kBM ? ((r + 7) & ~7) : 0;
+  };
+  const int tail_gu = lw.layout == MOE_LAYOUT_TILED ? tail_of(lw.I) : 0;
+  const int tail_d = lw.layout == MOE_LAYOUT_TILED ? tail_of(lw.H) : 0;
   const uint64_t H = lw.H, I = lw.I, E = weight_slots(lw);  // E: expert slots in the buffers
   const uint64_t KBg = H / kBK, KBd = I / kBK;
   if (lw.layout == MOE_LAYOUT_TILED) {
@@ -832,12 +856,18 @@ int ffn_tc_launch(const FfnArgs& a) {
       uint32_t box[3] = {kBK, 2 * kBM, 1};
       if (!make_tmap(&tm_g, lw.w_gate_up, 3, dims, str, box)) return MOE_ERR_CUDA;
       tm_u = tm_g;  // unused: one box carries both gate and up
+      tm_gt = tm_g;
+      uint32_t boxt[3] = {kBK, static_cast<uint32_t>(tail_gu), 1};
+      if (tail_gu && !make_tmap(&tm_gt, lw.w_gate_up, 3, dims, str, boxt)) return MOE_ERR_CUDA;
     }
     {
       uint64_t dims[3] = {kBK, kBM, E * g.MT_d * KBd}, str[2] = {kBK * 2, kABytes};
       uint32_t box2[3] = {kBK, kBM, 2}, box1[3] = {kBK, kBM, 1};
       if (!make_tmap(&tm_wd, lw.w_down, 3, dims, str, box2)) return MOE_ERR_CUDA;
       if (!make_tmap(&tm_wd1, lw.w_down, 3, dims, str, box1)) return MOE_ERR_CUDA;
+      tm_dt = tm_wd1;
+      uint32_t boxt[3] = {kBK, static_cast<uint32_t>(tail_d), 1};
+      if (tail_d && !make_tmap(&tm_dt, lw.w_down, 3, dims, str, boxt)) return MOE_ERR_CUDA;
     }
   } else {
     uint32_t box[3] = {kBK, kBM, 1};
@@ -852,6 +882,8 @@ int ffn_tc_launch(const FfnArgs& a) {
       if (!make_tmap(&tm_wd, lw.w_down, 3, dims, str, box)) return MOE_ERR_CUDA;
       tm_wd1 = tm_wd;
     }
+    tm_gt = tm_g;  // unused: rows past the matrix read as zeros without traffic
+    tm_dt = tm_wd;
   }
   if (g.dense) {
     // the T token rows; the box's rows past T read as zeros
@@ -940,7 +972,8 @@ int ffn_tc_launch(const FfnArgs& a) {
     return MOE_ERR_CUDA;
   {
     LaunchScope ls(kProfGateUp, s);
-    if (launch_k(ffn_tc_kernel<true>, dim3(g.G), dim3(kThreads), g.smem_gu, s, true, tm_g, tm_u, tm_x, tp) !=
+    tp.tail_rows = tail_gu;
+    if (launch_k(ffn_tc_kernel<true>, dim3(g.G), dim3(kThreads), g.smem_gu, s, true, tm_g, tm_u, tm_x, tm_gt, tp) !=
         MOE_OK)
       return MOE_ERR_CUDA;
   }
@@ -961,7 +994,8 @@ int ffn_tc_launch(const FfnArgs& a) {
     return MOE_ERR_CUDA;
   {
     LaunchScope ls(kProfDown, s);
-    if (launch_k(ffn_tc_kernel<false>, dim3(g.G), dim3(kThreads), g.smem_d, s, true, tm_wd, tm_wd1, tm_h, tp) !=
+    tp.tail_rows = tail_d;
+    if (launch_k(ffn_tc_kernel<false>, dim3(g.G), dim3(kThreads), g.smem_d, s, true, tm_wd, tm_wd1, tm_h, tm_dt, tp) !=
         MOE_OK)
       return MOE_ERR_CUDA;
   }
