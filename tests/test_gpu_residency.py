@@ -281,3 +281,34 @@ def test_pooled_step_in_a_cuda_graph(mv):
     torch.cuda.synchronize()
     assert step.dev_err.item() == 0
     assert torch.equal(step.y, y0)
+
+
+def test_step_mixing_pooled_and_resident_layers(mv):
+    """Resident layers hand their union straight from the head to gate/up
+    (no prep kernel); pooled layers stage their cold experts and keep the
+    prep kernel.  A step that alternates the two equals the all-resident step
+    bit for bit."""
+    from oracle import residency as R
+    from workload import device as wdev
+    from workload import gen
+    from workload import CONFIGS
+    cfg = CONFIGS["qwen3_235b_like"].replace(L=4, H=256, I=192, E=32, k=4)
+    wl = gen.make_workload(cfg)
+    t = wdev.workload_tensors(wl)
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), layout="tiled")
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    resident = [make_layer(mv, cfg, l, "tiled") for l in range(cfg.L)]
+    step = mv.VerifyStep(spec, resident)
+    y_res = step(*args).clone()
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    hot = [R.hot_experts((np.arange(32) * (l + 5)) % 32, 8) for l in range(cfg.L)]
+    pool = mv.ExpertPool([make_layer(mv, cfg, l, "tiled") for l in range(cfg.L)], hot, n_stage=32 - 8)
+    mixed = [resident[0], pool.layers[1], resident[2], pool.layers[3]]
+    mstep = mv.VerifyStep(spec, mixed)
+    for _ in range(2):
+        y_mix = mstep(*args)
+        torch.cuda.synchronize()
+        assert mstep.dev_err.item() == 0
+        assert torch.equal(y_mix, y_res)
