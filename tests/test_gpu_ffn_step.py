@@ -69,6 +69,8 @@ FFN_CASES = [
     ("e4m3", 256, 256, 32, 8, 28),
     ("e4m3", 256, 256, 8, 8, 32),      # every expert, maximum T of the FP8 tensor-core path
     ("e4m3", 384, 256, 16, 2, 40),     # T > 32: CUDA-core FP8 path
+    ("bf16", 256, 192, 32, 4, 32),     # largest T of the token-dense gate/up (N = 32)
+    ("bf16", 256, 192, 32, 4, 33),     # smallest T of the padded-group gate/up
     ("bf16", 128, 64, 1024, 4, 9),     # maximum E
     ("e4m3", 128, 128, 1024, 2, 5),    # maximum E, FP8
 ]
