@@ -379,8 +379,12 @@ int moe_verify_ffn_noalloc(const void* x, int32_t T, int32_t k, const moe_layer_
  *   union_size [nseq] int32 out: |B| after the last round (mode 2: the
  *            union of that sequence's own selected trajectories).
  * Scores are compared exactly: a beats b when
- * P_a * (c_b + eps) > P_b * (c_a + eps), computed in fp64 (exact under the
- * limits below); equal scores go to the lower node index.
+ * P_a * (c_b + eps) > P_b * (c_a + eps) in exact arithmetic.  The kernel
+ * writes P = m * 2^e and c + eps = X * 2^-s with X = c * 2^s + 1, and compares
+ * the integer products m_a * X_b and m_b * X_a (below 2^53) scaled by the
+ * exponent difference; where every X < 2^24 the correctly rounded fp32
+ * quotient P / X serves as a monotone key and only key ties fall back to the
+ * integer comparison.  Equal scores go to the lower node index.
  * Limits: eps = 2^-s with 0 <= s <= 20; W*32*2^s < 2^29; 1 <= N <= 1024;
  * 1 <= W <= 4096; N*W <= 40960; mode 2: nseq*N <= 1024, nseq*N*W <= 40960.
  * Device errors: MOE_DEV_BAD_TREE, MOE_DEV_BAD_PROB (that sequence's
@@ -536,6 +540,19 @@ const char* moe_status_str(int status);
 
 /* Number of kernels the library launched since load (host counter). */
 uint64_t moe_launch_count(void);
+
+/* Test hook, for exercising the failure paths without a fault.  The pages
+ * have no counterpart.  mask is 0 (normal operation, the default) or an OR of:
+ *   MOE_TEST_STALL_GATE_UP     the bf16 gate/up producer issues no copies, so
+ *                              every bounded wait of that launch runs out and
+ *                              the launch reports MOE_DEV_TIMEOUT;
+ *   MOE_TEST_STALL_READY_FLAG  the step's layer heads do not publish the
+ *                              union, so gate/up takes its slower fallback
+ *                              (results unchanged).
+ * Process-wide; read by the host at each launch.  Returns MOE_ERR_ARG for
+ * unknown bits. */
+enum { MOE_TEST_STALL_GATE_UP = 1, MOE_TEST_STALL_READY_FLAG = 2 };
+int moe_test_set_stall(int32_t mask);
 
 /* Library ABI version (major * 100 + minor). */
 int moe_version(void);

@@ -15,6 +15,13 @@ Byte accounting: an expert of hidden size H and intermediate size I stores
 block.  The EcoSpec write-up's figures pin this: a DeepSeek FP8 expert is
 44 MB (section 1), and 0.2 extra experts per layer over 61 MoE layers cost
 about 0.5 GB per round (section 1).
+
+Parity: pinned (tests/test_oracle_step.py: hand-worked two-sequence forest for
+the per-sequence, static and batch-global selections; verify rows root first
+then the selected nodes in selection order; bias confidences 1 for a root and
+the path probability for a node, checked through a hand-derived preferred set
+that other weightings would change; the token-subset switch touching only the
+FFN rows; tests/test_oracle_moe.py: the page's byte arithmetic).
 """
 from __future__ import annotations
 

@@ -15,13 +15,14 @@ DEV_NAN_LOGIT, DEV_BAD_ID, DEV_DUP_ID, DEV_BAD_TREE, DEV_BAD_PROB, DEV_TIMEOUT, 
     0x01, 0x02, 0x04, 0x08, 0x10, 0x20, 0x40)
 DTYPE_F32, DTYPE_BF16, DTYPE_E4M3_B128 = 0, 1, 2
 LAYOUT_ROWMAJOR, LAYOUT_TILED = 0, 1
+TEST_STALL_GATE_UP, TEST_STALL_READY_FLAG = 1, 2
 PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up", "ffn_down",
                 "combine", "router_logits", "s2_expand", "stage_experts"]
 
 EXPORTED = ["s2_expand", "moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
             "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_verify_plan", "moe_profile_begin",
             "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version", "moe_expert_bytes",
-            "moe_stage_experts"]
+            "moe_stage_experts", "moe_test_set_stall"]
 
 
 class S2Cfg(C.Structure):
@@ -120,5 +121,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_launch_count.restype = C.c_uint64
     lib.moe_version.argtypes = []
     lib.moe_version.restype = C.c_int
+    lib.moe_test_set_stall.argtypes = [i32]
+    lib.moe_test_set_stall.restype = C.c_int
     _lib = lib
     return lib

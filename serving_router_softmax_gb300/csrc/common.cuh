@@ -24,6 +24,8 @@ enum ProfClass { kProfEco = 0, kProfRoute = 1, kProfUnion = 2, kProfPrep = 3, kP
                  kProfDown = 5, kProfCombine = 6, kProfRouter = 7, kProfS2 = 8, kProfStage = 9 };
 
 int sm_count();
+// Test-hook bits set by moe_test_set_stall (0 in normal operation).
+int test_stall_mask();
 
 inline int check_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 

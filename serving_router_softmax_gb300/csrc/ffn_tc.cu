@@ -955,12 +955,11 @@ int ffn_tc_launch(const FfnArgs& a) {
   tp.n_slots = weight_slots(lw);
   tp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
   tp.pdl = 1;
-  // Test hook for the failure path (no fault is involved): with
-  // MOE_TEST_STALL=gate_up the gate/up producer issues no copies, every CTA's
-  // bounded wait runs out after its budget, and the launch reports
-  // MOE_DEV_TIMEOUT with the context intact.
-  const char* stall = std::getenv("MOE_TEST_STALL");
-  const bool stall_gu = stall && std::strcmp(stall, "gate_up") == 0;
+  // Test hook for the failure path (no fault is involved): after
+  // moe_test_set_stall(MOE_TEST_STALL_GATE_UP) the gate/up producer issues no
+  // copies, every CTA's bounded wait runs out after its budget, and the
+  // launch reports MOE_DEV_TIMEOUT with the context intact.
+  const bool stall_gu = (test_stall_mask() & MOE_TEST_STALL_GATE_UP) != 0;
 
   // gate/up
   tp.KS = 1;

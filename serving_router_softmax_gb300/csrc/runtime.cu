@@ -10,6 +10,7 @@ namespace moe {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_test_stall{0};
 
 struct Prof {
   std::mutex mu;
@@ -27,6 +28,8 @@ Prof& prof() {
 }
 
 }  // namespace
+
+int test_stall_mask() { return g_test_stall.load(std::memory_order_relaxed); }
 
 int sm_count() {
   static int cached[64] = {0};
@@ -127,4 +130,10 @@ extern "C" const char* moe_status_str(int status) {
 
 extern "C" uint64_t moe_launch_count(void) { return moe::g_launches.load(); }
 
-extern "C" int moe_version(void) { return 101; }
+extern "C" int moe_test_set_stall(int32_t mask) {
+  if (mask & ~(MOE_TEST_STALL_GATE_UP | MOE_TEST_STALL_READY_FLAG)) return MOE_ERR_ARG;
+  moe::g_test_stall.store(mask, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+extern "C" int moe_version(void) { return 102; }

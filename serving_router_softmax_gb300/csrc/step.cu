@@ -130,12 +130,11 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
              selected, union_size, dev_err, ws.verify_rows, ws.verify_conf, c.T, s, ws.ready};
   if ((st = eco_launch(ea)) != MOE_OK) return st;
 
-  // Test hook for the handshake's fallback (no fault is involved): with
-  // MOE_TEST_STALL=ready_flag the heads never publish the union, so every
-  // gate/up launch waits out its bounded handshake and reads the union after
-  // its dependency wait instead; results are unchanged.
-  const char* stall = std::getenv("MOE_TEST_STALL");
-  const bool stall_ready = stall && std::strcmp(stall, "ready_flag") == 0;
+  // Test hook for the handshake's fallback (no fault is involved): after
+  // moe_test_set_stall(MOE_TEST_STALL_READY_FLAG) the heads never publish the
+  // union, so every gate/up launch waits out its bounded handshake and reads
+  // the union after its dependency wait instead; results are unchanged.
+  const bool stall_ready = (test_stall_mask() & MOE_TEST_STALL_READY_FLAG) != 0;
   const int rows = c.nseq * (c.N + 1);
   const size_t xelem = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
   for (int l = 0; l < c.L; ++l) {

@@ -1,5 +1,6 @@
 """Failure path of the expert FFN without any GPU fault: with the test hook
-MOE_TEST_STALL=gate_up the gate/up producer issues no copies, so every bounded
+moe_test_set_stall(MOE_TEST_STALL_GATE_UP) the gate/up producer issues no
+copies, so every bounded
 wait of that launch runs out after its budget (2 s).  The launch must report
 MOE_DEV_TIMEOUT, release its resources and leave the context usable: the next
 call gives the oracle's result."""
@@ -21,7 +22,7 @@ def mv():
     return m
 
 
-def test_stalled_gate_up_reports_timeout_and_recovers(mv, monkeypatch):
+def test_stalled_gate_up_reports_timeout_and_recovers(mv):
     from test_gpu_ffn_step import host_experts, make_layer, rowwise_err, x_decode
     from oracle import moe_layer as ml
     from workload import gen
@@ -39,15 +40,18 @@ def test_stalled_gate_up_reports_timeout_and_recovers(mv, monkeypatch):
     torch.cuda.synchronize()
     assert dev_err.item() == 0
 
-    monkeypatch.setenv("MOE_TEST_STALL", "gate_up")
-    t0 = time.time()
-    mv.verify_ffn(x, cfg.k, layer, up, w, dev_err=dev_err)
-    torch.cuda.synchronize()
-    waited = time.time() - t0
+    lib = L.load()
+    assert lib.moe_test_set_stall(L.TEST_STALL_GATE_UP) == L.MOE_OK
+    try:
+        t0 = time.time()
+        mv.verify_ffn(x, cfg.k, layer, up, w, dev_err=dev_err)
+        torch.cuda.synchronize()
+        waited = time.time() - t0
+    finally:
+        lib.moe_test_set_stall(0)
     assert dev_err.item() & L.DEV_TIMEOUT
     assert 1.5 < waited < 30.0, waited  # the 2 s budget ran out, nothing hung
 
-    monkeypatch.delenv("MOE_TEST_STALL")
     dev_err.zero_()
     y = mv.verify_ffn(x, cfg.k, layer, up, w, dev_err=dev_err)
     torch.cuda.synchronize()

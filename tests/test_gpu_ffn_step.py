@@ -378,7 +378,7 @@ def test_ffn_group_order_checked(mv, T):
 
 
 @pytest.mark.parametrize("name", ["qwen3_235b_like", "gpt_oss_120b_like", "batched_qwen_like"])
-def test_step_union_handshake_fallback(mv, name, monkeypatch):
+def test_step_union_handshake_fallback(mv, name):
     """bf16 layers with T <= 32 hand each layer's union from the head kernel
     to the gate/up kernel through a release/acquire word, so gate/up can read
     it before its dependency wait.  With the test hook the heads never
@@ -399,10 +399,14 @@ def test_step_union_handshake_fallback(mv, name, monkeypatch):
     y0 = step(*args).clone()
     torch.cuda.synchronize()
     assert step.dev_err.item() == 0
-    monkeypatch.setenv("MOE_TEST_STALL", "ready_flag")
-    y1 = step(*args).clone()
-    torch.cuda.synchronize()
-    monkeypatch.delenv("MOE_TEST_STALL")
+    L = mv._lib
+    lib = L.load()
+    assert lib.moe_test_set_stall(L.TEST_STALL_READY_FLAG) == L.MOE_OK
+    try:
+        y1 = step(*args).clone()
+        torch.cuda.synchronize()
+    finally:
+        lib.moe_test_set_stall(0)
     assert step.dev_err.item() == 0
     assert torch.equal(y0, y1)
     y2 = step(*args)
