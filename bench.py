@@ -50,6 +50,10 @@ def parse():
                     help="profiling only: keep the first N layers of the workload (recorded in config)")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: use this many experts per layer (recorded in config)")
+    ap.add_argument("--workloads", default="all", choices=["all", "none"],
+                    help="all: after the headline workload, measure every other workload too")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the headline's sweeps (cost model, reuse bias, residency)")
     ap.add_argument("--cpu-layers", type=int, default=0,
                     help="layers in the CPU oracle sample (0: auto, about 10-30 s)")
     return ap.parse_args()
@@ -228,7 +232,7 @@ def cost_model_and_expansion(mv, cfg, layers, layout, dev, stream, steps=20):
     # nodes by path probability, the selection of a confidence-driven drafter.
     modes = (0, 1, 2, 3) if cfg.nseq > 1 else (0, 1, 3)
     for mode in modes:
-        for g in (0, 1, 2, 3, 4, 6, 8):
+        for g in (0, 1, 2, 3, 4, 5, 6, 8):
             c2 = cfg.replace(gamma=g, mode=0 if mode == 3 else mode, ragged=False)
             wl2 = gen.make_workload(c2)
             t2 = wdev.workload_tensors(wl2, dev)
@@ -395,8 +399,7 @@ def residency_expansion(mv, cfg, layout, dev, expansion, T_cold, hot_frac=0.5):
     n_hot = int(round(hot_frac * cfg.E))
     cold_bits = np.zeros(cfg.W, dtype=np.uint32)
     for l in range(cfg.L):
-        ids = plan.ids[l].reshape(-1).long()
-        hot = set(mv.hot_from_counts(torch.bincount(ids[ids >= 0], minlength=cfg.E).cpu(), n_hot))
+        hot = set(mv.hot_list(plan.ids[l].reshape(-1), cfg.E, n_hot)[0].cpu().tolist())
         for e in range(cfg.E):
             if e not in hot:
                 b = l * cfg.E + e
@@ -494,10 +497,7 @@ def residency_measure(mv, cfg, layers, layout, dev, stream, expansion=None, n_la
     plan_cal = mv.VerifyPlan(spec_cal, dev)
     plan_cal(t_cal["P"], t_cal["parent"], t_cal["own_fp"], t_cal["gamma"], t_cal["logits"])
     torch.cuda.synchronize()
-    counts = []
-    for l in range(cal.L):
-        ids = plan_cal.ids[l].reshape(-1).long()
-        counts.append(torch.bincount(ids[ids >= 0], minlength=cal.E).cpu())
+    prof_ids = [plan_cal.ids[l].reshape(-1).clone() for l in range(cal.L)]
 
     wl2 = gen.make_workload(c2)
     t2 = wdev.workload_tensors(wl2, dev)
@@ -538,7 +538,7 @@ def residency_measure(mv, cfg, layers, layout, dev, stream, expansion=None, n_la
     pts = []
     for frac in fracs:
         n_hot = int(round(frac * c2.E))
-        hot = [mv.hot_from_counts(counts[l], n_hot) for l in range(c2.L)]
+        hot = [mv.hot_list(prof_ids[l], c2.E, n_hot)[0].cpu().tolist() for l in range(c2.L)]
         pool = mv.ExpertPool(host, hot, n_stage=min(c2.E - n_hot, cap_union), device=dev)
         step = mv.VerifyStep(spec, pool.layers, dev)
         ms, stage_ms = timed(step)
@@ -607,22 +607,12 @@ def router_measure(mv, cfg, wl, dev, stream, iters=200):
                      f"({n_mats * per / 2**20:.0f} MiB > L2)"}
 
 
-def ours(args, rank, ws, local):
+def build_layers(mv, cfg, dev):
+    """Device weights of every layer: filled row-major, then (bf16, FP8) packed
+    once into the tiled layout the tensor-core FFN streams; a load-time step
+    outside every timed region."""
     import torch
-
-    import serving_router_softmax_gb300 as mv
-    from workload import CONFIGS, gen
     from workload import device as wdev
-
-    cfg = CONFIGS[args.config]
-    if args.layers:
-        cfg = cfg.replace(L=min(args.layers, cfg.L))
-    if args.experts:
-        cfg = cfg.replace(E=args.experts, cap=min(cfg.cap, args.experts - cfg.k) if cfg.use_bias else cfg.cap)
-    dev = torch.device("cuda", local)
-    wl = gen.make_workload(cfg)
-    # Weights: filled row-major, then packed once into the tiled layout the
-    # tensor-core FFN streams (bf16); a load-time step outside every timed region.
     layout = "tiled" if cfg.dtype in ("bf16", "e4m3") else "rowmajor"
     layers = []
     for l in range(cfg.L):
@@ -634,14 +624,96 @@ def ours(args, rank, ws, local):
             torch.cuda.synchronize()
             torch.cuda.empty_cache()
         layers.append(layer)
+    return layers, layout
+
+
+def step_spec(mv, cfg, wl, layout):
+    return mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k,
+                       H=cfg.H, I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap, alpha=cfg.alpha, layout=layout)
+
+
+def e2e_measure(mv, spec, layers, t, dev, stream, steps, ws, total_bytes):
+    """End to end through the public API with host buffers, as a serving loop
+    runs it: every step's inputs go host -> device from pinned memory and its
+    result comes back device -> host, all inside the timed region.  Two
+    input/output buffer sets: while step s runs (a CUDA graph of the whole
+    step), step s+1's inputs are copied in and step s-1's result is copied out
+    on two copy streams."""
+    import torch
+    names = ("P", "parent", "own_fp", "gamma", "logits", "x")
+    pinned = [{k: t[k].cpu().pin_memory() for k in names} for _ in range(2)]
+    steps2 = [mv.VerifyStep(spec, layers, dev) for _ in range(2)]
+    y_host = [torch.empty(steps2[0].y.shape, dtype=steps2[0].y.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(v.numel() * v.element_size() for v in pinned[0].values())
+    d2h = y_host[0].numel() * y_host[0].element_size()
+    dev_in = [{k: torch.empty_like(t[k]) for k in names} for _ in range(2)]
+    for b in range(2):
+        for k in names:
+            dev_in[b][k].copy_(t[k])
+    graphs = [steps2[b].capture(*[dev_in[b][k] for k in names]) for b in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_run = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def loop(n, start_event=None):
+        if start_event is not None:
+            s_in.wait_event(start_event)
+            s_out.wait_event(start_event)
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_run[b])  # step i-2 has read this input set
+                for k in names:
+                    dev_in[b][k].copy_(pinned[b][k], non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])  # step i-2's result has left this output buffer
+            graphs[b].replay()
+            ev_run[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[b])
+                y_host[b].copy_(steps2[b].y, non_blocking=True)
+                ev_out[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    loop(4)
+    torch.cuda.synchronize()
+    barrier(ws)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    loop(steps, a0)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    for b in range(2):
+        if int(steps2[b].dev_err.item()) != 0:
+            raise SystemExit(f"device error {int(steps2[b].dev_err.item())} in the e2e loop")
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1), ws)
+    del graphs, steps2
+    return {"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms / steps,
+            "loop": "pinned host inputs in and result out every step, double-buffered: the next step's "
+                    "inputs and the previous step's result cross on two copy streams while a step runs "
+                    "(CUDA graph replay)",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, config_name):
+    """The step's measurements on one workload: pass A (headline: CUDA graph
+    replays, clocks sampled), the same steps eager, pass B (events around the
+    FFN gate/up and down launches only: the roofline of each), pass C
+    (events around every launch: the per-kernel breakdown), the control path
+    alone, and the end-to-end loop with host buffers."""
+    import torch
+    from workload import device as wdev
+
     t = wdev.workload_tensors(wl, dev)
-    gmax = int(wl.gamma.max())
-    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k,
-                       H=cfg.H, I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=gmax, mode=cfg.mode,
-                       eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap, alpha=cfg.alpha,
-                       layout=layout)
+    spec = step_spec(mv, cfg, wl, layout)
     step = mv.VerifyStep(spec, layers, dev)
-    stream = torch.cuda.current_stream(dev)
 
     def one():
         step(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
@@ -653,6 +725,7 @@ def ours(args, rank, ws, local):
         raise RuntimeError(f"device error bits {int(step.dev_err.item())}")
     n_unique = step.n_unique.cpu().tolist()
     bytes_step = sum(n_unique) * expert_bytes(cfg)
+    y_first = step.y[0].cpu()
 
     # ---- the step as a CUDA graph: the library's step makes no allocation and
     # no host synchronisation, so one captured step replays with no host
@@ -686,7 +759,6 @@ def ours(args, rank, ws, local):
     # unique-expert bytes per step >> L2; no per-kernel events.
     with ClockSampler(local) as clk:
         ms_local = timed(graph.replay if graph is not None else one)
-    launches = launches_per_step * args.steps
     value, ms_total = job_throughput(bytes_step * args.steps, ms_local, ws)
     ms_step = ms_total / args.steps
     total_bytes = sum_over_ranks(bytes_step * args.steps, ws)
@@ -696,9 +768,9 @@ def ours(args, rank, ws, local):
     if graph is not None:
         del graph
 
-    # ---- pass B: the same K steps with CUDA events around the dominant
-    # kernel only (FFN gate/up), on the stream it runs on.
-    mv.profile_begin(max_launches=args.steps * cfg.L + 16, classes=["ffn_gate_up"])
+    # ---- pass B: the same K steps with CUDA events around the FFN gate/up
+    # and down launches only, on the stream they run on.
+    mv.profile_begin(max_launches=2 * args.steps * cfg.L + 16, classes=["ffn_gate_up", "ffn_down"])
     torch.cuda.synchronize()
     b0 = torch.cuda.Event(enable_timing=True)
     b1 = torch.cuda.Event(enable_timing=True)
@@ -707,7 +779,7 @@ def ours(args, rank, ws, local):
         one()
     b1.record(stream)
     torch.cuda.synchronize()
-    gu = mv.profile_end()["ffn_gate_up"]
+    pb = mv.profile_end()
     ms_pass_b = b0.elapsed_time(b1)
 
     # ---- pass C: per-kernel breakdown (events around every launch).
@@ -737,10 +809,155 @@ def ours(args, rank, ws, local):
     c1.record(stream)
     torch.cuda.synchronize()
     ctrl_ms = c0.elapsed_time(c1) / n_plan
+    del plan
+
+    # ---- roofline of the FFN kernels, from pass B.
+    peak, peak_kind = peaks()
+    lines = {}
+    for cls, per_unit in (("ffn_gate_up", gate_up_bytes(cfg)), ("ffn_down", expert_bytes(cfg) - gate_up_bytes(cfg))):
+        k_ms = pb[cls]["ms"]
+        nb = sum(n_unique) * per_unit * args.steps
+        ach = nb / (k_ms / 1e3) / 1e9 if k_ms > 0 else None
+        lines[cls] = {"bound": "hbm", "kernel": cls, "achieved": ach, "peak": peak, "peak_kind": peak_kind,
+                      "unit": "GB/s", "frac": (ach / peak) if ach else None,
+                      "algorithmic_bytes_per_launch": sum(n_unique) * per_unit / cfg.L,
+                      "avg_launch_us": k_ms * 1e3 / max(pb[cls]["launches"], 1),
+                      "launches": pb[cls]["launches"]}
+    roofline = dict(lines["ffn_gate_up"])
+    traffic_unit = committed_traffic(config_name)
+    roofline["traffic"] = traffic_unit * sum(n_unique) / cfg.L if traffic_unit is not None else None
+    roofline["timed_in"] = "pass B: the K timed steps repeated with events around the FFN launches only"
+    roofline["pass_b_ms_per_step"] = ms_pass_b / args.steps
+    roofline["ffn_down"] = lines["ffn_down"]
+
+    e2e = e2e_measure(mv, spec, layers, t, dev, stream, args.steps, ws, total_bytes)
+    core = {
+        "value": value, "ms_per_step": ms_step, "latency_us": ms_step * 1e3,
+        "tokens_per_s": tokens / (ms_total / 1e3),
+        "unique_experts_per_layer": n_unique, "unique_expert_gb_per_step": bytes_step / 1e9,
+        "frac_of_peak_step": value / peak / ws, "frac_of_8tbs_step": value / 8000.0 / ws,
+        "roofline": roofline,
+        "kernel_ms_per_step": {k: v["ms"] / n_c for k, v in prof.items()},
+        "launch": "CUDA graph replay of the whole step" if graph_error is None else "eager (" + graph_error + ")",
+        "eager_ms_per_step": eager_ms,
+        "control_path_ms": ctrl_ms,
+        "control_path_frac": ctrl_ms / max(ms_step, 1e-9),
+        "control_path_frac_events": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))
+        / n_c / max(ms_step, 1e-9),
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
+    }
+    del step
+    return core, y_first
+
+
+def gamma_sweep(mv, cfg, layers, layout, dev, stream, steps=20):
+    """EcoSpec's draft-budget ablation (write-up section 4.3, gamma 3..6) on
+    the workload, under marginal-cost and static-cost selection: the union per
+    layer, the verify tokens and the step time (CUDA graph replays)."""
+    import torch
+    from workload import gen
+    from workload import device as wdev
+    pts = []
+    for mode in (0, 1):
+        for g in (3, 4, 5, 6):
+            c2 = cfg.replace(gamma=g, mode=mode, ragged=False)
+            wl2 = gen.make_workload(c2)
+            t2 = wdev.workload_tensors(wl2, dev)
+            step = mv.VerifyStep(step_spec(mv, c2, wl2, layout), layers, dev)
+            args = (t2["P"], t2["parent"], t2["own_fp"], t2["gamma"], t2["logits"], t2["x"])
+            for _ in range(3):
+                step(*args)
+            torch.cuda.synchronize()
+            if int(step.dev_err.item()) != 0:
+                raise RuntimeError(f"device error bits {int(step.dev_err.item())}")
+            graph = step.capture(*args)
+            graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            nu = step.n_unique.cpu().tolist()
+            ms = e0.elapsed_time(e1) / steps
+            pts.append({"gamma": g, "selection": ["marginal", "static"][mode], "verify_tokens": int(wl2.T),
+                        "union_per_layer": sum(nu) / len(nu), "ms_per_step": ms,
+                        "gbs": sum(nu) * expert_bytes(c2) / (ms / 1e3) / 1e9})
+            del graph, step
+    return {"points": pts, "batch": cfg.nseq,
+            "note": "every sequence verifies gamma draft nodes; EcoSpec write-up section 4.3 sweeps gamma 3..6"}
+
+
+def workload_entry(core, cfg, wl, extra=None):
+    """The per-workload record of the bench line."""
+    d = {"config": {"layers": cfg.L, "hidden": cfg.H, "experts": cfg.E, "top_k": cfg.k,
+                    "intermediate": cfg.I, "weights": cfg.dtype, "batch": cfg.nseq, "verify_tokens": wl.T,
+                    "gamma": wl.gamma.tolist(), "reuse_bias": cfg.use_bias,
+                    "selection": "marginal" if cfg.mode == 0 else "static"}}
+    for k in ("value", "ms_per_step", "latency_us", "tokens_per_s", "unique_expert_gb_per_step",
+              "frac_of_peak_step", "frac_of_8tbs_step", "eager_ms_per_step", "control_path_ms",
+              "control_path_frac", "kernel_ms_per_step", "clocks", "e2e", "launches_per_step"):
+        d[k] = core[k]
+    d["unit"] = "GB/s"
+    d["union_per_layer"] = sum(core["unique_experts_per_layer"]) / len(core["unique_experts_per_layer"])
+    r = core["roofline"]
+    d["roofline"] = {"gate_up_frac": r["frac"], "gate_up_gbs": r["achieved"],
+                     "down_frac": r["ffn_down"]["frac"], "down_gbs": r["ffn_down"]["achieved"],
+                     "peak": r["peak"], "peak_kind": r["peak_kind"], "traffic": r["traffic"]}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def other_workloads(mv, args, rank, ws, local, skip):
+    """Every workload other than the headline one, each measured alone (its
+    weights built, measured and freed before the next)."""
+    import torch
+    from workload import CONFIGS, gen
+    out = {}
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    for name, cfg in CONFIGS.items():
+        if name == skip:
+            continue
+        wl = gen.make_workload(cfg)
+        layers, layout = build_layers(mv, cfg, dev)
+        core, _ = measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, name)
+        extra = None
+        if rank == 0 and cfg.nseq > 1:
+            extra = {"gamma_sweep": gamma_sweep(mv, cfg, layers, layout, dev, stream)}
+        out[name] = workload_entry(core, cfg, wl, extra)
+        del layers
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+def ours(args, rank, ws, local):
+    import torch
+
+    import serving_router_softmax_gb300 as mv
+    from workload import CONFIGS, gen
+
+    cfg = CONFIGS[args.config]
+    if args.layers:
+        cfg = cfg.replace(L=min(args.layers, cfg.L))
+    if args.experts:
+        cfg = cfg.replace(E=args.experts, cap=min(cfg.cap, args.experts - cfg.k) if cfg.use_bias else cfg.cap)
+    dev = torch.device("cuda", local)
+    wl = gen.make_workload(cfg)
+    layers, layout = build_layers(mv, cfg, dev)
+    stream = torch.cuda.current_stream(dev)
+    core, y_first = measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, args.config)
+    profiling = bool(args.layers or args.experts)
 
     # ---- verify-cost model check and S2-MoE expansion (rank 0 only).
     cost_model, expansion = (None, None)
-    if rank == 0 and not args.layers and not args.experts:
+    if rank == 0 and not profiling and not args.quick:
         cost_model, expansion = cost_model_and_expansion(mv, cfg, layers, layout, dev, stream)
 
     # ---- router logits, timed alone (the step routes the given node logits).
@@ -748,104 +965,28 @@ def ours(args, rank, ws, local):
 
     # ---- S2-MoE reuse-bias sweep (rank 0 only).
     bias_sweep = None
-    if rank == 0 and not args.layers and not args.experts:
+    if rank == 0 and not profiling and not args.quick:
         bias_sweep = reuse_bias_sweep(mv, cfg, layers, layout, dev, stream)
+
+    # ---- draft-budget sweep on batched workloads (rank 0 only).
+    gsweep = None
+    if rank == 0 and cfg.nseq > 1 and not profiling:
+        gsweep = gamma_sweep(mv, cfg, layers, layout, dev, stream)
 
     # ---- expert residency with on-demand staging from Grace memory (rank 0 only).
     residency = None
-    if rank == 0 and not args.no_residency and (args.residency or (not args.layers and not args.experts)):
+    if rank == 0 and not args.no_residency and (args.residency or (not profiling and not args.quick)):
         fracs = tuple(float(v) for v in args.residency_fracs.split(","))
         residency = residency_measure(mv, cfg, layers, layout, dev, stream, expansion, fracs=fracs)
 
-    # ---- roofline of the dominant kernel (FFN gate/up), from pass B.
-    gu_bytes = sum(n_unique) * gate_up_bytes(cfg) * args.steps
-    gu_ms = gu["ms"]
-    achieved = gu_bytes / (gu_ms / 1e3) / 1e9 if gu_ms > 0 else None
-    peak, peak_kind = peaks()
-    traffic_unit = committed_traffic(args.config)
-    traffic = None
-    if traffic_unit is not None and gu["launches"]:
-        traffic = traffic_unit * sum(n_unique) / cfg.L
-    roofline = {"bound": "hbm", "kernel": "ffn_gate_up", "achieved": achieved, "peak": peak,
-                "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": (achieved / peak) if achieved else None,
-                "traffic": traffic,
-                "algorithmic_bytes_per_launch": sum(n_unique) * gate_up_bytes(cfg) / cfg.L,
-                "avg_launch_us": gu_ms * 1e3 / max(gu["launches"], 1),
-                "launches": gu["launches"],
-                "timed_in": "pass B: the K timed steps repeated with events around gate/up only",
-                "pass_b_ms_per_step": ms_pass_b / args.steps}
-    step_frac = value / peak / ws
-
-    # ---- end to end through the public API with host buffers, as a serving
-    # loop runs it: every step's inputs go host -> device from pinned memory
-    # and its result comes back device -> host, all inside the timed region.
-    # Two input/output buffer sets: while step s runs (a CUDA graph of the
-    # whole step), step s+1's inputs are copied in and step s-1's result is
-    # copied out on two copy streams.
-    names = ("P", "parent", "own_fp", "gamma", "logits", "x")
-    pinned = [{k: t[k].cpu().pin_memory() for k in names} for _ in range(2)]
-    steps2 = [step, mv.VerifyStep(spec, layers, dev)]
-    y_host = [torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory() for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in pinned[0].values())
-    d2h = y_host[0].numel() * y_host[0].element_size()
-    dev_in = [{k: torch.empty_like(t[k]) for k in names} for _ in range(2)]
-    for b in range(2):
-        for k in names:
-            dev_in[b][k].copy_(t[k])
-    e2e_graphs = [steps2[b].capture(*[dev_in[b][k] for k in names]) for b in range(2)]
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_run = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-
-    def e2e_loop(n, start_event=None):
-        if start_event is not None:
-            s_in.wait_event(start_event)
-            s_out.wait_event(start_event)
-        for i in range(n):
-            b = i & 1
-            with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_run[b])  # step i-2 has read this input set
-                for k in names:
-                    dev_in[b][k].copy_(pinned[b][k], non_blocking=True)
-                ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_out[b])  # step i-2's result has left this output buffer
-            e2e_graphs[b].replay()
-            ev_run[b].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_run[b])
-                y_host[b].copy_(steps2[b].y, non_blocking=True)
-                ev_out[b].record(s_out)
-        stream.wait_stream(s_in)
-        stream.wait_stream(s_out)
-
-    e2e_loop(4)
-    torch.cuda.synchronize()
-    barrier(ws)
-    a0 = torch.cuda.Event(enable_timing=True)
-    a1 = torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    e2e_loop(args.steps, a0)
-    a1.record(stream)
-    torch.cuda.synchronize()
-    for b in range(2):
-        if int(steps2[b].dev_err.item()) != 0:
-            raise SystemExit(f"device error {int(steps2[b].dev_err.item())} in the e2e loop")
-    e2e_ms = max_over_ranks(a0.elapsed_time(a1), ws)
-    e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
-
     result = {
         "metric": "verify-step HBM GB/s on unique-expert bytes",
-        "value": value,
+        "value": core["value"],
         "unit": "GB/s",
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_step,
+        "ms_per_step": core["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -860,34 +1001,25 @@ def ours(args, rank, ws, local):
                    "weight_layout": layout,
                    "l2": "inputs larger than L2 (unique-expert bytes per step >> 129 MB)",
                    "parallelism": "replicas" if ws > 1 else "single-gpu"},
-        "latency_us": ms_step * 1e3,
-        "tokens_per_s": tokens / (ms_total / 1e3),
-        "unique_experts_per_layer": n_unique,
-        "unique_expert_gb_per_step": bytes_step / 1e9,
-        "frac_of_peak_step": step_frac,
-        "frac_of_8tbs_step": value / 8000.0 / ws,
-        "roofline": roofline,
-        "kernel_ms_per_step": {k: v["ms"] / n_c for k, v in prof.items()},
-        "launch": "CUDA graph replay of the whole step" if graph_error is None else "eager (" + graph_error + ")",
-        "eager_ms_per_step": eager_ms,
-        "control_path_ms": ctrl_ms,
-        "control_path_frac": ctrl_ms / max(ms_step, 1e-9),
-        "control_path_frac_events": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))
-        / n_c / max(ms_step, 1e-9),
-        "clocks": clk.summary(),
-        "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms / args.steps,
-                "loop": "pinned host inputs in and result out every step, double-buffered: the next step's "
-                        "inputs and the previous step's result cross on two copy streams while a step runs "
-                        "(CUDA graph replay)",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches,
-        "router_logits": router,
-        "cost_model": cost_model,
-        "s2_expand": expansion,
-        "residency": residency,
-        "reuse_bias": bias_sweep,
     }
-    return result, wl, cfg
+    for k in ("latency_us", "tokens_per_s", "unique_experts_per_layer", "unique_expert_gb_per_step",
+              "frac_of_peak_step", "frac_of_8tbs_step", "roofline", "kernel_ms_per_step", "launch",
+              "eager_ms_per_step", "control_path_ms", "control_path_frac", "control_path_frac_events",
+              "clocks", "e2e", "gpu_launches"):
+        result[k] = core[k]
+    result.update({"router_logits": router, "cost_model": cost_model, "s2_expand": expansion,
+                   "residency": residency, "reuse_bias": bias_sweep, "gamma_sweep": gsweep})
+    head_entry = workload_entry(core, cfg, wl, {"gamma_sweep": gsweep} if gsweep else None)
+    del layers
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # ---- every other workload, measured the same way (the headline stays
+    # the configuration named above).
+    if args.workloads == "all" and not profiling:
+        result["workloads"] = {cfg.name: head_entry}
+        result["workloads"].update(other_workloads(mv, args, rank, ws, local, skip=cfg.name))
+    return result, wl, cfg, y_first
 
 
 # ---------------------------------------------------------------------- oracle
@@ -923,17 +1055,35 @@ def oracle_run(cfg, wl, n_layers, stored):
 
     x_dec = (lambda a: np.asarray(a, np.float32).astype(np.float64)) if cfg.dtype == "f32" else ml.decode_bf16
     t0 = time.perf_counter()
-    ovs.run_step(wl, lambda l: (lambda e: ml.expert_matrices(stored[(l, e)], cfg.dtype)),
-                 layers=list(range(n_layers)), x_decode=x_dec)
-    return time.perf_counter() - t0
+    out = ovs.run_step(wl, lambda l: (lambda e: ml.expert_matrices(stored[(l, e)], cfg.dtype)),
+                       layers=list(range(n_layers)), x_decode=x_dec)
+    return time.perf_counter() - t0, out["layers"][0]["y"]
 
 
 def oracle_baseline(cfg, wl, n_layers, target_s=12.0, max_reps=200):
+    """Repeats the oracle sample for about target_s seconds; returns the time,
+    the unique-expert bytes covered, the repetitions and the oracle's layer-0
+    output of the last repetition."""
     stored, nbytes = oracle_prepare(cfg, wl, n_layers)
-    times = []
+    times, y = [], None
     while sum(times) < target_s and len(times) < max_reps:
-        times.append(oracle_run(cfg, wl, n_layers, stored))
-    return sum(times), nbytes * len(times), len(times)
+        dt, y = oracle_run(cfg, wl, n_layers, stored)
+        times.append(dt)
+    return sum(times), nbytes * len(times), len(times), y
+
+
+def ffn_errors(y, ref, dtype):
+    """FFN output error of the GPU step against the oracle on the same layer:
+    row-wise normwise max_t |y_t - ref_t|_inf / |ref_t|_inf (the bound the
+    parity tests hold), and element-wise max |y - ref| / max(|ref|, rms(ref))
+    (each element's error relative to its own size, floored at the layer's
+    rms so that near-zero outputs do not blow it up)."""
+    den = np.max(np.abs(ref), axis=1)
+    den = np.where(den == 0, 1.0, den)
+    row = float(np.max(np.max(np.abs(y - ref), axis=1) / den))
+    rms = float(np.sqrt(np.mean(ref * ref))) or 1.0
+    elem = float(np.max(np.abs(y - ref) / np.maximum(np.abs(ref), rms)))
+    return {"rowwise": row, "elementwise_rms_floor": elem, "bound": 1e-4 if dtype == "f32" else 2e-2}
 
 
 def cpu_threads():
@@ -956,7 +1106,7 @@ def reference(args, rank, ws):
     stored, nbytes = oracle_prepare(cfg, wl, n_layers)
     times = []
     for i in range(args.warmup + args.steps):
-        dt = oracle_run(cfg, wl, n_layers, stored)
+        dt, _ = oracle_run(cfg, wl, n_layers, stored)
         if i >= args.warmup:
             times.append(dt)
     tot = sum(times)
@@ -985,13 +1135,15 @@ def main():
             print(json.dumps(res))
         return
     rank, ws, local = dist_setup(args.gpus)
-    res, wl, cfg = ours(args, rank, ws, local)
+    res, wl, cfg, y_first = ours(args, rank, ws, local)
     if rank == 0 and not args.no_cpu_baseline:
         n_layers = args.cpu_layers or 1
-        dt, nbytes, reps = oracle_baseline(cfg, wl, n_layers)
+        dt, nbytes, reps, y_oracle = oracle_baseline(cfg, wl, n_layers)
         res["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cpu_threads(),
                                "kind": "oracle",
-                               "sample": f"oracle verify step on layer(s) 0..{n_layers - 1} of {cfg.L}, all {wl.T} verify tokens, repeated {reps}x: {dt:.1f} s"}
+                               "sample": f"oracle verify step on layer(s) 0..{n_layers - 1} of {cfg.L}, all {wl.T} verify tokens, repeated {reps}x: {dt:.1f} s",
+                               "parity_layer0": ffn_errors(y_first.numpy().astype(np.float64), y_oracle,
+                                                           cfg.dtype)}
     if rank == 0:
         print(json.dumps(res))
     if ws > 1:

@@ -11,6 +11,7 @@
  *   moe_verify_step    all of the above for L layers in one call
  *   moe_verify_plan    the step's selection and per-layer routing/union only
  *   moe_stage_experts  copies a layer's cold experts of the union from host memory
+ *   moe_hot_list       hot-expert list (and home-slot table) from profiled routing
  *   s2_expand          S2-MoE utility-driven draft expansion
  *
  * Conventions shared by every entry point
@@ -290,6 +291,30 @@ size_t moe_expert_bytes(const moe_layer_weights* lw, size_t* gate_up_bytes, size
 int moe_stage_experts(const moe_layer_weights* lw, const int32_t* n_unique, const int32_t* unique,
                       int32_t* n_staged, int32_t* dev_err, void* stream);
 
+/*
+ * moe_hot_list -- the hot-expert list of expert-level residency.
+ *
+ * Defined by: S2-MoE write-up, "system implementation: expert-level
+ * offloading" (frequently activated experts stay resident; the list comes
+ * from offline profiling of activation frequencies).  Reading: counts[e] is
+ * the number of entries of ids equal to e; the hot list is the n_hot experts
+ * with the largest counts, equal counts going to the lower id, written to
+ * hot[] in ascending id order; home_slot[e] = first_slot + j for hot[j] and
+ * -1 for every other expert (the home-slot table of moe_expert_pool, with
+ * layer l's hot experts at first_slot = l * n_hot).
+ *
+ *   ids        [n_ids] int32 profiled routing decisions (expert ids, any
+ *              layout; -1 entries are ignored).  0 <= n_ids <= 2^31 - 1.
+ *   E          experts, 1..4096.   n_hot  0..E.   first_slot >= 0.
+ *   counts     [E] int32 out, optional (NULL: not written).
+ *   hot        [n_hot] int32 out (may be NULL when n_hot = 0).
+ *   home_slot  [E] int32 out, optional.
+ * One CTA; a load-time step, not on the verify path.
+ * Device errors: MOE_DEV_BAD_ID (an id outside [-1, E): not counted).
+ */
+int moe_hot_list(const int32_t* ids, int64_t n_ids, int32_t E, int32_t n_hot, int32_t first_slot,
+                 int32_t* counts, int32_t* hot, int32_t* home_slot, int32_t* dev_err, void* stream);
+
 /* Bytes of workspace moe_verify_ffn needs for T tokens with top-k routing. */
 size_t moe_verify_ffn_workspace(const moe_layer_weights* lw, int32_t T, int32_t k);
 
@@ -527,10 +552,11 @@ int moe_verify_plan(const moe_step_cfg* cfg, const float* P, const int32_t* pare
  * synchronises those events (host blocking) and writes, per kernel class, the
  * summed milliseconds and the launch count.  Classes: 0 eco_select, 1 route,
  * 2 union/permute, 3 FFN prep, 4 FFN gate/up, 5 FFN down, 6 combine,
- * 7 router logits, 8 S2-MoE expansion, 9 expert staging.
+ * 7 router logits, 8 S2-MoE expansion, 9 expert staging, 10 hot list,
+ * 11 depth policy.
  * Not for use under stream capture.
  */
-enum { MOE_PROF_CLASSES = 10 };
+enum { MOE_PROF_CLASSES = 12 };
 int moe_profile_begin(int32_t max_launches, int32_t class_mask);
 int moe_profile_end(float* ms_per_class, int32_t* launches_per_class, int32_t n_classes);
 

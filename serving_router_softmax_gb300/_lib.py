@@ -17,12 +17,12 @@ DTYPE_F32, DTYPE_BF16, DTYPE_E4M3_B128 = 0, 1, 2
 LAYOUT_ROWMAJOR, LAYOUT_TILED = 0, 1
 TEST_STALL_GATE_UP, TEST_STALL_READY_FLAG = 1, 2
 PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up", "ffn_down",
-                "combine", "router_logits", "s2_expand", "stage_experts"]
+                "combine", "router_logits", "s2_expand", "stage_experts", "hot_list", "depth_policy"]
 
 EXPORTED = ["s2_expand", "moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
             "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_verify_plan", "moe_profile_begin",
             "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version", "moe_expert_bytes",
-            "moe_stage_experts", "moe_test_set_stall"]
+            "moe_stage_experts", "moe_test_set_stall", "moe_hot_list"]
 
 
 class S2Cfg(C.Structure):
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_expert_bytes.restype = sz
     lib.moe_stage_experts.argtypes = [P(LayerWeights), vp, vp, vp, vp, vp]
     lib.moe_stage_experts.restype = C.c_int
+    lib.moe_hot_list.argtypes = [vp, C.c_int64, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.moe_hot_list.restype = C.c_int
     lib.moe_verify_ffn_workspace.argtypes = [P(LayerWeights), i32, i32]
     lib.moe_verify_ffn_workspace.restype = sz
     lib.moe_verify_ffn.argtypes = [vp, i32, i32, P(LayerWeights), vp, vp, vp, vp, vp, vp, vp, vp,

@@ -104,14 +104,21 @@ def expert_bytes(layer: ExpertLayer):
     return gu.value, dn.value
 
 
-def hot_from_counts(counts: torch.Tensor, n_hot: int) -> List[int]:
-    """Hot list from profiled activation counts [E]: the n_hot largest counts, equal counts to the
-    lower expert id; returned in ascending id order."""
-    E = counts.numel()
+def hot_list(ids: torch.Tensor, E: int, n_hot: int, first_slot: int = 0, dev_err=None, stream=None):
+    """Hot-expert list from profiled routing decisions (moe_hot_list): returns device int32
+    tensors (hot [n_hot] in ascending id order, counts [E], home_slot [E])."""
     if not 0 <= n_hot <= E:
         raise MoEError("n_hot outside [0, E]")
-    order = torch.sort(-counts.to(torch.int64).cpu(), stable=True).indices[:n_hot]
-    return sorted(int(e) for e in order)
+    ids = ids.contiguous()
+    if ids.dtype != torch.int32:
+        raise MoEError("ids must be int32")
+    dev = ids.device
+    hot = torch.empty(max(n_hot, 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    home = torch.empty(E, dtype=torch.int32, device=dev)
+    _check(L.load().moe_hot_list(_ptr(ids), ids.numel(), E, n_hot, first_slot, _ptr(counts), _ptr(hot),
+                                 _ptr(home), _ptr(dev_err), _stream(stream)), "moe_hot_list")
+    return hot[:n_hot], counts, home
 
 
 class HostExperts:

@@ -21,7 +21,8 @@ struct LaunchScope {
 };
 
 enum ProfClass { kProfEco = 0, kProfRoute = 1, kProfUnion = 2, kProfPrep = 3, kProfGateUp = 4,
-                 kProfDown = 5, kProfCombine = 6, kProfRouter = 7, kProfS2 = 8, kProfStage = 9 };
+                 kProfDown = 5, kProfCombine = 6, kProfRouter = 7, kProfS2 = 8, kProfStage = 9,
+                 kProfHot = 10, kProfDepth = 11 };
 
 int sm_count();
 // Test-hook bits set by moe_test_set_stall (0 in normal operation).

@@ -80,7 +80,10 @@ def test_staged_ffn_matches_resident_and_oracle(mv, dtype, H, I, E, k, T, layout
     ids_prof, _ = ml.route(lg_prof, k)
     n_hot = int(round(frac * E))
     hot = R.hot_experts(R.activation_counts(ids_prof, E), n_hot)
-    assert mv.hot_from_counts(torch.from_numpy(R.activation_counts(ids_prof, E)), n_hot) == hot
+    hot_dev, counts_dev, home_dev = mv.hot_list(cuda(ids_prof.astype(np.int32).reshape(-1)), E, n_hot)
+    assert hot_dev.cpu().tolist() == hot
+    assert counts_dev.cpu().tolist() == R.activation_counts(ids_prof, E).tolist()
+    assert home_dev.cpu().tolist() == R.home_slots(hot, E).tolist()
     pool = mv.ExpertPool([layer], [hot], n_stage=E - n_hot)
     # The pooled FFN must not read the original device copy.
     layer.gate_up.zero_()
