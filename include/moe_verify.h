@@ -13,6 +13,7 @@
  *   moe_stage_experts  copies a layer's cold experts of the union from host memory
  *   moe_hot_list       hot-expert list (and home-slot table) from profiled routing
  *   s2_expand          S2-MoE utility-driven draft expansion
+ *   moe_depth_policy   confidence-gated depth per sequence (ragged speculation)
  *
  * Conventions shared by every entry point
  *   - Every array argument is a DEVICE pointer owned by the caller, unless a
@@ -510,6 +511,56 @@ typedef struct {
 int s2_expand(const float* P, const int32_t* parent, const uint32_t* own_fp, int32_t nseq,
               const s2_cfg* cfg, int32_t* selected, int32_t* n_selected, int32_t* union_size,
               int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------- depth policy
+ * moe_depth_policy -- the confidence-gated depth vector of ragged
+ * speculation: how many draft positions each sequence of the batch should
+ * verify this step.
+ *
+ * Defined by: the width-vs-depth note, section 2 ("where to spend depth"):
+ * choose the depth vector d that maximises the expected batch throughput,
+ * first one batch-common depth from the live sequences' confidences, then
+ * greedy truncation of single sequences while that raises the expected
+ * throughput; the draft's confidence at a depth is the cumulative product of
+ * its per-token confidences.  Readings used:
+ *   expected committed tokens of sequence i at depth d_i:
+ *     A_i = 1 + conf[i][0] + ... + conf[i][d_i - 1];
+ *   expected step cost: C0 + T_exp * U, U = the number of distinct bits in
+ *     the union over the batch of fp[i][0..d_i] (position 0 = the root token,
+ *     always verified), the verify-cost model of the S2-MoE write-up
+ *     (component 1: T_exp per unique expert);
+ *   throughput = sum_i A_i / cost;
+ *   common depth: d_i = min(D', max_depth[i]) for D' = 0..D, largest
+ *     throughput, equal throughputs to the smaller D';
+ *   truncation: repeatedly apply the single decrement d_i -> d_i - 1 with
+ *     the largest throughput if it is strictly larger than the current one
+ *     (equal candidates to the lower i).
+ * Arithmetic is fp64 in a fixed order with no contraction: A_i accumulates
+ * in depth order from 1; the numerator sums sequences in index order from 0;
+ * cost = C0 + (T_exp * U); throughput = numerator / cost.
+ *
+ *   conf       [nseq, D] fp32 cumulative confidences, each in [0, 1].
+ *   fp         [nseq, D+1, W] uint32 predicted footprints (bit l*E + e for
+ *              expert e of layer l): row 0 the root token, row j the j-th
+ *              draft position.
+ *   max_depth  [nseq] int32 per-sequence limits (clamped to [0, D]), or NULL.
+ *   cfg        nseq in 1..256, D in 1..32, W >= 1 with
+ *              nseq*(D+1)*(8 + 4*W) <= 200 KiB; C0 > 0 and T_exp >= 0,
+ *              finite, any consistent time unit.
+ *   depth      [nseq] int32 out: d.
+ *   common_depth  [1] int32 out, optional: the batch-common depth D'.
+ *   throughput [2] fp64 out, optional: at the common depth, and final.
+ * One CTA; a control-path call (microseconds).  Device errors:
+ * MOE_DEV_BAD_PROB (a confidence outside [0, 1] or NaN: every depth 0).
+ */
+typedef struct {
+  int32_t nseq, D, W;
+  float C0, T_exp;
+} moe_depth_cfg;
+
+int moe_depth_policy(const float* conf, const uint32_t* fp, const int32_t* max_depth,
+                     const moe_depth_cfg* cfg, int32_t* depth, int32_t* common_depth,
+                     double* throughput, int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------- plan
  * moe_verify_plan -- the control path of one verify step, without the

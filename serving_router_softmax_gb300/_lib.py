@@ -22,12 +22,17 @@ PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up
 EXPORTED = ["s2_expand", "moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
             "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_verify_plan", "moe_profile_begin",
             "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version", "moe_expert_bytes",
-            "moe_stage_experts", "moe_test_set_stall", "moe_hot_list"]
+            "moe_stage_experts", "moe_test_set_stall", "moe_hot_list", "moe_depth_policy"]
 
 
 class S2Cfg(C.Structure):
     _fields_ = [("N", C.c_int32), ("W", C.c_int32), ("T_AR", C.c_float), ("T_exp", C.c_float),
                 ("C_draft", C.c_float), ("T_cold", C.c_float), ("cold_fp", C.c_void_p)]
+
+
+class DepthCfg(C.Structure):
+    _fields_ = [("nseq", C.c_int32), ("D", C.c_int32), ("W", C.c_int32), ("C0", C.c_float),
+                ("T_exp", C.c_float)]
 
 
 class RouterCfg(C.Structure):
@@ -99,6 +104,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_stage_experts.restype = C.c_int
     lib.moe_hot_list.argtypes = [vp, C.c_int64, i32, i32, i32, vp, vp, vp, vp, vp]
     lib.moe_hot_list.restype = C.c_int
+    lib.moe_depth_policy.argtypes = [vp, vp, vp, P(DepthCfg), vp, vp, vp, vp, vp]
+    lib.moe_depth_policy.restype = C.c_int
     lib.moe_verify_ffn_workspace.argtypes = [P(LayerWeights), i32, i32]
     lib.moe_verify_ffn_workspace.restype = sz
     lib.moe_verify_ffn.argtypes = [vp, i32, i32, P(LayerWeights), vp, vp, vp, vp, vp, vp, vp, vp,

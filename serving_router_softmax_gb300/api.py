@@ -121,6 +121,30 @@ def hot_list(ids: torch.Tensor, E: int, n_hot: int, first_slot: int = 0, dev_err
     return hot[:n_hot], counts, home
 
 
+def depth_policy(conf: torch.Tensor, fp: torch.Tensor, C0: float, T_exp: float,
+                 max_depth: Optional[torch.Tensor] = None, dev_err=None, stream=None):
+    """Confidence-gated depth vector (moe_depth_policy).  conf [nseq, D] fp32 cumulative
+    confidences, fp [nseq, D+1, W] int32/uint32 footprints (row 0 = root).  Returns device
+    tensors (depth [nseq] int32, common [1] int32, throughput [2] fp64: common, final)."""
+    if conf.dim() != 2 or fp.dim() != 3:
+        raise MoEError("conf [nseq, D] and fp [nseq, D+1, W] expected")
+    nseq, D = conf.shape
+    _need(conf, torch.float32, (nseq, D), "conf")
+    if fp.shape[0] != nseq or fp.shape[1] != D + 1 or fp.dtype != torch.int32:
+        raise MoEError("fp must be int32 [nseq, D+1, W]")
+    if max_depth is not None:
+        _need(max_depth, torch.int32, (nseq,), "max_depth")
+    dev = conf.device
+    depth = torch.empty(nseq, dtype=torch.int32, device=dev)
+    common = torch.empty(1, dtype=torch.int32, device=dev)
+    thr = torch.empty(2, dtype=torch.float64, device=dev)
+    cfg = L.DepthCfg(nseq, D, fp.shape[2], C0, T_exp)
+    _check(L.load().moe_depth_policy(_ptr(conf), _ptr(fp), _ptr(max_depth), C.byref(cfg), _ptr(depth),
+                                     _ptr(common), _ptr(thr), _ptr(dev_err), _stream(stream)),
+           "moe_depth_policy")
+    return depth, common, thr
+
+
 class HostExperts:
     """All E experts of every layer of a stack in page-locked host (Grace) memory, in the layers'
     layout (one row of ``gate_up[l]`` / ``down[l]`` per expert).  FP8 block scales stay on the

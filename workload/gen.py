@@ -73,6 +73,9 @@ class MoEConfig:
     mode: int = 0         # 0 marginal, 1 static
     eps: float = EPS_DEFAULT
     seed: int = 0
+    tree_depth: int = TREE_DEPTH
+    tree_branch: int = TREE_BRANCH
+    chain_beta: float = 0.0   # > 0: per-sequence acceptance rate a ~ Beta(b, b), every child q = a
 
     def replace(self, **kw) -> "MoEConfig":
         return dataclasses.replace(self, **kw)
@@ -84,7 +87,7 @@ class MoEConfig:
 
     @property
     def n_nodes(self) -> int:
-        return sum(TREE_BRANCH ** d for d in range(1, TREE_DEPTH + 1))
+        return sum(self.tree_branch ** d for d in range(1, self.tree_depth + 1))
 
 
 # The five workloads.  The bias slope ``c`` of the Qwen-like shapes is set so
@@ -150,6 +153,7 @@ class Workload:
     logits: np.ndarray          # [L, nseq, N+1, E] float32; row 0 is the root
     x: np.ndarray               # [L, nseq, N+1, H] uint16 bf16 bits or float32
     weight_seed: int
+    root_fp: np.ndarray = None  # [nseq, W] uint32 footprint of each root token (its own top-k per layer)
     T: int = field(init=False)
 
     def __post_init__(self):
@@ -225,7 +229,7 @@ def expert_weights_host(cfg: MoEConfig, layer: int, expert: int) -> dict:
 
 def make_workload(cfg: MoEConfig) -> Workload:
     rng = np.random.default_rng([cfg.seed, 0xC0FFEE])
-    parent = tree_parents()
+    parent = tree_parents(cfg.tree_depth, cfg.tree_branch)
     N = parent.shape[0]
     L, E, H, k = cfg.L, cfg.E, cfg.H, cfg.k
 
@@ -233,7 +237,15 @@ def make_workload(cfg: MoEConfig) -> Workload:
     P = np.zeros((cfg.nseq, N), dtype=np.float32)
     for s in range(cfg.nseq):
         child_q = {}
-        for p in [-1] + list(range(N)):
+        if cfg.chain_beta > 0:
+            # Acceptance is bimodal across sequences (width-vs-depth note,
+            # section 2: drafts of a sequence tend to be all right or all
+            # wrong): one rate a_s ~ Beta(b, b) per sequence, q = a_s at
+            # every draft position, so P along a chain is a_s ** depth.
+            a_s = np.float32(rng.beta(cfg.chain_beta, cfg.chain_beta))
+            for t in range(N):
+                child_q[t] = a_s
+        for p in ([] if cfg.chain_beta > 0 else [-1] + list(range(N))):
             kids = [t for t in range(N) if parent[t] == p]
             if not kids:
                 continue
@@ -276,12 +288,31 @@ def make_workload(cfg: MoEConfig) -> Workload:
                     bit = l * E + int(e)
                     own_fp[s, t, bit // 32] |= np.uint32(1 << (bit % 32))
 
+    # The root tokens' own footprints (their top-k per layer), same rule.
+    root_fp = np.zeros((cfg.nseq, W), dtype=np.uint32)
+    for s in range(cfg.nseq):
+        for l in range(L):
+            for e in np.argsort(-logits[l, s, 0], kind="stable")[:k]:
+                bit = l * E + int(e)
+                root_fp[s, bit // 32] |= np.uint32(1 << (bit % 32))
+
     # Hidden states.
     xs = rng.standard_normal((L, cfg.nseq, N + 1, H)).astype(np.float32)
     x = xs if cfg.dtype == "f32" else bf16_bits_rne(xs)
 
     return Workload(cfg=cfg, parent=parent, P=P, own_fp=own_fp, gamma=gamma,
-                    logits=logits, x=x, weight_seed=cfg.seed)
+                    logits=logits, x=x, weight_seed=cfg.seed, root_fp=root_fp)
+
+
+def chain_config(base: MoEConfig, nseq: int, depth: int = 6, beta: float = 0.5, seed: int = 100,
+                 gamma: int = 0) -> MoEConfig:
+    """A batch of draft chains (one speculated token per position, the
+    depth strategy of the width-vs-depth note, section 1) on the layer shapes
+    of ``base``: ``depth`` draft positions per sequence, consecutive positions
+    correlated through the AR(1) logits (rho of ``base``), acceptance rate
+    a_s ~ Beta(beta, beta) per sequence (bimodal for beta < 1)."""
+    return base.replace(name=f"{base.name}_chains", nseq=nseq, tree_depth=depth, tree_branch=1,
+                        chain_beta=beta, gamma=gamma, ragged=False, mode=0, seed=seed)
 
 
 def perturbed_footprints(wl: Workload, accuracy: float, seed: int = 0) -> np.ndarray:
