@@ -892,6 +892,144 @@ def gamma_sweep(mv, cfg, layers, layout, dev, stream, steps=20):
             "note": "every sequence verifies gamma draft nodes; EcoSpec write-up section 4.3 sweeps gamma 3..6"}
 
 
+def _graph_ms(mv, spec, layers, t, dev, stream, steps):
+    """Step time (CUDA graph replays) and per-layer unions of one workload."""
+    import torch
+    step = mv.VerifyStep(spec, layers, dev)
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    for _ in range(3):
+        step(*args)
+    torch.cuda.synchronize()
+    if int(step.dev_err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(step.dev_err.item())}")
+    graph = step.capture(*args)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    nu = step.n_unique.cpu().tolist()
+    del graph, step
+    return e0.elapsed_time(e1) / steps, nu
+
+
+def width_depth_measure(mv, cfg, layers, layout, dev, stream, steps=20):
+    """The width-vs-depth note on this GPU, with the workload's layers.
+
+    Section 1: verifying d consecutive positions of one sequence (the root and
+    d - 1 chained drafts) against one token from each of d independent
+    sequences: union per layer (mean over 8 seeds, from the plan) and the step
+    time (first seed, CUDA graph replays).
+
+    Section 2: batches of draft chains (6 positions, acceptance bimodal across
+    sequences): every fixed depth 0..6 against the confidence-gated depth
+    vector (moe_depth_policy, its cost model fitted to the fixed-depth step
+    times).  Expected committed tokens per step = sum_i (1 + c_i1 + ... +
+    c_id_i) under calibrated confidences; expected tokens/s = that / step."""
+    import torch
+    from workload import gen
+    from workload import device as wdev
+
+    def spec_of(c, wl):
+        return step_spec(mv, c, wl, layout)
+
+    sec1 = []
+    for d in (2, 3, 4, 5, 6, 7):
+        row = {"positions": d}
+        for kind in ("depth", "width"):
+            unions, ms = [], None
+            for rep in range(8):
+                if kind == "depth":
+                    c = gen.chain_config(cfg, 1, depth=6, seed=2000 + 10 * d + rep, gamma=d - 1)
+                else:
+                    c = gen.chain_config(cfg, d, depth=6, seed=3000 + 10 * d + rep, gamma=0)
+                wl = gen.make_workload(c)
+                t = wdev.workload_tensors(wl, dev)
+                spec = spec_of(c, wl)
+                if rep == 0:
+                    ms, nu = _graph_ms(mv, spec, layers, t, dev, stream, steps)
+                else:
+                    plan = mv.VerifyPlan(spec, dev)
+                    plan(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+                    torch.cuda.synchronize()
+                    nu = plan.n_unique.cpu().tolist()
+                    del plan
+                unions.append(sum(nu) / len(nu))
+            row[kind] = {"union_per_layer": sum(unions) / len(unions), "ms_per_step": ms}
+        sec1.append(row)
+
+    # Section 2.  Every fixed depth on several seeded batches per batch size;
+    # one cost model fitted to all of them; then the gated depth vector.
+    runs = []
+    for nseq in (1, 2, 4, 8):
+        for rep in range(4):
+            c = gen.chain_config(cfg, nseq, depth=6, seed=4000 + 100 * nseq + rep)
+            wl = gen.make_workload(c)
+            conf = wl.P.astype(np.float32)
+            A = 1.0 + np.concatenate([np.zeros((nseq, 1)), np.cumsum(conf.astype(np.float64), axis=1)], axis=1)
+            fixed = []
+            for Dc in range(7):
+                c2 = c.replace(gamma=Dc)
+                wl2 = gen.make_workload(c2)
+                t2 = wdev.workload_tensors(wl2, dev)
+                ms, nu = _graph_ms(mv, spec_of(c2, wl2), layers, t2, dev, stream, steps // 2)
+                fixed.append({"union_experts": int(sum(nu)), "ms": ms, "exp_tokens": float(A[:, Dc].sum())})
+            runs.append({"nseq": nseq, "c": c, "wl": wl, "conf": conf, "A": A, "fixed": fixed})
+    x = np.array([f["union_experts"] for r in runs for f in r["fixed"]], np.float64)
+    y = np.array([f["ms"] for r in runs for f in r["fixed"]], np.float64) * 1e3
+    (C0, T_exp), *_ = np.linalg.lstsq(np.stack([np.ones_like(x), x], 1), y, rcond=None)
+    pred = C0 + T_exp * x
+    r2 = 1.0 - float(np.sum((y - pred) ** 2) / np.sum((y - y.mean()) ** 2))
+    C0, T_exp = max(float(C0), 1.0), max(float(T_exp), 0.0)
+    pol_us = []
+    for r in runs:
+        nseq, wl, conf = r["nseq"], r["wl"], r["conf"]
+        fp = np.concatenate([wl.root_fp[:, None, :], wl.own_fp], axis=1)
+        conf_d = torch.from_numpy(conf).to(dev)
+        fp_d = torch.from_numpy(fp.view(np.int32)).to(dev)
+        depth, common, thr = mv.depth_policy(conf_d, fp_d, C0, T_exp)
+        torch.cuda.synchronize()
+        mv.profile_begin(max_launches=64, classes=["depth_policy"])
+        for _ in range(20):
+            mv.depth_policy(conf_d, fp_d, C0, T_exp)
+        torch.cuda.synchronize()
+        pp = mv.profile_end()["depth_policy"]
+        pol_us.append((nseq, pp["ms"] * 1e3 / max(pp["launches"], 1)))
+        d = depth.cpu().numpy().astype(np.int32)
+        # the step verifies each sequence's chain prefix of length d_i
+        wl_g = gen.make_workload(r["c"].replace(gamma=int(d.max())))
+        wl_g.gamma = d.copy()
+        wl_g.T = int(np.sum(d + 1))
+        t_g = wdev.workload_tensors(wl_g, dev)
+        ms, nu = _graph_ms(mv, spec_of(r["c"], wl_g), layers, t_g, dev, stream, steps // 2)
+        r["gated"] = {"depth": d.tolist(), "common": int(common.item()), "union_experts": int(sum(nu)), "ms": ms,
+                      "exp_tokens": float(sum(r["A"][i, d[i]] for i in range(nseq)))}
+    sec2 = []
+    for nseq in (1, 2, 4, 8):
+        rs = [r for r in runs if r["nseq"] == nseq]
+        fixed_tps = [sum(r["fixed"][Dc]["exp_tokens"] for r in rs) / (sum(r["fixed"][Dc]["ms"] for r in rs) / 1e3)
+                     for Dc in range(7)]
+        gated_tps = sum(r["gated"]["exp_tokens"] for r in rs) / (sum(r["gated"]["ms"] for r in rs) / 1e3)
+        best = int(np.argmax(fixed_tps))
+        sec2.append({"batch": nseq, "batches": len(rs),
+                     "fixed_expected_tokens_per_s": fixed_tps,
+                     "gated_expected_tokens_per_s": gated_tps,
+                     "best_fixed_depth": best,
+                     "gated_over_best_fixed": gated_tps / fixed_tps[best],
+                     "gated_depths": [r["gated"]["depth"] for r in rs],
+                     "acceptance_rates": [[round(float(v), 4) for v in r["conf"][:, 0]] for r in rs],
+                     "policy_us_per_call": float(np.mean([u for n, u in pol_us if n == nseq]))})
+    sec2 = {"per_batch": sec2, "cost_model": {"C0_us": C0, "T_exp_us": T_exp, "r2": r2,
+                                              "fit": "step_us = C0 + T_exp * union experts, all fixed-depth runs"}}
+    return {"depth_vs_width": sec1, "confidence_gating": sec2,
+            "workload": "draft chains of 6 positions on the workload's layer shapes, AR(1) logits along "
+                        "each chain (consecutive positions co-activate), per-sequence acceptance "
+                        "a ~ Beta(0.5, 0.5), confidence at depth j = a^j"}
+
+
 def workload_entry(core, cfg, wl, extra=None):
     """The per-workload record of the bench line."""
     d = {"config": {"layers": cfg.L, "hidden": cfg.H, "experts": cfg.E, "top_k": cfg.k,
@@ -929,7 +1067,8 @@ def other_workloads(mv, args, rank, ws, local, skip):
         core, _ = measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, name)
         extra = None
         if rank == 0 and cfg.nseq > 1:
-            extra = {"gamma_sweep": gamma_sweep(mv, cfg, layers, layout, dev, stream)}
+            extra = {"gamma_sweep": gamma_sweep(mv, cfg, layers, layout, dev, stream),
+                     "width_vs_depth": width_depth_measure(mv, cfg, layers, layout, dev, stream)}
         out[name] = workload_entry(core, cfg, wl, extra)
         del layers
         torch.cuda.synchronize()
