@@ -369,6 +369,9 @@ int moe_verify_ffn(const void* x, int32_t T, int32_t k, const moe_layer_weights*
  * contents (the kernels reset what must start at zero); calls that overlap
  * on the GPU race on it.  The first call on a device looks up the array's
  * address with that device current; make it before any stream capture.
+ * The address is kept per device and driver context: after a context reset
+ * (cudaDeviceReset, or a framework recreating the primary context) the next
+ * call looks it up again, and that call too should precede any capture.
  */
 int moe_verify_ffn_noalloc(const void* x, int32_t T, int32_t k, const moe_layer_weights* lw,
                            const int32_t* n_unique, const int32_t* unique, const int32_t* offsets,

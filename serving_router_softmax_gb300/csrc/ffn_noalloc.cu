@@ -17,7 +17,13 @@
 //     race on the array and give wrong results.
 //   * The first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current); make that first call
-//     before any stream capture.
+//     before any stream capture.  The address belongs to the device's
+//     current context: after a context reset (cudaDeviceReset, or a host
+//     framework recreating the primary context) the module is loaded again
+//     and the array may move, so the next call on that device looks it up
+//     again, and that call too should come before any capture.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -32,16 +38,36 @@ static __device__ __align__(256) unsigned char g_ffn_scratch[kMaxScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+CUcontext g_scratch_ctx[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device, looked up once.
+// The current driver context (the identity of the loaded module's copy).
+bool current_context(CUcontext* ctx) {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+  }
+  return fn(ctx) == CUDA_SUCCESS && *ctx != nullptr;
+}
+
+// Device address of the scratch array on the current device, looked up once
+// per device and context.
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  void* p = nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
+  CUcontext ctx = nullptr;
+  const bool have_ctx = current_context(&ctx);
+  if (!g_scratch_ptr[dev] || !have_ctx || ctx != g_scratch_ctx[dev]) {
     if (cudaGetSymbolAddress(&p, g_ffn_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    // the context exists now (the lookup makes the runtime create it if needed)
+    g_scratch_ctx[dev] = current_context(&ctx) ? ctx : nullptr;
   }
   *out = g_scratch_ptr[dev];
   return MOE_OK;
