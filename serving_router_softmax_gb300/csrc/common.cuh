@@ -167,6 +167,13 @@ struct HeadPrep {
   int32_t n_counters;
   int32_t* ready_flag;      // written ready_value (release) once the union is out
   int32_t ready_value;
+  // FP8 layers: the token rows are quantized (hi/lo E4M3 rows of xq_hi /
+  // xq_lo with one power-of-two scale per row in xscale) instead of copied
+  // to xd; rows T..q_rows-1 get scale 1.  NULL for bf16 layers.
+  uint8_t* xq_hi;
+  uint8_t* xq_lo;
+  float* xscale;
+  int32_t q_rows;
 };
 bool ffn_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp);
 

@@ -61,7 +61,9 @@ int ffn_validate(const moe_layer_weights& lw, int T, int k) {
 }
 
 bool ffn_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp) {
-  return ffn_tc_head_prep(lw, T, k, ws, hp);
+  if (ffn_tc_supported(lw, T, k)) return ffn_tc_head_prep(lw, T, k, ws, hp);
+  if (ffn_fp8_supported(lw, T, k)) return ffn_fp8_head_prep(lw, T, k, ws, hp);
+  return false;
 }
 
 int ffn_launch(const FfnArgs& a) {

@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "ffn_internal.cuh"
 #include "tc_ptx.cuh"
+#include "fp8_quant.cuh"
 
 namespace moe {
 namespace {
@@ -43,36 +44,44 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kNBMax = 16;         // TMEM promotion buffers (at most)
 constexpr int kMaxNM = 32;         // padded token columns handled by this path
-constexpr float kLoScale = 16.f;
+using fp8q::kLoScale;
+using fp8q::pow2_scale;
+using fp8q::split_e4m3;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
+constexpr uint64_t kReadyBudgetNs = 100000ull;     // 100 us for the union handshake
 constexpr int kBarRegion = 512;    // mbarriers + flags of the CTA
 static_assert((2 * 12 + 2 * kNBMax + 1) * 8 + 5 * 4 <= kBarRegion, "barrier region too small");
 
 struct Fp8Params {
   int T, k, E, cap;
   int M, K;             // rows of each expert matrix, reduction length
-  int NM;               // max padded token columns (<= 32)
-  int Rmax;
+  int NM;               // padded token columns (16 or 32): the token-dense gate/up operand
+  int Rh;               // rows of the quantized intermediate: expert u's token rows from u * NM
   int tiled, KS, stages, pdl;
   int NB;               // TMEM promotion buffers in rotation
   uint32_t tmem_cols;
   const int32_t* n_unique;
   const int32_t* unique;
   const int32_t* offsets;
-  const int32_t* poff;
+  const int32_t* perm_token;
   const float* wscale;  // block scales of this matrix: [E][scale_rows][K/128]
   int scale_rows;       // gate/up: 2I/128 (gate blocks, then up blocks); down: H/128
-  const float* bscale;  // gate/up: [Rmax] per padded row; down: [K/128][hs_stride]
-  uint8_t* hq_hi;       // gate/up output [Rmax][M]
+  const float* bscale;  // gate/up: [NM] per token row; down: [K/128][hs_stride]
+  uint8_t* hq_hi;       // gate/up output [Rh][M]
   uint8_t* hq_lo;
   float* hscale;        // gate/up output [M/128][hs_stride]
-  int hs_stride;        // rows of hscale per k-block (Rmax rounded up to 16)
+  int hs_stride;        // rows of hscale per k-block (Rh)
   float* o;             // down output [T*k][M]
   float* partials;      // [grid][2][2*NM][128]
   int32_t* tile_cnt;
   int32_t* dev_err;
   const int32_t* slot_of;  // expert -> weight slot (NULL: identity); block scales stay per expert id
   int n_slots;
+  // Union-ready handshake with the layer-head kernel that gate/up follows
+  // directly (as in the bf16 kernel); NULL when a prep kernel sits between.
+  int32_t* ready_flag;
+  int32_t ready_value;
+  int32_t* ready_clear;
 };
 
 struct Tile {
@@ -92,8 +101,9 @@ __device__ __forceinline__ Tile tile_info(const Fp8Params& p, int U, int t, bool
           ti.off + ti.ne <= p.T * p.k;
   ti.ws = ti.ok ? weight_slot(p.slot_of, p.n_slots, ti.e) : -1;
   ti.ok = ti.ok && ti.ws >= 0;
-  ti.prow = with_prow ? p.poff[ti.u] : -1;
-  ti.prow_ok = with_prow && ti.prow >= 0 && ti.prow + ti.np <= p.Rmax;
+  ti.prow = ti.u * p.NM;
+  ti.prow_ok = ti.prow + p.NM <= p.Rh;
+  (void)with_prow;
   return ti;
 }
 
@@ -116,34 +126,6 @@ __device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-__device__ __forceinline__ float e4m3_to_float(uint8_t c) {
-  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
-  return __half2float(*reinterpret_cast<__half*>(&h));
-}
-
-__device__ __forceinline__ uint8_t float_to_e4m3(float v) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-
-// Splits v (already divided by its scale, |v| <= 448) into hi + lo / 16.
-__device__ __forceinline__ void split_e4m3(float v, uint8_t& hi, uint8_t& lo) {
-  hi = float_to_e4m3(v);
-  lo = float_to_e4m3((v - e4m3_to_float(hi)) * kLoScale);
-}
-
-// Power-of-two scale s with amax / s in [128, 256), and 1/s: dividing by s is
-// then an exact multiplication.  Zero, NaN or tiny amax give s = 1.
-__device__ __forceinline__ void pow2_scale(float amax, float& s, float& inv_s) {
-  const int f = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
-  if (!(amax > 0.f) || f < -119 || f > 127) {
-    s = 1.f;
-    inv_s = 1.f;
-    return;
-  }
-  s = __uint_as_float(static_cast<uint32_t>(f - 7 + 127) << 23);
-  inv_s = __uint_as_float(static_cast<uint32_t>(7 - f + 127) << 23);
 }
 
 template <bool kGateUp>
@@ -204,17 +186,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int U = *p.n_unique;
-  const bool valid = U >= 1 && U <= p.cap;
-  if (!valid && blockIdx.x == 0 && threadIdx.x == 0 && U != 0) flag_error(p.dev_err, MOE_DEV_CAPACITY);
   const int MT = (p.M + kBM - 1) / kBM;
   const int KB = p.K / kBK;
   const int KU = (KB + p.KS - 1) / p.KS;
-  const long long total = valid ? (long long)U * MT * KU : 0;
-  const int G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
   const int c = blockIdx.x;
-  const long long s0 = c < G ? total * c / G : total;
-  const long long s1 = c < G ? total * (c + 1) / G : total;
+  int U = 0, G = 0;
+  long long total = 0, s0 = 0, s1 = 0;
+  // Splits the layer's pipeline units over at most `total` CTAs (see the
+  // bf16 kernel); each role calls it once the union is visible to it.
+  auto partition = [&](int u) {
+    U = u;
+    const bool valid = U >= 1 && U <= p.cap;
+    total = valid ? (long long)U * MT * KU : 0;
+    G = static_cast<int>(total < gridDim.x ? total : gridDim.x);
+    s0 = c < G ? total * c / G : total;
+    s1 = c < G ? total * (c + 1) / G : total;
+  };
+  auto load_partition = [&]() { partition(*p.n_unique); };
+  if (!p.ready_flag) load_partition();  // complete before this grid started
   const uint32_t buf_cols = (kGateUp ? 4 : 2) * p.NM;  // per TMEM buffer: [gate hi|lo][up hi|lo]
 
   if (warp == 0) {
@@ -230,10 +219,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       int npend = 0;
       bool dep_done = !p.pdl;
       if (dep_done) tc::griddep_launch_dependents();
+      if (p.ready_flag) {
+        // The union comes from the head kernel this grid follows directly:
+        // read it early once the head has published it (acquire), else
+        // after the dependency wait (see the bf16 kernel).
+        int32_t word = 0;
+        if (!dep_done && tc::wait_flag_acquire(p.ready_flag, p.ready_value, kReadyBudgetNs, &word)) {
+          partition(static_cast<int>(static_cast<uint32_t>(word) >> 16));
+        } else {
+          if (!dep_done) {
+            tc::griddep_wait();
+            tc::griddep_launch_dependents();
+            dep_done = true;
+          }
+          load_partition();
+        }
+      }
       auto issue_b = [&](int t, int kb, int nq, int st) {
+        uint8_t* sB = base + (size_t)st * stageBytes + aBytes;
+        if (kGateUp) {
+          // token-dense: all NM token rows in one box each (rows past T read as zeros)
+          tc::tma_load_2d(sB, &tmBhi, kb * kBK, 0, &full[st], polB);
+          tc::tma_load_2d(sB + p.NM * 128, &tmBlo, kb * kBK, 0, &full[st], polB);
+          return;
+        }
         const Tile ti = tile_info(p, U, t, true);
         const int prow = ti.prow_ok ? ti.prow : 0;
-        uint8_t* sB = base + (size_t)st * stageBytes + aBytes;
         for (int q = 0; q < nq; ++q)
           for (int j = 0; j < ti.np / 16; ++j) {
             tc::tma_load_2d(sB + q * bStride + j * 2048, &tmBhi, (kb + q) * kBK, prow + 16 * j, &full[st], polB);
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb = uu * p.KS;
           const int nq = KB - kb < p.KS ? KB - kb : p.KS;
           uint8_t* sA = base + (size_t)stage * stageBytes;
-          const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * 2 * ti.np * 128;
+          const uint32_t tx = (kGateUp ? 2 * kABytes : nq * kABytes) + nq * 2 * (kGateUp ? p.NM : ti.np) * 128;
           tc::mbar_arrive_expect_tx(&full[stage], tx);
           if (p.tiled) {
             const int blk = (ti.ws * MT + ti.m) * KB + kb;
@@ -299,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     tc::griddep_wait();
+    if (p.ready_flag) load_partition();
     if (tc::elect_one()) {
       int stage = 0;
       uint32_t phase = 0;
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         x += u1 - u0;
         const Tile ti = tile_info(p, U, t, false);
         if (!ti.ok) continue;
-        const uint32_t idesc = idesc_e4m3_f32(kBM, 2 * ti.np);
+        const uint32_t idesc = idesc_e4m3_f32(kBM, 2 * (kGateUp ? p.NM : ti.np));
         // Groups are kGroup consecutive k-blocks counted from the segment's
         // first k-block; the epilogue walks the same groups.
         const int kb_first = u0 * p.KS;
@@ -379,6 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int etid = threadIdx.x - 64;
     tc::griddep_wait();
+    if (p.ready_flag) load_partition();
+    if (etid == 0 && blockIdx.x == 0 && U != 0 && !(U >= 1 && U <= p.cap)) flag_error(p.dev_err, MOE_DEV_CAPACITY);
+    // down: gate/up has finished, so no CTA still reads the handshake word
+    if (!kGateUp && p.ready_clear && etid == 0 && blockIdx.x == 0) *p.ready_clear = 0;
     const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
     const int KBs = p.K / 128;  // scale blocks along K (== KB)
     const int nbp = p.NB / kGroup;  // TMEM buffer groups
@@ -396,6 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (!ti.prow_ok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+      // gate/up is token-dense (column n is token n): the expert's tokens as
+      // a mask over the columns, a token's rank in it giving its Hq row
+      const int nb = kGateUp ? p.NM : ti.np;
+      uint32_t mask = 0;
+      bool mok = true;
+      if (kGateUp) {
+        const bool mine = lane < ti.ne;
+        const int tok = mine ? p.perm_token[ti.off + lane] : 0;
+        const int prev = __shfl_up_sync(0xFFFFFFFFu, tok, 1);
+        const bool okk = !mine || (tok >= 0 && tok < p.T && (lane == 0 || tok > prev));
+        mask = __reduce_or_sync(0xFFFFFFFFu, (mine && tok >= 0 && tok < 32) ? 1u << tok : 0u);
+        mok = __all_sync(0xFFFFFFFFu, okk);
+        if (!mok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+      }
       const int row = ti.m * kBM + r;
       const bool row_ok = row < p.M;
       float ga[kMaxNM], ua[kMaxNM];
@@ -416,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kGateUp) {
 #pragma unroll
         for (int cc = 0; cc < kMaxNM / 16; ++cc)
-          if (cc < ti.np / 16) {
+          if (cc < nb / 16) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float4 v = __ldg(reinterpret_cast<const float4*>(p.bscale + prow0 + cc * 16 + q * 4));
+              const float4 v = __ldg(reinterpret_cast<const float4*>(p.bscale + cc * 16 + q * 4));
               sbr[cc * 16 + q * 4] = v.x;
               sbr[cc * 16 + q * 4 + 1] = v.y;
               sbr[cc * 16 + q * 4 + 2] = v.z;
@@ -431,13 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto promote = [&](uint32_t tb, float sg, float su, const float* sb_row) {
 #pragma unroll
         for (int cc = 0; cc < kMaxNM / 16; ++cc) {
-          if (cc < ti.np / 16) {
+          if (cc < nb / 16) {
             float gh[16], gl[16], uh[16], ul[16];
             tc::tmem_ld16(tb + cc * 16, gh);
-            tc::tmem_ld16(tb + ti.np + cc * 16, gl);
+            tc::tmem_ld16(tb + nb + cc * 16, gl);
             if (kGateUp) {
               tc::tmem_ld16(tb + 2 * p.NM + cc * 16, uh);
-              tc::tmem_ld16(tb + 2 * p.NM + ti.np + cc * 16, ul);
+              tc::tmem_ld16(tb + 2 * p.NM + nb + cc * 16, ul);
             }
             tc::tmem_ld_wait();
 #pragma unroll
@@ -454,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* src = p.bscale + (size_t)kb * p.hs_stride + prow0;
 #pragma unroll
         for (int cc = 0; cc < kMaxNM / 16; ++cc)
-          if (cc < ti.np / 16) {
+          if (cc < nb / 16) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float4 v = __ldg(reinterpret_cast<const float4*>(src + cc * 16 + q * 4));
@@ -510,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* P = p.partials + ((size_t)c * 2 + (t == first_tile_c ? 0 : 1)) * (size_t)(2 * p.NM * 128);
 #pragma unroll
         for (int n = 0; n < kMaxNM; ++n) {
-          if (n < ti.np) {
+          if (n < nb) {
             P[(size_t)n * 128 + r] = ga[n];
             if (kGateUp) P[(size_t)(p.NM + n) * 128 + r] = ua[n];
           }
@@ -536,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* P2 = p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128);
 #pragma unroll
             for (int n = 0; n < kMaxNM; ++n) {
-              if (n < ti.np) {
+              if (n < nb) {
                 ga[n] += __ldcg(&P2[(size_t)n * 128 + r]);
                 if (kGateUp) ua[n] += __ldcg(&P2[(size_t)(p.NM + n) * 128 + r]);
               }
@@ -552,10 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block's rows.
         float h[kMaxNM];
 #pragma unroll
-        for (int n = 0; n < kMaxNM; ++n) h[n] = (n < ti.ne && row_ok) ? silu_mul(ga[n], ua[n]) : 0.f;
+        for (int n = 0; n < kMaxNM; ++n) h[n] = (((mask >> n) & 1u) && row_ok) ? silu_mul(ga[n], ua[n]) : 0.f;
 #pragma unroll
         for (int n = 0; n < kMaxNM; ++n) {
-          if (n < ti.np) {
+          if ((mask >> n) & 1u) {  // warp-uniform
             float a = fabsf(h[n]);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
@@ -565,16 +595,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::named_bar_sync(1, kEpiThreads);
 #pragma unroll
         for (int n = 0; n < kMaxNM; ++n) {
-          if (n < ti.ne) {
+          if ((mask >> n) & 1u) {
             const float amax = fmaxf(fmaxf(s_red[n], s_red[kMaxNM + n]), fmaxf(s_red[2 * kMaxNM + n], s_red[3 * kMaxNM + n]));
             float sc, inv_sc;
             pow2_scale(amax, sc, inv_sc);
             uint8_t hi, lo;
             split_e4m3(h[n] * inv_sc, hi, lo);
-            if (ti.prow_ok && row_ok) {
-              p.hq_hi[(size_t)(ti.prow + n) * p.M + row] = hi;
-              p.hq_lo[(size_t)(ti.prow + n) * p.M + row] = lo;
-              if (r == 0) p.hscale[(size_t)ti.m * p.hs_stride + ti.prow + n] = sc;
+            const int rr = ti.prow + __popc(mask & ((1u << n) - 1u));  // the token's row in the group
+            if (ti.prow_ok && mok && row_ok) {
+              p.hq_hi[(size_t)rr * p.M + row] = hi;
+              p.hq_lo[(size_t)rr * p.M + row] = lo;
+              if (r == 0) p.hscale[(size_t)ti.m * p.hs_stride + rr] = sc;
             }
           }
         }
@@ -603,145 +634,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Padded group offsets, zeroed fixup counters and the quantized activations.
-// One CTA per token: it finds max |x| over the token's row, quantizes the row
-// once (power-of-two scale, hi/lo E4M3 pair) and writes it to every padded
-// row the token occupies, one per routed slot (found through inv).
+// Token-dense prep (standalone calls and layers with an expert pool; in the
+// whole step the layer head's extra CTAs do this work): CTA t finds max |x|
+// of token row t, quantizes the row once (power-of-two scale, hi/lo E4M3
+// pair) into row t of Xq; padding rows up to NM get scale 1 (their operand
+// rows read as zeros).  All CTAs zero the fix-up counters.
 constexpr int kPrepThreads = 256;
 
 __global__ void __launch_bounds__(kPrepThreads) ffn_fp8_prep_kernel(
-    const uint16_t* __restrict__ x, const int32_t* __restrict__ x_rows, int x_rows_limit, int T, int k, int H,
-    int cap, const int32_t* __restrict__ n_unique, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ inv, uint8_t* __restrict__ xq_hi, uint8_t* __restrict__ xq_lo,
-    float* __restrict__ xscale, int32_t* __restrict__ poff, int32_t* __restrict__ counters, int n_counters,
-    float* __restrict__ y, int32_t* dev_err) {
-  __shared__ int32_t spoff[1025];
-  __shared__ int32_t soff[1025];  // offsets[0..U], for the group searches
-  __shared__ int32_t s_rr[16];
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ x_rows, int x_rows_limit, int T, int NM, int H,
+    uint8_t* __restrict__ xq_hi, uint8_t* __restrict__ xq_lo, float* __restrict__ xscale,
+    int32_t* __restrict__ counters, int n_counters, int32_t* dev_err) {
   __shared__ float s_max[kPrepThreads / 32];
-  __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
-  const int TK = T * k;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   for (int i = blockIdx.x * blockDim.x + tid; i < n_counters; i += gridDim.x * blockDim.x) counters[i] = 0;
-  const int U = *n_unique;
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
-  if (U < 1 || U > cap) {
-    if (U != 0 && blockIdx.x == 0 && tid == 0) flag_error(dev_err, MOE_DEV_CAPACITY);
-    for (long long i = blockIdx.x * (long long)blockDim.x + tid; i < (long long)T * H;
-         i += (long long)gridDim.x * blockDim.x)
-      y[i] = 0.f;
-    return;
-  }
-  if (warp == 0) {
-    const int per = (U + 31) / 32;
-    const int u0 = lane * per;
-    int sum = 0;
-    for (int u = u0; u < u0 + per && u < U; ++u) {
-      const int a = offsets[u], b = offsets[u + 1];
-      if (a < 0 || b > TK || b - a < 1 || b - a > T) s_bad = 1;
-      sum += ((b - a) + 15) & ~15;
-      soff[u] = a;
-    }
-    int ex = warp_inclusive_sum(sum, lane);
-    ex -= sum;
-    for (int u = u0; u < u0 + per && u < U; ++u) {
-      spoff[u] = ex;
-      ex += ((offsets[u + 1] - offsets[u]) + 15) & ~15;
-    }
-    if (lane == 31) {
-      spoff[U] = ex;
-      soff[U] = offsets[U];
-      if (offsets[U] != TK || offsets[0] != 0) s_bad = 1;
-    }
-  }
-  __syncthreads();
-  if (s_bad) {
-    if (blockIdx.x == 0 && tid == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
-    for (long long i = blockIdx.x * (long long)blockDim.x + tid; i < (long long)T * H;
-         i += (long long)gridDim.x * blockDim.x)
-      y[i] = 0.f;
-    return;
-  }
-  if (blockIdx.x == 0)
-    for (int u = tid; u <= U; u += blockDim.x) poff[u] = spoff[u];
-
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    // padded rows of the token's k slots (-1: invalid position)
-    if (tid < k) {
-      const int pp = inv[t * k + tid];
-      int rr = -1;
-      if (pp >= 0 && pp < TK) {
-        int lo = 0, hi = U - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (soff[mid] <= pp) lo = mid;
-          else hi = mid - 1;
-        }
-        rr = spoff[lo] + (pp - soff[lo]);
-      } else {
-        flag_error(dev_err, MOE_DEV_BAD_ID);
-      }
-      s_rr[tid] = rr;
-    }
-    int row = t;
-    bool ok = true;
-    if (x_rows) {
-      row = x_rows[t];
-      ok = row >= 0 && row < x_rows_limit;
-    }
-    if (!ok) {
-      if (tid == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
-      __syncthreads();
-      continue;
-    }
-    const uint16_t* xr = x + (size_t)row * H;
-    float amax = 0.f;
-    for (int c = tid * 8; c < H; c += kPrepThreads * 8) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] << 16)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] & 0xFFFF0000u)));
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    if (lane == 0) s_max[warp] = amax;
-    __syncthreads();
-    amax = s_max[0];
-#pragma unroll
-    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
-    float sc, inv_sc;
-    pow2_scale(amax, sc, inv_sc);
-    for (int c = tid * 16; c < H; c += kPrepThreads * 16) {
-      const uint4 va = *reinterpret_cast<const uint4*>(xr + c);
-      const uint4 vb = *reinterpret_cast<const uint4*>(xr + c + 8);
-      const uint32_t wv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-      uint32_t hw[4] = {0, 0, 0, 0}, lw[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint8_t ha, la, hb, lb;
-        split_e4m3(__uint_as_float(wv[i] << 16) * inv_sc, ha, la);
-        split_e4m3(__uint_as_float(wv[i] & 0xFFFF0000u) * inv_sc, hb, lb);
-        const int sh = 16 * (i & 1);
-        hw[i >> 1] |= (static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 8)) << sh;
-        lw[i >> 1] |= (static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 8)) << sh;
-      }
-      const uint4 qh = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      const uint4 ql = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      for (int j = 0; j < k; ++j) {
-        const int rr = s_rr[j];
-        if (rr < 0) continue;
-        *reinterpret_cast<uint4*>(xq_hi + (size_t)rr * H + c) = qh;
-        *reinterpret_cast<uint4*>(xq_lo + (size_t)rr * H + c) = ql;
-      }
-    }
-    if (tid < k && s_rr[tid] >= 0) xscale[s_rr[tid]] = sc;
-    __syncthreads();  // s_rr and s_max are rewritten for the next token
+  for (int t = blockIdx.x; t < NM; t += gridDim.x) {
+    const long long row = t < T ? (x_rows ? x_rows[t] : t) : -1;
+    const bool ok = t < T && row >= 0 && (!x_rows || row < x_rows_limit);
+    if (t < T && !ok && tid == 0) flag_error(dev_err, MOE_DEV_BAD_ID);
+    fp8q::quantize_row(ok ? x + (size_t)row * H : nullptr, H, xq_hi + (size_t)t * H, xq_lo + (size_t)t * H,
+                       t < T ? xscale + t : nullptr, s_max, t < T);
+    if (t >= T && tid == 0) xscale[t] = 1.f;
   }
 }
 
@@ -777,7 +692,7 @@ bool make_tmap_u8(CUtensorMap* tm, const void* base, int rank, const uint64_t* d
 }
 
 struct Fp8Geom {
-  int NM, MT_gu, MT_d, Rmax, G, KS_d, stages_gu, stages_d;
+  int NM, MT_gu, MT_d, Rh, G, KS_d, stages_gu, stages_d;
   size_t smem_gu, smem_d;
 };
 
@@ -791,7 +706,7 @@ Fp8Geom fp8_geom(const moe_layer_weights& lw, int T, int k) {
   g.NM = (T + 15) & ~15;
   g.MT_gu = lw.I / kBM;
   g.MT_d = lw.H / kBM;
-  g.Rmax = TK + 15 * cap;
+  g.Rh = cap * g.NM;  // expert u's token rows of the intermediate from u * NM
   g.G = sm_count();
   g.KS_d = lw.layout == MOE_LAYOUT_TILED ? 2 : 1;
   const size_t b = static_cast<size_t>(2 * g.NM) * 128;
@@ -825,7 +740,8 @@ uint32_t pow2_cols(int c) {
 struct Fp8Ws {
   uint8_t *xq_hi, *xq_lo, *hq_hi, *hq_lo;
   float *xscale, *hscale, *o, *partials;
-  int32_t *poff, *counters;
+  int32_t* counters;
+  int n_counters;
   size_t bytes;
 };
 
@@ -841,16 +757,16 @@ Fp8Ws fp8_carve(const moe_layer_weights& lw, int T, int k, void* base) {
     p += align_up(bytes, 256);
     return r;
   };
-  w.xq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.H));
-  w.xq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.H));
-  w.xscale = reinterpret_cast<float*>(take(static_cast<size_t>((g.Rmax + 15) & ~15) * 4));
-  w.hq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.I));
-  w.hq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rmax) * lw.I));
-  w.hscale = reinterpret_cast<float*>(take(static_cast<size_t>((g.Rmax + 15) & ~15) * (lw.I / 128) * 4));
+  w.xq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * lw.H));
+  w.xq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * lw.H));
+  w.xscale = reinterpret_cast<float*>(take(static_cast<size_t>(kMaxNM) * 4));
+  w.hq_hi = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rh) * lw.I));
+  w.hq_lo = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(g.Rh) * lw.I));
+  w.hscale = reinterpret_cast<float*>(take(static_cast<size_t>(g.Rh) * (lw.I / 128) * 4));
   w.o = reinterpret_cast<float*>(take(static_cast<size_t>(TK) * lw.H * 4));
   w.partials = reinterpret_cast<float*>(take(static_cast<size_t>(g.G) * 2 * 2 * g.NM * 128 * 4));
-  w.poff = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cap + 1) * 4));
-  w.counters = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cap) * (g.MT_gu + g.MT_d) * 4));
+  w.n_counters = cap * (g.MT_gu + g.MT_d);
+  w.counters = reinterpret_cast<int32_t*>(take(static_cast<size_t>(w.n_counters) * 4));
   w.bytes = static_cast<size_t>(p - p0);
   return w;
 }
@@ -870,13 +786,25 @@ size_t ffn_fp8_workspace_bytes(const moe_layer_weights& lw, int T, int k) {
   return fp8_carve(lw, T, k, nullptr).bytes;
 }
 
+bool ffn_fp8_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp) {
+  if (!ffn_fp8_supported(lw, T, k) || lw.pool) return false;
+  Fp8Ws w = fp8_carve(lw, T, k, ws);
+  hp->xq_hi = w.xq_hi;
+  hp->xq_lo = w.xq_lo;
+  hp->xscale = w.xscale;
+  hp->q_rows = fp8_geom(lw, T, k).NM;
+  hp->counters = w.counters;
+  hp->n_counters = w.n_counters;
+  hp->H = lw.H;
+  return true;
+}
+
 int ffn_fp8_launch(const FfnArgs& a) {
   const auto& lw = a.lw;
   const int T = a.T, k = a.k, TK = T * k;
   const int cap = lw.E < TK ? lw.E : TK;
   Fp8Geom g = fp8_geom(lw, T, k);
   Fp8Ws ws = fp8_carve(lw, T, k, a.ws);
-  const int n_counters = cap * (g.MT_gu + g.MT_d);
   int32_t* cnt_gu = ws.counters;
   int32_t* cnt_d = cnt_gu + static_cast<size_t>(cap) * g.MT_gu;
 
@@ -911,26 +839,25 @@ int ffn_fp8_launch(const FfnArgs& a) {
     }
   }
   {
-    uint64_t dims[2] = {H, static_cast<uint64_t>(g.Rmax)}, str[1] = {H};
-    uint32_t box[2] = {kBK, 16};
+    // the T quantized token rows; the box's rows past T read as zeros
+    uint64_t dims[2] = {H, static_cast<uint64_t>(T)}, str[1] = {H};
+    uint32_t box[2] = {kBK, static_cast<uint32_t>(g.NM)};
     if (!make_tmap_u8(&tm_xh, ws.xq_hi, 2, dims, str, box)) return MOE_ERR_CUDA;
     if (!make_tmap_u8(&tm_xl, ws.xq_lo, 2, dims, str, box)) return MOE_ERR_CUDA;
   }
   {
-    uint64_t dims[2] = {I, static_cast<uint64_t>(g.Rmax)}, str[1] = {I};
+    uint64_t dims[2] = {I, static_cast<uint64_t>(g.Rh)}, str[1] = {I};
     uint32_t box[2] = {kBK, 16};
     if (!make_tmap_u8(&tm_hh, ws.hq_hi, 2, dims, str, box)) return MOE_ERR_CUDA;
     if (!make_tmap_u8(&tm_hl, ws.hq_lo, 2, dims, str, box)) return MOE_ERR_CUDA;
   }
 
   cudaStream_t s = a.stream;
-  {
-    const int blocks = T;  // one CTA per token (T <= kMaxNM)
+  if (!a.head_prepared) {
     LaunchScope ls(kProfPrep, s);
-    if (launch_k(ffn_fp8_prep_kernel, dim3(blocks), dim3(kPrepThreads), 0, s, a.pdl_first,
-                 static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, k, lw.H, cap, a.n_unique,
-                 a.offsets, a.inv, ws.xq_hi, ws.xq_lo, ws.xscale, ws.poff, cnt_gu, n_counters, a.y,
-                 a.dev_err) != MOE_OK)
+    if (launch_k(ffn_fp8_prep_kernel, dim3(g.NM), dim3(kPrepThreads), 0, s, a.pdl_first,
+                 static_cast<const uint16_t*>(a.x), a.x_rows, a.x_rows_limit, T, g.NM, lw.H, ws.xq_hi, ws.xq_lo,
+                 ws.xscale, ws.counters, ws.n_counters, a.dev_err) != MOE_OK)
       return MOE_ERR_CUDA;
   }
 
@@ -940,14 +867,16 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.E = lw.E;
   fp.cap = cap;
   fp.NM = g.NM;
-  fp.Rmax = g.Rmax;
-  fp.hs_stride = (g.Rmax + 15) & ~15;
+  fp.Rh = g.Rh;
+  fp.hs_stride = g.Rh;
   fp.tiled = lw.layout == MOE_LAYOUT_TILED ? 1 : 0;
   fp.pdl = 1;
   fp.n_unique = a.n_unique;
   fp.unique = a.unique;
   fp.offsets = a.offsets;
-  fp.poff = ws.poff;
+  fp.perm_token = a.perm_token;
+  fp.ready_flag = a.head_prepared ? a.ready_flag : nullptr;
+  fp.ready_value = a.ready_value;
   fp.hq_hi = ws.hq_hi;
   fp.hq_lo = ws.hq_lo;
   fp.hscale = ws.hscale;
@@ -988,6 +917,8 @@ int ffn_fp8_launch(const FfnArgs& a) {
   fp.scale_rows = lw.H / 128;
   fp.bscale = ws.hscale;
   fp.tile_cnt = cnt_d;
+  fp.ready_clear = fp.ready_flag;
+  fp.ready_flag = nullptr;
   if (cudaFuncSetAttribute(ffn_fp8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(g.smem_d)) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -25,5 +25,6 @@ bool ffn_tc_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadP
 bool ffn_fp8_supported(const moe_layer_weights& lw, int T, int k);
 size_t ffn_fp8_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_fp8_launch(const FfnArgs& a);
+bool ffn_fp8_head_prep(const moe_layer_weights& lw, int T, int k, void* ws, HeadPrep* hp);
 
 }  // namespace moe

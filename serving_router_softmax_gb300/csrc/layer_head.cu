@@ -20,6 +20,7 @@
 // previous layer's last kernel.
 #include "common.cuh"
 #include "route_dev.cuh"
+#include "fp8_quant.cuh"
 
 namespace moe {
 namespace {
@@ -137,6 +138,21 @@ __global__ void __launch_bounds__(kHeadThreads) layer_head_kernel(RouteArgs ra, 
     const long long nth = (long long)(gridDim.x - 1) * blockDim.x;
     const long long tid = (long long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
     for (long long i = tid; i < hp.n_counters; i += nth) hp.counters[i] = 0;
+    if (hp.xq_hi) {
+      // FP8 layers: one CTA per token row quantizes it (max |x|, power-of-two
+      // scale, hi/lo E4M3 rows); padding rows up to q_rows get scale 1.
+      __shared__ float s_max[kHeadThreads / 32];
+      for (int t = blockIdx.x - 1; t < hp.q_rows; t += gridDim.x - 1) {
+        const long long row = t < ra.cfg.T ? hp.x_rows[t] : -1;
+        const bool ok = t < ra.cfg.T && row >= 0 && row < hp.x_rows_limit;
+        if (t < ra.cfg.T && !ok && threadIdx.x == 0) flag_error(ra.dev_err, MOE_DEV_BAD_ID);
+        fp8q::quantize_row(ok ? hp.x + (size_t)row * hp.H : nullptr, hp.H, hp.xq_hi + (size_t)t * hp.H,
+                           hp.xq_lo + (size_t)t * hp.H, t < ra.cfg.T ? hp.xscale + t : nullptr, s_max,
+                           t < ra.cfg.T);
+        if (t >= ra.cfg.T && threadIdx.x == 0) hp.xscale[t] = 1.f;
+      }
+      return;
+    }
     const int cpr = hp.H / 8;  // 16-byte chunks per row
     for (long long i = tid; i < (long long)ra.cfg.T * cpr; i += nth) {
       const int t = static_cast<int>(i / cpr);
@@ -462,6 +478,7 @@ int launch_npl(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t*
     const long long chunks = static_cast<long long>(ra.cfg.T) * (h.H / 8);
     const long long work = chunks > h.n_counters ? chunks : h.n_counters;
     long long extra = (work + kHeadThreads - 1) / kHeadThreads;
+    if (h.xq_hi && extra < h.q_rows) extra = h.q_rows;  // FP8: a CTA per token row
     if (extra > 32) extra = 32;
     grid = 1 + static_cast<int>(extra);
   }
@@ -476,7 +493,8 @@ int launch_npl(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t*
 int layer_head_launch(const RouteArgs& ra, int32_t* n_unique, int32_t* unique, int32_t* offsets,
                       int32_t* perm_token, int32_t* perm_slot, int32_t* inv, float* reuse_ratio, bool pdl,
                       bool rows_ready, const HeadPrep* hp) {
-  if (hp && (!hp->x || !hp->x_rows || !hp->xd || !hp->counters || hp->H % 8)) return MOE_ERR_ARG;
+  if (hp && (!hp->x || !hp->x_rows || !(hp->xd || hp->xq_hi) || !hp->counters || hp->H % 16)) return MOE_ERR_ARG;
+  if (hp && hp->xq_hi && (!hp->xq_lo || !hp->xscale || hp->q_rows < ra.cfg.T || hp->q_rows > 32)) return MOE_ERR_ARG;
   if (ra.cfg.T < 1 || ra.cfg.T > routing::kBiasMaxT || ra.cfg.E > 1024) return MOE_ERR_UNSUPPORTED;
   const int npl = (ra.cfg.E + 31) / 32;
   if (npl <= 1)
