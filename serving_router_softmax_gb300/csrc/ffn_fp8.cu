@@ -559,16 +559,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (arrived == cl - cf) {
           __threadfence();
           finished = true;
+          // Sum in CTA order from zero, 16 columns at a time: each other
+          // contributor's 16 (gate/up: 32) loads are unconditional, so they
+          // are all in flight before the first add; this CTA's own partial
+          // is still in registers.
 #pragma unroll
-          for (int n = 0; n < kMaxNM; ++n) ga[n] = ua[n] = 0.f;
-          for (int q2 = cf; q2 <= cl; ++q2) {
-            const int ft = static_cast<int>((total * q2 / G) / KU);
-            const float* P2 = p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128);
+          for (int cc = 0; cc < kMaxNM / 16; ++cc) {
+            if (cc < nb / 16) {
+              float g[16], v[16];
 #pragma unroll
-            for (int n = 0; n < kMaxNM; ++n) {
-              if (n < nb) {
-                ga[n] += __ldcg(&P2[(size_t)n * 128 + r]);
-                if (kGateUp) ua[n] += __ldcg(&P2[(size_t)(p.NM + n) * 128 + r]);
+              for (int j = 0; j < 16; ++j) g[j] = v[j] = 0.f;
+              for (int q2 = cf; q2 <= cl; ++q2) {
+                if (q2 == c) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    g[j] += ga[cc * 16 + j];
+                    if (kGateUp) v[j] += ua[cc * 16 + j];
+                  }
+                } else {
+                  const int ft = static_cast<int>((total * q2 / G) / KU);
+                  const float* P2 =
+                      p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128) + (size_t)cc * 16 * 128 + r;
+                  float lg[16], lv[16];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    lg[j] = __ldcg(P2 + (size_t)j * 128);
+                    if (kGateUp) lv[j] = __ldcg(P2 + (size_t)(p.NM + j) * 128);
+                  }
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    g[j] += lg[j];
+                    if (kGateUp) v[j] += lv[j];
+                  }
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                ga[cc * 16 + j] = g[j];
+                ua[cc * 16 + j] = v[j];
               }
             }
           }
@@ -580,32 +608,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         // h = silu(gate) * up, quantized per (token, 128-row block) for the
         // down projection, with the power-of-two scale of max |h| over the
         // block's rows.
+        // Every column of a 16-column chunk is computed (columns of tokens
+        // outside the expert's group hold finite values and are dropped at
+        // the store), so the shuffles and shared-memory reads of a chunk are
+        // independent and overlap instead of running one token at a time.
         float h[kMaxNM];
 #pragma unroll
-        for (int n = 0; n < kMaxNM; ++n) h[n] = (((mask >> n) & 1u) && row_ok) ? silu_mul(ga[n], ua[n]) : 0.f;
+        for (int cc = 0; cc < kMaxNM / 16; ++cc) {
+          if (cc < nb / 16) {
+            float a[16];
 #pragma unroll
-        for (int n = 0; n < kMaxNM; ++n) {
-          if ((mask >> n) & 1u) {  // warp-uniform
-            float a = fabsf(h[n]);
+            for (int j = 0; j < 16; ++j) {
+              const int n = cc * 16 + j;
+              const float s = silu_mul(ga[n], ua[n]);
+              h[n] = (((mask >> n) & 1u) && row_ok) ? s : 0.f;
+              a[j] = fabsf(h[n]);
+            }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-            if (lane == 0) s_red[q4 * kMaxNM + n] = a;
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) a[j] = fmaxf(a[j], __shfl_xor_sync(0xFFFFFFFFu, a[j], off));
+            if (lane == 0) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) s_red[q4 * kMaxNM + cc * 16 + j] = a[j];
+            }
           }
         }
         tc::named_bar_sync(1, kEpiThreads);
 #pragma unroll
-        for (int n = 0; n < kMaxNM; ++n) {
-          if ((mask >> n) & 1u) {
-            const float amax = fmaxf(fmaxf(s_red[n], s_red[kMaxNM + n]), fmaxf(s_red[2 * kMaxNM + n], s_red[3 * kMaxNM + n]));
-            float sc, inv_sc;
-            pow2_scale(amax, sc, inv_sc);
-            uint8_t hi, lo;
-            split_e4m3(h[n] * inv_sc, hi, lo);
-            const int rr = ti.prow + __popc(mask & ((1u << n) - 1u));  // the token's row in the group
-            if (ti.prow_ok && mok && row_ok) {
-              p.hq_hi[(size_t)rr * p.M + row] = hi;
-              p.hq_lo[(size_t)rr * p.M + row] = lo;
-              if (r == 0) p.hscale[(size_t)ti.m * p.hs_stride + rr] = sc;
+        for (int cc = 0; cc < kMaxNM / 16; ++cc) {
+          if (cc < nb / 16) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = cc * 16 + j;
+              const float amax =
+                  fmaxf(fmaxf(s_red[n], s_red[kMaxNM + n]), fmaxf(s_red[2 * kMaxNM + n], s_red[3 * kMaxNM + n]));
+              float sc, inv_sc;
+              pow2_scale(amax, sc, inv_sc);
+              uint8_t hi, lo;
+              split_e4m3(h[n] * inv_sc, hi, lo);
+              const int rr = ti.prow + __popc(mask & ((1u << n) - 1u));  // the token's row in the group
+              if (((mask >> n) & 1u) && ti.prow_ok && mok && row_ok) {
+                p.hq_hi[(size_t)rr * p.M + row] = hi;
+                p.hq_lo[(size_t)rr * p.M + row] = lo;
+                if (r == 0) p.hscale[(size_t)ti.m * p.hs_stride + rr] = sc;
+              }
             }
           }
         }
