@@ -111,7 +111,10 @@ __device__ __forceinline__ long long seg_owner(long long x, long long total, int
   return ((x + 1) * G - 1) / total;
 }
 
-__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+// silu(a) * b with the fast exponential and division (relative error near
+// 1e-6, far below the 2^-8 of the E4M3 split that h goes through next); the
+// tile end that calls it runs once per tile and is short for that reason.
+__device__ __forceinline__ float silu_mul(float a, float b) { return __fdividef(a, 1.f + __expf(-a)) * b; }
 
 // Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B E4M3
 // (format 0 in bits 7-9 and 10-12), both K-major, N >> 3 (17-22), M >> 4 (24-28).
@@ -152,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* consumed = issued + 1;
   // Barrier/flag block (at most 2*12 + 9 mbarriers + 5 words) then the combine's staging.
   float* s_red = reinterpret_cast<float*>(base + (size_t)S * stageBytes + kBarRegion);  // [4 warps][kMaxNM] column maxima
+  float* s_sc = s_red + 4 * kMaxNM;  // [kMaxNM] 1 / scale of each column of h
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -610,29 +614,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block's rows.
         // Every column of a 16-column chunk is computed (columns of tokens
         // outside the expert's group hold finite values and are dropped at
-        // the store), so the shuffles and shared-memory reads of a chunk are
-        // independent and overlap instead of running one token at a time.
+        // the store), with no per-token branch.  This code runs once per
+        // tile, so its instructions are usually not in the SM's instruction
+        // cache: it is kept short (one warp max instruction per column,
+        // each column's scale computed once by one thread).
         float h[kMaxNM];
 #pragma unroll
         for (int cc = 0; cc < kMaxNM / 16; ++cc) {
           if (cc < nb / 16) {
-            float a[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int n = cc * 16 + j;
               const float s = silu_mul(ga[n], ua[n]);
               h[n] = (((mask >> n) & 1u) && row_ok) ? s : 0.f;
-              a[j] = fabsf(h[n]);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-              for (int j = 0; j < 16; ++j) a[j] = fmaxf(a[j], __shfl_xor_sync(0xFFFFFFFFu, a[j], off));
-            if (lane == 0) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) s_red[q4 * kMaxNM + cc * 16 + j] = a[j];
+              // max |h| over the warp's rows; |h| >= 0 orders as its bits,
+              // and a NaN counts as 0 (as fmaxf would skip it)
+              const float a = fabsf(h[n]);
+              const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, a == a ? __float_as_uint(a) : 0u);
+              if (lane == 0) s_red[q4 * kMaxNM + n] = __uint_as_float(m);
             }
           }
+        }
+        tc::named_bar_sync(1, kEpiThreads);
+        if (etid < nb) {  // column etid's scale, from the four warps' maxima
+          const int n = etid;
+          const float amax =
+              fmaxf(fmaxf(s_red[n], s_red[kMaxNM + n]), fmaxf(s_red[2 * kMaxNM + n], s_red[3 * kMaxNM + n]));
+          float sc, inv_sc;
+          pow2_scale(amax, sc, inv_sc);
+          s_sc[n] = inv_sc;
+          if (((mask >> n) & 1u) && ti.prow_ok && mok)
+            p.hscale[(size_t)ti.m * p.hs_stride + ti.prow + __popc(mask & ((1u << n) - 1u))] = sc;
         }
         tc::named_bar_sync(1, kEpiThreads);
 #pragma unroll
@@ -641,22 +653,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int n = cc * 16 + j;
-              const float amax =
-                  fmaxf(fmaxf(s_red[n], s_red[kMaxNM + n]), fmaxf(s_red[2 * kMaxNM + n], s_red[3 * kMaxNM + n]));
-              float sc, inv_sc;
-              pow2_scale(amax, sc, inv_sc);
-              uint8_t hi, lo;
-              split_e4m3(h[n] * inv_sc, hi, lo);
-              const int rr = ti.prow + __popc(mask & ((1u << n) - 1u));  // the token's row in the group
               if (((mask >> n) & 1u) && ti.prow_ok && mok && row_ok) {
+                uint8_t hi, lo;
+                split_e4m3(h[n] * s_sc[n], hi, lo);
+                const int rr = ti.prow + __popc(mask & ((1u << n) - 1u));  // the token's row in the group
                 p.hq_hi[(size_t)rr * p.M + row] = hi;
                 p.hq_lo[(size_t)rr * p.M + row] = lo;
-                if (r == 0) p.hscale[(size_t)ti.m * p.hs_stride + rr] = sc;
               }
             }
           }
         }
-        tc::named_bar_sync(1, kEpiThreads);  // s_red is reused by the next tile
+        tc::named_bar_sync(1, kEpiThreads);  // s_red and s_sc are reused by the next tile
       } else {
 #pragma unroll
         for (int n = 0; n < kMaxNM; ++n)
@@ -744,7 +751,7 @@ struct Fp8Geom {
 };
 
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr size_t kSmemExtra = 1024 + kBarRegion + 4 * 4 * kMaxNM;
+constexpr size_t kSmemExtra = 1024 + kBarRegion + 4 * 5 * kMaxNM;
 
 Fp8Geom fp8_geom(const moe_layer_weights& lw, int T, int k) {
   Fp8Geom g;
