@@ -138,7 +138,10 @@ __device__ __forceinline__ Tile tile_core(const TcParams& p, int U, int t) {
   return ti;
 }
 
-__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+// silu(a) * b with the fast exponential and division (relative error near
+// 1e-6, below the bf16 rounding of h that follows); it sits in the tile end,
+// which runs once per tile and is kept short for that reason.
+__device__ __forceinline__ float silu_mul(float a, float b) { return __fdividef(a, 1.f + __expf(-a)) * b; }
 
 // Tokens of a tile's expert as a bit mask over the T <= 32 token columns.
 // The group lists its tokens in ascending order (the union's layout), so a
@@ -470,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         hp_ok = hp_ok && mok;
       }
       const bool whole = u0 == 0 && u1 == KU;
+      int cf = c, cl = c;  // the CTAs that share the tile
       const int row = ti.m * kBM + r;
       const bool row_ok = row < p.M;
       const uint32_t tacc = tmem_base + lane_off + acc * acc_cols;
@@ -477,43 +481,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Result column n: gate/up writes h to Hp (token-dense: column n is
       // token n, stored at its rank in the expert's group), down writes o.
       auto put = [&](int n, float gv, float vv) {
-        if (!row_ok) return;
         if (kGateUp) {
-          if (p.dense) {
-            if (hp_ok && n < 32 && ((mask >> n) & 1u))
-              p.hp[(size_t)(ti.prow + __popc(mask & ((1u << n) - 1u))) * p.M + row] =
-                  float_to_bf16_bits_rn(silu_mul(gv, vv));
-          } else if (n < ti.ne && hp_ok) {
-            p.hp[(size_t)(ti.prow + n) * p.M + row] = float_to_bf16_bits_rn(silu_mul(gv, vv));
-          }
-        } else if (n < ti.ne) {
+          const bool keep = p.dense ? (n < 32 && ((mask >> n) & 1u)) : n < ti.ne;
+          const int rr = ti.prow + (p.dense ? __popc(mask & ((1u << n) - 1u)) : n);
+          if (row_ok && hp_ok && keep) p.hp[(size_t)rr * p.M + row] = float_to_bf16_bits_rn(silu_mul(gv, vv));
+        } else if (row_ok && n < ti.ne) {
           p.o[(size_t)(ti.off + n) * p.M + row] = gv;
         }
       };
       const int ncols = (kGateUp && p.dense) ? p.NM : ti.np;
-      for (int cc = 0; cc < ncols / 16; ++cc) {
-        float g[16], v[16];
-        tc::tmem_ld16(tacc + cc * 16, g);
-        if (kGateUp) tc::tmem_ld16(tacc + p.NM + cc * 16, v);
-        tc::tmem_ld_wait();
-        if (whole) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) put(cc * 16 + j, g[j], kGateUp ? v[j] : 0.f);
-        } else {
+      bool finished = whole;
+      if (!whole) {
+        // Split tile: this CTA's sums go to its partial slot first.
+        for (int cc = 0; cc < ncols / 16; ++cc) {
+          float g[16], v[16];
+          tc::tmem_ld16(tacc + cc * 16, g);
+          if (kGateUp) tc::tmem_ld16(tacc + p.NM + cc * 16, v);
+          tc::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             P[(size_t)(cc * 16 + j) * 128 + r] = g[j];
             if (kGateUp) P[(size_t)(p.NM + cc * 16 + j) * 128 + r] = v[j];
           }
         }
-      }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&acce[acc]);
-      acc_phase[acc] ^= 1u;
-      if (p.acc_stages == 2) acc ^= 1;
-
-      bool finished = whole;
-      if (!whole) {
         // Last-arriver fixup across the CTAs that share this tile.  The CTA
         // barrier orders every thread's partial stores before thread 0's
         // fence and atomic (release); the finisher fences after observing
@@ -526,31 +516,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::named_bar_sync(1, kEpiThreads);
         const int arrived = *bcast;
         const long long t0 = (long long)t * KU;
-        const int cf = static_cast<int>(seg_owner(t0, total, G));
-        const int cl = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
+        cf = static_cast<int>(seg_owner(t0, total, G));
+        cl = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
         tc::named_bar_sync(1, kEpiThreads);
-        if (arrived == cl - cf) {
-          __threadfence();
-          finished = true;
-          for (int cc = 0; cc < ncols / 16; ++cc) {
-            float g[16], v[16];
+        finished = arrived == cl - cf;
+        if (finished) __threadfence();
+      }
+      if (finished) {
+        // One copy of the result code for whole and fixed-up tiles: it runs
+        // once per tile, mostly from a cold instruction cache.  Sums run in
+        // CTA order; this CTA's own share is still in the accumulator.  A
+        // whole tile starts from -0 (x + -0 == x for every x), a fixed-up
+        // one from +0.
+        for (int cc = 0; cc < ncols / 16; ++cc) {
+          float g[16], v[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) g[j] = v[j] = 0.f;
-            for (int q2 = cf; q2 <= cl; ++q2) {
+          for (int j = 0; j < 16; ++j) g[j] = v[j] = whole ? -0.f : 0.f;
+          for (int q2 = cf; q2 <= cl; ++q2) {
+            float lg[16], lv[16];
+            if (q2 == c) {
+              tc::tmem_ld16(tacc + cc * 16, lg);
+              if (kGateUp) tc::tmem_ld16(tacc + p.NM + cc * 16, lv);
+              tc::tmem_ld_wait();
+            } else {
               const int ft = static_cast<int>((total * q2 / G) / KU);
-              const float* P2 = p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128);
+              const float* P2 = p.partials + ((size_t)q2 * 2 + (t == ft ? 0 : 1)) * (size_t)(2 * p.NM * 128) +
+                                (size_t)cc * 16 * 128 + r;
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                g[j] += __ldcg(&P2[(size_t)(cc * 16 + j) * 128 + r]);
-                if (kGateUp) v[j] += __ldcg(&P2[(size_t)(p.NM + cc * 16 + j) * 128 + r]);
+                lg[j] = __ldcg(P2 + (size_t)j * 128);
+                if (kGateUp) lv[j] = __ldcg(P2 + (size_t)(p.NM + j) * 128);
               }
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) put(cc * 16 + j, g[j], kGateUp ? v[j] : 0.f);
+            for (int j = 0; j < 16; ++j) {
+              g[j] += lg[j];
+              if (kGateUp) v[j] += lv[j];
+            }
           }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) put(cc * 16 + j, g[j], kGateUp ? v[j] : 0.f);
         }
       }
-
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acce[acc]);
+      acc_phase[acc] ^= 1u;
+      if (p.acc_stages == 2) acc ^= 1;
     }
   }
 
