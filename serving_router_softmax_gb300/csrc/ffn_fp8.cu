@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "ffn_internal.cuh"
 #include "tc_ptx.cuh"
+#include "stream_k.cuh"
 #include "fp8_quant.cuh"
 
 namespace moe {
@@ -105,10 +106,6 @@ __device__ __forceinline__ Tile tile_info(const Fp8Params& p, int U, int t, bool
   ti.prow_ok = ti.prow + p.NM <= p.Rh;
   (void)with_prow;
   return ti;
-}
-
-__device__ __forceinline__ long long seg_owner(long long x, long long total, int G) {
-  return ((x + 1) * G - 1) / total;
 }
 
 // silu(a) * b with the fast exponential and division (relative error near
@@ -263,11 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         npend = 0;
         dep_done = true;
       };
-      for (long long x = s0; x < s1 && !*abort_flag;) {
-        const int t = static_cast<int>(x / KU);
-        const int u0 = static_cast<int>(x - (long long)t * KU);
-        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
-        x += u1 - u0;
+      Segments sg;
+      sg.init(s0, s1, KU, false);
+      for (int si = 0; si < sg.n && !*abort_flag; ++si) {
+        int t, u0, u1;
+        sg.get(si, t, u0, u1);
         const Tile ti = tile_info(p, U, t, false);
         if (!ti.ok) continue;
         for (int uu = u0; uu < u1; ++uu) {
@@ -324,11 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tphase = 0;      // bit b: phase parity of group b
       int n_consumed = 0;
       bool stop = false;
-      for (long long x = s0; x < s1 && !stop;) {
-        const int t = static_cast<int>(x / KU);
-        const int u0 = static_cast<int>(x - (long long)t * KU);
-        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
-        x += u1 - u0;
+      Segments sg;
+      sg.init(s0, s1, KU, false);
+      for (int si = 0; si < sg.n && !stop; ++si) {
+        int t, u0, u1;
+        sg.get(si, t, u0, u1);
         const Tile ti = tile_info(p, U, t, false);
         if (!ti.ok) continue;
         const uint32_t idesc = idesc_e4m3_f32(kBM, 2 * (kGateUp ? p.NM : ti.np));
@@ -405,11 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pc = 0;                 // groups consumed
     uint32_t tphase = 0;        // bit b: phase parity of group b
     bool stop = false;
-    for (long long x = s0; x < s1 && !stop;) {
-      const int t = static_cast<int>(x / KU);
-      const int u0 = static_cast<int>(x - (long long)t * KU);
-      const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
-      x += u1 - u0;
+    Segments sg;
+    sg.init(s0, s1, KU, false);
+    for (int si = 0; si < sg.n && !stop; ++si) {
+      int t, u0, u1;
+      sg.get(si, t, u0, u1);
       const Tile ti = tile_info(p, U, t, true);
       if (!ti.ok) {
         if (etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);

@@ -38,6 +38,7 @@
 #include "common.cuh"
 #include "ffn_internal.cuh"
 #include "tc_ptx.cuh"
+#include "stream_k.cuh"
 
 namespace moe {
 namespace {
@@ -96,10 +97,6 @@ struct Tile {
   int u, m, e, ws, ne, np, prow, off;  // ws: the expert's slot in the weight buffers
   bool ok, prow_ok;
 };
-
-__device__ __forceinline__ long long seg_owner(long long x, long long total, int G) {
-  return ((x + 1) * G - 1) / total;
-}
 
 __device__ __forceinline__ Tile tile_info(const TcParams& p, int U, int t) {
   Tile ti;
@@ -299,11 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         npend = 0;
         dep_done = true;
       };
-      for (long long x = p.stall ? s1 : s0; x < s1 && !*abort_flag;) {
-        const int t = static_cast<int>(x / KU);
-        const int u0 = static_cast<int>(x - (long long)t * KU);
-        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
-        x += u1 - u0;
+      Segments sg;
+      sg.init(s0, s1, KU, true);
+      for (int si = p.stall ? sg.n : 0; si < sg.n && !*abort_flag; ++si) {
+        int t, u0, u1;
+        sg.get(si, t, u0, u1);
         const Tile ti = tile_core(p, U, t);
         if (!ti.ok) continue;
         for (int uu = u0; uu < u1; ++uu) {
@@ -375,11 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase[2] = {0, 0};
       int n_consumed = 0;
       bool stop = false;
-      for (long long x = s0; x < s1 && !stop;) {
-        const int t = static_cast<int>(x / KU);
-        const int u0 = static_cast<int>(x - (long long)t * KU);
-        const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
-        x += u1 - u0;
+      Segments sg;
+      sg.init(s0, s1, KU, true);
+      for (int si = 0; si < sg.n && !stop; ++si) {
+        int t, u0, u1;
+        sg.get(si, t, u0, u1);
         const Tile ti = tile_core(p, U, t);
         if (!ti.ok) continue;
         if (!tc::mbar_wait_bounded(&acce[acc], acc_phase[acc] ^ 1u, abort_flag, kWaitBudgetNs)) {
@@ -444,11 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase[2] = {0, 0};
     const int first_tile_c = KU > 0 ? static_cast<int>(s0 / KU) : 0;
-    for (long long x = s0; x < s1;) {
-      const int t = static_cast<int>(x / KU);
-      const int u0 = static_cast<int>(x - (long long)t * KU);
-      const int u1 = static_cast<int>(u0 + (s1 - x) < KU ? u0 + (s1 - x) : KU);
-      x += u1 - u0;
+    Segments sg;
+    sg.init(s0, s1, KU, true);
+    for (int si = 0; si < sg.n; ++si) {
+      int t, u0, u1;
+      sg.get(si, t, u0, u1);
       const Tile ti = tile_info(p, U, t);
       if (!ti.ok) {
         if (etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
