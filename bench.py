@@ -171,10 +171,11 @@ class ClockSampler:
 
 def kernel_source_hash():
     """Hash of the sources that define the bf16 FFN kernels (their translation
-    unit and its PTX wrappers); ties committed ncu traffic to the code."""
+    unit, its PTX wrappers and the stream-K order); ties committed ncu traffic
+    to the code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_router_softmax_gb300", "csrc")
-    for f in ("ffn_tc.cu", "ffn_internal.cuh", "tc_ptx.cuh"):
+    for f in ("ffn_tc.cu", "ffn_internal.cuh", "tc_ptx.cuh", "stream_k.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
