@@ -634,6 +634,17 @@ uint64_t moe_launch_count(void);
 enum { MOE_TEST_STALL_GATE_UP = 1, MOE_TEST_STALL_READY_FLAG = 2 };
 int moe_test_set_stall(int32_t mask);
 
+/* Trace ranges for a timeline tool (NVTX; the pages have no counterpart).
+ * With on = 1, moe_verify_step and moe_verify_plan push a named NVTX range
+ * around their enqueue ("moe_verify_step" / "moe_verify_plan"), one around
+ * the selection launch ("selection") and one per layer ("layer <l>") on the
+ * calling host thread; a tool such as Nsight Systems projects them onto the
+ * GPU timeline of the stream.  on = 0 (the default) pushes nothing.  Host
+ * only, process-wide; returns MOE_ERR_ARG for any other value.  Ranges mark
+ * enqueue spans, so under stream capture they mark the capture, not the
+ * graph's replays. */
+int moe_set_nvtx(int32_t on);
+
 /* Library ABI version (major * 100 + minor). */
 int moe_version(void);
 

@@ -10,7 +10,7 @@ from . import _lib
 from .api import (ExpertLayer, ExpertPool, MoEError, StepSpec, VerifyPlan, VerifyStep, depth_policy,  # noqa: F401
                   eco_select,
                   expert_bytes, ffn_workspace_bytes, hot_list, HostExperts, launch_count, new_dev_err, pack_tiled,
-                  profile_begin, profile_end, route, router_logits, s2_expand, stage_experts,
+                  profile_begin, profile_end, route, router_logits, s2_expand, set_nvtx, stage_experts,
                   step_workspace_bytes, union_permute, verify_ffn)
 
 _lib.load()

@@ -22,7 +22,7 @@ PROF_CLASSES = ["eco_select", "route", "union_permute", "ffn_prep", "ffn_gate_up
 EXPORTED = ["s2_expand", "moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn_workspace", "moe_verify_ffn",
             "eco_select", "moe_verify_step_workspace", "moe_verify_step", "moe_verify_plan", "moe_profile_begin",
             "moe_profile_end", "moe_status_str", "moe_launch_count", "moe_version", "moe_expert_bytes",
-            "moe_stage_experts", "moe_test_set_stall", "moe_hot_list", "moe_depth_policy"]
+            "moe_stage_experts", "moe_test_set_stall", "moe_hot_list", "moe_depth_policy", "moe_set_nvtx"]
 
 
 class S2Cfg(C.Structure):
@@ -132,5 +132,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.moe_version.restype = C.c_int
     lib.moe_test_set_stall.argtypes = [i32]
     lib.moe_test_set_stall.restype = C.c_int
+    lib.moe_set_nvtx.argtypes = [i32]
+    lib.moe_set_nvtx.restype = C.c_int
     _lib = lib
     return lib

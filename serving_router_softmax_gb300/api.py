@@ -558,3 +558,8 @@ def profile_end() -> Dict[str, Dict[str, float]]:
 
 def launch_count() -> int:
     return int(L.load().moe_launch_count())
+
+
+def set_nvtx(on: bool) -> None:
+    """NVTX ranges around each step/plan enqueue, its selection and its layers (off by default)."""
+    _check(L.load().moe_set_nvtx(1 if on else 0), "moe_set_nvtx")

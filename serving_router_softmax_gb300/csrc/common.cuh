@@ -28,6 +28,16 @@ int sm_count();
 // Test-hook bits set by moe_test_set_stall (0 in normal operation).
 int test_stall_mask();
 
+// NVTX range around a host-side span (a step's or plan's enqueue, one of
+// their layers), pushed only while moe_set_nvtx(1) is in effect.
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char* name);
+  ~NvtxRange();
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 inline int check_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Launches `kernel`, optionally with programmatic dependent launch: the

@@ -1,5 +1,7 @@
 // Library runtime: status strings, launch accounting and optional per-kernel
 // event timing.
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -11,6 +13,7 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_test_stall{0};
+std::atomic<int> g_nvtx{0};
 
 struct Prof {
   std::mutex mu;
@@ -30,6 +33,13 @@ Prof& prof() {
 }  // namespace
 
 int test_stall_mask() { return g_test_stall.load(std::memory_order_relaxed); }
+
+NvtxRange::NvtxRange(const char* name) : on(g_nvtx.load(std::memory_order_relaxed) != 0) {
+  if (on) nvtxRangePushA(name);
+}
+NvtxRange::~NvtxRange() {
+  if (on) nvtxRangePop();
+}
 
 int sm_count() {
   static int cached[64] = {0};
@@ -136,4 +146,10 @@ extern "C" int moe_test_set_stall(int32_t mask) {
   return MOE_OK;
 }
 
-extern "C" int moe_version(void) { return 102; }
+extern "C" int moe_set_nvtx(int32_t on) {
+  if (on != 0 && on != 1) return MOE_ERR_ARG;
+  moe::g_nvtx.store(on, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+extern "C" int moe_version(void) { return 103; }

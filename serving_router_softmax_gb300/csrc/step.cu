@@ -4,6 +4,7 @@
 // EcoSpec write-up, section 2: a round drafts a tree, selects gamma nodes and
 // verifies gamma+1 tokens in one target forward; in every MoE layer the
 // verify tokens route to their top-k experts and the union is loaded once.
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -125,10 +126,14 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StepWs ws;
   step_ws(c, workspace, &ws);
+  NvtxRange trace_step("moe_verify_step");
 
   EcoArgs ea{P, parent, own_fp, c.nseq, gamma_per_seq, {c.N, c.W, c.gamma_max, c.mode, c.eps},
              selected, union_size, dev_err, ws.verify_rows, ws.verify_conf, c.T, s, ws.ready};
-  if ((st = eco_launch(ea)) != MOE_OK) return st;
+  {
+    NvtxRange trace_sel("selection");
+    if ((st = eco_launch(ea)) != MOE_OK) return st;
+  }
 
   // Test hook for the handshake's fallback (no fault is involved): after
   // moe_test_set_stall(MOE_TEST_STALL_READY_FLAG) the heads never publish the
@@ -137,7 +142,10 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
   const bool stall_ready = (test_stall_mask() & MOE_TEST_STALL_READY_FLAG) != 0;
   const int rows = c.nseq * (c.N + 1);
   const size_t xelem = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
+  char layer_name[24];
   for (int l = 0; l < c.L; ++l) {
+    snprintf(layer_name, sizeof(layer_name), "layer %d", l);
+    NvtxRange trace_layer(layer_name);
     RouteArgs ra{node_logits + static_cast<size_t>(l) * rows * c.E, ws.verify_rows, rows,
                  c.use_bias ? ws.verify_conf : nullptr, {c.T, c.E, c.k, c.use_bias, c.cap, c.alpha},
                  ws.ids, ws.w, dev_err, s};
@@ -188,13 +196,20 @@ extern "C" int moe_verify_plan(const moe_step_cfg* cfg, const float* P, const in
       (c.gamma_max > 0 && !selected))
     return MOE_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  NvtxRange trace_plan("moe_verify_plan");
   EcoArgs ea{P, parent, own_fp, c.nseq, gamma_per_seq, {c.N, c.W, c.gamma_max, c.mode, c.eps},
              selected, union_size, dev_err, verify_rows, verify_conf, c.T, s};
-  if ((st = eco_launch(ea)) != MOE_OK) return st;
+  {
+    NvtxRange trace_sel("selection");
+    if ((st = eco_launch(ea)) != MOE_OK) return st;
+  }
   const int rows = c.nseq * (c.N + 1);
   const size_t TK = static_cast<size_t>(c.T) * c.k;
   const size_t cap = static_cast<size_t>(c.E) < TK ? c.E : TK;
+  char layer_name[24];
   for (int l = 0; l < c.L; ++l) {
+    snprintf(layer_name, sizeof(layer_name), "layer %d", l);
+    NvtxRange trace_layer(layer_name);
     RouteArgs ra{node_logits + static_cast<size_t>(l) * rows * c.E, verify_rows, rows,
                  c.use_bias ? verify_conf : nullptr, {c.T, c.E, c.k, c.use_bias, c.cap, c.alpha},
                  ids + l * TK, w + l * TK, dev_err, s};

@@ -26,6 +26,17 @@ def lib():
     return ctypes.CDLL(LIB)
 
 
+def test_nvtx_switch_is_host_only(lib):
+    """moe_set_nvtx accepts 0 and 1 and rejects anything else, with no GPU call."""
+    lib.moe_set_nvtx.argtypes = [ctypes.c_int32]
+    lib.moe_set_nvtx.restype = ctypes.c_int
+    from serving_router_softmax_gb300 import _lib as L
+    assert lib.moe_set_nvtx(1) == L.MOE_OK
+    assert lib.moe_set_nvtx(0) == L.MOE_OK
+    assert lib.moe_set_nvtx(2) == L.MOE_ERR_ARG
+    assert lib.moe_set_nvtx(-1) == L.MOE_ERR_ARG
+
+
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["moe_router_logits", "moe_route", "moe_union_permute", "moe_verify_ffn", "moe_verify_ffn_workspace",

@@ -313,6 +313,37 @@ def test_step_in_a_cuda_graph(mv):
     assert not torch.equal(y_eager, y0)
 
 
+def test_step_with_nvtx_ranges(mv):
+    """moe_set_nvtx(1) only adds host-side trace ranges: the step's and the
+    plan's outputs are bit-identical to a run without them, and switching the
+    ranges off again leaves the library in its default state."""
+    from workload import CONFIGS, gen
+    from workload import device as wdev
+    cfg = CONFIGS["batched_qwen_like"].replace(L=2, H=512, I=256)
+    wl = gen.make_workload(cfg)
+    layers = [make_layer(mv, cfg, l, "tiled") for l in range(cfg.L)]
+    t = wdev.workload_tensors(wl)
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, layout="tiled")
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"], t["x"])
+    step = mv.VerifyStep(spec, layers)
+    plan = mv.VerifyPlan(spec)
+    y0 = step(*args).clone()
+    plan(*args[:5])
+    ids0 = plan.ids.clone()
+    try:
+        mv.set_nvtx(True)
+        y1 = step(*args).clone()
+        plan(*args[:5])
+        ids1 = plan.ids.clone()
+    finally:
+        mv.set_nvtx(False)
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0 and plan.dev_err.item() == 0
+    assert torch.equal(y0, y1) and torch.equal(ids0, ids1)
+
+
 def test_ffn_fuzz_shapes(mv):
     """Random FFN shapes, dtypes and layouts against the oracle: ragged tiles
     (H, I not multiples of 128), token groups of every size, all kernel paths."""
