@@ -23,6 +23,11 @@ Readings where the page is silent (the CUDA path applies the same ones):
   the excess get no slot.
 * A resident expert keeps its home slot; a home slot inside the staging range
   or outside the pool is an error (that expert gets no slot).
+
+Parity: pinned (tests/test_oracle_residency.py: hand-worked hot lists with
+tied counts, activation counts and home slots, hand-worked staging plans
+including a staging range placed first, the capacity limit and bad homes or
+ids, and random plans against the invariants every plan must satisfy).
 """
 from __future__ import annotations
 
