@@ -809,8 +809,20 @@ def measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, conf
         one_plan()
     c1.record(stream)
     torch.cuda.synchronize()
+    ctrl_eager_ms = c0.elapsed_time(c1) / n_plan
+    # The headline step is timed as CUDA-graph replays, so its control path
+    # is too (the same launches, without the host's per-launch work).
+    g_plan = plan.capture(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+    for _ in range(3):
+        g_plan.replay()
+    torch.cuda.synchronize()
+    c0.record(stream)
+    for _ in range(n_plan):
+        g_plan.replay()
+    c1.record(stream)
+    torch.cuda.synchronize()
     ctrl_ms = c0.elapsed_time(c1) / n_plan
-    del plan
+    del g_plan, plan
 
     # ---- roofline of the FFN kernels, from pass B.
     peak, peak_kind = peaks()
@@ -843,6 +855,8 @@ def measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, conf
         "eager_ms_per_step": eager_ms,
         "control_path_ms": ctrl_ms,
         "control_path_frac": ctrl_ms / max(ms_step, 1e-9),
+        "control_path_eager_ms": ctrl_eager_ms,
+        "control_path_eager_frac": ctrl_eager_ms / max(eager_ms, 1e-9),
         "control_path_frac_events": sum(prof[k]["ms"] for k in ("eco_select", "route", "union_permute"))
         / n_c / max(ms_step, 1e-9),
         "clocks": clk.summary(),
@@ -1039,7 +1053,8 @@ def workload_entry(core, cfg, wl, extra=None):
                     "selection": "marginal" if cfg.mode == 0 else "static"}}
     for k in ("value", "ms_per_step", "latency_us", "tokens_per_s", "unique_expert_gb_per_step",
               "frac_of_peak_step", "frac_of_8tbs_step", "eager_ms_per_step", "control_path_ms",
-              "control_path_frac", "kernel_ms_per_step", "clocks", "e2e", "launches_per_step"):
+              "control_path_frac", "control_path_eager_frac", "kernel_ms_per_step", "clocks", "e2e",
+              "launches_per_step"):
         d[k] = core[k]
     d["unit"] = "GB/s"
     d["union_per_layer"] = sum(core["unique_experts_per_layer"]) / len(core["unique_experts_per_layer"])
@@ -1144,8 +1159,8 @@ def ours(args, rank, ws, local):
     }
     for k in ("latency_us", "tokens_per_s", "unique_experts_per_layer", "unique_expert_gb_per_step",
               "frac_of_peak_step", "frac_of_8tbs_step", "roofline", "kernel_ms_per_step", "launch",
-              "eager_ms_per_step", "control_path_ms", "control_path_frac", "control_path_frac_events",
-              "clocks", "e2e", "gpu_launches"):
+              "eager_ms_per_step", "control_path_ms", "control_path_frac", "control_path_eager_ms",
+              "control_path_eager_frac", "control_path_frac_events", "clocks", "e2e", "gpu_launches"):
         result[k] = core[k]
     result.update({"router_logits": router, "cost_model": cost_model, "s2_expand": expansion,
                    "residency": residency, "reuse_bias": bias_sweep, "gamma_sweep": gsweep})

@@ -513,6 +513,21 @@ class VerifyPlan:
                "moe_verify_plan")
         return self
 
+    def capture(self, P, parent, own_fp, gamma_per_seq, node_logits, steps: int = 1):
+        """Records `steps` control paths on these input tensors into a CUDA graph and returns it
+        (as VerifyStep.capture: no host launch work at replay; inputs are read at replay time)."""
+        args = (P, parent, own_fp, gamma_per_seq, node_logits)
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self(*args)  # warm-up outside the capture
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(steps):
+                self(*args)
+        return graph
+
 
 def s2_expand(P: torch.Tensor, parent: torch.Tensor, own_fp: torch.Tensor, T_AR: float, T_exp: float,
               C_draft: float = 0.0, dev_err: Optional[torch.Tensor] = None, stream=None,

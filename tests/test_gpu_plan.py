@@ -155,3 +155,36 @@ def test_plan_fuzz_small_configs(mv):
         cfg = gen.small_case(f"fuzz{trial}", **kw)
         wl, plan = plan_for(mv, cfg)
         check_against_oracle(wl, plan)
+
+
+def test_plan_in_a_cuda_graph(mv):
+    """The control path alone is capturable: replaying a CUDA graph of it gives
+    the eager plan's outputs bit for bit."""
+    from workload import CONFIGS, gen
+    from workload import device as wdev
+    cfg = CONFIGS["gpt_oss_120b_like"].replace(L=3)
+    wl = gen.make_workload(cfg)
+    t = wdev.workload_tensors(wl, "cuda")
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap, alpha=cfg.alpha)
+    args = (t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+    eager = mv.VerifyPlan(spec)
+    eager(*args)
+    plan = mv.VerifyPlan(spec)
+    g = plan.capture(*args)
+    for x in (plan.ids, plan.unique, plan.perm_token, plan.n_unique):
+        x.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    assert plan.dev_err.item() == 0 and eager.dev_err.item() == 0
+    for name in ("selected", "verify_rows", "verify_conf", "ids", "w", "n_unique", "unique", "offsets",
+                 "perm_token", "perm_slot", "inv", "reuse_ratio"):
+        a, b = getattr(plan, name), getattr(eager, name)
+        if name in ("unique", "offsets"):
+            for l in range(cfg.L):
+                U = int(eager.n_unique[l])
+                n = U + 1 if name == "offsets" else U
+                assert torch.equal(a[l, :n], b[l, :n]), name
+        else:
+            assert torch.equal(a, b), name
