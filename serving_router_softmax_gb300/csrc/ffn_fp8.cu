@@ -413,6 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (!ti.prow_ok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
+      // A tile this CTA shares: if every other contributor has already
+      // counted in (acquire, read before this segment's k-blocks), this CTA
+      // is the last to arrive and can finish the tile at its end without
+      // writing its own partials or taking the atomic.
+      bool others_done = false;
+      if (etid == 0 && !(u0 == 0 && u1 == KU)) {
+        const long long t0 = (long long)t * KU;
+        const int cf0 = static_cast<int>(seg_owner(t0, total, G));
+        const int cl0 = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
+        int cnt;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cnt) : "l"(p.tile_cnt + t) : "memory");
+        others_done = cnt == cl0 - cf0;
+      }
       // gate/up is token-dense (column n is token n): the expert's tokens as
       // a mask over the columns, a token's rank in it giving its Hq row
       const int nb = kGateUp ? p.NM : ti.np;
@@ -538,26 +551,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = u0 == 0 && u1 == KU;
       bool finished = whole;
       if (!whole) {
-        float* P = p.partials + ((size_t)c * 2 + (t == first_tile_c ? 0 : 1)) * (size_t)(2 * p.NM * 128);
-#pragma unroll
-        for (int n = 0; n < kMaxNM; ++n) {
-          if (n < nb) {
-            P[(size_t)n * 128 + r] = ga[n];
-            if (kGateUp) P[(size_t)(p.NM + n) * 128 + r] = ua[n];
-          }
-        }
-        tc::named_bar_sync(1, kEpiThreads);
-        if (etid == 0) {
-          __threadfence();
-          *bcast = atomicAdd(&p.tile_cnt[t], 1);
-        }
-        tc::named_bar_sync(1, kEpiThreads);
-        const int arrived = *bcast;
         const long long t0 = (long long)t * KU;
         const int cf = static_cast<int>(seg_owner(t0, total, G));
         const int cl = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
+        if (etid == 0) *bcast = others_done ? -1 : 0;
         tc::named_bar_sync(1, kEpiThreads);
-        if (arrived == cl - cf) {
+        bool last = *bcast == -1;
+        tc::named_bar_sync(1, kEpiThreads);  // bcast is reused below
+        if (!last) {
+          float* P = p.partials + ((size_t)c * 2 + (t == first_tile_c ? 0 : 1)) * (size_t)(2 * p.NM * 128);
+#pragma unroll
+          for (int n = 0; n < kMaxNM; ++n) {
+            if (n < nb) {
+              P[(size_t)n * 128 + r] = ga[n];
+              if (kGateUp) P[(size_t)(p.NM + n) * 128 + r] = ua[n];
+            }
+          }
+          tc::named_bar_sync(1, kEpiThreads);
+          if (etid == 0) {
+            __threadfence();
+            *bcast = atomicAdd(&p.tile_cnt[t], 1);
+          }
+          tc::named_bar_sync(1, kEpiThreads);
+          last = *bcast == cl - cf;
+          tc::named_bar_sync(1, kEpiThreads);
+        }
+        if (last) {
           __threadfence();
           finished = true;
           // Sum in CTA order from zero, 16 columns at a time: each other
