@@ -453,13 +453,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kGateUp && !ti.prow_ok && etid == 0) flag_error(p.dev_err, MOE_DEV_BAD_ID);
       const int gtok = (kGateUp && p.dense) ? group_token(p, ti, lane) : 0;
+      // A tile this CTA shares: if every other contributor has already
+      // counted in (acquire, read before waiting for this tile's
+      // accumulator), this CTA is the last to arrive and finishes the tile
+      // without writing its own partials or taking the atomic.
+      bool others_done = false;
+      if (etid == 0 && !(u0 == 0 && u1 == KU)) {
+        const long long t0 = (long long)t * KU;
+        const int cf0 = static_cast<int>(seg_owner(t0, total, G));
+        const int cl0 = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
+        int cnt;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cnt) : "l"(p.tile_cnt + t) : "memory");
+        others_done = cnt == cl0 - cf0;
+      }
       // Every epilogue thread waits; the outcome is made uniform through a
       // shared vote so that no thread is left behind at a named barrier.
       if (!tc::mbar_wait_bounded(&accf[acc], acc_phase[acc], abort_flag, kWaitBudgetNs)) {
         *abort_flag = 1;
         flag_error(p.dev_err, MOE_DEV_TIMEOUT);
       }
+      if (etid == 0) *bcast = others_done ? -1 : 0;
       tc::named_bar_sync(1, kEpiThreads);
+      const bool early_last = *bcast == -1;
       if (*abort_flag) break;
       tc::tc_fence_after();
       uint32_t mask = 0;
@@ -488,7 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const int ncols = (kGateUp && p.dense) ? p.NM : ti.np;
       bool finished = whole;
-      if (!whole) {
+      if (!whole && early_last) {
+        const long long t0 = (long long)t * KU;
+        cf = static_cast<int>(seg_owner(t0, total, G));
+        cl = static_cast<int>(seg_owner(t0 + KU - 1, total, G));
+        finished = true;
+        __threadfence();
+      } else if (!whole) {
         // Split tile: this CTA's sums go to its partial slot first.
         for (int cc = 0; cc < ncols / 16; ++cc) {
           float g[16], v[16];
