@@ -116,6 +116,27 @@ def test_ffn_matches_oracle(mv, dtype, H, I, E, k, T, layout):
     assert err < TOL[dtype], (err, elementwise_err(yh, ref["y"]))
 
 
+@pytest.mark.parametrize("dtype,layout", [("bf16", "tiled"), ("bf16", "rowmajor"), ("e4m3", "tiled"),
+                                          ("f32", "rowmajor")])
+def test_ffn_empty_verify_set(mv, dtype, layout):
+    """T = 0, the empty verify set: the union is empty, and the FFN call succeeds
+    without launching anything or writing a flag."""
+    from workload import gen
+    cfg = gen.MoEConfig("ffn_empty", L=1, H=256, E=16, k=4, I=256, dtype=dtype, seed=5)
+    layer = make_layer(mv, cfg, 0, layout)
+    xdt = torch.float32 if dtype == "f32" else torch.int16
+    x = torch.zeros((0, cfg.H), dtype=xdt, device="cuda")
+    dev_err = mv.new_dev_err()
+    up = mv.union_permute(torch.zeros((0, cfg.k), dtype=torch.int32, device="cuda"), cfg.E, dev_err=dev_err)
+    w = torch.zeros((0, cfg.k), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    n0 = mv.launch_count()
+    y = mv.verify_ffn(x, cfg.k, layer, up, w, dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert mv.launch_count() == n0
+    assert y.shape == (0, cfg.H) and dev_err.item() == 0 and up["n_unique"].item() == 0
+
+
 def test_ffn_device_fill_matches_host_generator(mv):
     """The device weight fill and the host regeneration agree bit for bit."""
     from workload import gen
