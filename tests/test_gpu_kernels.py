@@ -90,6 +90,55 @@ def test_route_bias_matches_oracle(mv, T, E, k, cap, alpha):
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
 
 
+def crowded_rows(rng, T, E, k):
+    """Rows that load the top-k's warp layout (expert e sits in lane e mod 32)
+    unevenly.  Kind 0: the winners crowd into k + 1 lanes, each of which holds
+    only winners, in an order that interleaves the lanes' values; kind 1: one
+    value everywhere (the lower id decides every slot); kind 2: values on a
+    coarse grid (many ties); kind 3: plain normal rows."""
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lanes = min(32, E)
+    K = min(k + 1, lanes)
+    for t in range(T):
+        kind = t % 4
+        if kind == 0:
+            npl = -(-E // 32)
+            for r, lane in enumerate(rng.choice(lanes, size=K, replace=False)):
+                ex = np.arange(lane, E, 32)
+                lg[t, ex] = 10.0 + r * npl + np.arange(len(ex))
+        elif kind == 1:
+            lg[t] = 0.5
+        elif kind == 2:
+            lg[t] = np.round(lg[t] * 2.0) / 2.0
+    return lg
+
+
+@pytest.mark.parametrize("T,E,k", [(8, 128, 8), (8, 128, 16), (8, 256, 8), (8, 300, 16), (8, 1024, 16),
+                                   (8, 40, 4), (8, 17, 16)])
+def test_route_crowded_and_tied_rows(mv, T, E, k):
+    from oracle import moe_layer as ml
+    lg = crowded_rows(np.random.default_rng(E * 31 + k), T, E, k)
+    dev_err = mv.new_dev_err()
+    ids, w = mv.route(cuda(lg), k, dev_err=dev_err)
+    torch.cuda.synchronize()
+    rid, rw = ml.route(lg, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
+    assert dev_err.item() == 0
+
+
+@pytest.mark.parametrize("T,E,k,cap", [(8, 128, 16, 8), (8, 256, 8, 12), (9, 1024, 16, 12), (8, 20, 16, 3)])
+def test_route_bias_crowded_and_tied_rows(mv, T, E, k, cap):
+    from oracle import moe_layer as ml
+    rng = np.random.default_rng(E * 17 + k)
+    lg = crowded_rows(rng, T, E, k)
+    wc = rng.uniform(0, 1, T).astype(np.float32)
+    ids, w = mv.route(cuda(lg), k, w_conf=cuda(wc), cap=cap, alpha=0.5)
+    rid, rw = ml.route(ml.reuse_bias(lg, wc, k, cap, 0.5), k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
+
+
 # ------------------------------------------------------------------ union
 @pytest.mark.parametrize("T,E,k", [(1, 16, 2), (5, 128, 8), (20, 128, 8), (28, 256, 8),
                                    (256, 1024, 16), (7, 8, 8), (4096, 16, 2)])

@@ -72,8 +72,7 @@ SMALL = [dict(name="plan_bf16"), dict(name="plan_bias", use_bias=True, cap=8, al
          dict(name="plan_static", mode=1),
          dict(name="plan_batch_global", nseq=4, ragged=True, tau=0.1, mode=2),
          dict(name="plan_batch_global_bias", nseq=3, mode=2, use_bias=True, cap=6, alpha=0.5),
-         # the head's biased pass ranks the candidates (unbiased top-k | E*) when lam_b >= 0 and there
-         # are at most 32 of them; otherwise it runs the k rounds over every expert
+         # negative and zero lam_b: the biased pass may lower the preferred experts
          dict(name="plan_bias_neg_alpha", use_bias=True, cap=8, alpha=-0.5),
          dict(name="plan_bias_zero_alpha", use_bias=True, cap=8, alpha=0.0),
          dict(name="plan_bias_big_cap", E=64, k=6, use_bias=True, cap=40, alpha=0.25),
@@ -127,6 +126,30 @@ def test_plan_bias_with_tied_logits(mv, alpha):
     spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
                        I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
                        eps=cfg.eps, use_bias=True, cap=cfg.cap, alpha=cfg.alpha)
+    plan = mv.VerifyPlan(spec)
+    plan(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
+    torch.cuda.synchronize()
+    check_against_oracle(wl, plan)
+
+
+@pytest.mark.parametrize("E,k,use_bias", [(128, 16, True), (256, 16, True), (1024, 16, False), (128, 8, False)])
+def test_plan_crowded_and_tied_rows(mv, E, k, use_bias):
+    """The layer head's top-k on rows whose winners crowd into a few lanes of
+    its warp layout, and on all-equal and coarse-grid rows (test_gpu_kernels'
+    crowded_rows), with and without the reuse bias."""
+    from test_gpu_kernels import crowded_rows
+    from workload import device as wdev
+    from workload import gen
+    kw = dict(use_bias=True, cap=8, alpha=0.5) if use_bias else {}
+    cfg = gen.small_case(f"plan_crowded_{E}_{k}", L=2, E=E, k=k, **kw)
+    wl = gen.make_workload(cfg)
+    shape = wl.logits.shape
+    flat = wl.logits.reshape(-1, E)
+    wl.logits = crowded_rows(np.random.default_rng(E + k), flat.shape[0], E, k).reshape(shape)
+    t = wdev.workload_tensors(wl, "cuda")
+    spec = mv.StepSpec(L=cfg.L, nseq=cfg.nseq, N=wl.parent.shape[0], W=cfg.W, E=cfg.E, k=cfg.k, H=cfg.H,
+                       I=cfg.I, dtype=cfg.dtype, T=wl.T, gamma_max=int(wl.gamma.max()), mode=cfg.mode,
+                       eps=cfg.eps, use_bias=cfg.use_bias, cap=cfg.cap, alpha=cfg.alpha)
     plan = mv.VerifyPlan(spec)
     plan(t["P"], t["parent"], t["own_fp"], t["gamma"], t["logits"])
     torch.cuda.synchronize()
