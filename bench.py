@@ -116,41 +116,67 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling during the timed region."""
+    """nvidia-smi clocks/throttle sampling around and during the timed region.
+
+    A reader thread collects one line every 50 ms with its host time.  Entering
+    waits (at most 3 s) until the first line has arrived, so the sampler is
+    live before the caller loads the GPU; the caller marks the timed region
+    (`mark_start`, `mark_end`) and keeps the same load on the GPU for a few
+    hundred ms on either side of it, so that a region of tens of ms still
+    has samples under its own load around it."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
+        self.lines = []  # (host time, line)
+        self.t_start = self.t_end = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t0 = time.perf_counter()
+        while not self.lines and time.perf_counter() - t0 < 3.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.lines.clear()  # the first line may precede the load
         return self
 
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_end(self):
+        self.t_end = time.perf_counter()
+
     def __exit__(self, *a):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self.proc.wait()
+            self.reader.join(timeout=5)
 
     def summary(self):
-        if not getattr(self, "out", ""):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm, smax, reasons = [], [], set()
+        sm, smax, reasons, inside = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
+        for t, line in list(self.lines):
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -162,11 +188,15 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+            if self.t_start is not None and self.t_end is not None and self.t_start <= t <= self.t_end:
+                inside += 1
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        loaded = [v for v in sm if v > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_min_mhz": min(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": inside,
+                "interval_ms": self.INTERVAL_MS,
+                "window": "the timed region plus about 0.3 s of the same work before and after it"}
 
 
 def kernel_source_hash():
@@ -758,8 +788,22 @@ def measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, conf
 
     # ---- pass A (headline): device-timed region, inputs resident in HBM,
     # unique-expert bytes per step >> L2; no per-kernel events.
+    def keep_loaded(fn, seconds=0.3):
+        # untimed repeats of the same step around the timed region, so that
+        # the clock samples see this load (the region itself is tens of ms)
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(4):
+                fn()
+            torch.cuda.synchronize()
+
+    step_fn = graph.replay if graph is not None else one
     with ClockSampler(local) as clk:
-        ms_local = timed(graph.replay if graph is not None else one)
+        keep_loaded(step_fn)
+        clk.mark_start()
+        ms_local = timed(step_fn)
+        clk.mark_end()
+        keep_loaded(step_fn)
     value, ms_total = job_throughput(bytes_step * args.steps, ms_local, ws)
     ms_step = ms_total / args.steps
     total_bytes = sum_over_ranks(bytes_step * args.steps, ws)
