@@ -881,6 +881,16 @@ def measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, conf
                       "avg_launch_us": k_ms * 1e3 / max(pb[cls]["launches"], 1),
                       "launches": pb[cls]["launches"]}
     roofline = dict(lines["ffn_gate_up"])
+    # Both FFN launches together: unaffected by the L2 prefetch that moves
+    # part of the next layer's gate/up bytes into the down launch's time.
+    pair_ms = pb["ffn_gate_up"]["ms"] + pb["ffn_down"]["ms"]
+    pair_gbs = sum(n_unique) * expert_bytes(cfg) * args.steps / (pair_ms / 1e3) / 1e9 if pair_ms > 0 else None
+    roofline["ffn_pair_frac"] = pair_gbs / peak if pair_gbs else None
+    if cfg.dtype == "bf16" and layout == "tiled" and cfg.L > 1:
+        roofline["l2_prefetch"] = ("each down launch but the last asks L2 to fetch 30 MB of the next layer's "
+                                   "predicted experts' gate/up weights (the selection's footprint union), which "
+                                   "that gate/up launch then reads from L2: its fraction counts those bytes, the "
+                                   "down fraction carries their time; ffn_pair_frac is unaffected")
     traffic_unit = committed_traffic(config_name)
     roofline["traffic"] = traffic_unit * sum(n_unique) / cfg.L if traffic_unit is not None else None
     roofline["timed_in"] = "pass B: the K timed steps repeated with events around the FFN launches only"
@@ -1105,6 +1115,7 @@ def workload_entry(core, cfg, wl, extra=None):
     r = core["roofline"]
     d["roofline"] = {"gate_up_frac": r["frac"], "gate_up_gbs": r["achieved"],
                      "down_frac": r["ffn_down"]["frac"], "down_gbs": r["ffn_down"]["achieved"],
+                     "ffn_pair_frac": r.get("ffn_pair_frac"),
                      "peak": r["peak"], "peak_kind": r["peak_kind"], "traffic": r["traffic"]}
     if extra:
         d.update(extra)

@@ -156,6 +156,14 @@ struct FfnArgs {
   bool head_prepared;
   int32_t* ready_flag;
   int32_t ready_value;
+  // Whole step, bf16 tensor-core layers: once a down CTA has issued its last
+  // weight load it asks L2 to fetch a share of the next layer's predicted
+  // experts' gate/up weights (see TcParams::pf_base).  NULL: none.
+  const uint8_t* pf_base;    // next layer's tiled gate/up weights
+  long long pf_expert_bytes; // per expert
+  long long pf_budget;       // bytes over the whole grid
+  const uint32_t* pred_B;    // [pred_rows][pred_W] predicted (layer, expert) bits
+  int32_t pred_rows, pred_W, pred_bit0;
 };
 size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_validate(const moe_layer_weights& lw, int T, int k);
@@ -254,6 +262,11 @@ struct EcoArgs {
   // every step (so that a value left by an interrupted step is never taken
   // for a fresh one).  NULL: nothing to clear.
   int32_t* ready_flag;
+  // Optional: the final expert buffer B of each sequence ([nseq][W] words;
+  // one buffer for the whole batch in mode 2, written to row 0 with the
+  // other rows zero): the predicted (layer, expert) union of the verify
+  // tokens other than the roots.
+  uint32_t* pred_B;
 };
 int eco_validate(const eco_cfg& c, int nseq);
 int eco_launch(const EcoArgs& a);

@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(512) eco_kernel(
     const uint32_t* __restrict__ own_fp, const int32_t* __restrict__ gamma_per_seq, int N, int W,
     int gamma_max, int mode, int eps_shift, int fast_key, int32_t* __restrict__ selected,
     int32_t* __restrict__ union_size, int32_t* dev_err, int32_t* __restrict__ verify_rows,
-    float* __restrict__ verify_conf, int T_expected, int nseq, int32_t* ready_flag) {
+    float* __restrict__ verify_conf, int T_expected, int nseq, int32_t* ready_flag,
+    uint32_t* __restrict__ pred_B) {
   extern __shared__ uint32_t smem[];
   if (ready_flag && blockIdx.x == 0 && threadIdx.x == 0) *ready_flag = 0;
   uint32_t* traj = smem;                 // [N][W]
@@ -261,6 +262,8 @@ __global__ void __launch_bounds__(512) eco_kernel(
     for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
     if (lane == 0) union_size[s] = c;
   }
+  if (pred_B)
+    for (int w = threadIdx.x; w < W; w += blockDim.x) pred_B[(size_t)s * W + w] = B[w];
   for (int r = gamma + threadIdx.x; r < gamma_max; r += blockDim.x) sel[r] = -1;
 
   if (verify_rows) {
@@ -282,7 +285,8 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
     const float* __restrict__ P, const int32_t* __restrict__ parent, const uint32_t* __restrict__ own_fp,
     const int32_t* __restrict__ gamma_per_seq, int N, int W, int nseq, int gamma_max, int eps_shift,
     int32_t* __restrict__ selected, int32_t* __restrict__ union_size, int32_t* dev_err,
-    int32_t* __restrict__ verify_rows, float* __restrict__ verify_conf, int T_expected, int32_t* ready_flag) {
+    int32_t* __restrict__ verify_rows, float* __restrict__ verify_conf, int T_expected, int32_t* ready_flag,
+    uint32_t* __restrict__ pred_B) {
   extern __shared__ uint32_t smem[];
   if (ready_flag && threadIdx.x == 0) *ready_flag = 0;
   const int G = nseq * N;
@@ -404,6 +408,8 @@ __global__ void __launch_bounds__(512) eco_batch_kernel(
     for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
     if (lane == 0) union_size[s] = c;
   }
+  if (pred_B)  // the batch's one buffer in row 0, the other rows empty
+    for (int i = threadIdx.x; i < nseq * W; i += blockDim.x) pred_B[i] = i < W ? B[i] : 0u;
   if (verify_rows && threadIdx.x == 0) {
     int tok = 0;
     for (int s = 0; s < nseq; ++s) {
@@ -455,7 +461,8 @@ int eco_launch(const EcoArgs& a) {
     LaunchScope ls(kProfEco, a.stream);
     eco_batch_kernel<<<1, 512, smem, a.stream>>>(a.P, a.parent, a.own_fp, a.gamma, c.N, c.W, a.nseq, c.gamma_max,
                                                   eps_shift(c.eps), a.selected, a.union_size, a.dev_err,
-                                                  a.verify_rows, a.verify_conf, a.T_expected, a.ready_flag);
+                                                  a.verify_rows, a.verify_conf, a.T_expected, a.ready_flag,
+                                                  a.pred_B);
     return check_launch();
   }
   size_t smem = (static_cast<size_t>(c.N) * c.W + c.W) * sizeof(uint32_t);
@@ -470,7 +477,7 @@ int eco_launch(const EcoArgs& a) {
                                                   (static_cast<long long>(c.W) * 32) << eps_shift(c.eps) < (1ll << 24) - 1,
                                                   a.selected, a.union_size, a.dev_err,
                                                   a.verify_rows, a.verify_conf, a.T_expected,
-                                                  a.nseq, a.ready_flag);
+                                                  a.nseq, a.ready_flag, a.pred_B);
   return check_launch();
 }
 
@@ -485,6 +492,6 @@ extern "C" int eco_select(const float* P, const int32_t* parent, const uint32_t*
   if (nseq > 0 && (!P || !parent || !own_fp || !union_size || (cfg->gamma_max > 0 && !selected)))
     return MOE_ERR_ARG;
   moe::EcoArgs a{P, parent, own_fp, nseq, gamma_per_seq, *cfg, selected, union_size, dev_err,
-                 nullptr, nullptr, 0, static_cast<cudaStream_t>(stream)};
+                 nullptr, nullptr, 0, static_cast<cudaStream_t>(stream), nullptr, nullptr};
   return moe::eco_launch(a);
 }

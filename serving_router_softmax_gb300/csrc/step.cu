@@ -13,6 +13,15 @@
 namespace moe {
 namespace {
 
+// Bytes of the next layer's predicted experts' gate/up weights that a
+// layer's down CTAs ask L2 to fetch once they have issued their last weight
+// load (about 200 KB per CTA).  HBM is underused from the end of a down
+// launch until the next layer's gate/up stream starts (the down launch's
+// last CTAs, the combine, the next head); the next gate/up then reads these
+// bytes from L2.  Larger budgets delay the down launch's end by more than
+// they save.
+constexpr long long kPrefetchBudget = 30ll << 20;
+
 struct StepWs {
   int32_t* verify_rows;
   float* verify_conf;
@@ -25,6 +34,7 @@ struct StepWs {
   int32_t* inv;
   float* ratio;
   int32_t* ready;  // union-ready word of the head -> gate/up handshake
+  uint32_t* pred_B;  // [nseq][W] the selection's expert buffers (predicted union)
   void* ffn;
   size_t ffn_bytes;
 };
@@ -41,6 +51,7 @@ size_t step_ws(const moe_step_cfg& c, void* base, StepWs* out) {
   size_t o_rows = take(T * 4), o_conf = take(T * 4), o_ids = take(TK * 4), o_w = take(TK * 4);
   size_t o_u = take(cap * 4), o_off = take((cap + 1) * 4), o_pt = take(TK * 4), o_ps = take(TK * 4);
   size_t o_inv = take(TK * 4), o_ratio = take(4), o_ready = take(4);
+  size_t o_pred = take(static_cast<size_t>(c.nseq) * (c.W > 0 ? c.W : 0) * 4);
   moe_layer_weights lw{c.H, c.I, c.E, c.dtype, c.layout, nullptr, nullptr, nullptr, nullptr};
   size_t fb = ffn_workspace_bytes(lw, c.T, c.k);
   size_t o_ffn = take(fb);
@@ -57,6 +68,7 @@ size_t step_ws(const moe_step_cfg& c, void* base, StepWs* out) {
     out->inv = reinterpret_cast<int32_t*>(b + o_inv);
     out->ratio = reinterpret_cast<float*>(b + o_ratio);
     out->ready = reinterpret_cast<int32_t*>(b + o_ready);
+    out->pred_B = reinterpret_cast<uint32_t*>(b + o_pred);
     out->ffn = b + o_ffn;
     out->ffn_bytes = fb;
   }
@@ -129,7 +141,7 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
   NvtxRange trace_step("moe_verify_step");
 
   EcoArgs ea{P, parent, own_fp, c.nseq, gamma_per_seq, {c.N, c.W, c.gamma_max, c.mode, c.eps},
-             selected, union_size, dev_err, ws.verify_rows, ws.verify_conf, c.T, s, ws.ready};
+             selected, union_size, dev_err, ws.verify_rows, ws.verify_conf, c.T, s, ws.ready, ws.pred_B};
   {
     NvtxRange trace_sel("selection");
     if ((st = eco_launch(ea)) != MOE_OK) return st;
@@ -175,6 +187,20 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     FfnArgs fa{xl, ws.verify_rows, rows, c.T, c.k, layers[l], n_unique + l, ws.unique, ws.offsets,
                ws.perm_token, ws.inv, ws.w, y + static_cast<size_t>(l) * c.T * c.H, ws.ffn,
                ws.ffn_bytes, dev_err, s, true, head_prep, ws.ready, l % 65535 + 1};
+    // The next layer's predicted experts (the selection's buffers B), for
+    // the L2 prefetch at the end of this layer's down launch.
+    if (l + 1 < c.L && c.W > 0) {
+      const moe_layer_weights& nx = layers[l + 1];
+      if (nx.dtype == MOE_DTYPE_BF16 && nx.layout == MOE_LAYOUT_TILED && !nx.pool) {
+        fa.pf_base = static_cast<const uint8_t*>(nx.w_gate_up);
+        fa.pf_expert_bytes = static_cast<long long>((nx.I + 127) / 128) * 256 * nx.H * 2;
+        fa.pf_budget = kPrefetchBudget;
+        fa.pred_B = ws.pred_B;
+        fa.pred_rows = c.nseq;
+        fa.pred_W = c.W;
+        fa.pred_bit0 = (l + 1) * c.E;
+      }
+    }
     if ((st = ffn_launch(fa)) != MOE_OK) return st;
   }
   return MOE_OK;
