@@ -201,11 +201,11 @@ class ClockSampler:
 
 def kernel_source_hash():
     """Hash of the sources that define the bf16 FFN kernels (their translation
-    unit, its PTX wrappers and the stream-K order); ties committed ncu traffic
-    to the code."""
+    unit, its PTX wrappers, the stream-K order and the next-layer L2
+    prefetch); ties committed ncu traffic to the code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_router_softmax_gb300", "csrc")
-    for f in ("ffn_tc.cu", "ffn_internal.cuh", "tc_ptx.cuh", "stream_k.cuh"):
+    for f in ("ffn_tc.cu", "ffn_internal.cuh", "tc_ptx.cuh", "stream_k.cuh", "l2_prefetch.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -886,7 +886,7 @@ def measure_step(mv, cfg, wl, layers, layout, args, dev, stream, ws, local, conf
     pair_ms = pb["ffn_gate_up"]["ms"] + pb["ffn_down"]["ms"]
     pair_gbs = sum(n_unique) * expert_bytes(cfg) * args.steps / (pair_ms / 1e3) / 1e9 if pair_ms > 0 else None
     roofline["ffn_pair_frac"] = pair_gbs / peak if pair_gbs else None
-    if cfg.dtype == "bf16" and layout == "tiled" and cfg.L > 1:
+    if cfg.dtype in ("bf16", "e4m3") and layout == "tiled" and cfg.L > 1:
         roofline["l2_prefetch"] = ("each down launch but the last asks L2 to fetch 30 MB of the next layer's "
                                    "predicted experts' gate/up weights (the selection's footprint union), which "
                                    "that gate/up launch then reads from L2: its fraction counts those bytes, the "

@@ -130,6 +130,23 @@ __device__ __forceinline__ int weight_slot(const int32_t* slot_of, int n_slots, 
   return s >= 0 && s < n_slots ? s : -1;
 }
 
+// The next layer's predicted experts, prefetched into L2 by the tensor-core
+// down kernels of the whole step once each CTA has issued its last weight
+// load: HBM is underused from the end of a down launch until the next
+// layer's gate/up stream starts.  The predicted experts are the set bits
+// [bit0, bit0 + E) of the OR of `rows` rows of pred_B (W words each: the
+// selection's final expert buffers); expert e's gate/up weights are the
+// bytes [e * expert_bytes, (e + 1) * expert_bytes) of base (tiled layout,
+// resident weights).  `budget` bytes over the whole grid, split evenly over
+// the predicted experts from the start of each one's weights.
+struct NextLayerPrefetch {
+  const uint8_t* base;  // NULL: no prefetch
+  long long expert_bytes;
+  long long budget;
+  const uint32_t* pred_B;
+  int32_t rows, W, bit0;
+};
+
 // Host-side FFN internals shared by the standalone call and the whole step.
 struct FfnArgs {
   const void* x;            // [*, H] activations (fp32 or bf16 bits)
@@ -156,14 +173,9 @@ struct FfnArgs {
   bool head_prepared;
   int32_t* ready_flag;
   int32_t ready_value;
-  // Whole step, bf16 tensor-core layers: once a down CTA has issued its last
-  // weight load it asks L2 to fetch a share of the next layer's predicted
-  // experts' gate/up weights (see TcParams::pf_base).  NULL: none.
-  const uint8_t* pf_base;    // next layer's tiled gate/up weights
-  long long pf_expert_bytes; // per expert
-  long long pf_budget;       // bytes over the whole grid
-  const uint32_t* pred_B;    // [pred_rows][pred_W] predicted (layer, expert) bits
-  int32_t pred_rows, pred_W, pred_bit0;
+  // Whole step, tensor-core layers: the next layer's predicted experts,
+  // which the down CTAs ask L2 to fetch after their last weight load.
+  NextLayerPrefetch pf;
 };
 size_t ffn_workspace_bytes(const moe_layer_weights& lw, int T, int k);
 int ffn_validate(const moe_layer_weights& lw, int T, int k);

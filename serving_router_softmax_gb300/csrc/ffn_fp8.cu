@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "l2_prefetch.cuh"
 #include "ffn_internal.cuh"
 #include "tc_ptx.cuh"
 #include "stream_k.cuh"
@@ -83,6 +84,9 @@ struct Fp8Params {
   int32_t* ready_flag;
   int32_t ready_value;
   int32_t* ready_clear;
+  // down only: the next layer's predicted experts, which each CTA asks L2
+  // to fetch (its round-robin share) once it has issued its last weight load.
+  NextLayerPrefetch pf;
 };
 
 struct Tile {
@@ -307,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!dep_done) resolve();
       *issued = n_issued;
+      if (!kGateUp && p.pf.base && !*abort_flag) l2_prefetch_next_layer(p.pf, p.E, c, gridDim.x);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -977,6 +982,7 @@ int ffn_fp8_launch(const FfnArgs& a) {
       return MOE_ERR_CUDA;
   }
   // down + combine
+  fp.pf = a.pf;
   fp.M = lw.H;
   fp.K = lw.I;
   fp.KS = g.KS_d;

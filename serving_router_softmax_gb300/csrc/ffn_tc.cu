@@ -39,6 +39,7 @@
 #include "ffn_internal.cuh"
 #include "tc_ptx.cuh"
 #include "stream_k.cuh"
+#include "l2_prefetch.cuh"
 
 namespace moe {
 namespace {
@@ -91,18 +92,9 @@ struct TcParams {
   int32_t* ready_clear;
   const int32_t* slot_of;  // expert -> weight slot (NULL: identity)
   int n_slots;
-  // down only: after its last weight load each CTA asks L2 to fetch its share
-  // (pieces c, c + grid, ...) of the next layer's predicted experts' gate/up
-  // weights: pf_pieces pieces of kPfPiece bytes from the start of each
-  // expert whose bit is set in [pred_bit0, pred_bit0 + E) of the OR of
-  // pred_rows rows of pred_B.  The gap between this launch's last CTAs and
-  // the next layer's gate/up stream leaves HBM idle; the prefetched lines
-  // are read from L2 by that launch.  NULL pf_base: none.
-  const uint8_t* pf_base;
-  long long pf_expert_bytes;
-  long long pf_budget;
-  const uint32_t* pred_B;
-  int pred_rows, pred_W, pred_bit0;
+  // down only: the next layer's predicted experts, which each CTA asks L2
+  // to fetch (its round-robin share) once it has issued its last weight load.
+  NextLayerPrefetch pf;
 };
 
 struct Tile {
@@ -110,55 +102,6 @@ struct Tile {
   bool ok, prow_ok;
 };
 
-// The L2 prefetch of TcParams::pf_base, issued by one thread of CTA c of G.
-// The predicted experts are listed in ascending order; the budget is split
-// evenly over them in kPfPiece pieces from the start of each expert's
-// weights.  Prefetching changes no result.
-constexpr long long kPfPiece = 32 << 10;
-__device__ __noinline__ void prefetch_next_layer(const TcParams& p, int c, int G) {
-  const int EW = (p.E + 31) >> 5;
-  uint32_t mask[32];
-  int n = 0;
-  for (int w = 0; w < EW; ++w) {
-    uint32_t m = 0;
-    const long long b = p.pred_bit0 + 32ll * w;
-    const long long w0 = b >> 5;
-    const int sh = static_cast<int>(b & 31);
-    for (int r = 0; r < p.pred_rows; ++r) {
-      const uint32_t* row = p.pred_B + (size_t)r * p.pred_W;
-      const uint32_t lo = w0 < p.pred_W ? row[w0] : 0u;
-      const uint32_t hi = (sh && w0 + 1 < p.pred_W) ? row[w0 + 1] : 0u;
-      m |= sh ? (lo >> sh) | (hi << (32 - sh)) : lo;
-    }
-    const int valid = p.E - 32 * w;
-    if (valid < 32) m &= (1u << valid) - 1u;
-    mask[w] = m;
-    n += __popc(m);
-  }
-  if (n == 0) return;
-  long long ppe = p.pf_budget / n / kPfPiece;  // pieces per expert
-  const long long cap = (p.pf_expert_bytes + kPfPiece - 1) / kPfPiece;
-  if (ppe > cap) ppe = cap;
-  for (long long i = c; i < n * ppe; i += G) {
-    int j = static_cast<int>(i / ppe);
-    const long long off = (i % ppe) * kPfPiece;
-    int e = -1;
-    for (int w = 0; w < EW && e < 0; ++w) {
-      const int cnt = __popc(mask[w]);
-      if (j < cnt) {
-        uint32_t mm = mask[w];
-        for (int q = 0; q < j; ++q) mm &= mm - 1;
-        e = 32 * w + __ffs(mm) - 1;
-      } else {
-        j -= cnt;
-      }
-    }
-    if (e < 0 || off >= p.pf_expert_bytes) continue;
-    const long long sz = p.pf_expert_bytes - off < kPfPiece ? p.pf_expert_bytes - off : kPfPiece;
-    const uint8_t* a = p.pf_base + e * p.pf_expert_bytes + off;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(static_cast<uint32_t>(sz)) : "memory");
-  }
-}
 
 __device__ __forceinline__ Tile tile_info(const TcParams& p, int U, int t) {
   Tile ti;
@@ -422,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!dep_done) resolve();
       *issued = n_issued;
-      if (!kGateUp && p.pf_base && !*abort_flag) prefetch_next_layer(p, c, gridDim.x);
+      if (!kGateUp && p.pf.base && !*abort_flag) l2_prefetch_next_layer(p.pf, p.E, c, gridDim.x);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -1074,13 +1017,7 @@ int ffn_tc_launch(const FfnArgs& a) {
   }
 
   // down + combine
-  tp.pf_base = a.pf_base;
-  tp.pf_expert_bytes = a.pf_expert_bytes;
-  tp.pf_budget = a.pf_budget;
-  tp.pred_B = a.pred_B;
-  tp.pred_rows = a.pred_rows;
-  tp.pred_W = a.pred_W;
-  tp.pred_bit0 = a.pred_bit0;
+  tp.pf = a.pf;
   tp.KS = g.KS_d;
   tp.M = lw.H;
   tp.K = lw.I;

@@ -191,14 +191,15 @@ extern "C" int moe_verify_step(const moe_step_cfg* cfg, const float* P, const in
     // the L2 prefetch at the end of this layer's down launch.
     if (l + 1 < c.L && c.W > 0) {
       const moe_layer_weights& nx = layers[l + 1];
-      if (nx.dtype == MOE_DTYPE_BF16 && nx.layout == MOE_LAYOUT_TILED && !nx.pool) {
-        fa.pf_base = static_cast<const uint8_t*>(nx.w_gate_up);
-        fa.pf_expert_bytes = static_cast<long long>((nx.I + 127) / 128) * 256 * nx.H * 2;
-        fa.pf_budget = kPrefetchBudget;
-        fa.pred_B = ws.pred_B;
-        fa.pred_rows = c.nseq;
-        fa.pred_W = c.W;
-        fa.pred_bit0 = (l + 1) * c.E;
+      const int eb = nx.dtype == MOE_DTYPE_BF16 ? 2 : (nx.dtype == MOE_DTYPE_E4M3_B128 ? 1 : 0);
+      if (eb && nx.layout == MOE_LAYOUT_TILED && !nx.pool) {
+        fa.pf.base = static_cast<const uint8_t*>(nx.w_gate_up);
+        fa.pf.expert_bytes = static_cast<long long>((nx.I + 127) / 128) * 256 * nx.H * eb;
+        fa.pf.budget = kPrefetchBudget;
+        fa.pf.pred_B = ws.pred_B;
+        fa.pf.rows = c.nseq;
+        fa.pf.W = c.W;
+        fa.pf.bit0 = (l + 1) * c.E;
       }
     }
     if ((st = ffn_launch(fa)) != MOE_OK) return st;
