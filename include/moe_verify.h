@@ -451,6 +451,10 @@ int eco_select(const float* P, const int32_t* parent, const uint32_t* own_fp, in
  *   y           [L, T, H] fp32 out.
  * cfg->T must equal sum over sequences of (gamma_i + 1) with gamma_i clamped
  * to N; the device checks it (MOE_DEV_CAPACITY if not).
+ * Layers with tiled, resident tensor-core weights: each layer's down launch
+ * also asks L2 to fetch part of the next layer's gate/up weights for the
+ * experts the selection predicts (the selected nodes' footprints).  This
+ * changes no result.
  */
 typedef struct {
   int32_t L, nseq, N, W, E, k, H, I, dtype, layout;
